@@ -1,0 +1,166 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of an oracle function (on the CPU, in
+this process only) and checks that at least one pin of that function fails.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.numerics as onum
+import oracle.ops as oops
+import test_oracle_numerics as tn
+import test_oracle_ops as to
+
+
+def _dequant_offset7(packed, scales, K, g):
+    u = onum.unpack_int4(packed, K).astype(np.float64)
+    s = np.asarray(scales, np.float16).astype(np.float64)
+    N = u.shape[0]
+    return ((u - 7.0).reshape(N, K // g, g) * s[:, :, None]).reshape(N, K)
+
+
+def _unpack_swapped(packed, K):
+    packed = np.asarray(packed, np.uint8)
+    u = np.empty((packed.shape[0], K), np.uint8)
+    u[:, 0::2] = packed >> 4
+    u[:, 1::2] = packed & 0x0F
+    return u
+
+
+def _dequant_scale_by_row_block(packed, scales, K, g):
+    u = onum.unpack_int4(packed, K).astype(np.float64)
+    s = np.asarray(scales, np.float16).astype(np.float64)
+    N = u.shape[0]
+    # wrong index: scale chosen by k % (K/g) instead of k // g
+    idx = np.arange(K) % (K // g)
+    return (u - 8.0) * s[:, idx]
+
+
+def _rope_sign(x, pos, base):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    h = d // 2
+    th = base ** (-2.0 * np.arange(h) / d)
+    a = pos * th
+    c, s = np.cos(a), np.sin(a)
+    return np.concatenate([x[..., :h] * c + x[..., h:] * s, x[..., h:] * c - x[..., :h] * s], -1)
+
+
+def _rope_adjacent_pairs(x, pos, base):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    th = base ** (-2.0 * np.arange(d // 2) / d)
+    a = pos * th
+    c, s = np.cos(a), np.sin(a)
+    y = x.copy()
+    y[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * s
+    y[..., 1::2] = x[..., 1::2] * c + x[..., 0::2] * s
+    return y
+
+
+def _attn_no_scale(q, K, V):
+    q, K, V = (np.asarray(a, np.float64) for a in (q, K, V))
+    qh, d = q.shape
+    grp = qh // K.shape[0]
+    out = np.empty_like(q)
+    for h in range(qh):
+        s = K[h // grp] @ q[h]
+        p = np.exp(s - s.max())
+        out[h] = (p / p.sum()) @ V[h // grp]
+    return out
+
+
+def _attn_gqa_modulo(q, K, V):
+    q, K, V = (np.asarray(a, np.float64) for a in (q, K, V))
+    qh, d = q.shape
+    out = np.empty_like(q)
+    for h in range(qh):
+        kv = h % K.shape[0]
+        s = K[kv] @ q[h] / math.sqrt(d)
+        p = np.exp(s - s.max())
+        out[h] = (p / p.sum()) @ V[kv]
+    return out
+
+
+def _route_ties_high(xn, Wr, k, renorm=True):
+    logits = np.asarray(xn, np.float64) @ np.asarray(Wr, np.float64).T
+    p = np.exp(logits - logits.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    E = p.shape[1]
+    ids = np.array([(E - 1 - np.argsort(-p[b][::-1], kind="stable"))[:k] for b in range(len(p))])
+    w = np.take_along_axis(p, ids, 1)
+    return ids.astype(np.int32), w / w.sum(1, keepdims=True)
+
+
+def _route_no_renorm(xn, Wr, k, renorm=True):
+    ids, _ = oops.route_topk(xn, Wr, k, renorm)
+    logits = np.asarray(xn, np.float64) @ np.asarray(Wr, np.float64).T
+    p = np.exp(logits - logits.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    return ids, np.take_along_axis(p, ids, 1)
+
+
+def _rmsnorm_sum(x, weight=None, eps=1e-6):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps)
+
+
+def _combine_no_residual(h, outs, weights):
+    return sum(w * np.asarray(o, np.float64) for w, o in zip(weights, outs))
+
+
+def _silu_wrong(x):
+    x = np.asarray(x, np.float64)
+    return x / (1.0 + np.exp(x))
+
+
+def _gemm_transposed_scale(X, packed, scales, K, g):
+    W = _dequant_scale_by_row_block(packed, scales, K, g)
+    return np.asarray(X, np.float64) @ W.T
+
+
+MUTANTS = [
+    ("dequant offset 7", [(oracle, "dequant_w4"), (oops, "dequant_w4")], _dequant_offset7,
+     [tn.test_int4_dequant_hand_values, tn.test_int4_dequant_exhaustive_codes, to.test_gemm_hand_value]),
+    ("nibble order swapped", [(oracle, "unpack_int4"), (onum, "unpack_int4")], _unpack_swapped,
+     [tn.test_int4_dequant_hand_values, tn.test_quantize_hand_values, to.test_gemm_closed_forms_and_row_independence]),
+    ("scale index", [(oracle, "dequant_w4"), (oops, "dequant_w4")], _dequant_scale_by_row_block,
+     [tn.test_int4_group_scale_indexing]),
+    ("gemm scale index", [(oracle, "w4_gemm")], _gemm_transposed_scale,
+     [to.test_gemm_brute_force_tiny]),
+    ("rope sign", [(oracle, "rope_rotate_half")], _rope_sign,
+     [to.test_rope_hand_value]),
+    ("rope pairing", [(oracle, "rope_rotate_half")], _rope_adjacent_pairs,
+     [to.test_rope_hand_value]),
+    ("attention scale", [(oracle, "slot_attention")], _attn_no_scale,
+     [to.test_attention_hand_value, to.test_attention_brute_force_and_gqa_map]),
+    ("gqa map", [(oracle, "slot_attention")], _attn_gqa_modulo,
+     [to.test_attention_special_cases, to.test_attention_brute_force_and_gqa_map]),
+    ("router ties", [(oracle, "route_topk")], _route_ties_high,
+     [to.test_router_hand_values]),
+    ("router renorm", [(oracle, "route_topk")], _route_no_renorm,
+     [to.test_router_hand_values, to.test_router_invariants]),
+    ("rmsnorm sum", [(oracle, "rmsnorm")], _rmsnorm_sum,
+     [to.test_rmsnorm_hand_and_invariants]),
+    ("combine residual", [(oracle, "moe_combine")], _combine_no_residual,
+     [to.test_expert_ffn_special_cases]),
+    ("silu sign", [(oracle, "silu")], _silu_wrong,
+     [to.test_silu_values]),
+]
+
+
+@pytest.mark.parametrize("name,targets,mutant,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(monkeypatch, name, targets, mutant, pins):
+    for mod, attr in targets:
+        monkeypatch.setattr(mod, attr, mutant)
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1, f"no pin caught the planted mistake: {name}"

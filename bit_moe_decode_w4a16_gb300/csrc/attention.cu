@@ -1,0 +1,253 @@
+// Slot-indexed decode attention over the fixed KV arena.
+//
+// The arena is [layer][slot][kv head][position][d] bf16 for K and for V; a
+// stream's K/V live in its stable slot and nothing here reads or writes any
+// other slot (the KV-slot isolation page, §1: the batched arena is indexed by
+// a stable per-stream slot and never wiped on a batch-composition change).
+//
+//   k_rope_append  RoPE (rotate-half) of q and k at pos = len[slot]; q to a
+//                  query buffer, k and v to the arena at pos
+//   k_kv_append    the same append for k, v that are already rotated
+//   k_attn_part    split-K: one CTA per (128-position chunk, kv head, stream)
+//                  computes, for the q heads of that kv head, the chunk's
+//                  running max, exp-sum and unnormalised p·V
+//   k_attn_combine merges a stream's chunks in ascending order
+// The chunk grid depends only on a stream's own length, so its output does
+// not depend on the other streams of the batch.
+#include <float.h>
+
+#include "kernels.cuh"
+
+namespace bm {
+
+namespace {
+
+constexpr int kMaxGroup = 8;   // q heads per kv head handled by one CTA
+
+__global__ void k_rope_append(AttnArena ar, int layer, const int32_t* slots, const bf16* qkv, int ld_qkv,
+                              int qh, const double* theta, bf16* qout, DevCheck chk) {
+  extern __shared__ float cs[];   // [d/2] cos, [d/2] sin
+  const int b = blockIdx.x;
+  const int slot = slots[b];
+  if (slot < 0 || slot >= ar.S) { if (threadIdx.x == 0) chk.fail(1); return; }
+  const int pos = ar.len[slot];
+  if (pos < 0 || pos >= ar.cap) { if (threadIdx.x == 0) chk.fail(2); return; }
+  const int d = ar.d, half = d / 2;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    double sn, cn;
+    sincos((double)pos * theta[i], &sn, &cn);
+    cs[i] = (float)cn;
+    cs[half + i] = (float)sn;
+  }
+  __syncthreads();
+  const bf16* row = qkv + (size_t)b * ld_qkv;
+  const int heads = qh + ar.kvh;
+  for (int idx = threadIdx.x; idx < heads * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    const bf16* src = row + (size_t)h * d;
+    const float x0 = bf2f(src[i]), x1 = bf2f(src[i + half]);
+    const float c = cs[i], s = cs[half + i];
+    const bf16 y0 = f2bf(x0 * c - x1 * s);
+    const bf16 y1 = f2bf(x1 * c + x0 * s);
+    if (h < qh) {
+      bf16* dst = qout + ((size_t)b * qh + h) * d;
+      dst[i] = y0;
+      dst[i + half] = y1;
+    } else {
+      const int kh = h - qh;
+      bf16* dst = ar.K + layer * ar.layer_stride() + slot * ar.slot_stride() + ((size_t)kh * ar.cap + pos) * d;
+      dst[i] = y0;
+      dst[i + half] = y1;
+    }
+  }
+  const bf16* vsrc = row + (size_t)(qh + ar.kvh) * d;
+  for (int idx = threadIdx.x; idx < ar.kvh * d; idx += blockDim.x) {
+    const int kh = idx / d, i = idx - kh * d;
+    ar.V[layer * ar.layer_stride() + slot * ar.slot_stride() + ((size_t)kh * ar.cap + pos) * d + i] = vsrc[idx];
+  }
+}
+
+__global__ void k_kv_append(AttnArena ar, int layer, const int32_t* slots, const bf16* k, const bf16* v,
+                            DevCheck chk) {
+  const int b = blockIdx.x;
+  const int slot = slots[b];
+  if (slot < 0 || slot >= ar.S) { if (threadIdx.x == 0) chk.fail(1); return; }
+  const int pos = ar.len[slot];
+  if (pos < 0 || pos >= ar.cap) { if (threadIdx.x == 0) chk.fail(2); return; }
+  for (int idx = threadIdx.x; idx < ar.kvh * ar.d; idx += blockDim.x) {
+    const int kh = idx / ar.d, i = idx - kh * ar.d;
+    const size_t o = layer * ar.layer_stride() + slot * ar.slot_stride() + ((size_t)kh * ar.cap + pos) * ar.d + i;
+    ar.K[o] = k[(size_t)b * ar.kvh * ar.d + idx];
+    ar.V[o] = v[(size_t)b * ar.kvh * ar.d + idx];
+  }
+}
+
+// Partials layout: [B][qh][max_chunks] records of (d floats o, m, l).
+__device__ __forceinline__ size_t part_index(int b, int h, int c, int qh, int max_chunks, int d) {
+  return (((size_t)b * qh + h) * max_chunks + c) * (size_t)(d + 2);
+}
+
+// blockDim.x == kAttnChunk == 128 threads; d <= 128.
+__global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int layer, const int32_t* slots,
+                                                          const bf16* q, int qh, float* part, int max_chunks,
+                                                          DevCheck chk) {
+  __shared__ float qs[kMaxGroup][128];
+  __shared__ float ps[kMaxGroup][kAttnChunk];
+  __shared__ float red[kMaxGroup][kAttnChunk / 32];
+  __shared__ float stat[kMaxGroup][2];
+  const int c = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  const int slot = slots[b];
+  if (slot < 0 || slot >= ar.S) { if (c == 0 && kh == 0 && threadIdx.x == 0) chk.fail(1); return; }
+  const int L = ar.len[slot] + 1;   // committed prefix + this step's position
+  if (L < 1 || L > ar.cap) { if (c == 0 && kh == 0 && threadIdx.x == 0) chk.fail(2); return; }
+  const int j0 = c * kAttnChunk;
+  if (j0 >= L) return;
+  const int d = ar.d, G = qh / ar.kvh, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const float scale = 1.0f / sqrtf((float)d);
+  for (int idx = t; idx < G * d; idx += blockDim.x) {
+    const int g = idx / d, i = idx - g * d;
+    qs[g][i] = bf2f(q[((size_t)b * qh + kh * G + g) * d + i]);
+  }
+  __syncthreads();
+  const size_t base = layer * ar.layer_stride() + slot * ar.slot_stride() + (size_t)kh * ar.cap * d;
+  const bf16* Kb = ar.K + base;
+  const bf16* Vb = ar.V + base;
+  const int j = j0 + t;
+  float sc[kMaxGroup];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) sc[g] = 0.f;
+  if (j < L) {
+    const uint4* kr = reinterpret_cast<const uint4*>(Kb + (size_t)j * d);
+    for (int i8 = 0; i8 < d / 8; ++i8) {
+      const uint4 kv = kr[i8];
+      const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
+      const float k4 = bf_lo(kv.z), k5 = bf_hi(kv.z), k6 = bf_lo(kv.w), k7 = bf_hi(kv.w);
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) {
+        if (g < G) {
+          const float* qq = &qs[g][i8 * 8];
+          float a = sc[g];
+          a = fmaf(qq[0], k0, a); a = fmaf(qq[1], k1, a); a = fmaf(qq[2], k2, a); a = fmaf(qq[3], k3, a);
+          a = fmaf(qq[4], k4, a); a = fmaf(qq[5], k5, a); a = fmaf(qq[6], k6, a); a = fmaf(qq[7], k7, a);
+          sc[g] = a;
+        }
+      }
+    }
+  }
+  // chunk max per head
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    if (g >= G) break;
+    const float s = (j < L) ? sc[g] * scale : -FLT_MAX;
+    sc[g] = s;
+    const float m = warp_max(s);
+    if (lane == 0) red[g][warp] = m;
+  }
+  __syncthreads();
+  if (t < G) {
+    float m = red[t][0];
+    for (int w = 1; w < kAttnChunk / 32; ++w) m = fmaxf(m, red[t][w]);
+    stat[t][0] = m;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    if (g >= G) break;
+    const float p = (j < L) ? expf(sc[g] - stat[g][0]) : 0.f;
+    ps[g][t] = p;
+    const float sum = warp_sum(p);
+    if (lane == 0) red[g][warp] = sum;
+  }
+  __syncthreads();
+  if (t < G) {
+    float l = 0.f;
+    for (int w = 0; w < kAttnChunk / 32; ++w) l += red[t][w];
+    stat[t][1] = l;
+  }
+  __syncthreads();
+  // p·V: thread t owns dimension t of every head of the group.
+  const int n = min(kAttnChunk, L - j0);
+  if (t < d) {
+    float o[kMaxGroup];
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) o[g] = 0.f;
+    for (int jj = 0; jj < n; ++jj) {
+      const float v = bf2f(Vb[(size_t)(j0 + jj) * d + t]);
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g)
+        if (g < G) o[g] = fmaf(ps[g][jj], v, o[g]);
+    }
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) {
+      if (g >= G) break;
+      float* rec = part + part_index(b, kh * G + g, c, qh, max_chunks, d);
+      rec[t] = o[g];
+      if (t == 0) {
+        rec[d] = stat[g][0];
+        rec[d + 1] = stat[g][1];
+      }
+    }
+  }
+}
+
+__global__ void k_attn_combine(AttnArena ar, const int32_t* slots, const float* part, int qh, int max_chunks,
+                               bf16* out) {
+  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x, d = ar.d;
+  const int slot = slots[b];
+  if (slot < 0 || slot >= ar.S) return;
+  const int L = ar.len[slot] + 1;
+  if (L < 1 || L > ar.cap) return;
+  const int nc = (L + kAttnChunk - 1) / kAttnChunk;
+  float M = -FLT_MAX;
+  for (int c = 0; c < nc; ++c) M = fmaxf(M, part[part_index(b, h, c, qh, max_chunks, d) + d]);
+  float den = 0.f, acc = 0.f;
+  for (int c = 0; c < nc; ++c) {
+    const float* rec = part + part_index(b, h, c, qh, max_chunks, d);
+    const float w = expf(rec[d] - M);
+    den = fmaf(rec[d + 1], w, den);
+    if (t < d) acc = fmaf(rec[t], w, acc);
+  }
+  if (t < d) out[((size_t)b * qh + h) * d + t] = f2bf(acc / den);
+}
+
+__global__ void k_set_len(int32_t* len, int slot, int value) { len[slot] = value; }
+
+}  // namespace
+
+size_t attn_partial_floats(int B, int qh, int cap, int d) {
+  const int max_chunks = (cap + kAttnChunk - 1) / kAttnChunk;
+  return (size_t)B * qh * max_chunks * (d + 2);
+}
+
+cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* qkv, int ld_qkv,
+                               int qh, const double* theta, bf16* qout, int B, DevCheck chk, cudaStream_t st) {
+  k_rope_append<<<B, 256, sizeof(float) * ar.d, st>>>(ar, layer, slots, qkv, ld_qkv, qh, theta, qout, chk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* k, const bf16* v,
+                             int B, DevCheck chk, cudaStream_t st) {
+  k_kv_append<<<B, 256, 0, st>>>(ar, layer, slots, k, v, chk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q, bf16* out,
+                             int qh, int B, float* partials, DevCheck chk, cudaStream_t st, int* launches) {
+  if (ar.d > 128 || ar.d % 8 != 0 || qh % ar.kvh != 0 || qh / ar.kvh > kMaxGroup) return cudaErrorInvalidValue;
+  const int max_chunks = (ar.cap + kAttnChunk - 1) / kAttnChunk;
+  dim3 g1(max_chunks, ar.kvh, B);
+  k_attn_part<<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2(qh, B);
+  k_attn_combine<<<g2, 128, 0, st>>>(ar, slots, partials, qh, max_chunks, out);
+  if (launches) *launches += 2;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st) {
+  k_set_len<<<1, 1, 0, st>>>(len, slot, value);
+  return cudaGetLastError();
+}
+
+}  // namespace bm

@@ -1,0 +1,70 @@
+// Shared device helpers of the W4A16 decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bm {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kWarp = 32;
+
+// Device-side index check: an out-of-range slot, token or expert id is
+// skipped and recorded here; the host reads it in bm_engine_sync.
+struct DevCheck {
+  int* flag;  // may be null
+  __device__ __forceinline__ void fail(int code) const {
+    if (flag) atomicExch(flag, code);
+  }
+};
+
+__device__ __forceinline__ float bf2f(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ bf16 f2bf(float v) { return __float2bfloat16_rn(v); }
+// Round an fp32 value to the nearest bf16 value and return it as fp32.
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// Low / high bf16 of a packed pair, as fp32 (exact).
+__device__ __forceinline__ float bf_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
+
+// The int4 code at nibble `p` (0..7) of a packed word, as the exact fp32 value
+// q = u - 8.  0x4B000000 | u is the float 2^23 + u; subtracting 2^23 + 8 is exact.
+template <int P>
+__device__ __forceinline__ float nib_q(uint32_t w) {
+  const uint32_t u = (w >> (4 * P)) & 0xFu;
+  return __uint_as_float(0x4B000000u | u) - 8388616.0f;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum over the groups of `Width` consecutive lanes, fixed butterfly order.
+template <int Width>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = Width / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+}  // namespace bm

@@ -1,0 +1,676 @@
+// Host runtime of the decode step: engine memory, the slot arena, weight
+// loading, the per-B CUDA graph cache and the C ABI entry points.
+//
+// One decode step = one cudaGraphLaunch (the batched-serving page, §1: all
+// layers plus the per-stream output projection are folded into one command
+// buffer, one submit for the whole batch).  The host crosses to the device
+// once per step: a small copy of slot ids and tokens into the graph's static
+// input buffers, the launch, and a copy of the next tokens back.
+#include <array>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <new>
+#include <set>
+#include <string>
+#include <vector>
+
+#include <cmath>
+
+#include "errors.h"
+#include "kernels.cuh"
+#include "slot_map.h"
+
+namespace bm {
+
+std::string& last_error_slot() {
+  thread_local std::string s;
+  return s;
+}
+
+cudaError_t init_gemv_attributes();
+cudaError_t init_moe_attributes();
+cudaError_t init_misc_attributes();
+
+namespace {
+
+#define BM_CUDA(call, what)                                                                     \
+  do {                                                                                          \
+    cudaError_t _e = (call);                                                                    \
+    if (_e != cudaSuccess) return set_error(BM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(_e)); \
+  } while (0)
+
+std::mutex g_attr_mu;
+std::set<int> g_attr_devices;
+
+bm_status ensure_attributes() {
+  int dev = 0;
+  BM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (g_attr_devices.count(dev)) return BM_OK;
+  BM_CUDA(init_gemv_attributes(), "kernel attributes (dense)");
+  BM_CUDA(init_moe_attributes(), "kernel attributes (experts)");
+  BM_CUDA(init_misc_attributes(), "kernel attributes (lm_head)");
+  g_attr_devices.insert(dev);
+  return BM_OK;
+}
+
+size_t al(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+struct LayerW {
+  uint8_t* wqkv = nullptr; __half* wqkv_s = nullptr;
+  uint8_t* wo = nullptr;   __half* wo_s = nullptr;
+  float* wr = nullptr;
+  uint8_t* wg = nullptr;   __half* wg_s = nullptr;
+  uint8_t* wu = nullptr;   __half* wu_s = nullptr;
+  uint8_t* wd = nullptr;   __half* wd_s = nullptr;
+  bf16* attn_norm_buf = nullptr; bf16* ffn_norm_buf = nullptr;
+  bool has_attn_norm = false, has_ffn_norm = false;
+  bool set = false;
+};
+
+}  // namespace
+}  // namespace bm
+
+using namespace bm;
+
+struct bm_engine {
+  bm_config cfg{};
+  int family = BM_POLICY_SIMT;
+  SlotMap slots;
+  std::mutex mu;
+  int device = 0;
+  int qkv_rows = 0;
+  // weights
+  void* wslab = nullptr;
+  size_t wbytes = 0;
+  std::vector<LayerW> L;
+  bf16* embed = nullptr;
+  bf16* lm_head = nullptr;
+  bf16* final_norm_buf = nullptr;
+  bool has_final_norm = false;
+  bool emb_set = false;
+  // arena
+  AttnArena arena{};
+  void* arena_mem = nullptr;
+  size_t arena_bytes = 0;
+  double* d_theta = nullptr;
+  // scratch
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  bf16 *x = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr;
+  float* attn_part = nullptr;
+  void* moe_ws = nullptr;
+  float* logits = nullptr;
+  int32_t *d_slots = nullptr, *d_tokens = nullptr, *d_next = nullptr, *d_slots_aux = nullptr;
+  int* d_err = nullptr;
+  // host staging (pinned)
+  int32_t* h_stage = nullptr;   // [2 * max_streams]: slots, tokens
+  int32_t* h_aux = nullptr;     // [max_streams]: slots of standalone kv calls
+  cudaEvent_t ev_stage = nullptr, ev_aux = nullptr;
+  cudaStream_t cap_stream = nullptr;
+  std::map<int, cudaGraphExec_t> graphs;
+  bm_stats st{};
+
+  bm_engine(const bm_config& c) : cfg(c), slots(c.max_streams, c.ctx_cap) {}
+};
+
+namespace bm {
+namespace {
+
+DevCheck chk_of(bm_engine* e) { return DevCheck{e->d_err}; }
+
+// Enqueue one decode step for B streams reading e->d_slots / e->d_tokens.
+cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches) {
+  const bm_config& c = e->cfg;
+  const int H = c.hidden, qd = c.q_heads * c.head_dim;
+  cudaError_t err;
+  int n = 0;
+  if ((err = launch_embed(e->embed, c.vocab, H, e->d_tokens, e->x, B, chk_of(e), s)) != cudaSuccess) return err;
+  ++n;
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerW& w = e->L[l];
+    GemvArgs g1{w.wqkv, w.wqkv_s, e->x, H, nullptr, 0, e->qkv, e->qkv_rows, B, e->qkv_rows, H, c.group,
+                1, w.has_attn_norm ? w.attn_norm_buf : nullptr, c.rms_eps};
+    if ((err = launch_w4_gemv(g1, s)) != cudaSuccess) return err;
+    ++n;
+    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
+                                  chk_of(e), s)) != cudaSuccess)
+      return err;
+    ++n;
+    if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
+                                &n)) != cudaSuccess)
+      return err;
+    GemvArgs g2{w.wo, w.wo_s, e->attn, qd, e->x, H, e->h, H, B, H, qd, c.group, 0, nullptr, c.rms_eps};
+    if ((err = launch_w4_gemv(g2, s)) != cudaSuccess) return err;
+    ++n;
+    MoeArgs ma{B, c.experts, c.top_k, H, c.ffn, c.group, c.renorm_topk,
+               w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
+               e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x};
+    const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, c.ffn);
+    if ((err = launch_moe(ma, mb, s, &n)) != cudaSuccess) return err;
+  }
+  if ((err = launch_lm_head(e->lm_head, c.vocab, H, e->x, e->has_final_norm ? e->final_norm_buf : nullptr,
+                            c.rms_eps, e->logits, B, s)) != cudaSuccess)
+    return err;
+  ++n;
+  if ((err = launch_argmax(e->logits, c.vocab, B, e->d_next, e->arena.len, e->d_slots, 1, s)) != cudaSuccess)
+    return err;
+  ++n;
+  if (launches) *launches = n;
+  return cudaSuccess;
+}
+
+bm_status check_config(const bm_config& c) {
+  auto bad = [](const std::string& m) { return set_error(BM_ERR_INVALID_ARG, "bm_engine_create: " + m); };
+  if (c.hidden <= 0 || c.hidden % 32 != 0) return bad("hidden must be a positive multiple of 32");
+  if (c.q_heads <= 0 || c.kv_heads <= 0 || c.q_heads % c.kv_heads != 0) return bad("q_heads % kv_heads != 0");
+  if (c.q_heads / c.kv_heads > 8) return bad("at most 8 query heads per kv head");
+  if (c.head_dim != 64 && c.head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c.experts < 1 || c.experts > 256) return bad("experts must be in [1, 256]");
+  if (c.top_k < 1 || c.top_k > 16 || c.top_k > c.experts) return bad("top_k must be in [1, min(16, experts)]");
+  if (c.ffn <= 0 || c.ffn % 32 != 0) return bad("ffn must be a positive multiple of 32");
+  if (c.group != 32 && c.group != 64 && c.group != 128) return bad("group must be 32, 64 or 128");
+  if (c.hidden % c.group || c.ffn % c.group || (c.q_heads * c.head_dim) % c.group)
+    return bad("every reduction length must be a multiple of group");
+  if (c.vocab < 1 || c.layers < 1) return bad("vocab and layers must be >= 1");
+  if (c.max_streams < 1 || c.max_streams > 64) return bad("max_streams must be in [1, 64]");
+  if (c.max_streams * c.top_k > 1024) return bad("max_streams * top_k must be <= 1024");
+  if (c.ctx_cap < 1) return bad("ctx_cap must be >= 1");
+  if (!(c.rope_base > 0.f) || !(c.rms_eps >= 0.f)) return bad("rope_base > 0 and rms_eps >= 0 required");
+  if (!simt_supports_k(c.hidden) || !simt_supports_k(c.ffn) || !simt_supports_k(c.q_heads * c.head_dim))
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: a reduction length has no kernel shape in this build");
+  if (c.kernel_policy == BM_POLICY_TC)
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: the tensor-core family is not available in this build");
+  if (c.kernel_policy < 0 || c.kernel_policy > 2) return bad("unknown kernel_policy");
+  return BM_OK;
+}
+
+void free_engine(bm_engine* e) {
+  if (!e) return;
+  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
+  if (e->ev_stage) cudaEventDestroy(e->ev_stage);
+  if (e->ev_aux) cudaEventDestroy(e->ev_aux);
+  if (e->h_stage) cudaFreeHost(e->h_stage);
+  if (e->wslab) cudaFree(e->wslab);
+  if (e->arena_mem) cudaFree(e->arena_mem);
+  if (e->scratch) cudaFree(e->scratch);
+  delete e;
+}
+
+// Upload the host slot list of a standalone kv call into d_slots_aux.
+bm_status stage_aux_slots(bm_engine* e, const int32_t* slots, int B, cudaStream_t s) {
+  BM_CUDA(cudaEventSynchronize(e->ev_aux), "staging event");
+  std::memcpy(e->h_aux, slots, sizeof(int32_t) * B);
+  BM_CUDA(cudaMemcpyAsync(e->d_slots_aux, e->h_aux, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s), "slot upload");
+  BM_CUDA(cudaEventRecord(e->ev_aux, s), "staging event");
+  return BM_OK;
+}
+
+}  // namespace
+}  // namespace bm
+
+// =================================================================== C ABI
+
+extern "C" {
+
+const char* bm_last_error(void) { return bm::last_error_slot().c_str(); }
+
+bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
+  if (!cfg || !out) return set_error(BM_ERR_INVALID_ARG, "bm_engine_create: null argument");
+  *out = nullptr;
+  bm_status st = check_config(*cfg);
+  if (st != BM_OK) return st;
+  if ((st = ensure_attributes()) != BM_OK) return st;
+  bm_engine* e = new (std::nothrow) bm_engine(*cfg);
+  if (!e) return set_error(BM_ERR_OOM, "bm_engine_create: out of host memory");
+  std::unique_ptr<bm_engine, void (*)(bm_engine*)> guard(e, free_engine);
+  const bm_config& c = e->cfg;
+  cudaGetDevice(&e->device);
+  e->family = BM_POLICY_SIMT;
+  e->qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim;
+  const int H = c.hidden, E = c.experts, F = c.ffn, g = c.group, qd = c.q_heads * c.head_dim;
+  const size_t S = c.max_streams;
+
+  // ---- weight slab
+  struct Part { size_t off, bytes; };
+  size_t off = 0;
+  auto take = [&](size_t bytes) { Part p{off, bytes}; off += al(bytes); return p; };
+  std::vector<std::array<Part, 13>> lp(c.layers);
+  for (int l = 0; l < c.layers; ++l) {
+    auto& p = lp[l];
+    p[0] = take((size_t)e->qkv_rows * H / 2);
+    p[1] = take((size_t)e->qkv_rows * (H / g) * 2);
+    p[2] = take((size_t)H * qd / 2);
+    p[3] = take((size_t)H * (qd / g) * 2);
+    p[4] = take((size_t)E * H * 4);
+    p[5] = take((size_t)E * F * H / 2);
+    p[6] = take((size_t)E * F * (H / g) * 2);
+    p[7] = take((size_t)E * F * H / 2);
+    p[8] = take((size_t)E * F * (H / g) * 2);
+    p[9] = take((size_t)E * H * F / 2);
+    p[10] = take((size_t)E * H * (F / g) * 2);
+    p[11] = take((size_t)H * 2);
+    p[12] = take((size_t)H * 2);
+  }
+  const Part p_emb = take((size_t)c.vocab * H * 2), p_lm = take((size_t)c.vocab * H * 2), p_fn = take((size_t)H * 2);
+  e->wbytes = off;
+  BM_CUDA(cudaMalloc(&e->wslab, e->wbytes), "weight slab allocation");
+  char* wb = static_cast<char*>(e->wslab);
+  e->L.resize(c.layers);
+  for (int l = 0; l < c.layers; ++l) {
+    auto& p = lp[l];
+    LayerW& w = e->L[l];
+    w.wqkv = reinterpret_cast<uint8_t*>(wb + p[0].off); w.wqkv_s = reinterpret_cast<__half*>(wb + p[1].off);
+    w.wo = reinterpret_cast<uint8_t*>(wb + p[2].off);   w.wo_s = reinterpret_cast<__half*>(wb + p[3].off);
+    w.wr = reinterpret_cast<float*>(wb + p[4].off);
+    w.wg = reinterpret_cast<uint8_t*>(wb + p[5].off);   w.wg_s = reinterpret_cast<__half*>(wb + p[6].off);
+    w.wu = reinterpret_cast<uint8_t*>(wb + p[7].off);   w.wu_s = reinterpret_cast<__half*>(wb + p[8].off);
+    w.wd = reinterpret_cast<uint8_t*>(wb + p[9].off);   w.wd_s = reinterpret_cast<__half*>(wb + p[10].off);
+    w.attn_norm_buf = reinterpret_cast<bf16*>(wb + p[11].off);
+    w.ffn_norm_buf = reinterpret_cast<bf16*>(wb + p[12].off);
+  }
+  e->embed = reinterpret_cast<bf16*>(wb + p_emb.off);
+  e->lm_head = reinterpret_cast<bf16*>(wb + p_lm.off);
+  e->final_norm_buf = reinterpret_cast<bf16*>(wb + p_fn.off);
+
+  // ---- KV arena: [layer][slot][kv head][position][d], K then V
+  AttnArena& ar = e->arena;
+  ar.layers = c.layers; ar.S = c.max_streams; ar.kvh = c.kv_heads; ar.cap = c.ctx_cap; ar.d = c.head_dim;
+  const size_t kv_elems = (size_t)c.layers * ar.layer_stride();
+  e->arena_bytes = al(kv_elems * 2) * 2 + al(S * 4) + al((size_t)c.head_dim / 2 * sizeof(double));
+  BM_CUDA(cudaMalloc(&e->arena_mem, e->arena_bytes), "KV arena allocation");
+  char* am = static_cast<char*>(e->arena_mem);
+  ar.K = reinterpret_cast<bf16*>(am);
+  ar.V = reinterpret_cast<bf16*>(am + al(kv_elems * 2));
+  ar.len = reinterpret_cast<int32_t*>(am + 2 * al(kv_elems * 2));
+  e->d_theta = reinterpret_cast<double*>(am + 2 * al(kv_elems * 2) + al(S * 4));
+  BM_CUDA(cudaMemset(ar.len, 0, S * 4), "arena length reset");
+  {
+    std::vector<double> theta(c.head_dim / 2);
+    for (int i = 0; i < c.head_dim / 2; ++i) theta[i] = std::pow((double)c.rope_base, -2.0 * i / c.head_dim);
+    BM_CUDA(cudaMemcpy(e->d_theta, theta.data(), theta.size() * sizeof(double), cudaMemcpyHostToDevice),
+            "rope table upload");
+  }
+
+  // ---- scratch
+  off = 0;
+  const Part s_x = take(S * H * 2), s_qkv = take(S * e->qkv_rows * 2), s_q = take(S * qd * 2),
+             s_attn = take(S * qd * 2), s_h = take(S * H * 2),
+             s_part = take(attn_partial_floats(c.max_streams, c.q_heads, c.ctx_cap, c.head_dim) * 4),
+             s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
+             s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
+             s_sa = take(S * 4), s_err = take(4);
+  e->scratch_bytes = off;
+  BM_CUDA(cudaMalloc(&e->scratch, e->scratch_bytes), "scratch allocation");
+  char* sb = static_cast<char*>(e->scratch);
+  e->x = reinterpret_cast<bf16*>(sb + s_x.off);
+  e->qkv = reinterpret_cast<bf16*>(sb + s_qkv.off);
+  e->q = reinterpret_cast<bf16*>(sb + s_q.off);
+  e->attn = reinterpret_cast<bf16*>(sb + s_attn.off);
+  e->h = reinterpret_cast<bf16*>(sb + s_h.off);
+  e->attn_part = reinterpret_cast<float*>(sb + s_part.off);
+  e->moe_ws = sb + s_moe.off;
+  e->logits = reinterpret_cast<float*>(sb + s_log.off);
+  e->d_slots = reinterpret_cast<int32_t*>(sb + s_sl.off);
+  e->d_tokens = reinterpret_cast<int32_t*>(sb + s_tk.off);
+  e->d_next = reinterpret_cast<int32_t*>(sb + s_nx.off);
+  e->d_slots_aux = reinterpret_cast<int32_t*>(sb + s_sa.off);
+  e->d_err = reinterpret_cast<int*>(sb + s_err.off);
+  BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");
+
+  BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * 3 * S), "pinned staging allocation");
+  e->h_aux = e->h_stage + 2 * S;
+  BM_CUDA(cudaEventCreateWithFlags(&e->ev_stage, cudaEventDisableTiming), "event");
+  BM_CUDA(cudaEventCreateWithFlags(&e->ev_aux, cudaEventDisableTiming), "event");
+  BM_CUDA(cudaEventRecord(e->ev_stage, 0), "event");
+  BM_CUDA(cudaEventRecord(e->ev_aux, 0), "event");
+  BM_CUDA(cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking), "capture stream");
+  BM_CUDA(cudaDeviceSynchronize(), "engine setup");
+
+  e->st.weight_bytes = e->wbytes;
+  e->st.arena_bytes = e->arena_bytes;
+  e->st.scratch_bytes = e->scratch_bytes;
+  std::fprintf(stderr,
+               "bitmoe: engine on device %d: weights %.3f GB, KV arena %.3f GB (%d layers x %d slots x %d "
+               "positions x %d kv heads x %d), scratch %.1f MB, kernel family %s\n",
+               e->device, e->wbytes / 1e9, e->arena_bytes / 1e9, c.layers, c.max_streams, c.ctx_cap, c.kv_heads,
+               c.head_dim, e->scratch_bytes / 1e6, e->family == BM_POLICY_TC ? "tc" : "simt");
+  *out = guard.release();
+  return bm::ok();
+}
+
+void bm_engine_destroy(bm_engine* e) {
+  if (!e) return;
+  cudaDeviceSynchronize();
+  free_engine(e);
+}
+
+bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w, void* stream) {
+  if (!e || !w) return set_error(BM_ERR_INVALID_ARG, "bm_engine_set_layer: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  if (layer < 0 || layer >= c.layers) return set_error(BM_ERR_INVALID_ARG, "bm_engine_set_layer: layer out of range");
+  if (!w->wqkv || !w->wqkv_s || !w->wo || !w->wo_s || !w->wr || !w->wg || !w->wg_s || !w->wu || !w->wu_s ||
+      !w->wd || !w->wd_s)
+    return set_error(BM_ERR_INVALID_ARG, "bm_engine_set_layer: a weight pointer is null");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerW& d = e->L[layer];
+  const int H = c.hidden, E = c.experts, F = c.ffn, g = c.group, qd = c.q_heads * c.head_dim;
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s);
+  };
+  BM_CUDA(cp(d.wqkv, w->wqkv, (size_t)e->qkv_rows * H / 2), "set_layer wqkv");
+  BM_CUDA(cp(d.wqkv_s, w->wqkv_s, (size_t)e->qkv_rows * (H / g) * 2), "set_layer wqkv scales");
+  BM_CUDA(cp(d.wo, w->wo, (size_t)H * qd / 2), "set_layer wo");
+  BM_CUDA(cp(d.wo_s, w->wo_s, (size_t)H * (qd / g) * 2), "set_layer wo scales");
+  BM_CUDA(cp(d.wr, w->wr, (size_t)E * H * 4), "set_layer router");
+  BM_CUDA(cp(d.wg, w->wg, (size_t)E * F * H / 2), "set_layer wg");
+  BM_CUDA(cp(d.wg_s, w->wg_s, (size_t)E * F * (H / g) * 2), "set_layer wg scales");
+  BM_CUDA(cp(d.wu, w->wu, (size_t)E * F * H / 2), "set_layer wu");
+  BM_CUDA(cp(d.wu_s, w->wu_s, (size_t)E * F * (H / g) * 2), "set_layer wu scales");
+  BM_CUDA(cp(d.wd, w->wd, (size_t)E * H * F / 2), "set_layer wd");
+  BM_CUDA(cp(d.wd_s, w->wd_s, (size_t)E * H * (F / g) * 2), "set_layer wd scales");
+  d.has_attn_norm = w->attn_norm != nullptr;
+  d.has_ffn_norm = w->ffn_norm != nullptr;
+  if (w->attn_norm) BM_CUDA(cp(d.attn_norm_buf, w->attn_norm, (size_t)H * 2), "set_layer attn norm");
+  if (w->ffn_norm) BM_CUDA(cp(d.ffn_norm_buf, w->ffn_norm, (size_t)H * 2), "set_layer ffn norm");
+  d.set = true;
+  return bm::ok();
+}
+
+bm_status bm_engine_set_embeddings(bm_engine* e, const uint16_t* embed, const uint16_t* lm_head,
+                                   const uint16_t* final_norm, void* stream) {
+  if (!e || !embed || !lm_head) return set_error(BM_ERR_INVALID_ARG, "bm_engine_set_embeddings: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)c.vocab * c.hidden * 2;
+  BM_CUDA(cudaMemcpyAsync(e->embed, embed, bytes, cudaMemcpyDefault, s), "set_embeddings embed");
+  BM_CUDA(cudaMemcpyAsync(e->lm_head, lm_head, bytes, cudaMemcpyDefault, s), "set_embeddings lm_head");
+  e->has_final_norm = final_norm != nullptr;
+  if (final_norm)
+    BM_CUDA(cudaMemcpyAsync(e->final_norm_buf, final_norm, (size_t)c.hidden * 2, cudaMemcpyDefault, s),
+            "set_embeddings final norm");
+  e->emb_set = true;
+  return bm::ok();
+}
+
+bm_status bm_engine_sync(bm_engine* e, void* stream) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "bm_engine_sync: null engine");
+  BM_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronise");
+  int flag = 0;
+  BM_CUDA(cudaMemcpy(&flag, e->d_err, sizeof(int), cudaMemcpyDeviceToHost), "device check read");
+  if (flag) {
+    BM_CUDA(cudaMemset(e->d_err, 0, sizeof(int)), "device check reset");
+    return set_error(BM_ERR_DEVICE_CHECK, "a kernel skipped an out-of-range index (code " + std::to_string(flag) +
+                                              ": 1 slot id, 2 position, 3 token id)");
+  }
+  return bm::ok();
+}
+
+bm_status bm_engine_stats(const bm_engine* e, bm_stats* out) {
+  if (!e || !out) return set_error(BM_ERR_INVALID_ARG, "bm_engine_stats: null argument");
+  *out = e->st;
+  return bm::ok();
+}
+
+int bm_engine_kernel_family(const bm_engine* e) { return e ? e->family : -1; }
+
+// ------------------------------------------------------------------ slots
+
+bm_status kv_slot_seed(bm_engine* e, const uint16_t* K, const uint16_t* V, int len, int* slot_out, void* stream) {
+  if (!e || !slot_out) return set_error(BM_ERR_INVALID_ARG, "kv_slot_seed: null argument");
+  if (len > 0 && (!K || !V)) return set_error(BM_ERR_INVALID_ARG, "kv_slot_seed: null K or V with len > 0");
+  std::lock_guard<std::mutex> lk(e->mu);
+  std::string err;
+  int slot = -1;
+  bm_status st = e->slots.acquire(len, &slot, &err);
+  if (st != BM_OK) return set_error(st, "kv_slot_seed: " + err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const AttnArena& ar = e->arena;
+  const size_t d = ar.d;
+  cudaError_t ce = cudaSuccess;
+  for (int l = 0; l < ar.layers && len > 0 && ce == cudaSuccess; ++l) {
+    const size_t src_off = (size_t)l * ar.kvh * len * d;
+    const size_t dst_off = l * ar.layer_stride() + slot * ar.slot_stride();
+    ce = cudaMemcpy2DAsync(ar.K + dst_off, ar.cap * d * 2, K + src_off, len * d * 2, len * d * 2, ar.kvh,
+                           cudaMemcpyDefault, s);
+    if (ce == cudaSuccess)
+      ce = cudaMemcpy2DAsync(ar.V + dst_off, ar.cap * d * 2, V + src_off, len * d * 2, len * d * 2, ar.kvh,
+                             cudaMemcpyDefault, s);
+  }
+  if (ce == cudaSuccess) ce = launch_set_len(ar.len, slot, len, s);
+  if (ce != cudaSuccess) {
+    e->slots.release(slot, &err);
+    return set_error(BM_ERR_CUDA, std::string("kv_slot_seed: ") + cudaGetErrorString(ce));
+  }
+  *slot_out = slot;
+  return bm::ok();
+}
+
+bm_status kv_slot_append(bm_engine* e, int layer, const int32_t* slots, const uint16_t* Knew, const uint16_t* Vnew,
+                         int B, void* stream) {
+  if (!e || !Knew || !Vnew) return set_error(BM_ERR_INVALID_ARG, "kv_slot_append: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  if (layer < 0 || layer >= e->cfg.layers) return set_error(BM_ERR_INVALID_ARG, "kv_slot_append: layer out of range");
+  std::string err;
+  bm_status st = e->slots.check_batch(slots, B, &err);
+  if (st != BM_OK) return set_error(st, "kv_slot_append: " + err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = stage_aux_slots(e, slots, B, s)) != BM_OK) return st;
+  BM_CUDA(launch_kv_append(e->arena, layer, e->d_slots_aux, reinterpret_cast<const bf16*>(Knew),
+                           reinterpret_cast<const bf16*>(Vnew), B, chk_of(e), s),
+          "kv_slot_append launch");
+  e->st.kernel_launches += 1;
+  return bm::ok();
+}
+
+bm_status kv_slot_attend(bm_engine* e, int layer, const int32_t* slots, const uint16_t* Q, uint16_t* O, int B,
+                         void* stream) {
+  if (!e || !Q || !O) return set_error(BM_ERR_INVALID_ARG, "kv_slot_attend: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  if (layer < 0 || layer >= e->cfg.layers) return set_error(BM_ERR_INVALID_ARG, "kv_slot_attend: layer out of range");
+  std::string err;
+  bm_status st = e->slots.check_batch(slots, B, &err);
+  if (st != BM_OK) return set_error(st, "kv_slot_attend: " + err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = stage_aux_slots(e, slots, B, s)) != BM_OK) return st;
+  int n = 0;
+  BM_CUDA(launch_attention(e->arena, layer, e->d_slots_aux, reinterpret_cast<const bf16*>(Q),
+                           reinterpret_cast<bf16*>(O), e->cfg.q_heads, B, e->attn_part, chk_of(e), s, &n),
+          "kv_slot_attend launch");
+  e->st.kernel_launches += n;
+  return bm::ok();
+}
+
+bm_status kv_slot_advance(bm_engine* e, const int32_t* slots, int B, void* stream) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "kv_slot_advance: null engine");
+  std::lock_guard<std::mutex> lk(e->mu);
+  std::string err;
+  bm_status st = e->slots.check_batch(slots, B, &err);
+  if (st != BM_OK) return set_error(st, "kv_slot_advance: " + err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = stage_aux_slots(e, slots, B, s)) != BM_OK) return st;
+  BM_CUDA(launch_advance(e->arena.len, e->d_slots_aux, B, s), "kv_slot_advance launch");
+  e->slots.advance(slots, B);
+  e->st.kernel_launches += 1;
+  return bm::ok();
+}
+
+bm_status kv_slot_release(bm_engine* e, int slot) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "kv_slot_release: null engine");
+  std::lock_guard<std::mutex> lk(e->mu);
+  std::string err;
+  const bm_status st = e->slots.release(slot, &err);
+  return st == BM_OK ? bm::ok() : set_error(st, "kv_slot_release: " + err);
+}
+
+bm_status kv_slot_length(const bm_engine* e, int slot, int* len_out) {
+  if (!e || !len_out) return set_error(BM_ERR_INVALID_ARG, "kv_slot_length: null argument");
+  if (!e->slots.active(slot)) return set_error(BM_ERR_SLOT_FREE, "kv_slot_length: slot is not active");
+  *len_out = e->slots.length(slot);
+  return bm::ok();
+}
+
+bm_status kv_slot_read(bm_engine* e, int layer, int slot, int count, uint16_t* K_out, uint16_t* V_out,
+                       void* stream) {
+  if (!e || !K_out || !V_out) return set_error(BM_ERR_INVALID_ARG, "kv_slot_read: null argument");
+  const AttnArena& ar = e->arena;
+  if (layer < 0 || layer >= ar.layers || slot < 0 || slot >= ar.S || count < 0 || count > ar.cap)
+    return set_error(BM_ERR_INVALID_ARG, "kv_slot_read: layer, slot or count out of range");
+  if (count == 0) return bm::ok();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t d = ar.d, src = layer * ar.layer_stride() + slot * ar.slot_stride();
+  BM_CUDA(cudaMemcpy2DAsync(K_out, count * d * 2, ar.K + src, ar.cap * d * 2, count * d * 2, ar.kvh,
+                            cudaMemcpyDefault, s),
+          "kv_slot_read K");
+  BM_CUDA(cudaMemcpy2DAsync(V_out, count * d * 2, ar.V + src, ar.cap * d * 2, count * d * 2, ar.kvh,
+                            cudaMemcpyDefault, s),
+          "kv_slot_read V");
+  return bm::ok();
+}
+
+// ------------------------------------------------------------------ step
+
+bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, int32_t* next_tokens,
+                      float* logits, void* stream) {
+  if (!e || !slots || !tokens || !next_tokens) return set_error(BM_ERR_INVALID_ARG, "decode_step: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  if (!e->emb_set) return set_error(BM_ERR_NOT_READY, "decode_step: embeddings not set");
+  for (int l = 0; l < c.layers; ++l)
+    if (!e->L[l].set) return set_error(BM_ERR_NOT_READY, "decode_step: layer " + std::to_string(l) + " not set");
+  std::string err;
+  bm_status st = e->slots.check_batch(slots, B, &err);
+  if (st != BM_OK) return set_error(st, "decode_step: " + err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t S = c.max_streams;
+  BM_CUDA(cudaEventSynchronize(e->ev_stage), "staging event");
+  std::memcpy(e->h_stage, slots, sizeof(int32_t) * B);
+  BM_CUDA(cudaMemcpyAsync(e->d_slots, e->h_stage, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s), "slot upload");
+  if (is_device_ptr(tokens)) {
+    BM_CUDA(cudaMemcpyAsync(e->d_tokens, tokens, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice, s), "token copy");
+  } else {
+    std::memcpy(e->h_stage + S, tokens, sizeof(int32_t) * B);
+    BM_CUDA(cudaMemcpyAsync(e->d_tokens, e->h_stage + S, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s),
+            "token upload");
+  }
+  BM_CUDA(cudaEventRecord(e->ev_stage, s), "staging event");
+  int n = 0;
+  if (c.use_graph) {
+    auto it = e->graphs.find(B);
+    if (it == e->graphs.end()) {
+      cudaGraph_t graph = nullptr;
+      BM_CUDA(cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal), "graph capture begin");
+      const cudaError_t ce = enqueue_step(e, B, e->cap_stream, &n);
+      const cudaError_t ee = cudaStreamEndCapture(e->cap_stream, &graph);
+      if (ce != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return set_error(BM_ERR_CUDA, std::string("decode_step capture: ") + cudaGetErrorString(ce));
+      }
+      BM_CUDA(ee, "graph capture end");
+      cudaGraphExec_t exec = nullptr;
+      const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      BM_CUDA(ie, "graph instantiate");
+      it = e->graphs.emplace(B, exec).first;
+      e->st.graph_captures += 1;
+      e->st.kernels_per_step = n;
+    }
+    BM_CUDA(cudaGraphLaunch(it->second, s), "graph launch");
+    e->st.graph_launches += 1;
+  } else {
+    BM_CUDA(enqueue_step(e, B, s, &n), "decode_step launch");
+    e->st.kernels_per_step = n;
+  }
+  e->st.kernel_launches += e->st.kernels_per_step;
+  BM_CUDA(cudaMemcpyAsync(next_tokens, e->d_next, sizeof(int32_t) * B, cudaMemcpyDefault, s), "next token copy");
+  if (logits)
+    BM_CUDA(cudaMemcpyAsync(logits, e->logits, sizeof(float) * B * (size_t)c.vocab, cudaMemcpyDefault, s),
+            "logits copy");
+  e->slots.advance(slots, B);
+  e->st.steps += 1;
+  e->st.tokens += B;
+  return bm::ok();
+}
+
+// ------------------------------------------------------------------ ops
+
+bm_status w4_gemm_batched(const uint8_t* W, const uint16_t* S, const uint16_t* X, uint16_t* Y, const uint16_t* R,
+                          int M, int N, int K, int g, void* stream) {
+  if (!W || !S || !X || !Y) return set_error(BM_ERR_INVALID_ARG, "w4_gemm_batched: null pointer");
+  if (M < 1 || N < 1 || K < 32 || K % 32 || (g != 32 && g != 64 && g != 128) || K % g)
+    return set_error(BM_ERR_INVALID_ARG, "w4_gemm_batched: need M, N >= 1, K % 32 == 0, g in {32, 64, 128}, K % g == 0");
+  if (!simt_supports_k(K)) return set_error(BM_ERR_UNSUPPORTED, "w4_gemm_batched: no kernel shape for this K");
+  bm_status st = ensure_attributes();
+  if (st != BM_OK) return st;
+  GemvArgs a{W, reinterpret_cast<const __half*>(S), reinterpret_cast<const bf16*>(X), K,
+             reinterpret_cast<const bf16*>(R), N, reinterpret_cast<bf16*>(Y), N, M, N, K, g, 0, nullptr, 0.f};
+  BM_CUDA(launch_w4_gemv(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched launch");
+  return bm::ok();
+}
+
+size_t bm_moe_workspace_bytes(int B, int experts, int top_k, int hidden, int ffn) {
+  if (B < 1 || experts < 1 || top_k < 1 || hidden < 1 || ffn < 1) return 0;
+  return moe_scratch_bytes(B, experts, top_k, hidden, ffn);
+}
+
+bm_status moe_grouped_w4(const bm_moe_weights* w, const uint16_t* X, const uint16_t* Hres, uint16_t* Y,
+                         int32_t* topk_ids, float* topk_w, int B, void* ws, size_t ws_bytes, void* stream) {
+  if (!w || !X || !Y || !ws || !w->wr || !w->wg || !w->wg_s || !w->wu || !w->wu_s || !w->wd || !w->wd_s)
+    return set_error(BM_ERR_INVALID_ARG, "moe_grouped_w4: null pointer");
+  if (B < 1 || w->experts < 1 || w->experts > 256 || w->top_k < 1 || w->top_k > 16 || w->top_k > w->experts ||
+      B * w->top_k > 1024)
+    return set_error(BM_ERR_INVALID_ARG, "moe_grouped_w4: need 1 <= top_k <= min(16, experts), experts <= 256, "
+                                         "B * top_k <= 1024");
+  if ((w->group != 32 && w->group != 64 && w->group != 128) || w->hidden % w->group || w->ffn % w->group ||
+      w->hidden % 32 || w->ffn % 32)
+    return set_error(BM_ERR_INVALID_ARG, "moe_grouped_w4: bad group or sizes");
+  if (!simt_supports_k(w->hidden) || !simt_supports_k(w->ffn))
+    return set_error(BM_ERR_UNSUPPORTED, "moe_grouped_w4: no kernel shape for these sizes");
+  const size_t need = moe_scratch_bytes(B, w->experts, w->top_k, w->hidden, w->ffn);
+  if (ws_bytes < need)
+    return set_error(BM_ERR_INVALID_ARG, "moe_grouped_w4: workspace of " + std::to_string(ws_bytes) +
+                                             " bytes, need " + std::to_string(need));
+  bm_status st = ensure_attributes();
+  if (st != BM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MoeBufs b = moe_carve(ws, B, w->experts, w->top_k, w->hidden, w->ffn);
+  MoeArgs a{B, w->experts, w->top_k, w->hidden, w->ffn, w->group, w->renorm_topk,
+            w->wr, w->wg, reinterpret_cast<const __half*>(w->wg_s), w->wu,
+            reinterpret_cast<const __half*>(w->wu_s), w->wd, reinterpret_cast<const __half*>(w->wd_s),
+            reinterpret_cast<const bf16*>(X), 0, nullptr, 0.f, reinterpret_cast<const bf16*>(Hres),
+            reinterpret_cast<bf16*>(Y)};
+  BM_CUDA(launch_moe(a, b, s, nullptr), "moe_grouped_w4 launch");
+  if (topk_ids)
+    BM_CUDA(cudaMemcpyAsync(topk_ids, b.topk_ids, sizeof(int32_t) * B * w->top_k, cudaMemcpyDeviceToDevice, s),
+            "topk ids copy");
+  if (topk_w)
+    BM_CUDA(cudaMemcpyAsync(topk_w, b.topk_w, sizeof(float) * B * w->top_k, cudaMemcpyDeviceToDevice, s),
+            "topk weights copy");
+  return bm::ok();
+}
+
+bm_status bm_w4_quantize(const float* W, int N, int K, int g, uint8_t* packed, uint16_t* scales, void* stream) {
+  if (!W || !packed || !scales) return set_error(BM_ERR_INVALID_ARG, "bm_w4_quantize: null pointer");
+  if (N < 1 || K < 2 || (g != 32 && g != 64 && g != 128) || K % g)
+    return set_error(BM_ERR_INVALID_ARG, "bm_w4_quantize: need N >= 1, g in {32, 64, 128}, K % g == 0");
+  BM_CUDA(launch_quantize(W, N, K, g, packed, reinterpret_cast<__half*>(scales), static_cast<cudaStream_t>(stream)),
+          "bm_w4_quantize launch");
+  return bm::ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// Launchers of the decode-step kernels.  Each returns cudaSuccess or the
+// launch error; none synchronises.
+#pragma once
+
+#include "common.cuh"
+
+namespace bm {
+
+// ---------------------------------------------------------------- dense
+struct GemvArgs {
+  const uint8_t* W;   // packed int4 [N][K/2]
+  const __half* S;    // fp16 [N][K/g]
+  const bf16* X;      // [M][ldx]
+  int ldx;
+  const bf16* Res;    // [M][ldr] or null
+  int ldr;
+  bf16* Y;            // [M][ldy]
+  int ldy;
+  int M, N, K, g;
+  int do_norm;        // stage RMSNorm(X) instead of X
+  const bf16* norm_w; // [K] or null
+  float eps;
+};
+// True if the CUDA-core W4 kernels handle reduction length K.
+bool simt_supports_k(int K);
+cudaError_t launch_w4_gemv(const GemvArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------- experts
+struct MoeBufs {
+  // routing
+  float* logits;        // [B][E]
+  int32_t* topk_ids;    // [B][k]
+  float* topk_w;        // [B][k]
+  bf16* xn;             // [B][H] normed router / expert input (written when norm is fused)
+  // grouping (counting sort of the B*k (token, rank) pairs by expert)
+  int32_t* n_active;    // [1]
+  int32_t* active_e;    // [E]
+  int32_t* active_off;  // [E+1]
+  int32_t* pair_token;  // [B*k] token of the p-th pair in expert order
+  int32_t* pos_of;      // [B*k] sorted position of pair (b, r) = b*k + r
+  bf16* act;            // [B*k][F]
+  float* out;           // [B*k][H]
+};
+size_t moe_scratch_bytes(int B, int E, int k, int H, int F);
+MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F);
+
+struct MoeArgs {
+  int B, E, k, H, F, g, renorm;
+  const float* wr;                 // [E][H]
+  const uint8_t* wg; const __half* wg_s;
+  const uint8_t* wu; const __half* wu_s;
+  const uint8_t* wd; const __half* wd_s;
+  const bf16* x;                   // [B][H] input (raw when do_norm)
+  int do_norm;                     // route/experts on RMSNorm(x) (written to bufs.xn)
+  const bf16* norm_w;
+  float eps;
+  const bf16* res;                 // [B][H] residual or null
+  bf16* y;                         // [B][H]
+};
+// Router logits + top-k + sort, gate/up, down, combine: 5 launches.
+cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches);
+
+// ---------------------------------------------------------------- attention
+struct AttnArena {
+  bf16* K;        // [layers][S][kvh][cap][d]
+  bf16* V;
+  int32_t* len;   // [S] committed lengths (device)
+  int layers, S, kvh, cap, d;
+  __host__ __device__ size_t slot_stride() const { return (size_t)kvh * cap * d; }
+  __host__ __device__ size_t layer_stride() const { return (size_t)S * slot_stride(); }
+};
+constexpr int kAttnChunk = 128;
+size_t attn_partial_floats(int B, int qh, int cap, int d);
+
+// RoPE on q and k at pos = len[slot], q -> qout [B][qh][d], k,v -> arena.
+cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* qkv,
+                               int ld_qkv, int qh, const double* theta, bf16* qout, int B,
+                               DevCheck chk, cudaStream_t st);
+// Plain append of already-rotated k, v ([B][kvh][d]) at pos = len[slot].
+cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* k,
+                             const bf16* v, int B, DevCheck chk, cudaStream_t st);
+// Split-K attention over positions 0..len[slot] (inclusive) and the combine.
+cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q,
+                             bf16* out, int qh, int B, float* partials, DevCheck chk,
+                             cudaStream_t st, int* launches);
+cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st);
+
+// ---------------------------------------------------------------- model glue
+cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, int B,
+                         DevCheck chk, cudaStream_t st);
+// logits[b][v] = RMSNorm(x[b]) . W[v] (bf16 weights, fp32 out).
+cudaError_t launch_lm_head(const bf16* W, int V, int H, const bf16* x, const bf16* norm_w, float eps,
+                           float* logits, int B, cudaStream_t st);
+// next[b] = argmax_v logits[b][v] (ties: lowest v); len[slots[b]] += advance.
+cudaError_t launch_argmax(const float* logits, int V, int B, int32_t* next, int32_t* len,
+                          const int32_t* slots, int advance, cudaStream_t st);
+cudaError_t launch_advance(int32_t* len, const int32_t* slots, int B, cudaStream_t st);
+cudaError_t launch_quantize(const float* W, int N, int K, int g, uint8_t* packed, __half* scales,
+                            cudaStream_t st);
+
+// Kernel attributes (large dynamic shared memory); call once before capture.
+cudaError_t init_kernel_attributes();
+
+}  // namespace bm

@@ -1,0 +1,364 @@
+// Grouped int4 expert op of B tokens (the batched-serving page, §1: "the
+// selected experts of all B streams are dispatched as one grouped
+// sparse-expert operation against the device-resident expert bank").
+//
+//   1. k_router      fp32 router logits of every token (RMSNorm fused; CTA 0
+//                    also writes the normed input for the experts)
+//   2. k_topk_sort   softmax top-k per token (ties: lower expert id), weights,
+//                    then a stable counting sort of the B*k (token, rank)
+//                    pairs by expert and the list of active experts
+//   3. k_gateup      per active expert and tile of F: SiLU(x W_g) * (x W_u)
+//                    for all of its tokens; each packed byte read once
+//   4. k_down        per active expert and tile of H: the down projection of
+//                    its tokens, fp32 out
+//   5. k_combine     y_b = res_b + sum_r w_{b,r} out_{b,r}, rank order
+//
+// Sorting by expert reads every active expert's weights once however many
+// streams picked it, which is what the pages' de-dup pass tried to achieve;
+// no separate compaction step exists.  Every reduction has a fixed order and
+// no floating-point atomics are used, so a token's result does not depend on
+// which other tokens share the launch.
+#include <float.h>
+
+#include "kernels.cuh"
+#include "w4_simt.cuh"
+
+namespace bm {
+
+namespace {
+
+constexpr int kRouterWarps = 8;
+constexpr int kMaxPairs = 1024;   // B * k handled by the single-CTA sort
+
+__global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
+  extern __shared__ float rinv_s[];   // [B]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.do_norm) {
+    for (int t = warp; t < a.B; t += kRouterWarps) {
+      const float r = row_rinv(a.x + (size_t)t * a.H, a.H, a.eps, lane);
+      if (lane == 0) rinv_s[t] = r;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i < a.B * a.H; i += blockDim.x) {
+        const int t = i / a.H, k = i - t * a.H;
+        const float w = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
+        b.xn[i] = f2bf(bf2f(a.x[i]) * rinv_s[t] * w);
+      }
+    }
+  }
+  const int e = blockIdx.x * kRouterWarps + warp;
+  if (e >= a.E) return;
+  const float* wr = a.wr + (size_t)e * a.H;
+  for (int t = 0; t < a.B; ++t) {
+    const bf16* x = a.x + (size_t)t * a.H;
+    const float r = a.do_norm ? rinv_s[t] : 1.f;
+    float acc = 0.f;
+    for (int k = lane * 4; k < a.H; k += 128) {
+      const float4 w4 = *reinterpret_cast<const float4*>(wr + k);
+      const uint2 p = *reinterpret_cast<const uint2*>(x + k);
+      float x0 = bf_lo(p.x), x1 = bf_hi(p.x), x2 = bf_lo(p.y), x3 = bf_hi(p.y);
+      if (a.do_norm) {
+        const float n0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f, n1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
+        const float n2 = a.norm_w ? bf2f(a.norm_w[k + 2]) : 1.f, n3 = a.norm_w ? bf2f(a.norm_w[k + 3]) : 1.f;
+        x0 = round_bf16(x0 * r * n0); x1 = round_bf16(x1 * r * n1);
+        x2 = round_bf16(x2 * r * n2); x3 = round_bf16(x3 * r * n3);
+      }
+      acc = fmaf(x0, w4.x, acc); acc = fmaf(x1, w4.y, acc);
+      acc = fmaf(x2, w4.z, acc); acc = fmaf(x3, w4.w, acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) b.logits[(size_t)t * a.E + e] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
+  __shared__ int ids_s[kMaxPairs];
+  __shared__ int cnt_s[256];
+  __shared__ int off_s[257];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int E = a.E, k = a.k, P = a.B * a.k;
+  for (int t = warp; t < a.B; t += nwarps) {
+    const float* lg = b.logits + (size_t)t * E;
+    // A NaN logit ranks as -inf; every token still gets k distinct valid ids.
+    float v[8];
+    bool taken[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      const float x = e < E ? lg[e] : -INFINITY;
+      v[i] = isnan(x) ? -INFINITY : x;
+      taken[i] = e >= E;
+    }
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lmax = fmaxf(lmax, v[i]);
+    lmax = warp_max(lmax);
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) z += taken[i] ? 0.f : expf(v[i] - lmax);
+    z = warp_sum(z);
+    float sel_v[16];
+    int sel_e[16];
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      }
+      sel_v[r] = bv;
+      sel_e[r] = be;   // k <= E, so an untaken id always exists
+      if ((be & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i == (be >> 5)) taken[i] = true;
+      }
+    }
+    if (lane == 0) {
+      float ex[16], sum = 0.f;
+      for (int r = 0; r < k; ++r) { ex[r] = expf(sel_v[r] - lmax); sum += ex[r]; }
+      const float den = a.renorm ? sum : z;
+      for (int r = 0; r < k; ++r) {
+        b.topk_ids[t * k + r] = sel_e[r];
+        b.topk_w[t * k + r] = ex[r] / den;
+        ids_s[t * k + r] = sel_e[r];
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int p = 0; p < P; ++p) c += (ids_s[p] == e);
+    cnt_s[e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0, u = 0;
+    for (int e = 0; e < E; ++e) {
+      off_s[e] = acc;
+      if (cnt_s[e] > 0) {
+        b.active_e[u] = e;
+        b.active_off[u] = acc;
+        ++u;
+      }
+      acc += cnt_s[e];
+    }
+    off_s[E] = acc;
+    b.active_off[u] = acc;
+    *b.n_active = u;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = ids_s[p];
+    int rank = 0;
+    for (int q = 0; q < p; ++q) rank += (ids_s[q] == e);
+    const int pos = off_s[e] + rank;
+    b.pair_token[pos] = p / k;
+    b.pos_of[p] = pos;
+  }
+}
+
+// Gate/up: a lane group computes rows f of W_g[e] and W_u[e] together.
+template <int LPR, int CPL>
+__global__ void __launch_bounds__(kSimtThreads) k_gateup(MoeArgs a, MoeBufs b, const bf16* xin) {
+  extern __shared__ float xs[];
+  __shared__ const bf16* rows[kMaxTile];
+  __shared__ float rinv_unused[kMaxTile];
+  const int u = blockIdx.y;
+  if (u >= *b.n_active) return;
+  const int e = b.active_e[u], off = b.active_off[u], cnt = b.active_off[u + 1] - off;
+  constexpr int kGroups = kWarp / LPR;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPR, gl = lane % LPR;
+  const int f = blockIdx.x * (kSimtWarps * kGroups) + warp * kGroups + grp;
+  const bool ok = f < a.F;
+  const size_t row = (size_t)e * a.F + f;
+  const uint8_t* wrow[2] = {ok ? a.wg + row * (a.H >> 1) : nullptr, ok ? a.wu + row * (a.H >> 1) : nullptr};
+  const __half* srow[2] = {ok ? a.wg_s + row * (a.H / a.g) : nullptr, ok ? a.wu_s + row * (a.H / a.g) : nullptr};
+  uint4 w[2][CPL];
+  float s[2][CPL];
+  load_w4<LPR, CPL, 2>(wrow, srow, a.g, gl, w, s);
+  const int nch = a.H >> 5;
+  for (int t0 = 0; t0 < cnt; t0 += kMaxTile) {
+    const int mc = min(kMaxTile, cnt - t0);
+    __syncthreads();
+    if (threadIdx.x < mc) rows[threadIdx.x] = xin + (size_t)b.pair_token[off + t0 + threadIdx.x] * a.H;
+    __syncthreads();
+    stage_rows(xs, rows, mc, a.H, false, nullptr, 0.f, rinv_unused);
+    __syncthreads();
+    float gate[kMaxTile];
+    dot_tile<LPR, CPL, 2>(w, s, xs, nch, gl, mc, [&](int r, int m, float v) {
+      if (r == 0) {
+        gate[m] = v;
+      } else if (ok && gl == (m % LPR)) {
+        const float gv = gate[m];
+        const float sv = gv / (1.f + expf(-gv));
+        b.act[(size_t)(off + t0 + m) * a.F + f] = f2bf(sv * v);
+      }
+    });
+  }
+}
+
+template <int LPR, int CPL>
+__global__ void __launch_bounds__(kSimtThreads) k_down(MoeArgs a, MoeBufs b) {
+  extern __shared__ float xs[];
+  __shared__ const bf16* rows[kMaxTile];
+  __shared__ float rinv_unused[kMaxTile];
+  const int u = blockIdx.y;
+  if (u >= *b.n_active) return;
+  const int e = b.active_e[u], off = b.active_off[u], cnt = b.active_off[u + 1] - off;
+  constexpr int kGroups = kWarp / LPR;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPR, gl = lane % LPR;
+  const int h0 = blockIdx.x * (kSimtWarps * kGroups * 2) + (warp * kGroups + grp) * 2;
+  const uint8_t* wrow[2];
+  const __half* srow[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const bool ok = h0 + r < a.H;
+    const size_t row = (size_t)e * a.H + h0 + r;
+    wrow[r] = ok ? a.wd + row * (a.F >> 1) : nullptr;
+    srow[r] = ok ? a.wd_s + row * (a.F / a.g) : nullptr;
+  }
+  uint4 w[2][CPL];
+  float s[2][CPL];
+  load_w4<LPR, CPL, 2>(wrow, srow, a.g, gl, w, s);
+  const int nch = a.F >> 5;
+  for (int t0 = 0; t0 < cnt; t0 += kMaxTile) {
+    const int mc = min(kMaxTile, cnt - t0);
+    __syncthreads();
+    if (threadIdx.x < mc) rows[threadIdx.x] = b.act + (size_t)(off + t0 + threadIdx.x) * a.F;
+    __syncthreads();
+    stage_rows(xs, rows, mc, a.F, false, nullptr, 0.f, rinv_unused);
+    __syncthreads();
+    dot_tile<LPR, CPL, 2>(w, s, xs, nch, gl, mc, [&](int r, int m, float v) {
+      if (wrow[r] && gl == ((r * kMaxTile + m) % LPR))
+        b.out[(size_t)(off + t0 + m) * a.H + h0 + r] = v;
+    });
+  }
+}
+
+__global__ void __launch_bounds__(256) k_combine(MoeArgs a, MoeBufs b) {
+  const int t = blockIdx.x;
+  for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+    float acc = 0.f;
+    for (int r = 0; r < a.k; ++r) {
+      const int pos = b.pos_of[t * a.k + r];
+      acc = fmaf(b.topk_w[t * a.k + r], b.out[(size_t)pos * a.H + h], acc);
+    }
+    const float res = a.res ? bf2f(a.res[(size_t)t * a.H + h]) : 0.f;
+    a.y[(size_t)t * a.H + h] = f2bf(res + acc);
+  }
+}
+
+template <int LPR, int CPL>
+cudaError_t run_gateup(const MoeArgs& a, const MoeBufs& b, const bf16* xin, int max_u, cudaStream_t st) {
+  constexpr int kGroups = kWarp / LPR;
+  dim3 grid((a.F + kSimtWarps * kGroups - 1) / (kSimtWarps * kGroups), max_u);
+  const size_t smem = (size_t)min(a.B, kMaxTile) * a.H * sizeof(float);
+  k_gateup<LPR, CPL><<<grid, kSimtThreads, smem, st>>>(a, b, xin);
+  return cudaGetLastError();
+}
+
+template <int LPR, int CPL>
+cudaError_t run_down(const MoeArgs& a, const MoeBufs& b, int max_u, cudaStream_t st) {
+  constexpr int rows = kSimtWarps * (kWarp / LPR) * 2;
+  dim3 grid((a.H + rows - 1) / rows, max_u);
+  const size_t smem = (size_t)min(a.B, kMaxTile) * a.F * sizeof(float);
+  k_down<LPR, CPL><<<grid, kSimtThreads, smem, st>>>(a, b);
+  return cudaGetLastError();
+}
+
+#define BM_EXPERT_SHAPES(X) X(32, 1) X(32, 2) X(32, 3) X(32, 4) X(16, 1) X(16, 3) X(8, 1) X(8, 3)
+
+cudaError_t dispatch_gateup(const MoeArgs& a, const MoeBufs& b, const bf16* xin, int max_u, cudaStream_t st) {
+  const int nch = a.H / 32;
+#define BM_CASE(L, C) if (nch == (L) * (C)) return run_gateup<L, C>(a, b, xin, max_u, st);
+  BM_EXPERT_SHAPES(BM_CASE)
+#undef BM_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_down(const MoeArgs& a, const MoeBufs& b, int max_u, cudaStream_t st) {
+  const int nch = a.F / 32;
+#define BM_CASE(L, C) if (nch == (L) * (C)) return run_down<L, C>(a, b, max_u, st);
+  BM_EXPERT_SHAPES(BM_CASE)
+#undef BM_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <int L, int C>
+cudaError_t set_attr_pair() {
+  const int bytes = kMaxTile * L * C * 32 * (int)sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_gateup<L, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down<L, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
+}
+
+size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t moe_scratch_bytes(int B, int E, int k, int H, int F) {
+  const size_t P = (size_t)B * k;
+  return align_up(sizeof(float) * B * E) + align_up(sizeof(int32_t) * P) + align_up(sizeof(float) * P) +
+         align_up(sizeof(bf16) * B * H) + align_up(sizeof(int32_t)) + align_up(sizeof(int32_t) * E) +
+         align_up(sizeof(int32_t) * (E + 1)) + align_up(sizeof(int32_t) * P) + align_up(sizeof(int32_t) * P) +
+         align_up(sizeof(bf16) * P * F) + align_up(sizeof(float) * P * H);
+}
+
+MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
+  char* p = static_cast<char*>(ws);
+  const size_t P = (size_t)B * k;
+  auto take = [&](size_t bytes) { char* r = p; p += align_up(bytes); return r; };
+  MoeBufs b;
+  b.logits = reinterpret_cast<float*>(take(sizeof(float) * B * E));
+  b.topk_ids = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
+  b.topk_w = reinterpret_cast<float*>(take(sizeof(float) * P));
+  b.xn = reinterpret_cast<bf16*>(take(sizeof(bf16) * B * H));
+  b.n_active = reinterpret_cast<int32_t*>(take(sizeof(int32_t)));
+  b.active_e = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * E));
+  b.active_off = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
+  b.pair_token = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
+  b.pos_of = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
+  b.act = reinterpret_cast<bf16*>(take(sizeof(bf16) * P * F));
+  b.out = reinterpret_cast<float*>(take(sizeof(float) * P * H));
+  return b;
+}
+
+cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches) {
+  if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
+  const int nblk = (a.E + kRouterWarps - 1) / kRouterWarps;
+  k_router<<<nblk, 256, sizeof(float) * a.B, st>>>(a, b);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  k_topk_sort<<<1, 1024, 0, st>>>(a, b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const bf16* xin = a.do_norm ? b.xn : a.x;
+  const int max_u = a.B * a.k < a.E ? a.B * a.k : a.E;
+  // A token routes to k distinct experts, so no expert has more than B
+  // tokens and the staging buffer needs min(B, 4) rows.
+  if ((err = dispatch_gateup(a, b, xin, max_u, st)) != cudaSuccess) return err;
+  if ((err = dispatch_down(a, b, max_u, st)) != cudaSuccess) return err;
+  k_combine<<<a.B, 256, 0, st>>>(a, b);
+  if (launches) *launches += 5;
+  return cudaGetLastError();
+}
+
+cudaError_t init_moe_attributes() {
+  cudaError_t e = cudaSuccess;
+#define BM_CASE(L, C) if (e == cudaSuccess) e = set_attr_pair<L, C>();
+  BM_EXPERT_SHAPES(BM_CASE)
+#undef BM_CASE
+  return e;
+}
+
+}  // namespace bm

@@ -1,0 +1,300 @@
+/*
+ * bitmoe.h — C ABI of the batched W4A16 mixture-of-experts decode step on one
+ * GB300 (sm_103a).
+ *
+ * Pages cited by abbreviated title:
+ *   [KV-slot isolation]  "Per-stream KV-slot isolation for parallel low-bit
+ *                         decode on Apple Silicon: crash fix with
+ *                         byte-identical solo parity and no-regression"
+ *   [Crash root cause]   "A falsify-first root cause for a concurrent 4-bit
+ *                         decode crash: batch-composition KV-pool wipe trips a
+ *                         re-seed precondition"
+ *   [Batched serving]    "Batched-concurrent 4-bit serving on Apple Silicon:
+ *                         weight-stream amortization with an honest sublinear
+ *                         ceiling"
+ *
+ * Conventions for every call:
+ *  - Plain pointers and sizes only.  bf16 and fp16 tensors are passed as
+ *    uint16_t bit patterns.  "device" pointers must be CUDA device memory of
+ *    the current device; "host" pointers are ordinary host memory.
+ *  - Streams are cudaStream_t values passed as void* (NULL = legacy stream).
+ *    Every call that takes a stream only enqueues work on it and returns;
+ *    outputs are valid once that stream has been synchronised.
+ *  - No call throws, traps or aborts.  Errors come back as bm_status; the
+ *    calling thread's last error message is available from bm_last_error().
+ *    An asynchronous CUDA error surfaces as BM_ERR_CUDA from a later call or
+ *    from bm_engine_sync().
+ *  - Packed int4 weight layout ("canonical"): row-major [N][K/2] bytes along
+ *    K, element 2j in the low nibble of byte j and element 2j+1 in the high
+ *    nibble; code u in [0,15] stands for q = u - 8; scales fp16 [N][K/g];
+ *    weight = q * scale.  ([Batched serving] §1, §3: packed int4 with
+ *    per-group scales; the nibble order and offset are this library's
+ *    stated reading, the pages print none.)
+ *  - Activations are bf16; every accumulation is fp32; each op rounds its
+ *    output to bf16 once.
+ */
+#ifndef BITMOE_H
+#define BITMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bm_status {
+  BM_OK = 0,
+  BM_ERR_INVALID_ARG = 1,   /* a size, pointer or layout the call rejects      */
+  BM_ERR_CTX_CAP = 2,       /* admission: the stream would exceed the context cap */
+  BM_ERR_NO_SLOT = 3,       /* admission: every slot is in use                 */
+  BM_ERR_SLOT_FREE = 4,     /* a slot that is not active was used or released  */
+  BM_ERR_CUDA = 5,          /* a CUDA runtime call failed                       */
+  BM_ERR_OOM = 6,           /* device or pinned host allocation failed         */
+  BM_ERR_NOT_READY = 7,     /* decode_step before every layer's weights were set */
+  BM_ERR_DEVICE_CHECK = 8,  /* a kernel found an out-of-range index and skipped it */
+  BM_ERR_UNSUPPORTED = 9    /* a shape or option this build does not handle    */
+} bm_status;
+
+/* Kernel family of the dense and expert projections.  Chosen once per engine,
+ * never per step, so that a stream's bytes never depend on the batch it runs
+ * in ([KV-slot isolation] follow-up update: one reduction order for solo and
+ * batched).  AUTO picks the family measured fastest for the engine's
+ * max_streams.  SIMT = CUDA-core W4A16 GEMV; TC = tcgen05 tensor cores. */
+typedef enum bm_kernel_policy {
+  BM_POLICY_AUTO = 0,
+  BM_POLICY_SIMT = 1,
+  BM_POLICY_TC = 2
+} bm_kernel_policy;
+
+/* Model geometry and engine limits. */
+typedef struct bm_config {
+  int hidden;        /* H                                                     */
+  int q_heads;       /* query heads                                           */
+  int kv_heads;      /* key/value heads; q_heads % kv_heads == 0              */
+  int head_dim;      /* d; 64 or 128                                          */
+  int experts;       /* E (<= 256)                                            */
+  int top_k;         /* k (<= 16, <= E)                                       */
+  int ffn;           /* expert FFN width F                                    */
+  int group;         /* int4 group size g along K: 32, 64 or 128             */
+  int vocab;         /* V                                                     */
+  int layers;        /* decoder layers                                        */
+  float rope_base;   /* RoPE base (rotate-half pairing)                       */
+  float rms_eps;     /* RMSNorm epsilon                                       */
+  int max_streams;   /* slots in the KV arena (<= 64)                         */
+  int ctx_cap;       /* positions per slot                                    */
+  int renorm_topk;   /* 1: top-k weights renormalised to sum to one           */
+  int kernel_policy; /* bm_kernel_policy                                      */
+  int use_graph;     /* 1: decode_step replays one captured CUDA graph per B  */
+} bm_config;
+
+/* One decoder layer's weights, canonical layout, DEVICE pointers.  Borrowed
+ * only for the duration of bm_engine_set_layer, which copies them. */
+typedef struct bm_layer_weights {
+  const uint8_t* wqkv;   const uint16_t* wqkv_s;  /* [(qh+2kvh)d][H/2], [..][H/g]: q rows, then k, then v, head-major */
+  const uint8_t* wo;     const uint16_t* wo_s;    /* [H][qh*d/2], [H][qh*d/g]        */
+  const float* wr;                                /* router, fp32 [E][H]            */
+  const uint8_t* wg;     const uint16_t* wg_s;    /* [E][F][H/2], [E][F][H/g]       */
+  const uint8_t* wu;     const uint16_t* wu_s;    /* [E][F][H/2], [E][F][H/g]       */
+  const uint8_t* wd;     const uint16_t* wd_s;    /* [E][H][F/2], [E][H][F/g]       */
+  const uint16_t* attn_norm;                      /* bf16 [H] or NULL (all ones)    */
+  const uint16_t* ffn_norm;                       /* bf16 [H] or NULL (all ones)    */
+} bm_layer_weights;
+
+/* Expert bank of one layer for the standalone grouped op, DEVICE pointers,
+ * canonical layout as in bm_layer_weights. */
+typedef struct bm_moe_weights {
+  int experts, top_k, hidden, ffn, group, renorm_topk;
+  const float* wr;
+  const uint8_t* wg; const uint16_t* wg_s;
+  const uint8_t* wu; const uint16_t* wu_s;
+  const uint8_t* wd; const uint16_t* wd_s;
+} bm_moe_weights;
+
+typedef struct bm_engine bm_engine;
+typedef struct bm_slot_map bm_slot_map;
+
+typedef struct bm_stats {
+  uint64_t steps;             /* decode_step calls that succeeded            */
+  uint64_t tokens;            /* sum of B over those calls                   */
+  uint64_t graph_launches;    /* cudaGraphLaunch calls made by decode_step   */
+  uint64_t graph_captures;    /* graphs captured (one per distinct B)        */
+  uint64_t kernel_launches;   /* kernels enqueued outside graphs + per graph replay */
+  uint64_t kernels_per_step;  /* kernels in one decode step (graph nodes)    */
+  size_t weight_bytes;        /* device bytes holding the model weights      */
+  size_t arena_bytes;         /* device bytes of the KV arena                */
+  size_t scratch_bytes;       /* device bytes of activations and partials    */
+} bm_stats;
+
+/* ---------------------------------------------------------------- errors */
+
+/* Message of the last failed call on this thread ("" if none).  The pointer
+ * stays valid until the next call on this thread. */
+const char* bm_last_error(void);
+
+/* ---------------------------------------------------------------- engine */
+
+/* Create an engine on the current CUDA device.  Allocates the weight slab,
+ * the fixed KV arena (layers x max_streams x ctx_cap x kv_heads x head_dim x
+ * 2 tensors, bf16) and scratch, and writes the standing byte counts to
+ * stderr once ([KV-slot isolation] §5: the fixed arena's standing cost is
+ * reported at boot).  Errors: BM_ERR_INVALID_ARG (geometry out of range),
+ * BM_ERR_UNSUPPORTED, BM_ERR_OOM, BM_ERR_CUDA. */
+bm_status bm_engine_create(const bm_config* cfg, bm_engine** out);
+
+/* Free everything the engine owns.  NULL is ignored.  The caller must not
+ * have work for this engine in flight. */
+void bm_engine_destroy(bm_engine* e);
+
+/* Copy one layer's weights (DEVICE pointers, canonical layout) into the
+ * engine, on `stream`.  The source buffers may be freed once the stream has
+ * been synchronised.  Errors: BM_ERR_INVALID_ARG (layer out of range or a
+ * NULL weight), BM_ERR_CUDA. */
+bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w, void* stream);
+
+/* Copy the bf16 embedding [V][H], lm_head [V][H] and final norm [H] (NULL =
+ * ones), DEVICE pointers.  ([Batched serving] §1: the per-stream output
+ * projection is part of the fused step.) */
+bm_status bm_engine_set_embeddings(bm_engine* e, const uint16_t* embed, const uint16_t* lm_head,
+                                   const uint16_t* final_norm, void* stream);
+
+/* Synchronise `stream` and report device-side index checks (BM_ERR_DEVICE_CHECK
+ * if any kernel of this engine skipped an out-of-range slot, token or
+ * expert id since the last call; the flag is then cleared). */
+bm_status bm_engine_sync(bm_engine* e, void* stream);
+
+/* Counters and standing memory. */
+bm_status bm_engine_stats(const bm_engine* e, bm_stats* out);
+
+/* The kernel family this engine resolved its policy to (SIMT or TC). */
+int bm_engine_kernel_family(const bm_engine* e);
+
+/* ---------------------------------------------------------------- slots
+ * [KV-slot isolation] §1: the batched KV arena is indexed by a stable
+ * per-stream slot; a slot is seeded once at join, released at retire (a
+ * logical reset, the buffer is reused without a wipe), and a change of batch
+ * composition never touches a continuing stream's K/V.  [Crash root cause]
+ * §3 is the failure this rules out: pools wiped on a batch-size change and
+ * a re-seed that only the host prefix could feed. */
+
+/* Join: take the lowest free slot, copy `len` positions of K and V into it
+ * and set its length to `len`.  K, V: bf16 [layers][kv_heads][len][head_dim],
+ * host or device memory (NULL allowed when len == 0).  Errors:
+ * BM_ERR_CTX_CAP if len >= ctx_cap (no room for one decode token: rejected,
+ * never truncated — [KV-slot isolation] §5), BM_ERR_NO_SLOT if every slot
+ * is active, BM_ERR_INVALID_ARG for len < 0. */
+bm_status kv_slot_seed(bm_engine* e, const uint16_t* K, const uint16_t* V, int len,
+                       int* slot_out, void* stream);
+
+/* Write this step's K/V of one layer for B streams at position = each slot's
+ * length.  slots: HOST int32 [B]; Knew, Vnew: DEVICE bf16 [B][kv_heads][d]
+ * (K already rotated).  The length does not advance (kv_slot_advance does).
+ * Errors: BM_ERR_SLOT_FREE, BM_ERR_CTX_CAP (length == ctx_cap),
+ * BM_ERR_INVALID_ARG (duplicate slot, layer or B out of range). */
+bm_status kv_slot_append(bm_engine* e, int layer, const int32_t* slots, const uint16_t* Knew,
+                         const uint16_t* Vnew, int B, void* stream);
+
+/* Decode attention of one layer for B streams: query head h of stream i
+ * attends over positions 0..len of slot slots[i] (its committed prefix plus
+ * the position this step appended), with KV head h / (q_heads/kv_heads).
+ * Reads nothing outside those slots.  slots: HOST int32 [B]; Q: DEVICE bf16
+ * [B][q_heads][d] (rotated); O: DEVICE bf16 [B][q_heads][d].  Split-K over
+ * fixed 128-position chunks with a fixed-order combine, so a stream's output
+ * depends only on its own slot.  Errors as kv_slot_append. */
+bm_status kv_slot_attend(bm_engine* e, int layer, const int32_t* slots, const uint16_t* Q,
+                         uint16_t* O, int B, void* stream);
+
+/* Commit one appended position for B streams (length += 1).  decode_step
+ * does this itself once per step, after all layers. */
+bm_status kv_slot_advance(bm_engine* e, const int32_t* slots, int B, void* stream);
+
+/* Retire: mark the slot free and its length 0.  Host only; the slot's K/V
+ * bytes are left as they are and overwritten by the next stream.  Errors:
+ * BM_ERR_SLOT_FREE on a slot that is not active (double release). */
+bm_status kv_slot_release(bm_engine* e, int slot);
+
+/* Committed length of an active slot (host mirror). */
+bm_status kv_slot_length(const bm_engine* e, int slot, int* len_out);
+
+/* Copy `count` positions (from 0) of one layer of a slot to DEVICE or HOST
+ * buffers K_out, V_out bf16 [kv_heads][count][d].  For tests and checkpoints. */
+bm_status kv_slot_read(bm_engine* e, int layer, int slot, int count, uint16_t* K_out,
+                       uint16_t* V_out, void* stream);
+
+/* ---------------------------------------------------------------- ops */
+
+/* Batched W4A16 GEMM: Y[m][n] = sum_k X[m][k] * W[n][k] (+ R[m][n]).
+ * W: DEVICE packed int4 [N][K/2], S: fp16 [N][K/g]; X: bf16 [M][K];
+ * R: bf16 [M][N] or NULL; Y: bf16 [M][N].  All DEVICE, row-major, dense.
+ * Each packed weight byte is read from HBM once for all M rows ([Batched
+ * serving] §1); a row's result does not depend on M or on the other rows
+ * ([Batched serving] §3).  Uses the CUDA-core kernel family.
+ * Errors: BM_ERR_INVALID_ARG if M < 1, N < 1, K % 32 != 0, K % g != 0,
+ * g not in {32, 64, 128}, or a NULL pointer. */
+bm_status w4_gemm_batched(const uint8_t* W, const uint16_t* S, const uint16_t* X, uint16_t* Y,
+                          const uint16_t* R, int M, int N, int K, int g, void* stream);
+
+/* Bytes of DEVICE workspace moe_grouped_w4 needs for B tokens. */
+size_t bm_moe_workspace_bytes(int B, int experts, int top_k, int hidden, int ffn);
+
+/* Grouped int4 expert op of B tokens: softmax top-k routing of X, every
+ * selected (token, expert) pair sorted by expert, each active expert's
+ * gate/up (SiLU) and down projections over its tokens, then
+ * Y[b] = Hres[b] + sum_r w[b][r] * out[b][r] in rank order.
+ * ([Batched serving] §1: the selected experts of all B streams run as one
+ * grouped operation against the resident expert bank.)
+ * X: DEVICE bf16 [B][H] (the router and experts' input); Hres: DEVICE bf16
+ * [B][H] or NULL (zero); Y: DEVICE bf16 [B][H]; topk_ids: DEVICE int32
+ * [B][k] (out, rank order); topk_w: DEVICE fp32 [B][k] (out); ws: DEVICE,
+ * at least bm_moe_workspace_bytes(B, ...) bytes, caller-owned.
+ * Errors: BM_ERR_INVALID_ARG (bad sizes, NULL, ws too small). */
+bm_status moe_grouped_w4(const bm_moe_weights* w, const uint16_t* X, const uint16_t* Hres,
+                         uint16_t* Y, int32_t* topk_ids, float* topk_w, int B, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* One batched decode step of B streams through every layer and the output
+ * projection ([Batched serving] §1: one fused forward per token for all B
+ * streams; the host crosses to the device once per step).
+ * slots: HOST int32 [B], distinct active slots, in any order; tokens: int32
+ * [B] in HOST or DEVICE memory, token i sits at position length(slots[i]);
+ * next_tokens: int32 [B], HOST or DEVICE, greedy argmax (ties: lowest id);
+ * logits: DEVICE fp32 [B][V] or NULL.  Row i of every output belongs to
+ * slots[i].  Appends each layer's K/V at that position and advances every
+ * slot's length by one.  With use_graph, the step is one cudaGraphLaunch of
+ * a graph captured on the first step with this B.
+ * Errors: BM_ERR_NOT_READY, BM_ERR_SLOT_FREE, BM_ERR_CTX_CAP,
+ * BM_ERR_INVALID_ARG (B out of range, duplicate slot), BM_ERR_CUDA. */
+bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens,
+                      int32_t* next_tokens, float* logits, void* stream);
+
+/* Encode fp32 weights to the canonical int4 layout: per row and group of g,
+ * s = fp16(absmax / 7) (fp32 division, round to nearest even), q =
+ * clamp(rint(w / s), -8, 7) (fp32 division), u = q + 8; an all-zero group
+ * gets s = 0.  W: DEVICE fp32 [N][K]; packed: DEVICE [N][K/2]; scales:
+ * DEVICE fp16 [N][K/g].  Errors: BM_ERR_INVALID_ARG. */
+bm_status bm_w4_quantize(const float* W, int N, int K, int g, uint8_t* packed, uint16_t* scales,
+                         void* stream);
+
+/* ---------------------------------------------------------------- host slot map
+ * The engine's slot bookkeeping on its own, with no device involved, for
+ * schedulers that want to plan admissions. */
+
+bm_status bm_slot_map_create(int max_streams, int ctx_cap, bm_slot_map** out);
+void bm_slot_map_destroy(bm_slot_map* m);
+/* Lowest free slot, length = len.  BM_ERR_CTX_CAP if len >= ctx_cap or len < 0
+ * is BM_ERR_INVALID_ARG; BM_ERR_NO_SLOT when full. */
+bm_status bm_slot_map_acquire(bm_slot_map* m, int len, int* slot_out);
+/* BM_ERR_SLOT_FREE on a free slot. */
+bm_status bm_slot_map_release(bm_slot_map* m, int slot);
+/* Check a batch: slot ids in range, distinct, active, length < ctx_cap. */
+bm_status bm_slot_map_check_batch(const bm_slot_map* m, const int32_t* slots, int B);
+/* length += 1 for each slot of a checked batch. */
+bm_status bm_slot_map_advance(bm_slot_map* m, const int32_t* slots, int B);
+bm_status bm_slot_map_length(const bm_slot_map* m, int slot, int* len_out);
+int bm_slot_map_active_count(const bm_slot_map* m);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITMOE_H */

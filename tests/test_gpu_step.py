@@ -1,0 +1,207 @@
+"""GPU parity of the whole decode step on the tiny MoE layer (hidden 512,
+8/2 heads of 64, 8 experts top-2, FFN 256, group 32; a bf16 head of vocab
+4096), solo-vs-batched byte identity, a ragged join/finish schedule, one
+graph launch per step, and the step at full model width."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_side import build_engine, seed_stream
+from oracle_side import oracle_config, oracle_weights
+from parity import assert_close_rows, check_greedy
+
+pytestmark = pytest.mark.gpu
+
+NAME = "tiny_layer"
+CFG = synth.CONFIGS[NAME]
+
+
+@pytest.fixture(scope="module")
+def bm():
+    import bit_moe_decode_w4a16_gb300 as m
+    m.build()
+    return m
+
+
+def _step(bm, e, slots, toks, V):
+    B = len(slots)
+    nxt = torch.empty(B, dtype=torch.int32)
+    logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    bm.decode_step(e, slots, torch.tensor(toks, dtype=torch.int32), nxt, logits)
+    bm.bm_engine_sync(e)
+    return nxt.numpy().copy(), logits
+
+
+def _oracle_kv(cfg, layers):
+    return oracle.OracleKV(cfg, oracle.OracleSlotMap(cfg.max_streams, cfg.ctx_cap))
+
+
+def _prefix_np(stream, length, layers):
+    k, v = synth.kv_prefix(NAME, CFG, stream, length, layers=layers)
+    return k.double().numpy(), v.double().numpy()
+
+
+@pytest.mark.parametrize("layers", [1, 2])
+def test_tiny_layer_step_matches_oracle_and_solo(bm, layers):
+    lens = CFG["lens"]                       # 17 and 40
+    toks = [int(t) for t in synth.tokens(NAME, "step", 2, CFG["vocab"])]
+    e = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, gen_device="cpu")
+    try:
+        slots = [seed_stream(e, NAME, CFG, i, L, layers, gen_device="cpu") for i, L in enumerate(lens)]
+        nxt, logits = _step(bm, e, slots, toks, CFG["vocab"])
+        ocfg = oracle_config(CFG, layers=layers, max_streams=4, ctx_cap=128)
+        ow = oracle_weights(NAME, CFG, layers)
+        kv = _oracle_kv(ocfg, layers)
+        oslots = [kv.seed(*_prefix_np(i, L, layers)) for i, L in enumerate(lens)]
+        ref_logits, ref_ids = oracle.model_step(ocfg, ow, kv, oslots, toks)
+        err, _ = assert_close_rows(logits, ref_logits, what=f"tiny step logits, {layers} layer(s)")
+        check_greedy(nxt, ref_logits, err)
+        # the K/V this step appended at position len matches the oracle's
+        for i, s in enumerate(slots):
+            n = lens[i] + 1
+            Kr = torch.empty((CFG["kv_heads"], n, CFG["head_dim"]), dtype=torch.bfloat16, device="cuda")
+            Vr = torch.empty_like(Kr)
+            bm.kv_slot_read(e, layers - 1, s, n, Kr, Vr)
+            bm.bm_engine_sync(e)
+            assert_close_rows(Kr[:, -1], kv.K[oslots[i]][layers - 1][:, -1], what="appended k (rotated)")
+            assert_close_rows(Vr[:, -1], kv.V[oslots[i]][layers - 1][:, -1], what="appended v")
+        # solo == batched: each stream alone in a fresh slot gives the same bytes
+        for i, L in enumerate(lens):
+            bm.kv_slot_release(e, slots[i])
+        for i, L in enumerate(lens):
+            s = seed_stream(e, NAME, CFG, i, L, layers, gen_device="cpu")
+            n1, l1 = _step(bm, e, [s], [toks[i]], CFG["vocab"])
+            assert torch.equal(l1[0], logits[i]) and n1[0] == nxt[i]
+            bm.kv_slot_release(e, s)
+    finally:
+        bm.bm_engine_destroy(e)
+
+
+def test_graph_count_paths_and_determinism(bm):
+    layers = 1
+    e = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, gen_device="cpu")
+    e2 = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, use_graph=0, gen_device="cpu")
+    try:
+        s1 = [seed_stream(e, NAME, CFG, i, 10 + i, layers, gen_device="cpu") for i in range(3)]
+        s2 = [seed_stream(e2, NAME, CFG, i, 10 + i, layers, gen_device="cpu") for i in range(3)]
+        st0 = bm.bm_engine_stats(e)
+        toks = [5, 6, 7]
+        dev_toks = torch.tensor(toks, dtype=torch.int32, device="cuda")
+        nxt_dev = torch.empty(3, dtype=torch.int32, device="cuda")
+        for step in range(4):
+            B = 3 if step % 2 == 0 else 2
+            a, la = _step(bm, e, s1[:B], toks[:B], CFG["vocab"])
+            b, lb = _step(bm, e2, s2[:B], toks[:B], CFG["vocab"])
+            assert torch.equal(la, lb) and np.array_equal(a, b)      # graph == eager, bytes
+        st1 = bm.bm_engine_stats(e)
+        assert st1["graph_launches"] - st0["graph_launches"] == 4     # one launch per step
+        assert st1["graph_captures"] == 2                             # one graph per distinct B
+        assert st1["kernels_per_step"] == 1 + 10 * layers + 2
+        # device-resident tokens and outputs take the same path
+        bm.decode_step(e, s1, dev_toks, nxt_dev)
+        bm.decode_step(e2, s2, torch.tensor(toks, dtype=torch.int32), torch.empty(3, dtype=torch.int32))
+        bm.bm_engine_sync(e)
+        bm.bm_engine_sync(e2)
+        # lengths advanced once per step
+        assert [bm.kv_slot_length(e, s) for s in s1] == [15, 16, 15]
+    finally:
+        bm.bm_engine_destroy(e)
+        bm.bm_engine_destroy(e2)
+
+
+def _schedule_run(bm, e, events, layers):
+    """Greedy decode of a join/finish schedule on the GPU; returns per-stream
+    token lists and per-stream lists of logits rows."""
+    live, nxt, toks, rows, sid = [], {}, {}, {}, 0
+    for ev in events:
+        for L in ev["join"]:
+            s = seed_stream(e, NAME, CFG, 100 + sid, L, layers, gen_device="cpu")
+            live.append((sid, s))
+            nxt[sid] = (sid * 977 + 13) % CFG["vocab"]
+            toks[sid], rows[sid] = [], []
+            sid += 1
+        ids, logits = _step(bm, e, [s for _, s in live], [nxt[i] for i, _ in live], CFG["vocab"])
+        for j, (i, _) in enumerate(live):
+            toks[i].append(int(ids[j]))
+            rows[i].append(logits[j].clone())
+            nxt[i] = int(ids[j])
+        fin = set(ev["finish"])
+        for j, (_, s) in enumerate(live):
+            if j in fin:
+                bm.kv_slot_release(e, s)
+        live = [x for j, x in enumerate(live) if j not in fin]
+    return toks, rows
+
+
+def test_ragged_schedule_solo_batched_bytes_and_oracle(bm):
+    layers = 2
+    events = synth.schedule(seed=7, steps=14, max_streams=6, ctx_cap=48, min_len=1, max_batch=4)
+    e = build_engine(NAME, CFG, layers, max_streams=6, ctx_cap=48, gen_device="cpu")
+    try:
+        toks, rows = _schedule_run(bm, e, events, layers)
+        # each stream decoded alone, through the same engine, gives the same bytes
+        lens, steps, sid, live = {}, {}, 0, []
+        for ev in events:
+            for L in ev["join"]:
+                lens[sid], steps[sid] = L, 0
+                live.append(sid)
+                sid += 1
+            for i in live:
+                steps[i] += 1
+            fin = set(ev["finish"])
+            live = [i for j, i in enumerate(live) if j not in fin]
+        for i in lens:
+            s = seed_stream(e, NAME, CFG, 100 + i, lens[i], layers, gen_device="cpu")
+            t = (i * 977 + 13) % CFG["vocab"]
+            for k in range(steps[i]):
+                ids, lg = _step(bm, e, [s], [t], CFG["vocab"])
+                assert torch.equal(lg[0], rows[i][k]), f"stream {i} step {k}: solo bytes differ from batched"
+                t = int(ids[0])
+                assert t == toks[i][k]
+            bm.kv_slot_release(e, s)
+        # teacher-forced oracle on two streams, feeding the GPU's own tokens
+        ocfg = oracle_config(CFG, layers=layers, max_streams=6, ctx_cap=48)
+        ow = oracle_weights(NAME, CFG, layers)
+        for i in list(lens)[:2]:
+            kv = _oracle_kv(ocfg, layers)
+            s = kv.seed(*_prefix_np(100 + i, lens[i], layers))
+            t = (i * 977 + 13) % CFG["vocab"]
+            for k in range(steps[i]):
+                ref, _ = oracle.model_step(ocfg, ow, kv, [s], [t])
+                err, _ = assert_close_rows(rows[i][k][None], ref, what=f"schedule stream {i} step {k}")
+                check_greedy([toks[i][k]], ref, err)
+                t = toks[i][k]
+    finally:
+        bm.bm_engine_destroy(e)
+
+
+def test_step_at_full_width(bm):
+    # Two layers of the 30B-class shape (hidden 2048, 32/4 heads of 128,
+    # 128 experts top-8, FFN 768, group 64), a bf16 head of vocab 4096.
+    cfg = dict(synth.CONFIGS["full_model"])
+    cfg["vocab"] = 4096
+    layers = 2
+    e = build_engine("full_width", cfg, layers, max_streams=4, ctx_cap=256, gen_device="cpu")
+    try:
+        lens = [33, 200, 1]
+        slots = []
+        for i, L in enumerate(lens):
+            k, v = synth.kv_prefix("full_width", cfg, i, L, layers=layers)
+            slots.append(bm.kv_slot_seed(e, k.cuda(), v.cuda(), L))
+        toks = [11, 4000, 257]
+        nxt, logits = _step(bm, e, slots, toks, cfg["vocab"])
+        ocfg = oracle_config(cfg, layers=layers, max_streams=4, ctx_cap=256)
+        ow = oracle_weights("full_width", cfg, layers)
+        kv = _oracle_kv(ocfg, layers)
+        oslots = []
+        for i, L in enumerate(lens):
+            k, v = synth.kv_prefix("full_width", cfg, i, L, layers=layers)
+            oslots.append(kv.seed(k.double().numpy(), v.double().numpy()))
+        ref, _ = oracle.model_step(ocfg, ow, kv, oslots, toks)
+        err, _ = assert_close_rows(logits, ref, what="full-width 2-layer step")
+        check_greedy(nxt, ref, err)
+    finally:
+        bm.bm_engine_destroy(e)

@@ -51,6 +51,11 @@ class bm_moe_weights(ctypes.Structure):
                [(n, _P) for n in ("wr", "wg", "wg_s", "wu", "wu_s", "wd", "wd_s")]
 
 
+class bm_kernel_profile(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", ctypes.c_int), ("ms", ctypes.c_float),
+                ("bytes", ctypes.c_double), ("flops", ctypes.c_double)]
+
+
 class bm_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("steps", "tokens", "graph_launches", "graph_captures",
                                                "kernel_launches", "kernels_per_step")] + \
@@ -89,6 +94,7 @@ def lib():
             "bm_moe_workspace_bytes": ([I, I, I, I, I], SZ),
             "moe_grouped_w4": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V, SZ, V], S),
             "decode_step": ([V, I, V, V, V, V, V], S),
+            "bm_engine_profile_step": ([V, I, V, V, V, ctypes.POINTER(bm_kernel_profile), I, PI, V], S),
             "bm_w4_quantize": ([V, I, I, I, V, V, V], S),
             "bm_slot_map_create": ([I, I, ctypes.POINTER(V)], S),
             "bm_slot_map_destroy": ([V], None),
@@ -248,6 +254,18 @@ def decode_step(e, slots, tokens, next_tokens, logits=None, stream=None):
     arr = _i32_array(slots)
     _check(lib().decode_step(e, len(slots), ctypes.addressof(arr), ptr(tokens), ptr(next_tokens), ptr(logits),
                              stream_handle(stream)))
+
+
+def bm_engine_profile_step(e, slots, tokens, next_tokens, stream=None):
+    """One eager decode step with per-kernel CUDA-event times; returns a list
+    of dicts (name, launches, ms, bytes, flops), one per kernel class."""
+    arr = _i32_array(slots)
+    out = (bm_kernel_profile * 32)()
+    n = ctypes.c_int(0)
+    _check(lib().bm_engine_profile_step(e, len(slots), ctypes.addressof(arr), ptr(tokens), ptr(next_tokens), out,
+                                        32, ctypes.byref(n), stream_handle(stream)))
+    return [{"name": out[i].name.decode(), "launches": out[i].launches, "ms": out[i].ms,
+             "bytes": out[i].bytes, "flops": out[i].flops} for i in range(n.value)]
 
 
 def bm_w4_quantize(W, N, K, g, packed, scales, stream=None):

@@ -232,17 +232,21 @@ cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slot
 }
 
 cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q, bf16* out,
-                             int qh, int B, float* partials, DevCheck chk, cudaStream_t st, int* launches) {
+                             int qh, int B, float* partials, DevCheck chk, cudaStream_t st, int* launches,
+                             const Marker& mark) {
   if (ar.d > 128 || ar.d % 8 != 0 || qh % ar.kvh != 0 || qh / ar.kvh > kMaxGroup) return cudaErrorInvalidValue;
   const int max_chunks = (ar.cap + kAttnChunk - 1) / kAttnChunk;
   dim3 g1(max_chunks, ar.kvh, B);
   k_attn_part<<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  mark(KT_ATTN_PART);
   dim3 g2(qh, B);
   k_attn_combine<<<g2, 128, 0, st>>>(ar, slots, partials, qh, max_chunks, out);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  mark(KT_ATTN_COMBINE);
   if (launches) *launches += 2;
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st) {

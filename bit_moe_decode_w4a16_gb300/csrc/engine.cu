@@ -116,9 +116,16 @@ struct bm_engine {
   int32_t *d_slots = nullptr, *d_tokens = nullptr, *d_next = nullptr, *d_slots_aux = nullptr;
   int* d_err = nullptr;
   // host staging (pinned)
-  int32_t* h_stage = nullptr;   // [2 * max_streams]: slots, tokens
+  // A ring of kStageRing staging entries of [2 * max_streams] (slots, tokens)
+  // lets the host run up to kStageRing steps ahead of the device.
+  static constexpr int kStageRing = 8;
+  int32_t* h_stage = nullptr;
   int32_t* h_aux = nullptr;     // [max_streams]: slots of standalone kv calls
-  cudaEvent_t ev_stage = nullptr, ev_aux = nullptr;
+  cudaEvent_t ev_ring[kStageRing] = {};
+  int ring_pos = 0;
+  cudaEvent_t ev_aux = nullptr;
+  int32_t* d_u_log = nullptr;   // [layers] active experts of the last step, per layer
+  std::vector<cudaEvent_t> prof_events;
   cudaStream_t cap_stream = nullptr;
   std::map<int, cudaGraphExec_t> graphs;
   bm_stats st{};
@@ -132,44 +139,87 @@ namespace {
 DevCheck chk_of(bm_engine* e) { return DevCheck{e->d_err}; }
 
 // Enqueue one decode step for B streams reading e->d_slots / e->d_tokens.
-cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches) {
+cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark = Marker()) {
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim;
   cudaError_t err;
   int n = 0;
   if ((err = launch_embed(e->embed, c.vocab, H, e->d_tokens, e->x, B, chk_of(e), s)) != cudaSuccess) return err;
+  mark(KT_EMBED);
   ++n;
   for (int l = 0; l < c.layers; ++l) {
     const LayerW& w = e->L[l];
     GemvArgs g1{w.wqkv, w.wqkv_s, e->x, H, nullptr, 0, e->qkv, e->qkv_rows, B, e->qkv_rows, H, c.group,
                 1, w.has_attn_norm ? w.attn_norm_buf : nullptr, c.rms_eps};
     if ((err = launch_w4_gemv(g1, s)) != cudaSuccess) return err;
+    mark(KT_QKV);
     ++n;
     if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
                                   chk_of(e), s)) != cudaSuccess)
       return err;
+    mark(KT_ROPE_APPEND);
     ++n;
     if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
-                                &n)) != cudaSuccess)
+                                &n, mark)) != cudaSuccess)
       return err;
     GemvArgs g2{w.wo, w.wo_s, e->attn, qd, e->x, H, e->h, H, B, H, qd, c.group, 0, nullptr, c.rms_eps};
     if ((err = launch_w4_gemv(g2, s)) != cudaSuccess) return err;
+    mark(KT_OPROJ);
     ++n;
     MoeArgs ma{B, c.experts, c.top_k, H, c.ffn, c.group, c.renorm_topk,
                w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
-               e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x};
+               e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l};
     const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, c.ffn);
-    if ((err = launch_moe(ma, mb, s, &n)) != cudaSuccess) return err;
+    if ((err = launch_moe(ma, mb, s, &n, mark)) != cudaSuccess) return err;
   }
   if ((err = launch_lm_head(e->lm_head, c.vocab, H, e->x, e->has_final_norm ? e->final_norm_buf : nullptr,
                             c.rms_eps, e->logits, B, s)) != cudaSuccess)
     return err;
+  mark(KT_LM_HEAD);
   ++n;
   if ((err = launch_argmax(e->logits, c.vocab, B, e->d_next, e->arena.len, e->d_slots, 1, s)) != cudaSuccess)
     return err;
+  mark(KT_ARGMAX);
   ++n;
   if (launches) *launches = n;
   return cudaSuccess;
+}
+
+const char* kTagNames[KT_COUNT] = {"embed", "qkv_w4", "rope_append", "attn_partial", "attn_combine", "oproj_w4",
+                                   "router", "topk_sort", "expert_gateup", "expert_down", "moe_combine",
+                                   "lm_head", "argmax"};
+
+// Algorithmic HBM bytes and flops of one launch of a kernel class for a
+// batch of B streams: each weight byte once, each activation once, and the
+// K/V positions actually attended (`kv_pos` = sum over streams of len + 1);
+// `U` = active experts of the layer.
+void algo_cost(const bm_config& c, int qkv_rows, int tag, int B, double U, double kv_pos, double* bytes,
+               double* flops) {
+  const double H = c.hidden, qd = (double)c.q_heads * c.head_dim, kvd = (double)c.kv_heads * c.head_dim;
+  const double g = c.group, E = c.experts, F = c.ffn, V = c.vocab, P = (double)B * c.top_k;
+  const double chunks = std::ceil(kv_pos / B / kAttnChunk) * B;
+  auto w4 = [&](double rows, double K) { return rows * (K / 2 + K / g * 2); };
+  double b = 0, f = 0;
+  switch (tag) {
+    case KT_EMBED: b = 4.0 * B * H; break;
+    case KT_QKV: b = w4(qkv_rows, H) + 2.0 * B * H + 2.0 * B * qkv_rows; f = 2.0 * B * qkv_rows * H; break;
+    case KT_ROPE_APPEND: b = 2.0 * B * qkv_rows + 2.0 * B * (qd + 2 * kvd); break;
+    case KT_ATTN_PART:
+      b = kv_pos * kvd * 2 * 2 + 2.0 * B * qd + chunks * c.q_heads * (c.head_dim + 2) * 4;
+      f = kv_pos * c.q_heads * c.head_dim * 4;
+      break;
+    case KT_ATTN_COMBINE: b = chunks * c.q_heads * (c.head_dim + 2) * 4 + 2.0 * B * qd; break;
+    case KT_OPROJ: b = w4(H, qd) + 2.0 * B * qd + 4.0 * B * H; f = 2.0 * B * H * qd; break;
+    case KT_ROUTER: b = E * H * 4 + 4.0 * B * H + 4.0 * B * E; f = 2.0 * B * E * H; break;
+    case KT_TOPK_SORT: b = 4.0 * B * E + 8.0 * P; break;
+    case KT_GATEUP: b = U * w4(2 * F, H) + 2.0 * P * H + 2.0 * P * F; f = 2.0 * P * 2 * F * H; break;
+    case KT_DOWN: b = U * w4(H, F) + 2.0 * P * F + 4.0 * P * H; f = 2.0 * P * H * F; break;
+    case KT_COMBINE: b = 4.0 * P * H + 4.0 * B * H; break;
+    case KT_LM_HEAD: b = 2.0 * V * H + 2.0 * B * H + 4.0 * B * V; f = 2.0 * B * V * H; break;
+    case KT_ARGMAX: b = 4.0 * B * V; break;
+  }
+  *bytes = b;
+  *flops = f;
 }
 
 bm_status check_config(const bm_config& c) {
@@ -201,7 +251,9 @@ void free_engine(bm_engine* e) {
   if (!e) return;
   for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
   if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
-  if (e->ev_stage) cudaEventDestroy(e->ev_stage);
+  for (cudaEvent_t ev : e->ev_ring)
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : e->prof_events) cudaEventDestroy(ev);
   if (e->ev_aux) cudaEventDestroy(e->ev_aux);
   if (e->h_stage) cudaFreeHost(e->h_stage);
   if (e->wslab) cudaFree(e->wslab);
@@ -312,7 +364,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
              s_part = take(attn_partial_floats(c.max_streams, c.q_heads, c.ctx_cap, c.head_dim) * 4),
              s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
              s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
-             s_sa = take(S * 4), s_err = take(4);
+             s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4);
   e->scratch_bytes = off;
   BM_CUDA(cudaMalloc(&e->scratch, e->scratch_bytes), "scratch allocation");
   char* sb = static_cast<char*>(e->scratch);
@@ -329,13 +381,17 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   e->d_next = reinterpret_cast<int32_t*>(sb + s_nx.off);
   e->d_slots_aux = reinterpret_cast<int32_t*>(sb + s_sa.off);
   e->d_err = reinterpret_cast<int*>(sb + s_err.off);
+  e->d_u_log = reinterpret_cast<int32_t*>(sb + s_ulog.off);
   BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");
 
-  BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * 3 * S), "pinned staging allocation");
-  e->h_aux = e->h_stage + 2 * S;
-  BM_CUDA(cudaEventCreateWithFlags(&e->ev_stage, cudaEventDisableTiming), "event");
+  BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * (2 * bm_engine::kStageRing + 1) * S),
+          "pinned staging allocation");
+  e->h_aux = e->h_stage + 2 * bm_engine::kStageRing * S;
+  for (cudaEvent_t& ev : e->ev_ring) {
+    BM_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "event");
+    BM_CUDA(cudaEventRecord(ev, 0), "event");
+  }
   BM_CUDA(cudaEventCreateWithFlags(&e->ev_aux, cudaEventDisableTiming), "event");
-  BM_CUDA(cudaEventRecord(e->ev_stage, 0), "event");
   BM_CUDA(cudaEventRecord(e->ev_aux, 0), "event");
   BM_CUDA(cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking), "capture stream");
   BM_CUDA(cudaDeviceSynchronize(), "engine setup");
@@ -545,30 +601,76 @@ bm_status kv_slot_read(bm_engine* e, int layer, int slot, int count, uint16_t* K
 
 // ------------------------------------------------------------------ step
 
-bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, int32_t* next_tokens,
-                      float* logits, void* stream) {
-  if (!e || !slots || !tokens || !next_tokens) return set_error(BM_ERR_INVALID_ARG, "decode_step: null argument");
-  std::lock_guard<std::mutex> lk(e->mu);
+}  // extern "C"
+
+namespace bm {
+namespace {
+
+// Checks shared by decode_step and bm_engine_profile_step, then the upload of
+// slot ids and tokens into the step's static device inputs (through the next
+// entry of the pinned staging ring).
+bm_status prepare_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, int32_t* next_tokens,
+                       cudaStream_t s, const char* who) {
+  if (!e || !slots || !tokens || !next_tokens) return set_error(BM_ERR_INVALID_ARG, std::string(who) + ": null argument");
   const bm_config& c = e->cfg;
-  if (!e->emb_set) return set_error(BM_ERR_NOT_READY, "decode_step: embeddings not set");
+  if (!e->emb_set) return set_error(BM_ERR_NOT_READY, std::string(who) + ": embeddings not set");
   for (int l = 0; l < c.layers; ++l)
-    if (!e->L[l].set) return set_error(BM_ERR_NOT_READY, "decode_step: layer " + std::to_string(l) + " not set");
+    if (!e->L[l].set) return set_error(BM_ERR_NOT_READY, std::string(who) + ": layer " + std::to_string(l) + " not set");
   std::string err;
-  bm_status st = e->slots.check_batch(slots, B, &err);
-  if (st != BM_OK) return set_error(st, "decode_step: " + err);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bm_status st = e->slots.check_batch(slots, B, &err);
+  if (st != BM_OK) return set_error(st, std::string(who) + ": " + err);
   const size_t S = c.max_streams;
-  BM_CUDA(cudaEventSynchronize(e->ev_stage), "staging event");
-  std::memcpy(e->h_stage, slots, sizeof(int32_t) * B);
-  BM_CUDA(cudaMemcpyAsync(e->d_slots, e->h_stage, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s), "slot upload");
+  const int slot = e->ring_pos;
+  e->ring_pos = (e->ring_pos + 1) % bm_engine::kStageRing;
+  int32_t* stage = e->h_stage + 2 * S * slot;
+  BM_CUDA(cudaEventSynchronize(e->ev_ring[slot]), "staging event");
+  std::memcpy(stage, slots, sizeof(int32_t) * B);
+  BM_CUDA(cudaMemcpyAsync(e->d_slots, stage, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s), "slot upload");
   if (is_device_ptr(tokens)) {
     BM_CUDA(cudaMemcpyAsync(e->d_tokens, tokens, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice, s), "token copy");
   } else {
-    std::memcpy(e->h_stage + S, tokens, sizeof(int32_t) * B);
-    BM_CUDA(cudaMemcpyAsync(e->d_tokens, e->h_stage + S, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s),
-            "token upload");
+    std::memcpy(stage + S, tokens, sizeof(int32_t) * B);
+    BM_CUDA(cudaMemcpyAsync(e->d_tokens, stage + S, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s), "token upload");
   }
-  BM_CUDA(cudaEventRecord(e->ev_stage, s), "staging event");
+  BM_CUDA(cudaEventRecord(e->ev_ring[slot], s), "staging event");
+  return BM_OK;
+}
+
+struct ProfCtx {
+  bm_engine* e;
+  cudaStream_t s;
+  std::vector<int> tags;
+  cudaError_t err = cudaSuccess;
+};
+
+void prof_mark(void* ctx, int tag) {
+  ProfCtx* p = static_cast<ProfCtx*>(ctx);
+  const size_t i = p->tags.size() + 1;
+  while (p->e->prof_events.size() <= i) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) {
+      p->err = cudaErrorMemoryAllocation;
+      return;
+    }
+    p->e->prof_events.push_back(ev);
+  }
+  if (p->err == cudaSuccess) p->err = cudaEventRecord(p->e->prof_events[i], p->s);
+  p->tags.push_back(tag);
+}
+
+}  // namespace
+}  // namespace bm
+
+extern "C" {
+
+bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, int32_t* next_tokens,
+                      float* logits, void* stream) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "decode_step: null engine");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bm_status st = prepare_step(e, B, slots, tokens, next_tokens, s, "decode_step");
+  if (st != BM_OK) return st;
   int n = 0;
   if (c.use_graph) {
     auto it = e->graphs.find(B);
@@ -604,6 +706,68 @@ bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* 
   e->slots.advance(slots, B);
   e->st.steps += 1;
   e->st.tokens += B;
+  return bm::ok();
+}
+
+bm_status bm_engine_profile_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens,
+                                 int32_t* next_tokens, bm_kernel_profile* out, int max_out, int* n_out,
+                                 void* stream) {
+  if (!e || !out || !n_out || max_out < 1) return set_error(BM_ERR_INVALID_ARG, "bm_engine_profile_step: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bm_status st = prepare_step(e, B, slots, tokens, next_tokens, s, "bm_engine_profile_step");
+  if (st != BM_OK) return st;
+  double kv_pos = 0;
+  for (int i = 0; i < B; ++i) kv_pos += e->slots.length(slots[i]) + 1;
+  // prof_events[0] marks the start; kernel i (tags[i]) ends at prof_events[i + 1].
+  if (e->prof_events.empty()) {
+    cudaEvent_t ev;
+    BM_CUDA(cudaEventCreate(&ev), "profile event");
+    e->prof_events.push_back(ev);
+  }
+  ProfCtx ctx{e, s, {}};
+  int n = 0;
+  Marker mark{prof_mark, &ctx};
+  BM_CUDA(cudaEventRecord(e->prof_events[0], s), "profile start event");
+  BM_CUDA(enqueue_step(e, B, s, &n, mark), "bm_engine_profile_step launch");
+  BM_CUDA(ctx.err, "profile events");
+  BM_CUDA(cudaMemcpyAsync(next_tokens, e->d_next, sizeof(int32_t) * B, cudaMemcpyDefault, s), "next token copy");
+  BM_CUDA(cudaStreamSynchronize(s), "profile synchronise");
+  std::vector<int32_t> ulog(c.layers);
+  BM_CUDA(cudaMemcpy(ulog.data(), e->d_u_log, sizeof(int32_t) * c.layers, cudaMemcpyDeviceToHost), "expert count read");
+  std::vector<double> ms(KT_COUNT, 0.0), bytes(KT_COUNT, 0.0), flops(KT_COUNT, 0.0);
+  std::vector<int> cnt(KT_COUNT, 0);
+  int layer = 0;
+  for (size_t i = 0; i < ctx.tags.size(); ++i) {
+    const int tag = ctx.tags[i];
+    float t = 0.f;
+    BM_CUDA(cudaEventElapsedTime(&t, e->prof_events[i], e->prof_events[i + 1]), "event time");
+    double b = 0, f = 0;
+    const double U = ulog[layer < c.layers ? layer : c.layers - 1];
+    algo_cost(c, e->qkv_rows, tag, B, U, kv_pos, &b, &f);
+    ms[tag] += t;
+    bytes[tag] += b;
+    flops[tag] += f;
+    cnt[tag] += 1;
+    if (tag == KT_COMBINE) ++layer;
+  }
+  int k = 0;
+  for (int tag = 0; tag < KT_COUNT && k < max_out; ++tag) {
+    if (!cnt[tag]) continue;
+    bm_kernel_profile& p = out[k++];
+    std::memset(p.name, 0, sizeof(p.name));
+    std::strncpy(p.name, kTagNames[tag], sizeof(p.name) - 1);
+    p.launches = cnt[tag];
+    p.ms = (float)ms[tag];
+    p.bytes = bytes[tag];
+    p.flops = flops[tag];
+  }
+  *n_out = k;
+  e->slots.advance(slots, B);
+  e->st.steps += 1;
+  e->st.tokens += B;
+  e->st.kernel_launches += n;
   return bm::ok();
 }
 

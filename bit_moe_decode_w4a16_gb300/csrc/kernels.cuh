@@ -6,6 +6,21 @@
 
 namespace bm {
 
+// Kernel classes of one decode step (for the per-kernel profiler).
+enum KernelTag {
+  KT_EMBED = 0, KT_QKV, KT_ROPE_APPEND, KT_ATTN_PART, KT_ATTN_COMBINE, KT_OPROJ, KT_ROUTER, KT_TOPK_SORT,
+  KT_GATEUP, KT_DOWN, KT_COMBINE, KT_LM_HEAD, KT_ARGMAX, KT_COUNT
+};
+
+// Called after each kernel launch with its class; a no-op unless profiling.
+struct Marker {
+  void (*fn)(void* ctx, int tag) = nullptr;
+  void* ctx = nullptr;
+  void operator()(int tag) const {
+    if (fn) fn(ctx, tag);
+  }
+};
+
 // ---------------------------------------------------------------- dense
 struct GemvArgs {
   const uint8_t* W;   // packed int4 [N][K/2]
@@ -56,9 +71,11 @@ struct MoeArgs {
   float eps;
   const bf16* res;                 // [B][H] residual or null
   bf16* y;                         // [B][H]
+  int32_t* u_log;                  // if set, the number of active experts is also written here
 };
 // Router logits + top-k + sort, gate/up, down, combine: 5 launches.
-cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches);
+cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches,
+                       const Marker& mark = Marker());
 
 // ---------------------------------------------------------------- attention
 struct AttnArena {
@@ -82,7 +99,7 @@ cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slot
 // Split-K attention over positions 0..len[slot] (inclusive) and the combine.
 cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q,
                              bf16* out, int qh, int B, float* partials, DevCheck chk,
-                             cudaStream_t st, int* launches);
+                             cudaStream_t st, int* launches, const Marker& mark = Marker());
 cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st);
 
 // ---------------------------------------------------------------- model glue

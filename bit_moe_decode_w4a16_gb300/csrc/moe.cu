@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
     off_s[E] = acc;
     b.active_off[u] = acc;
     *b.n_active = u;
+    if (a.u_log) *a.u_log = u;
   }
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
@@ -334,23 +335,29 @@ MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
   return b;
 }
 
-cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches) {
+cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches, const Marker& mark) {
   if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
   const int nblk = (a.E + kRouterWarps - 1) / kRouterWarps;
   k_router<<<nblk, 256, sizeof(float) * a.B, st>>>(a, b);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  mark(KT_ROUTER);
   k_topk_sort<<<1, 1024, 0, st>>>(a, b);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  mark(KT_TOPK_SORT);
   const bf16* xin = a.do_norm ? b.xn : a.x;
   const int max_u = a.B * a.k < a.E ? a.B * a.k : a.E;
   // A token routes to k distinct experts, so no expert has more than B
   // tokens and the staging buffer needs min(B, 4) rows.
   if ((err = dispatch_gateup(a, b, xin, max_u, st)) != cudaSuccess) return err;
+  mark(KT_GATEUP);
   if ((err = dispatch_down(a, b, max_u, st)) != cudaSuccess) return err;
+  mark(KT_DOWN);
   k_combine<<<a.B, 256, 0, st>>>(a, b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  mark(KT_COMBINE);
   if (launches) *launches += 5;
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t init_moe_attributes() {

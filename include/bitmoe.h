@@ -126,6 +126,16 @@ typedef struct bm_stats {
   size_t scratch_bytes;       /* device bytes of activations and partials    */
 } bm_stats;
 
+/* Per-kernel-class measurement of one profiled decode step. */
+typedef struct bm_kernel_profile {
+  char name[24];    /* kernel class, e.g. "expert_gateup"                      */
+  int launches;     /* launches of this class in the step                      */
+  float ms;         /* summed CUDA-event time of those launches                */
+  double bytes;     /* algorithmic HBM bytes of those launches (weights read once,
+                       activations, K/V positions actually attended)          */
+  double flops;     /* algorithmic flops (2 per multiply-add)                  */
+} bm_kernel_profile;
+
 /* ---------------------------------------------------------------- errors */
 
 /* Message of the last failed call on this thread ("" if none).  The pointer
@@ -266,6 +276,16 @@ bm_status moe_grouped_w4(const bm_moe_weights* w, const uint16_t* X, const uint1
  * BM_ERR_INVALID_ARG (B out of range, duplicate slot), BM_ERR_CUDA. */
 bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens,
                       int32_t* next_tokens, float* logits, void* stream);
+
+/* decode_step run without the graph, with a CUDA event recorded after every
+ * kernel launch on `stream`, then synchronised.  Same arguments and the same
+ * effect on slots and outputs as decode_step (logits are not returned).  Fills
+ * out[0..*n_out) with one entry per kernel class (at most max_out).  Event
+ * times include the launch gaps between kernels of an eager launch sequence.
+ * Errors as decode_step. */
+bm_status bm_engine_profile_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens,
+                                 int32_t* next_tokens, bm_kernel_profile* out, int max_out, int* n_out,
+                                 void* stream);
 
 /* Encode fp32 weights to the canonical int4 layout: per row and group of g,
  * s = fp16(absmax / 7) (fp32 division, round to nearest even), q =

@@ -93,6 +93,8 @@ def lib():
             "w4_gemm_batched": ([V, V, V, V, V, I, I, I, I, V], S),
             "bm_moe_workspace_bytes": ([I, I, I, I, I], SZ),
             "moe_grouped_w4": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V, SZ, V], S),
+            "moe_grouped_w4_noalloc": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V], S),
+            "bm_moe_noalloc_max_bytes": ([], SZ),
             "decode_step": ([V, I, V, V, V, V, V], S),
             "bm_engine_profile_step": ([V, I, V, V, V, ctypes.POINTER(bm_kernel_profile), I, PI, V], S),
             "bm_w4_quantize": ([V, I, I, I, V, V, V], S),
@@ -247,6 +249,19 @@ def moe_grouped_w4(weights, X, Hres, Y, topk_ids, topk_w, B, ws, ws_bytes, strea
                           for k, t in bm_moe_weights._fields_})
     _check(lib().moe_grouped_w4(ctypes.byref(w), ptr(X), ptr(Hres), ptr(Y), ptr(topk_ids), ptr(topk_w), B,
                                 ptr(ws), ws_bytes, stream_handle(stream)))
+
+
+def moe_grouped_w4_noalloc(weights, X, Hres, Y, topk_ids, topk_w, B, stream=None):
+    """The grouped expert op with the library's built-in workspace (no
+    allocation); weights as for moe_grouped_w4."""
+    w = bm_moe_weights(**{k: (weights[k] if t is ctypes.c_int else ptr(weights[k]))
+                          for k, t in bm_moe_weights._fields_})
+    _check(lib().moe_grouped_w4_noalloc(ctypes.byref(w), ptr(X), ptr(Hres), ptr(Y), ptr(topk_ids), ptr(topk_w), B,
+                                        stream_handle(stream)))
+
+
+def bm_moe_noalloc_max_bytes():
+    return lib().bm_moe_noalloc_max_bytes()
 
 
 def decode_step(e, slots, tokens, next_tokens, logits=None, stream=None):

@@ -262,6 +262,31 @@ bm_status moe_grouped_w4(const bm_moe_weights* w, const uint16_t* X, const uint1
                          uint16_t* Y, int32_t* topk_ids, float* topk_w, int B, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* The grouped expert op for callers that cannot allocate device memory: a
+ * plugin inside a host engine that owns the whole device memory pool (an
+ * extra cudaMalloc would fail or break the pool's accounting), or code on a
+ * latency-critical path where cudaMalloc / cudaFree, which can synchronise
+ * the device, are not allowed.  No counterpart on the pages: it exists for
+ * those callers only.
+ * Same arguments, computation and results as moe_grouped_w4, minus the
+ * workspace: the scratch lives in a fixed array of bm_moe_noalloc_max_bytes()
+ * (4 MiB) compiled into the library, which every device that loads the
+ * library keeps for the life of the process.  The call allocates nothing.
+ * Its first call on a device looks up that array's device address and sets
+ * kernel attributes for that device; make that first call before any stream
+ * capture.  All calls on a device share the one array (no call needs it
+ * cleared first): calls whose work overlaps on the GPU — concurrent streams,
+ * or host threads without ordering — race on it and must be serialised by the
+ * caller.  Errors: as moe_grouped_w4, plus BM_ERR_INVALID_ARG when the sizes
+ * need more workspace than the array holds (bm_moe_workspace_bytes(B, ...) >
+ * bm_moe_noalloc_max_bytes()), and BM_ERR_CUDA if the array's address cannot
+ * be obtained. */
+bm_status moe_grouped_w4_noalloc(const bm_moe_weights* w, const uint16_t* X, const uint16_t* Hres,
+                                 uint16_t* Y, int32_t* topk_ids, float* topk_w, int B, void* stream);
+
+/* Size of the built-in workspace of moe_grouped_w4_noalloc, in bytes. */
+size_t bm_moe_noalloc_max_bytes(void);
+
 /* One batched decode step of B streams through every layer and the output
  * projection ([Batched serving] §1: one fused forward per token for all B
  * streams; the host crosses to the device once per step).

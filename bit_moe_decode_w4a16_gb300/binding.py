@@ -92,6 +92,8 @@ def lib():
             "kv_slot_read": ([V, I, I, I, V, V, V], S),
             "w4_gemm_batched": ([V, V, V, V, V, I, I, I, I, V], S),
             "bm_moe_workspace_bytes": ([I, I, I, I, I], SZ),
+            "bm_w4_repack_tc": ([V, V, I, I, I, V, V, V], S),
+            "w4_gemm_batched_tc": ([V, V, V, V, V, I, I, I, I, V], S),
             "moe_grouped_w4": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V, SZ, V], S),
             "moe_grouped_w4_noalloc": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V], S),
             "bm_moe_noalloc_max_bytes": ([], SZ),
@@ -237,6 +239,14 @@ def kv_slot_read(e, layer, slot, count, K_out, V_out, stream=None):
 
 def w4_gemm_batched(W, S, X, Y, R, M, N, K, g, stream=None):
     _check(lib().w4_gemm_batched(ptr(W), ptr(S), ptr(X), ptr(Y), ptr(R), M, N, K, g, stream_handle(stream)))
+
+
+def bm_w4_repack_tc(W, S, N, K, g, Wtc, Stc, stream=None):
+    _check(lib().bm_w4_repack_tc(ptr(W), ptr(S), N, K, g, ptr(Wtc), ptr(Stc), stream_handle(stream)))
+
+
+def w4_gemm_batched_tc(Wtc, Stc, X, Y, R, M, N, K, g, stream=None):
+    _check(lib().w4_gemm_batched_tc(ptr(Wtc), ptr(Stc), ptr(X), ptr(Y), ptr(R), M, N, K, g, stream_handle(stream)))
 
 
 def bm_moe_workspace_bytes(B, experts, top_k, hidden, ffn):

@@ -53,6 +53,7 @@ bm_status ensure_attributes() {
   BM_CUDA(init_gemv_attributes(), "kernel attributes (dense)");
   BM_CUDA(init_moe_attributes(), "kernel attributes (experts)");
   BM_CUDA(init_misc_attributes(), "kernel attributes (lm_head)");
+  BM_CUDA(init_tc_attributes(), "kernel attributes (tensor-core projections)");
   g_attr_devices.insert(dev);
   return BM_OK;
 }
@@ -142,6 +143,7 @@ DevCheck chk_of(bm_engine* e) { return DevCheck{e->d_err}; }
 cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark = Marker()) {
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim;
+  const bool tc = e->family == BM_POLICY_TC;
   cudaError_t err;
   int n = 0;
   if ((err = launch_embed(e->embed, c.vocab, H, e->d_tokens, e->x, B, chk_of(e), s)) != cudaSuccess) return err;
@@ -149,9 +151,18 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
   ++n;
   for (int l = 0; l < c.layers; ++l) {
     const LayerW& w = e->L[l];
-    GemvArgs g1{w.wqkv, w.wqkv_s, e->x, H, nullptr, 0, e->qkv, e->qkv_rows, B, e->qkv_rows, H, c.group,
-                1, w.has_attn_norm ? w.attn_norm_buf : nullptr, c.rms_eps};
-    if ((err = launch_w4_gemv(g1, s)) != cudaSuccess) return err;
+    const bf16* attn_nw = w.has_attn_norm ? w.attn_norm_buf : nullptr;
+    if (tc) {
+      TcArgs t1{};
+      t1.W = w.wqkv; t1.S = w.wqkv_s; t1.rows = e->qkv_rows; t1.K = H; t1.g = c.group;
+      t1.X = e->x; t1.ldx = H; t1.ntok = B; t1.do_norm = 1; t1.norm_w = attn_nw; t1.eps = c.rms_eps;
+      t1.Y = e->qkv; t1.ldy = e->qkv_rows; t1.err = e->d_err;
+      if ((err = launch_w4_tc_dense(t1, s)) != cudaSuccess) return err;
+    } else {
+      GemvArgs g1{w.wqkv, w.wqkv_s, e->x, H, nullptr, 0, e->qkv, e->qkv_rows, B, e->qkv_rows, H, c.group,
+                  1, attn_nw, c.rms_eps};
+      if ((err = launch_w4_gemv(g1, s)) != cudaSuccess) return err;
+    }
     mark(KT_QKV);
     ++n;
     if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
@@ -162,15 +173,44 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
     if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
                                 &n, mark)) != cudaSuccess)
       return err;
-    GemvArgs g2{w.wo, w.wo_s, e->attn, qd, e->x, H, e->h, H, B, H, qd, c.group, 0, nullptr, c.rms_eps};
-    if ((err = launch_w4_gemv(g2, s)) != cudaSuccess) return err;
+    if (tc) {
+      TcArgs t2{};
+      t2.W = w.wo; t2.S = w.wo_s; t2.rows = H; t2.K = qd; t2.g = c.group;
+      t2.X = e->attn; t2.ldx = qd; t2.ntok = B; t2.Res = e->x; t2.ldr = H; t2.Y = e->h; t2.ldy = H;
+      t2.err = e->d_err;
+      if ((err = launch_w4_tc_dense(t2, s)) != cudaSuccess) return err;
+    } else {
+      GemvArgs g2{w.wo, w.wo_s, e->attn, qd, e->x, H, e->h, H, B, H, qd, c.group, 0, nullptr, c.rms_eps};
+      if ((err = launch_w4_gemv(g2, s)) != cudaSuccess) return err;
+    }
     mark(KT_OPROJ);
     ++n;
     MoeArgs ma{B, c.experts, c.top_k, H, c.ffn, c.group, c.renorm_topk,
                w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
                e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l};
     const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, c.ffn);
-    if ((err = launch_moe(ma, mb, s, &n, mark)) != cudaSuccess) return err;
+    if (tc) {
+      if ((err = launch_moe_route(ma, mb, s, mark)) != cudaSuccess) return err;
+      const int max_u = B * c.top_k < c.experts ? B * c.top_k : c.experts;
+      TcArgs t3{};
+      t3.W = w.wg; t3.S = w.wg_s; t3.rows = 2 * c.ffn; t3.K = H; t3.g = c.group; t3.X = mb.xn; t3.ldx = H;
+      t3.n_active = mb.n_active; t3.active_e = mb.active_e; t3.active_off = mb.active_off;
+      t3.pair_token = mb.pair_token; t3.w_expert_stride = (size_t)2 * c.ffn * H / 2;
+      t3.s_expert_stride = (size_t)2 * c.ffn * (H / c.group); t3.act = mb.act; t3.F = c.ffn; t3.err = e->d_err;
+      if ((err = launch_w4_tc_gateup(t3, max_u, B, s)) != cudaSuccess) return err;
+      mark(KT_GATEUP);
+      TcArgs t4{};
+      t4.W = w.wd; t4.S = w.wd_s; t4.rows = H; t4.K = c.ffn; t4.g = c.group; t4.X = mb.act; t4.ldx = c.ffn;
+      t4.n_active = mb.n_active; t4.active_e = mb.active_e; t4.active_off = mb.active_off;
+      t4.pair_token = mb.pair_token; t4.w_expert_stride = (size_t)H * c.ffn / 2;
+      t4.s_expert_stride = (size_t)H * (c.ffn / c.group); t4.out = mb.out; t4.H = H; t4.err = e->d_err;
+      if ((err = launch_w4_tc_down(t4, max_u, B, s)) != cudaSuccess) return err;
+      mark(KT_DOWN);
+      if ((err = launch_moe_combine(ma, mb, s, mark)) != cudaSuccess) return err;
+      n += 5;
+    } else {
+      if ((err = launch_moe(ma, mb, s, &n, mark)) != cudaSuccess) return err;
+    }
   }
   if ((err = launch_lm_head(e->lm_head, c.vocab, H, e->x, e->has_final_norm ? e->final_norm_buf : nullptr,
                             c.rms_eps, e->logits, B, s)) != cudaSuccess)
@@ -222,6 +262,12 @@ void algo_cost(const bm_config& c, int qkv_rows, int tag, int B, double U, doubl
   *flops = f;
 }
 
+bool tc_shapes_ok(const bm_config& c) {
+  const int qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim, qd = c.q_heads * c.head_dim;
+  return tc_supports(qkv_rows, c.hidden, c.group) && tc_supports(c.hidden, qd, c.group) &&
+         tc_supports(2 * c.ffn, c.hidden, c.group) && tc_supports(c.hidden, c.ffn, c.group);
+}
+
 bm_status check_config(const bm_config& c) {
   auto bad = [](const std::string& m) { return set_error(BM_ERR_INVALID_ARG, "bm_engine_create: " + m); };
   if (c.hidden <= 0 || c.hidden % 32 != 0) return bad("hidden must be a positive multiple of 32");
@@ -241,9 +287,10 @@ bm_status check_config(const bm_config& c) {
   if (!(c.rope_base > 0.f) || !(c.rms_eps >= 0.f)) return bad("rope_base > 0 and rms_eps >= 0 required");
   if (!simt_supports_k(c.hidden) || !simt_supports_k(c.ffn) || !simt_supports_k(c.q_heads * c.head_dim))
     return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: a reduction length has no kernel shape in this build");
-  if (c.kernel_policy == BM_POLICY_TC)
-    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: the tensor-core family is not available in this build");
   if (c.kernel_policy < 0 || c.kernel_policy > 2) return bad("unknown kernel_policy");
+  if (c.kernel_policy == BM_POLICY_TC && !tc_shapes_ok(c))
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: shapes outside the tensor-core family (rows must be "
+                                         "multiples of 128, reduction lengths multiples of 64 up to 4096)");
   return BM_OK;
 }
 
@@ -291,7 +338,9 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   std::unique_ptr<bm_engine, void (*)(bm_engine*)> guard(e, free_engine);
   const bm_config& c = e->cfg;
   cudaGetDevice(&e->device);
-  e->family = BM_POLICY_SIMT;
+  // The family is fixed for the engine's life, never chosen per step, so a
+  // stream's bytes never depend on the batch it is decoded in.
+  e->family = (c.kernel_policy == BM_POLICY_SIMT || !tc_shapes_ok(c)) ? BM_POLICY_SIMT : BM_POLICY_TC;
   e->qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim;
   const int H = c.hidden, E = c.experts, F = c.ffn, g = c.group, qd = c.q_heads * c.head_dim;
   const size_t S = c.max_streams;
@@ -308,10 +357,12 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
     p[2] = take((size_t)H * qd / 2);
     p[3] = take((size_t)H * (qd / g) * 2);
     p[4] = take((size_t)E * H * 4);
-    p[5] = take((size_t)E * F * H / 2);
-    p[6] = take((size_t)E * F * (H / g) * 2);
-    p[7] = take((size_t)E * F * H / 2);
-    p[8] = take((size_t)E * F * (H / g) * 2);
+    // gate and up banks share one region: [wg | wu] (CUDA-core family) or
+    // one row-interleaved bank of 2F rows per expert (tensor-core family)
+    p[5] = take((size_t)E * 2 * F * H / 2);
+    p[6] = take((size_t)E * 2 * F * (H / g) * 2);
+    p[7] = take(0);
+    p[8] = take(0);
     p[9] = take((size_t)E * H * F / 2);
     p[10] = take((size_t)E * H * (F / g) * 2);
     p[11] = take((size_t)H * 2);
@@ -329,7 +380,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
     w.wo = reinterpret_cast<uint8_t*>(wb + p[2].off);   w.wo_s = reinterpret_cast<__half*>(wb + p[3].off);
     w.wr = reinterpret_cast<float*>(wb + p[4].off);
     w.wg = reinterpret_cast<uint8_t*>(wb + p[5].off);   w.wg_s = reinterpret_cast<__half*>(wb + p[6].off);
-    w.wu = reinterpret_cast<uint8_t*>(wb + p[7].off);   w.wu_s = reinterpret_cast<__half*>(wb + p[8].off);
+    w.wu = w.wg + (size_t)E * F * H / 2;                w.wu_s = w.wg_s + (size_t)E * F * (H / g);
     w.wd = reinterpret_cast<uint8_t*>(wb + p[9].off);   w.wd_s = reinterpret_cast<__half*>(wb + p[10].off);
     w.attn_norm_buf = reinterpret_cast<bf16*>(wb + p[11].off);
     w.ffn_norm_buf = reinterpret_cast<bf16*>(wb + p[12].off);
@@ -428,17 +479,32 @@ bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w
   auto cp = [&](void* dst, const void* src, size_t bytes) {
     return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s);
   };
-  BM_CUDA(cp(d.wqkv, w->wqkv, (size_t)e->qkv_rows * H / 2), "set_layer wqkv");
-  BM_CUDA(cp(d.wqkv_s, w->wqkv_s, (size_t)e->qkv_rows * (H / g) * 2), "set_layer wqkv scales");
-  BM_CUDA(cp(d.wo, w->wo, (size_t)H * qd / 2), "set_layer wo");
-  BM_CUDA(cp(d.wo_s, w->wo_s, (size_t)H * (qd / g) * 2), "set_layer wo scales");
-  BM_CUDA(cp(d.wr, w->wr, (size_t)E * H * 4), "set_layer router");
-  BM_CUDA(cp(d.wg, w->wg, (size_t)E * F * H / 2), "set_layer wg");
-  BM_CUDA(cp(d.wg_s, w->wg_s, (size_t)E * F * (H / g) * 2), "set_layer wg scales");
-  BM_CUDA(cp(d.wu, w->wu, (size_t)E * F * H / 2), "set_layer wu");
-  BM_CUDA(cp(d.wu_s, w->wu_s, (size_t)E * F * (H / g) * 2), "set_layer wu scales");
-  BM_CUDA(cp(d.wd, w->wd, (size_t)E * H * F / 2), "set_layer wd");
-  BM_CUDA(cp(d.wd_s, w->wd_s, (size_t)E * H * (F / g) * 2), "set_layer wd scales");
+  if (e->family == BM_POLICY_TC) {
+    // repack into the tensor-core layout; the gate and up banks interleave
+    // row by row (row 2f = gate f, row 2f+1 = up f) so a TMEM lane pair holds
+    // both halves of one SiLU(g)*u
+    auto h = [](const uint16_t* p) { return reinterpret_cast<const __half*>(p); };
+    BM_CUDA(launch_repack_tc(w->wqkv, h(w->wqkv_s), nullptr, nullptr, e->qkv_rows, H, g, d.wqkv, d.wqkv_s, s),
+            "set_layer wqkv repack");
+    BM_CUDA(launch_repack_tc(w->wo, h(w->wo_s), nullptr, nullptr, H, qd, g, d.wo, d.wo_s, s), "set_layer wo repack");
+    BM_CUDA(launch_repack_tc(w->wg, h(w->wg_s), w->wu, h(w->wu_s), 2 * E * F, H, g, d.wg, d.wg_s, s),
+            "set_layer gate/up repack");
+    BM_CUDA(launch_repack_tc(w->wd, h(w->wd_s), nullptr, nullptr, E * H, F, g, d.wd, d.wd_s, s),
+            "set_layer down repack");
+    BM_CUDA(cp(d.wr, w->wr, (size_t)E * H * 4), "set_layer router");
+  } else {
+    BM_CUDA(cp(d.wqkv, w->wqkv, (size_t)e->qkv_rows * H / 2), "set_layer wqkv");
+    BM_CUDA(cp(d.wqkv_s, w->wqkv_s, (size_t)e->qkv_rows * (H / g) * 2), "set_layer wqkv scales");
+    BM_CUDA(cp(d.wo, w->wo, (size_t)H * qd / 2), "set_layer wo");
+    BM_CUDA(cp(d.wo_s, w->wo_s, (size_t)H * (qd / g) * 2), "set_layer wo scales");
+    BM_CUDA(cp(d.wr, w->wr, (size_t)E * H * 4), "set_layer router");
+    BM_CUDA(cp(d.wg, w->wg, (size_t)E * F * H / 2), "set_layer wg");
+    BM_CUDA(cp(d.wg_s, w->wg_s, (size_t)E * F * (H / g) * 2), "set_layer wg scales");
+    BM_CUDA(cp(d.wu, w->wu, (size_t)E * F * H / 2), "set_layer wu");
+    BM_CUDA(cp(d.wu_s, w->wu_s, (size_t)E * F * (H / g) * 2), "set_layer wu scales");
+    BM_CUDA(cp(d.wd, w->wd, (size_t)E * H * F / 2), "set_layer wd");
+    BM_CUDA(cp(d.wd_s, w->wd_s, (size_t)E * H * (F / g) * 2), "set_layer wd scales");
+  }
   d.has_attn_norm = w->attn_norm != nullptr;
   d.has_ffn_norm = w->ffn_norm != nullptr;
   if (w->attn_norm) BM_CUDA(cp(d.attn_norm_buf, w->attn_norm, (size_t)H * 2), "set_layer attn norm");
@@ -784,6 +850,34 @@ bm_status w4_gemm_batched(const uint8_t* W, const uint16_t* S, const uint16_t* X
   GemvArgs a{W, reinterpret_cast<const __half*>(S), reinterpret_cast<const bf16*>(X), K,
              reinterpret_cast<const bf16*>(R), N, reinterpret_cast<bf16*>(Y), N, M, N, K, g, 0, nullptr, 0.f};
   BM_CUDA(launch_w4_gemv(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched launch");
+  return bm::ok();
+}
+
+bm_status bm_w4_repack_tc(const uint8_t* W, const uint16_t* S, int N, int K, int g, uint8_t* Wtc, uint16_t* Stc,
+                          void* stream) {
+  if (!W || !S || !Wtc || !Stc) return set_error(BM_ERR_INVALID_ARG, "bm_w4_repack_tc: null pointer");
+  if (!tc_supports(N, K, g))
+    return set_error(BM_ERR_INVALID_ARG, "bm_w4_repack_tc: need N % 128 == 0, K % 64 == 0, K <= 4096, "
+                                         "g in {32, 64, 128}, K % g == 0");
+  BM_CUDA(launch_repack_tc(W, reinterpret_cast<const __half*>(S), nullptr, nullptr, N, K, g, Wtc,
+                           reinterpret_cast<__half*>(Stc), static_cast<cudaStream_t>(stream)),
+          "bm_w4_repack_tc launch");
+  return bm::ok();
+}
+
+bm_status w4_gemm_batched_tc(const uint8_t* Wtc, const uint16_t* Stc, const uint16_t* X, uint16_t* Y,
+                             const uint16_t* R, int M, int N, int K, int g, void* stream) {
+  if (!Wtc || !Stc || !X || !Y) return set_error(BM_ERR_INVALID_ARG, "w4_gemm_batched_tc: null pointer");
+  if (M < 1 || !tc_supports(N, K, g))
+    return set_error(BM_ERR_INVALID_ARG, "w4_gemm_batched_tc: need M >= 1, N % 128 == 0, K % 64 == 0, "
+                                         "K <= 4096, g in {32, 64, 128}, K % g == 0");
+  bm_status st = ensure_attributes();
+  if (st != BM_OK) return st;
+  TcArgs a{};
+  a.W = Wtc; a.S = reinterpret_cast<const __half*>(Stc); a.rows = N; a.K = K; a.g = g;
+  a.X = reinterpret_cast<const bf16*>(X); a.ldx = K; a.ntok = M;
+  a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
+  BM_CUDA(launch_w4_tc_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched_tc launch");
   return bm::ok();
 }
 

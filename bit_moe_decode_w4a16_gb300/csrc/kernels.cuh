@@ -76,6 +76,47 @@ struct MoeArgs {
 // Router logits + top-k + sort, gate/up, down, combine: 5 launches.
 cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches,
                        const Marker& mark = Marker());
+// The routing half (router logits, top-k + sort: 2 launches) and the
+// combine (1 launch) on their own, for the tensor-core expert path.
+cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
+cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
+
+// ---------------------------------------------------------------- tensor-core W4A16
+struct TcArgs {
+  const uint8_t* W;          // tc layout (whole bank for experts)
+  const __half* S;           // [tiles][K/g][128]
+  int rows, K, g;            // rows of one matrix (one expert for the banks)
+  const bf16* X;             // activations: dense rows / expert input rows / act rows
+  int ldx;
+  int ntok;                  // dense: number of activation rows
+  int do_norm;               // dense: RMSNorm of X fused into staging
+  const bf16* norm_w;
+  float eps;
+  const bf16* Res;           // dense: residual [ntok][ldr] or null
+  int ldr;
+  bf16* Y;                   // dense output [ntok][ldy]
+  int ldy;
+  const int32_t* n_active;   // experts: routing work list
+  const int32_t* active_e;
+  const int32_t* active_off;
+  const int32_t* pair_token;
+  size_t w_expert_stride;    // bytes of one expert's matrix
+  size_t s_expert_stride;    // halves of one expert's scales
+  bf16* act;                 // gate/up output [pairs][F]
+  int F;
+  float* out;                // down output [pairs][H]
+  int H;
+  int* err;                  // device error flag or null
+};
+bool tc_supports(int rows, int K, int g);
+// Canonical [rows][K/2] (+ scales) -> tc layout; with W2/S2 the output rows
+// interleave (row 2i from W, 2i+1 from W2).
+cudaError_t launch_repack_tc(const uint8_t* W, const __half* S, const uint8_t* W2, const __half* S2, int rows,
+                             int K, int g, uint8_t* Wtc, __half* Stc, cudaStream_t st);
+cudaError_t launch_w4_tc_dense(const TcArgs& a, cudaStream_t st);
+cudaError_t launch_w4_tc_gateup(const TcArgs& a, int max_u, int max_tok, cudaStream_t st);
+cudaError_t launch_w4_tc_down(const TcArgs& a, int max_u, int max_tok, cudaStream_t st);
+cudaError_t init_tc_attributes();
 
 // ---------------------------------------------------------------- attention
 struct AttnArena {

@@ -360,6 +360,26 @@ cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int*
   return cudaSuccess;
 }
 
+cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark) {
+  if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
+  const int nblk = (a.E + kRouterWarps - 1) / kRouterWarps;
+  k_router<<<nblk, 256, sizeof(float) * a.B, st>>>(a, b);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  mark(KT_ROUTER);
+  k_topk_sort<<<1, 1024, 0, st>>>(a, b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  mark(KT_TOPK_SORT);
+  return cudaSuccess;
+}
+
+cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark) {
+  k_combine<<<a.B, 256, 0, st>>>(a, b);
+  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) mark(KT_COMBINE);
+  return err;
+}
+
 cudaError_t init_moe_attributes() {
   cudaError_t e = cudaSuccess;
 #define BM_CASE(L, C) if (e == cudaSuccess) e = set_attr_pair<L, C>();

@@ -244,6 +244,25 @@ bm_status kv_slot_read(bm_engine* e, int layer, int slot, int count, uint16_t* K
 bm_status w4_gemm_batched(const uint8_t* W, const uint16_t* S, const uint16_t* X, uint16_t* Y,
                           const uint16_t* R, int M, int N, int K, int g, void* stream);
 
+/* Repack canonical int4 weights W [N][K/2] and scales S [N][K/g] (DEVICE)
+ * into the tensor-core layout consumed by w4_gemm_batched_tc: Wtc (N*K/2
+ * bytes) and Stc (N*K/g fp16), both DEVICE, caller-owned.  The layout: for
+ * each tile of 128 rows and each 64-wide K stage, two 32-wide halves of 128
+ * rows x 16 bytes; inside each 32-bit word the codes are ordered
+ * (k0 k2 k4 k6 k1 k3 k5 k7); scales [N/128][K/g][128].  Errors:
+ * BM_ERR_INVALID_ARG unless N % 128 == 0, K % 64 == 0, K <= 4096, g in
+ * {32, 64, 128}, K % g == 0. */
+bm_status bm_w4_repack_tc(const uint8_t* W, const uint16_t* S, int N, int K, int g, uint8_t* Wtc,
+                          uint16_t* Stc, void* stream);
+
+/* The batched W4A16 GEMM of w4_gemm_batched on the tensor cores (tcgen05,
+ * fp16 operands, fp32 accumulation in tensor memory), with weights in the
+ * layout of bm_w4_repack_tc.  Each weight is dequantized to fp16 as
+ * fp16((q - 8) * scale) before the MMA.  Weight bytes are read from HBM once
+ * per group of 16 rows of X.  Shapes as bm_w4_repack_tc, M >= 1. */
+bm_status w4_gemm_batched_tc(const uint8_t* Wtc, const uint16_t* Stc, const uint16_t* X, uint16_t* Y,
+                             const uint16_t* R, int M, int N, int K, int g, void* stream);
+
 /* Bytes of DEVICE workspace moe_grouped_w4 needs for B tokens. */
 size_t bm_moe_workspace_bytes(int B, int experts, int top_k, int hidden, int ffn);
 

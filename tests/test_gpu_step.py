@@ -44,11 +44,17 @@ def _prefix_np(stream, length, layers):
     return k.double().numpy(), v.double().numpy()
 
 
+SIMT, TC = 1, 2
+FAMILIES = pytest.mark.parametrize("policy", [SIMT, TC], ids=["simt", "tc"])
+
+
+@FAMILIES
 @pytest.mark.parametrize("layers", [1, 2])
-def test_tiny_layer_step_matches_oracle_and_solo(bm, layers):
+def test_tiny_layer_step_matches_oracle_and_solo(bm, layers, policy):
     lens = CFG["lens"]                       # 17 and 40
     toks = [int(t) for t in synth.tokens(NAME, "step", 2, CFG["vocab"])]
-    e = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, gen_device="cpu")
+    e = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, policy=policy, gen_device="cpu")
+    assert bm.bm_engine_kernel_family(e) == policy
     try:
         slots = [seed_stream(e, NAME, CFG, i, L, layers, gen_device="cpu") for i, L in enumerate(lens)]
         nxt, logits = _step(bm, e, slots, toks, CFG["vocab"])
@@ -80,10 +86,11 @@ def test_tiny_layer_step_matches_oracle_and_solo(bm, layers):
         bm.bm_engine_destroy(e)
 
 
-def test_graph_count_paths_and_determinism(bm):
+@FAMILIES
+def test_graph_count_paths_and_determinism(bm, policy):
     layers = 1
-    e = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, gen_device="cpu")
-    e2 = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, use_graph=0, gen_device="cpu")
+    e = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, policy=policy, gen_device="cpu")
+    e2 = build_engine(NAME, CFG, layers, max_streams=4, ctx_cap=128, policy=policy, use_graph=0, gen_device="cpu")
     try:
         s1 = [seed_stream(e, NAME, CFG, i, 10 + i, layers, gen_device="cpu") for i in range(3)]
         s2 = [seed_stream(e2, NAME, CFG, i, 10 + i, layers, gen_device="cpu") for i in range(3)]
@@ -136,10 +143,11 @@ def _schedule_run(bm, e, events, layers):
     return toks, rows
 
 
-def test_ragged_schedule_solo_batched_bytes_and_oracle(bm):
+@FAMILIES
+def test_ragged_schedule_solo_batched_bytes_and_oracle(bm, policy):
     layers = 2
     events = synth.schedule(seed=7, steps=14, max_streams=6, ctx_cap=48, min_len=1, max_batch=4)
-    e = build_engine(NAME, CFG, layers, max_streams=6, ctx_cap=48, gen_device="cpu")
+    e = build_engine(NAME, CFG, layers, max_streams=6, ctx_cap=48, policy=policy, gen_device="cpu")
     try:
         toks, rows = _schedule_run(bm, e, events, layers)
         # each stream decoded alone, through the same engine, gives the same bytes
@@ -178,13 +186,14 @@ def test_ragged_schedule_solo_batched_bytes_and_oracle(bm):
         bm.bm_engine_destroy(e)
 
 
-def test_step_at_full_width(bm):
+@FAMILIES
+def test_step_at_full_width(bm, policy):
     # Two layers of the 30B-class shape (hidden 2048, 32/4 heads of 128,
     # 128 experts top-8, FFN 768, group 64), a bf16 head of vocab 4096.
     cfg = dict(synth.CONFIGS["full_model"])
     cfg["vocab"] = 4096
     layers = 2
-    e = build_engine("full_width", cfg, layers, max_streams=4, ctx_cap=256, gen_device="cpu")
+    e = build_engine("full_width", cfg, layers, max_streams=4, ctx_cap=256, policy=policy, gen_device="cpu")
     try:
         lens = [33, 200, 1]
         slots = []

@@ -2,23 +2,26 @@
 // expert gate/up and down GEMMs.
 //
 // One CTA of 128 threads owns a tile of 128 weight rows and up to 16 tokens
-// (M = 128 weight rows x N = 16 tokens, the swap that puts the large
-// dimension on the MMA's M).  Thread t streams the packed int4 of row t,
-// dequantizes it in registers to fp16 ((q - 8) * scale) and writes it with
-// tcgen05.st into TMEM lane t, where it is the MMA's A operand; the tokens'
-// activations (fp16) sit in shared memory as the B operand; the fp32
-// accumulator lives in TMEM.  Three 64-column A stages rotate through TMEM:
-// the producers wait on a stage's mbarrier (arrived by tcgen05.commit when
-// the MMAs that read it finish) before overwriting it.  Every packed weight
-// byte is read from HBM once per token group of 16; K is walked in a fixed
-// order, so a row's result depends only on its own activations.
+// (M = 128 weight rows x N = 16 tokens: the large dimension on the MMA's M).
+// Thread t streams the packed int4 of row t, turns each code into the exact
+// fp16 integer q - 8 in registers and writes it with tcgen05.st into TMEM
+// lane t, where it is the MMA's A operand; the tokens' activations (fp16) sit
+// in shared memory as the B operand.  Each 64-wide K stage accumulates into
+// its own fp32 TMEM region (one per 32-wide half, so every region covers a
+// single int4 group when g >= 32): the products q * x are exact in fp32, and
+// the threads apply the fp32 group scale when they drain the region, so the
+// weights are never rounded.  Three stages rotate through TMEM: before
+// rewriting a stage's columns the producers wait on its mbarrier (arrived by
+// tcgen05.commit when the MMAs that read it finish) and drain its
+// accumulator.  A row's result is the sum over stages in ascending K of
+// scale * (exact group sum), whatever the other tokens of the tile are.
 //
 // Weight layout ("tc layout", written once by the repack kernel): for tile
 // t, stage s (64 K) and half h (32 K): 128 rows x 16 bytes, row-contiguous,
 // so a warp's loads of one half are 512 contiguous bytes.  Inside each 32-bit
 // word the 8 codes are ordered (k0 k2 k4 k6 k1 k3 k5 k7), so one
-// (w >> 4i) & 0x000F000F | 0x64006400 yields the fp16 pair (1024 + q_2i,
-// 1024 + q_2i+1) of one TMEM column.  Scales: [tile][K/g][128 rows] fp16.
+// (w >> 4i) & 0x000F000F | 0x64006400 yields the fp16 pair (1024 + u_2i,
+// 1024 + u_2i+1) of one TMEM column.  Scales: [tile][K/g][128 rows] fp16.
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
 
@@ -28,29 +31,28 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kTokens = 16;            // MMA N
-constexpr int kStageK = 64;            // K per A stage (32 TMEM columns)
-constexpr int kStages = 3;             // A stages in TMEM
-constexpr int kDCol = kStages * 32;    // accumulator column
-constexpr uint32_t kTmemCols = 128;
-constexpr int kPrefetch = 4;           // stages of weights in flight per thread
+constexpr int kStageK = 64;            // K per stage: A 32 columns, D 2 x 16 columns
+constexpr int kStages = 3;             // stages in TMEM
+constexpr int kSlotCols = 64;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kPrefetch = 6;           // stages of weights in flight per thread
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w, int i, __half2 s2) {
+// (u_lo, u_hi) codes of one TMEM column -> the fp16 pair (u_lo - 8, u_hi - 8), exact.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w, int i) {
   const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;   // (1024 + u_lo, 1024 + u_hi)
   __half2 h = *reinterpret_cast<const __half2*>(&v);
-  h = __hsub2(h, __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));   // - 1032: q = u - 8
-  h = __hmul2(h, s2);
+  h = __hsub2(h, __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));   // - 1032
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // 16 packed bytes (32 codes) -> 16 TMEM columns of fp16 pairs.
-__device__ __forceinline__ void dq16(const uint4 w, __half s, uint32_t* out) {
-  const __half2 s2 = __halves2half2(s, s);
+__device__ __forceinline__ void dq16(const uint4 w, uint32_t* out) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int q = 0; q < 4; ++q)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) out[q * 4 + i] = dq_pair(ws[q], i, s2);
+    for (int i = 0; i < 4; ++i) out[q * 4 + i] = dq_pair(ws[q], i);
 }
 
 enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2 };
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
   __shared__ __align__(8) uint64_t mbar[kStages + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ float rinv_s[kTokens];
+  __shared__ float2 scale_s[kStages][kThreads];   // group scales of the stage in each slot
   __shared__ int abort_s;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -117,8 +120,7 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     uint4 packed = make_uint4(0, 0, 0, 0);
     if (r < ntok) {
       const bf16* x;
-      if (MODE == TC_DENSE) x = a.X + (size_t)(row0 + r) * a.ldx;
-      else if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
+      if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
       else x = a.X + (size_t)(row0 + r) * a.ldx;
       const uint4 raw = *reinterpret_cast<const uint4*>(x + j * 8);
       const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -162,6 +164,21 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     sc[0] = st_[(size_t)((s * kStageK) / a.g) * 128];
     sc[1] = st_[(size_t)((s * kStageK + 32) / a.g) * 128];
   };
+  float acc[kTokens];
+#pragma unroll
+  for (int j = 0; j < kTokens; ++j) acc[j] = 0.f;
+  // acc += scale_lo * D_lo + scale_hi * D_hi of the stage held in `slot`
+  auto drain = [&](int slot) {
+    uint32_t d[32];
+    tc::tmem_ld32(tmem + lane_base + slot * kSlotCols + 32, d);
+    tc::tmem_wait_ld();
+    const float2 sc = scale_s[slot][t];
+#pragma unroll
+    for (int j = 0; j < kTokens; ++j) {
+      acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
+      acc[j] = fmaf(sc.y, __uint_as_float(d[16 + j]), acc[j]);
+    }
+  };
 #pragma unroll
   for (int p = 0; p < kPrefetch; ++p)
     if (p < nst) load(p, ring[p], sring[p]);
@@ -172,20 +189,23 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
       const int s = s0 + p;
       if (s < nst) {
         const uint4 w0 = ring[p][0], w1 = ring[p][1];
-        const __half sc0 = sring[p][0], sc1 = sring[p][1];
+        const float2 sc = make_float2(__half2float(sring[p][0]), __half2float(sring[p][1]));
         if (s + kPrefetch < nst) load(s + kPrefetch, ring[p], sring[p]);
         uint32_t v[32];
-        dq16(w0, sc0, v);
-        dq16(w1, sc1, v + 16);
+        dq16(w0, v);
+        dq16(w1, v + 16);
         const int slot = s % kStages;
-        if (s >= kStages && !abort_s) {
-          if (!tc::mbar_wait(tc::smem_u32(&mbar[slot]), (uint32_t)((s / kStages) - 1) & 1u, kWaitLimit)) {
+        if (s >= kStages) {
+          if (!abort_s &&
+              !tc::mbar_wait(tc::smem_u32(&mbar[slot]), (uint32_t)((s / kStages) - 1) & 1u, kWaitLimit)) {
             abort_s = 1;
             ok = false;
           }
           tc::fence_after_sync();
+          drain(slot);   // stage s - kStages, in ascending order
         }
-        tc::tmem_st32(tmem + lane_base + slot * 32, v);
+        scale_s[slot][t] = sc;
+        tc::tmem_st32(tmem + lane_base + slot * kSlotCols, v);
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncthreads();
@@ -194,7 +214,8 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(s * 4 + q) * 256u, 128u, sbo);
-            tc::mma_f16_tmem_a(tmem + kDCol, tmem + slot * 32 + q * 8, bd, idesc, (s > 0 || q > 0) ? 1u : 0u);
+            const uint32_t dcol = slot * kSlotCols + 32 + (q >> 1) * 16;
+            tc::mma_f16_tmem_a(tmem + dcol, tmem + slot * kSlotCols + q * 8, bd, idesc, (uint32_t)(q & 1));
           }
           tc::mma_commit(tc::smem_u32(&mbar[slot]));
           if (s == nst - 1) tc::mma_commit(tc::smem_u32(&mbar[kStages]));
@@ -203,16 +224,11 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     }
   }
 
-  // ---- epilogue: accumulator lane t = weight row t, columns = tokens
+  // ---- drain the last stages, then the epilogue: lane t = weight row t
   if (!tc::mbar_wait(tc::smem_u32(&mbar[kStages]), 0u, kWaitLimit)) ok = false;
   tc::fence_after_sync();
-  uint32_t acc_u[16];
-  tc::tmem_ld16(tmem + lane_base + kDCol, acc_u);
-  tc::tmem_wait_ld();
+  for (int s = (nst > kStages ? nst - kStages : 0); s < nst; ++s) drain(s % kStages);
   if (!ok && a.err) atomicExch(a.err, 4);
-  float acc[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(acc_u[j]);
   if (MODE == TC_DENSE) {
     const size_t n = (size_t)tile * 128 + t;
 #pragma unroll

@@ -20,15 +20,29 @@ def to64(t):
     return np.asarray(t, dtype=np.float64)
 
 
-def assert_close_rows(gpu, ref, max_abs=MAX_ABS, min_cos=MIN_COS, what=""):
+def bf16_ulp(x):
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def assert_close_rows(gpu, ref, max_abs=MAX_ABS, min_cos=MIN_COS, what="", bf16_out=True):
+    """Rows of gpu vs oracle.  For bf16 outputs an element may also differ by
+    one bf16 ulp of the oracle value: both sides round once to bf16 from
+    values that differ only by accumulation order, and a rounding boundary
+    between them flips one ulp (0.031 at |y| in [4, 8))."""
     g, r = to64(gpu), to64(ref)
     assert g.shape == r.shape, (what, g.shape, r.shape)
     g2, r2 = g.reshape(g.shape[0], -1), r.reshape(r.shape[0], -1)
-    err = np.abs(g2 - r2).max(axis=1)
+    diff = np.abs(g2 - r2)
+    allowed = np.maximum(max_abs, bf16_ulp(r2)) if bf16_out else max_abs
+    bad = diff > allowed
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond max(2e-2, 1 bf16 ulp); worst "
+                           f"|diff| {diff[bad].max():.3g} at |y| {np.abs(r2[bad]).max():.3g}")
+    err = diff.max(axis=1)
     num = (g2 * r2).sum(axis=1)
     den = np.linalg.norm(g2, axis=1) * np.linalg.norm(r2, axis=1)
     cos = np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)
-    assert np.all(err <= max_abs), f"{what}: max abs err {err.max():.3g} > {max_abs} (rows {np.argmax(err)})"
     assert np.all(cos >= min_cos), f"{what}: cosine {cos.min():.8f} < {min_cos}"
     return float(err.max()), float(cos.min())
 

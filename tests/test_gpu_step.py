@@ -63,7 +63,7 @@ def test_tiny_layer_step_matches_oracle_and_solo(bm, layers, policy):
         kv = _oracle_kv(ocfg, layers)
         oslots = [kv.seed(*_prefix_np(i, L, layers)) for i, L in enumerate(lens)]
         ref_logits, ref_ids = oracle.model_step(ocfg, ow, kv, oslots, toks)
-        err, _ = assert_close_rows(logits, ref_logits, what=f"tiny step logits, {layers} layer(s)")
+        err, _ = assert_close_rows(logits, ref_logits, what=f"tiny step logits, {layers} layer(s)", bf16_out=False)
         check_greedy(nxt, ref_logits, err)
         # the K/V this step appended at position len matches the oracle's
         for i, s in enumerate(slots):
@@ -179,7 +179,7 @@ def test_ragged_schedule_solo_batched_bytes_and_oracle(bm, policy):
             t = (i * 977 + 13) % CFG["vocab"]
             for k in range(steps[i]):
                 ref, _ = oracle.model_step(ocfg, ow, kv, [s], [t])
-                err, _ = assert_close_rows(rows[i][k][None], ref, what=f"schedule stream {i} step {k}")
+                err, _ = assert_close_rows(rows[i][k][None], ref, what=f"schedule stream {i} step {k}", bf16_out=False)
                 check_greedy([toks[i][k]], ref, err)
                 t = toks[i][k]
     finally:
@@ -210,7 +210,7 @@ def test_step_at_full_width(bm, policy):
             k, v = synth.kv_prefix("full_width", cfg, i, L, layers=layers)
             oslots.append(kv.seed(k.double().numpy(), v.double().numpy()))
         ref, _ = oracle.model_step(ocfg, ow, kv, oslots, toks)
-        err, _ = assert_close_rows(logits, ref, what="full-width 2-layer step")
+        err, _ = assert_close_rows(logits, ref, what="full-width 2-layer step", bf16_out=False)
         check_greedy(nxt, ref, err)
     finally:
         bm.bm_engine_destroy(e)

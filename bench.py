@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--policy", type=int, default=0)
+    ap.add_argument("--prefill", default="decode", choices=["decode", "kv"],
+                    help="decode: prompts through decode_step (teacher-forced); kv: seed synthetic K/V of the "
+                         "same lengths (faster start, for profiler runs)")
     return ap.parse_args()
 
 
@@ -91,11 +94,14 @@ def timed_region(step, sync, dist, steps, warmup, new_event=None, device="cpu"):
     dist.barrier()
     sync()
     if new_event:
+        import torch
         t0, t1 = new_event(), new_event()
+        torch.cuda.nvtx.range_push("timed")
         t0.record()
         for _ in range(steps):
             step()
         t1.record()
+        torch.cuda.nvtx.range_pop()
         sync()
         dt = t0.elapsed_time(t1) / 1e3
     else:
@@ -186,12 +192,21 @@ def build_model(bm, cfg, layers, max_streams, policy):
     return e, time.time() - t
 
 
-def prefill(bm, e, cfg, B, layers):
+def prefill(bm, e, cfg, B, layers, mode="decode"):
     """Join B streams with empty slots and feed their prompts through
-    decode_step, teacher-forced; returns (slots, next device tokens)."""
+    decode_step, teacher-forced; returns (slots, next device tokens).  With
+    mode "kv" the slots are seeded with synthetic K/V of the same lengths."""
     import torch
     import synth
     lens = synth.prompt_lengths(B, cfg["prompt"][0], cfg["prompt"][1], synth.seed_of(WORKLOAD, "prompt_lens"))
+    if mode == "kv":
+        slots = []
+        for i, L in enumerate(lens):
+            k, v = synth.kv_prefix(WORKLOAD, cfg, i, L, layers=layers, device="cuda")
+            slots.append(bm.kv_slot_seed(e, k, v, L))
+        last = synth.tokens(WORKLOAD, "first", B, cfg["vocab"], device="cuda")
+        torch.cuda.synchronize()
+        return slots, last, lens
     prompts = [synth.tokens(WORKLOAD, f"prompt{i}", L, cfg["vocab"]).tolist() for i, L in enumerate(lens)]
     empty = torch.empty((layers, cfg["kv_heads"], 0, cfg["head_dim"]), dtype=torch.bfloat16, device="cuda")
     slots = [bm.kv_slot_seed(e, empty, empty, 0) for _ in range(B)]
@@ -219,7 +234,7 @@ def run_ours(args, dist, world, rank, local):
     cfg = dict(synth.CONFIGS[WORKLOAD])
     B = args.batch
     e, t_build = build_model(bm, cfg, args.layers, cfg["max_streams"], args.policy)
-    slots, last, lens = prefill(bm, e, cfg, B, args.layers)
+    slots, last, lens = prefill(bm, e, cfg, B, args.layers, args.prefill)
     stream = torch.cuda.current_stream()
     cur = last.clone()
     nxt = torch.empty_like(cur)

@@ -98,49 +98,64 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     abort_s = 0;
   }
 
-  // ---- activations -> shared memory, fp16, no-swizzle K-major core matrices
+  // ---- activations -> shared memory, fp16, no-swizzle K-major core matrices.
+  // Warp w stages rows w, w+4, ...; a lane's chunks of a row are loaded
+  // together (up to 16 x 16 bytes in flight) before they are used.
   const int nk8 = K / 8;
   const uint32_t sbo = (uint32_t)nk8 * 128u;   // bytes between the two 8-row groups
-  if (MODE == TC_DENSE && a.do_norm) {
-    for (int r = warp; r < ntok; r += kThreads / 32) {
-      const bf16* x = a.X + (size_t)(row0 + r) * a.ldx;
+  for (int r = warp; r < kTokens; r += kThreads / 32) {
+    unsigned char* rowp = smem + (r >> 3) * sbo + (r & 7) * 16;
+    if (r >= ntok) {
+      for (int j = lane; j < nk8; j += 32) *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const bf16* x;
+    if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
+    else x = a.X + (size_t)(row0 + r) * a.ldx;
+    constexpr int kMaxChunks = 4096 / 8 / 32;   // K <= 4096
+    uint4 raw[kMaxChunks];
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i)
+      if (lane + 32 * i < nk8) raw[i] = *reinterpret_cast<const uint4*>(x + (lane + 32 * i) * 8);
+    float rinv = 1.f;
+    if (MODE == TC_DENSE && a.do_norm) {
       float ss = 0.f;
-      for (int k = lane * 2; k < K; k += 64) {
-        const float v0 = bf2f(x[k]), v1 = bf2f(x[k + 1]);
-        ss = fmaf(v0, v0, ss);
-        ss = fmaf(v1, v1, ss);
+#pragma unroll
+      for (int i = 0; i < kMaxChunks; ++i) {
+        if (lane + 32 * i < nk8) {
+          const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
+            ss = fmaf(v0, v0, ss);
+            ss = fmaf(v1, v1, ss);
+          }
+        }
       }
       ss = warp_sum(ss);
-      if (lane == 0) rinv_s[r] = 1.0f / sqrtf(ss / (float)K + a.eps);
+      rinv = 1.0f / sqrtf(ss / (float)K + a.eps);
     }
-    __syncthreads();
-  }
-  for (int idx = t; idx < kTokens * nk8; idx += kThreads) {
-    const int r = idx / nk8, j = idx - r * nk8;
-    uint4 packed = make_uint4(0, 0, 0, 0);
-    if (r < ntok) {
-      const bf16* x;
-      if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
-      else x = a.X + (size_t)(row0 + r) * a.ldx;
-      const uint4 raw = *reinterpret_cast<const uint4*>(x + j * 8);
-      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t o[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
-        if (MODE == TC_DENSE && a.do_norm) {
-          const float r_ = rinv_s[r];
-          const float w0 = a.norm_w ? bf2f(a.norm_w[j * 8 + 2 * q]) : 1.f;
-          const float w1 = a.norm_w ? bf2f(a.norm_w[j * 8 + 2 * q + 1]) : 1.f;
-          v0 = round_bf16(v0 * r_ * w0);
-          v1 = round_bf16(v1 * r_ * w1);
+    for (int i = 0; i < kMaxChunks; ++i) {
+      const int j = lane + 32 * i;
+      if (j < nk8) {
+        const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
+          if (MODE == TC_DENSE && a.do_norm) {
+            const float w0 = a.norm_w ? bf2f(a.norm_w[j * 8 + 2 * q]) : 1.f;
+            const float w1 = a.norm_w ? bf2f(a.norm_w[j * 8 + 2 * q + 1]) : 1.f;
+            v0 = round_bf16(v0 * rinv * w0);
+            v1 = round_bf16(v1 * rinv * w1);
+          }
+          __half2 h = __floats2half2_rn(v0, v1);
+          o[q] = *reinterpret_cast<uint32_t*>(&h);
         }
-        __half2 h = __floats2half2_rn(v0, v1);
-        o[q] = *reinterpret_cast<uint32_t*>(&h);
+        *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      packed = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    *reinterpret_cast<uint4*>(smem + (r >> 3) * sbo + j * 128 + (r & 7) * 16) = packed;
   }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();

@@ -126,6 +126,8 @@ struct bm_engine {
   int ring_pos = 0;
   cudaEvent_t ev_aux = nullptr;
   int32_t* d_u_log = nullptr;   // [layers] active experts of the last step, per layer
+  float* tc_part = nullptr;     // split-K partial sums of the tensor-core projections
+  int* tc_counters = nullptr;   // split-K arrival counters (zero between launches)
   std::vector<cudaEvent_t> prof_events;
   cudaStream_t cap_stream = nullptr;
   std::map<int, cudaGraphExec_t> graphs;
@@ -138,6 +140,32 @@ namespace bm {
 namespace {
 
 DevCheck chk_of(bm_engine* e) { return DevCheck{e->d_err}; }
+
+// K split of a tensor-core launch of `jobs` (tile, token group, expert) jobs.
+void tc_split(bm_engine* e, TcArgs& t, int jobs) {
+  t.ksplit = tc_pick_ksplit(jobs, t.K / 64);
+  t.part = e->tc_part;
+  t.counters = e->tc_counters;
+}
+
+// Largest (jobs, jobs * ksplit) over the engine's tensor-core launches.
+void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* max_part) {
+  *max_jobs = 0;
+  *max_part = 0;
+  const int H = c.hidden, qd = c.q_heads * c.head_dim;
+  for (int B = 1; B <= c.max_streams; ++B) {
+    const int tg = (B + 15) / 16, max_u = B * c.top_k < c.experts ? B * c.top_k : c.experts;
+    const int jobs[4] = {(qkv_rows / 128) * tg, (H / 128) * tg, (2 * c.ffn / 128) * tg * max_u,
+                         (H / 128) * tg * max_u};
+    const int nst[4] = {H / 64, qd / 64, H / 64, c.ffn / 64};
+    for (int i = 0; i < 4; ++i) {
+      const size_t j = jobs[i];
+      *max_jobs = j > *max_jobs ? j : *max_jobs;
+      const size_t p = tc_part_floats(jobs[i], tc_pick_ksplit(jobs[i], nst[i]));
+      *max_part = p > *max_part ? p : *max_part;
+    }
+  }
+}
 
 // Enqueue one decode step for B streams reading e->d_slots / e->d_tokens.
 cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark = Marker()) {
@@ -157,6 +185,7 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
       t1.W = w.wqkv; t1.S = w.wqkv_s; t1.rows = e->qkv_rows; t1.K = H; t1.g = c.group;
       t1.X = e->x; t1.ldx = H; t1.ntok = B; t1.do_norm = 1; t1.norm_w = attn_nw; t1.eps = c.rms_eps;
       t1.Y = e->qkv; t1.ldy = e->qkv_rows; t1.err = e->d_err;
+      tc_split(e, t1, (e->qkv_rows / 128) * ((B + 15) / 16));
       if ((err = launch_w4_tc_dense(t1, s)) != cudaSuccess) return err;
     } else {
       GemvArgs g1{w.wqkv, w.wqkv_s, e->x, H, nullptr, 0, e->qkv, e->qkv_rows, B, e->qkv_rows, H, c.group,
@@ -178,6 +207,7 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
       t2.W = w.wo; t2.S = w.wo_s; t2.rows = H; t2.K = qd; t2.g = c.group;
       t2.X = e->attn; t2.ldx = qd; t2.ntok = B; t2.Res = e->x; t2.ldr = H; t2.Y = e->h; t2.ldy = H;
       t2.err = e->d_err;
+      tc_split(e, t2, (H / 128) * ((B + 15) / 16));
       if ((err = launch_w4_tc_dense(t2, s)) != cudaSuccess) return err;
     } else {
       GemvArgs g2{w.wo, w.wo_s, e->attn, qd, e->x, H, e->h, H, B, H, qd, c.group, 0, nullptr, c.rms_eps};
@@ -197,6 +227,7 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
       t3.n_active = mb.n_active; t3.active_e = mb.active_e; t3.active_off = mb.active_off;
       t3.pair_token = mb.pair_token; t3.w_expert_stride = (size_t)2 * c.ffn * H / 2;
       t3.s_expert_stride = (size_t)2 * c.ffn * (H / c.group); t3.act = mb.act; t3.F = c.ffn; t3.err = e->d_err;
+      tc_split(e, t3, (2 * c.ffn / 128) * ((B + 15) / 16) * max_u);
       if ((err = launch_w4_tc_gateup(t3, max_u, B, s)) != cudaSuccess) return err;
       mark(KT_GATEUP);
       TcArgs t4{};
@@ -204,6 +235,7 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
       t4.n_active = mb.n_active; t4.active_e = mb.active_e; t4.active_off = mb.active_off;
       t4.pair_token = mb.pair_token; t4.w_expert_stride = (size_t)H * c.ffn / 2;
       t4.s_expert_stride = (size_t)H * (c.ffn / c.group); t4.out = mb.out; t4.H = H; t4.err = e->d_err;
+      tc_split(e, t4, (H / 128) * ((B + 15) / 16) * max_u);
       if ((err = launch_w4_tc_down(t4, max_u, B, s)) != cudaSuccess) return err;
       mark(KT_DOWN);
       if ((err = launch_moe_combine(ma, mb, s, mark)) != cudaSuccess) return err;
@@ -416,6 +448,9 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
              s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
              s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
              s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4);
+  size_t tc_jobs = 0, tc_floats = 0;
+  if (e->family == BM_POLICY_TC) tc_workspace(c, e->qkv_rows, &tc_jobs, &tc_floats);
+  const Part s_tcp = take(tc_floats * 4), s_tcc = take(tc_jobs * 4);
   e->scratch_bytes = off;
   BM_CUDA(cudaMalloc(&e->scratch, e->scratch_bytes), "scratch allocation");
   char* sb = static_cast<char*>(e->scratch);
@@ -433,6 +468,8 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   e->d_slots_aux = reinterpret_cast<int32_t*>(sb + s_sa.off);
   e->d_err = reinterpret_cast<int*>(sb + s_err.off);
   e->d_u_log = reinterpret_cast<int32_t*>(sb + s_ulog.off);
+  e->tc_part = tc_floats ? reinterpret_cast<float*>(sb + s_tcp.off) : nullptr;
+  e->tc_counters = tc_jobs ? reinterpret_cast<int*>(sb + s_tcc.off) : nullptr;
   BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");
 
   BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * (2 * bm_engine::kStageRing + 1) * S),
@@ -877,6 +914,7 @@ bm_status w4_gemm_batched_tc(const uint8_t* Wtc, const uint16_t* Stc, const uint
   a.W = Wtc; a.S = reinterpret_cast<const __half*>(Stc); a.rows = N; a.K = K; a.g = g;
   a.X = reinterpret_cast<const bf16*>(X); a.ldx = K; a.ntok = M;
   a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
+  a.ksplit = 1;
   BM_CUDA(launch_w4_tc_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched_tc launch");
   return bm::ok();
 }

@@ -107,7 +107,14 @@ struct TcArgs {
   float* out;                // down output [pairs][H]
   int H;
   int* err;                  // device error flag or null
+  int ksplit;                // K split across CTAs (1 = none); the last CTA of a job reduces
+  float* part;               // split partial sums [jobs][ksplit][16][128]
+  int* counters;             // [jobs] arrival counters, zero between launches
 };
+// Split factor and workspace the launchers below use for `jobs` CTAs-worth
+// of (tile, token group, expert) work with `nst` K stages each.
+int tc_pick_ksplit(int jobs, int nst);
+size_t tc_part_floats(int jobs, int ksplit);
 bool tc_supports(int rows, int K, int g);
 // Canonical [rows][K/2] (+ scales) -> tc layout; with W2/S2 the output rows
 // interleave (row 2i from W, 2i+1 from W2).

@@ -115,6 +115,9 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar_smem) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar_smem) : "memory");
+}
 // Wait until the phase with the given parity has completed; gives up after
 // `limit` polls (each poll may suspend the thread for a bounded time) and
 // returns false.

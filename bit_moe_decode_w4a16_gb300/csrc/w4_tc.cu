@@ -1,20 +1,27 @@
 // Tensor-core (tcgen05) W4A16 projections: dense Y = X·Wᵀ and the grouped
 // expert gate/up and down GEMMs.
 //
-// One CTA of 128 threads owns a tile of 128 weight rows and up to 16 tokens
-// (M = 128 weight rows x N = 16 tokens: the large dimension on the MMA's M).
-// Thread t streams the packed int4 of row t, turns each code into the exact
-// fp16 integer q - 8 in registers and writes it with tcgen05.st into TMEM
-// lane t, where it is the MMA's A operand; the tokens' activations (fp16) sit
-// in shared memory as the B operand.  Each 64-wide K stage accumulates into
-// its own fp32 TMEM region (one per 32-wide half, so every region covers a
-// single int4 group when g >= 32): the products q * x are exact in fp32, and
-// the threads apply the fp32 group scale when they drain the region, so the
-// weights are never rounded.  Three stages rotate through TMEM: before
-// rewriting a stage's columns the producers wait on its mbarrier (arrived by
-// tcgen05.commit when the MMAs that read it finish) and drain its
-// accumulator.  A row's result is the sum over stages in ascending K of
-// scale * (exact group sum), whatever the other tokens of the tile are.
+// A CTA owns a job: a tile of 128 weight rows, up to 16 tokens (M = 128
+// weight rows x N = 16 tokens: the large dimension on the MMA's M) and a
+// range of K (the whole K, or 1/ksplit of it when there are too few jobs to
+// fill the GPU).  Warps 0-3 are producers: thread t streams the packed int4
+// of row t, turns each code into the exact fp16 integer q - 8 and writes it
+// with tcgen05.st into TMEM lane t, where it is the MMA's A operand.  Warp 4
+// issues the MMAs.  The tokens' activations (fp16) sit in shared memory as
+// the B operand.  Each 64-wide K stage accumulates into its own fp32 TMEM
+// region (one per 32-wide half, so a region never spans two int4 groups):
+// the products q * x are exact in fp32, and the producers apply the fp32
+// group scale when they drain the region, so weights are never rounded.
+//
+// Three stages rotate through TMEM, with two mbarriers each: `full` (the four
+// producer warps arrive once their A columns are written) and `done`
+// (tcgen05.commit arrives once the stage's MMAs finish).  Before rewriting a
+// stage the producers wait on its `done`, drain its accumulator, then write.
+// There is no CTA-wide barrier in the K loop.
+//
+// A row's result is the sum over stages, in ascending K, of scale x (exact
+// group sum); with a K split, the CTA that arrives last sums the splits'
+// partials in split order.  Nothing depends on the other tokens of the tile.
 //
 // Weight layout ("tc layout", written once by the repack kernel): for tile
 // t, stage s (64 K) and half h (32 K): 128 rows x 16 bytes, row-contiguous,
@@ -29,14 +36,16 @@ namespace bm {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kTokens = 16;            // MMA N
-constexpr int kStageK = 64;            // K per stage: A 32 columns, D 2 x 16 columns
-constexpr int kStages = 3;             // stages in TMEM
+constexpr int kProducers = 128;
+constexpr int kThreads = kProducers + 32;   // + the MMA warp
+constexpr int kTokens = 16;                 // MMA N
+constexpr int kStageK = 64;                 // K per stage: A 32 columns, D 2 x 16 columns
+constexpr int kStages = 3;                  // stages in TMEM
 constexpr int kSlotCols = 64;
 constexpr uint32_t kTmemCols = 256;
-constexpr int kPrefetch = 6;           // stages of weights in flight per thread
+constexpr int kPrefetch = 6;                // stages of weights in flight per producer thread
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kMaxSplit = 8;
 
 // (u_lo, u_hi) codes of one TMEM column -> the fp16 pair (u_lo - 8, u_hi - 8), exact.
 __device__ __forceinline__ uint32_t dq_pair(uint32_t w, int i) {
@@ -60,14 +69,19 @@ enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2 };
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t mbar[kStages + 1];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t done_bar[kStages];
+  __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
-  __shared__ float rinv_s[kTokens];
-  __shared__ float2 scale_s[kStages][kThreads];   // group scales of the stage in each slot
-  __shared__ int abort_s;
+  __shared__ float2 scale_s[kStages][kProducers];   // group scales of the stage in each slot
+  __shared__ int flag_s;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int tile = blockIdx.x, tg = blockIdx.y;
+  const int ksplit = a.ksplit;
+  const int tiles = gridDim.x / ksplit;
+  const int tile = blockIdx.x / ksplit, ks = blockIdx.x - tile * ksplit;
+  const int tg = blockIdx.y;
+  const int job = (blockIdx.z * gridDim.y + tg) * tiles + tile;
   const int K = a.K;
   const uint8_t* W = a.W;
   const __half* S = a.S;
@@ -86,6 +100,10 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     S += (size_t)e * a.s_expert_stride;
   }
   if (ntok <= 0) return;
+  const int nst_all = K / kStageK;
+  const int nst = nst_all / ksplit;          // stages of this split
+  const int s_begin = ks * nst;
+  const int k_begin = s_begin * kStageK, Kc = nst * kStageK;
 
   // ---- TMEM and barriers
   if (warp == 0) {
@@ -93,17 +111,23 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     tc::tmem_relinquish();
   }
   if (t == 0) {
-    for (int i = 0; i <= kStages; ++i) tc::mbar_init(tc::smem_u32(&mbar[i]), 1);
+    for (int i = 0; i < kStages; ++i) {
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), kProducers / 32);
+      tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&final_bar), 1);
     tc::fence_mbar_init();
-    abort_s = 0;
+    flag_s = 0;
   }
 
-  // ---- activations -> shared memory, fp16, no-swizzle K-major core matrices.
-  // Warp w stages rows w, w+4, ...; a lane's chunks of a row are loaded
-  // together (up to 16 x 16 bytes in flight) before they are used.
-  const int nk8 = K / 8;
+  // ---- activations (this split's K range) -> shared memory, fp16,
+  // no-swizzle K-major core matrices.  Warp w stages rows w, w+5, ...; a
+  // lane's chunks of a row are loaded together before they are used.  With
+  // the fused RMSNorm the whole row is read for its mean square.
+  const int nk8 = Kc / 8;
   const uint32_t sbo = (uint32_t)nk8 * 128u;   // bytes between the two 8-row groups
-  for (int r = warp; r < kTokens; r += kThreads / 32) {
+  constexpr int kWarps = kThreads / 32;
+  for (int r = warp; r < kTokens; r += kWarps) {
     unsigned char* rowp = smem + (r >> 3) * sbo + (r & 7) * 16;
     if (r >= ntok) {
       for (int j = lane; j < nk8; j += 32) *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(0, 0, 0, 0);
@@ -112,17 +136,17 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     const bf16* x;
     if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
     else x = a.X + (size_t)(row0 + r) * a.ldx;
-    constexpr int kMaxChunks = 4096 / 8 / 32;   // K <= 4096
-    uint4 raw[kMaxChunks];
-#pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i)
-      if (lane + 32 * i < nk8) raw[i] = *reinterpret_cast<const uint4*>(x + (lane + 32 * i) * 8);
     float rinv = 1.f;
     if (MODE == TC_DENSE && a.do_norm) {
+      constexpr int kMaxAll = 4096 / 8 / 32;
       float ss = 0.f;
+      uint4 raw[kMaxAll];
 #pragma unroll
-      for (int i = 0; i < kMaxChunks; ++i) {
-        if (lane + 32 * i < nk8) {
+      for (int i = 0; i < kMaxAll; ++i)
+        if (lane + 32 * i < K / 8) raw[i] = *reinterpret_cast<const uint4*>(x + (lane + 32 * i) * 8);
+#pragma unroll
+      for (int i = 0; i < kMaxAll; ++i) {
+        if (lane + 32 * i < K / 8) {
           const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -135,6 +159,12 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
       ss = warp_sum(ss);
       rinv = 1.0f / sqrtf(ss / (float)K + a.eps);
     }
+    constexpr int kMaxChunks = 4096 / 8 / 32;
+    uint4 raw[kMaxChunks];
+    const bf16* xk = x + k_begin;
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i)
+      if (lane + 32 * i < nk8) raw[i] = *reinterpret_cast<const uint4*>(xk + (lane + 32 * i) * 8);
 #pragma unroll
     for (int i = 0; i < kMaxChunks; ++i) {
       const int j = lane + 32 * i;
@@ -145,8 +175,9 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
         for (int q = 0; q < 4; ++q) {
           float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
           if (MODE == TC_DENSE && a.do_norm) {
-            const float w0 = a.norm_w ? bf2f(a.norm_w[j * 8 + 2 * q]) : 1.f;
-            const float w1 = a.norm_w ? bf2f(a.norm_w[j * 8 + 2 * q + 1]) : 1.f;
+            const int k = k_begin + j * 8 + 2 * q;
+            const float w0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
+            const float w1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
             v0 = round_bf16(v0 * rinv * w0);
             v1 = round_bf16(v1 * rinv * w1);
           }
@@ -162,116 +193,162 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t b_base = tc::smem_u32(smem);
-  const uint32_t idesc = tc::idesc_f16_f32(128, kTokens);
-
-  // ---- main loop over K stages
-  const int nst = K / kStageK;
-  const int ng = K / a.g;
-  const uint8_t* wt = W + (size_t)tile * nst * 2 * 2048 + (size_t)t * 16;
-  const __half* st_ = S + (size_t)tile * ng * 128 + t;
-  uint4 ring[kPrefetch][2];
-  __half sring[kPrefetch][2];
-  auto load = [&](int s, uint4 (&w)[2], __half (&sc)[2]) {
-    w[0] = ldg_nc_v4(wt + (size_t)(s * 2) * 2048);
-    w[1] = ldg_nc_v4(wt + (size_t)(s * 2 + 1) * 2048);
-    sc[0] = st_[(size_t)((s * kStageK) / a.g) * 128];
-    sc[1] = st_[(size_t)((s * kStageK + 32) / a.g) * 128];
-  };
+  bool ok = true;
   float acc[kTokens];
 #pragma unroll
   for (int j = 0; j < kTokens; ++j) acc[j] = 0.f;
-  // acc += scale_lo * D_lo + scale_hi * D_hi of the stage held in `slot`
-  auto drain = [&](int slot) {
-    uint32_t d[32];
-    tc::tmem_ld32(tmem + lane_base + slot * kSlotCols + 32, d);
-    tc::tmem_wait_ld();
-    const float2 sc = scale_s[slot][t];
+
+  if (warp == kProducers / 32) {
+    // ---------------- MMA warp: one elected lane issues, the others idle
+    if (lane == 0) {
+      const uint32_t b_base = tc::smem_u32(smem);
+      const uint32_t idesc = tc::idesc_f16_f32(128, kTokens);
+      for (int i = 0; i < nst; ++i) {
+        const int slot = i % kStages;
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), (uint32_t)(i / kStages) & 1u, kWaitLimit)) ok = false;
+        tc::fence_after_sync();
 #pragma unroll
-    for (int j = 0; j < kTokens; ++j) {
-      acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
-      acc[j] = fmaf(sc.y, __uint_as_float(d[16 + j]), acc[j]);
-    }
-  };
-#pragma unroll
-  for (int p = 0; p < kPrefetch; ++p)
-    if (p < nst) load(p, ring[p], sring[p]);
-  bool ok = true;
-  for (int s0 = 0; s0 < nst; s0 += kPrefetch) {
-#pragma unroll
-    for (int p = 0; p < kPrefetch; ++p) {
-      const int s = s0 + p;
-      if (s < nst) {
-        const uint4 w0 = ring[p][0], w1 = ring[p][1];
-        const float2 sc = make_float2(__half2float(sring[p][0]), __half2float(sring[p][1]));
-        if (s + kPrefetch < nst) load(s + kPrefetch, ring[p], sring[p]);
-        uint32_t v[32];
-        dq16(w0, v);
-        dq16(w1, v + 16);
-        const int slot = s % kStages;
-        if (s >= kStages) {
-          if (!abort_s &&
-              !tc::mbar_wait(tc::smem_u32(&mbar[slot]), (uint32_t)((s / kStages) - 1) & 1u, kWaitLimit)) {
-            abort_s = 1;
-            ok = false;
-          }
-          tc::fence_after_sync();
-          drain(slot);   // stage s - kStages, in ascending order
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(i * 4 + q) * 256u, 128u, sbo);
+          const uint32_t dcol = slot * kSlotCols + 32 + (q >> 1) * 16;
+          tc::mma_f16_tmem_a(tmem + dcol, tmem + slot * kSlotCols + q * 8, bd, idesc, (uint32_t)(q & 1));
         }
-        scale_s[slot][t] = sc;
-        tc::tmem_st32(tmem + lane_base + slot * kSlotCols, v);
-        tc::tmem_wait_st();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (t == 0) {
-          tc::fence_after_sync();
+        tc::mma_commit(tc::smem_u32(&done_bar[slot]));
+      }
+      tc::mma_commit(tc::smem_u32(&final_bar));
+    }
+    __syncwarp();
+  } else {
+    // ---------------- producers: thread t owns weight row t / TMEM lane t
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int ng = K / a.g;
+    const uint8_t* wt = W + ((size_t)tile * nst_all * 2) * 2048 + (size_t)t * 16;
+    const __half* st_ = S + (size_t)tile * ng * 128 + t;
+    uint4 ring[kPrefetch][2];
+    __half sring[kPrefetch][2];
+    auto load = [&](int i, uint4 (&w)[2], __half (&sc)[2]) {
+      const int s = s_begin + i;
+      w[0] = ldg_nc_v4(wt + (size_t)(s * 2) * 2048);
+      w[1] = ldg_nc_v4(wt + (size_t)(s * 2 + 1) * 2048);
+      sc[0] = st_[(size_t)((s * kStageK) / a.g) * 128];
+      sc[1] = st_[(size_t)((s * kStageK + 32) / a.g) * 128];
+    };
+    // acc += scale_lo * D_lo + scale_hi * D_hi of the stage held in `slot`
+    auto drain = [&](int slot) {
+      uint32_t d[32];
+      tc::tmem_ld32(tmem + lane_base + slot * kSlotCols + 32, d);
+      tc::tmem_wait_ld();
+      const float2 sc = scale_s[slot][t];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(s * 4 + q) * 256u, 128u, sbo);
-            const uint32_t dcol = slot * kSlotCols + 32 + (q >> 1) * 16;
-            tc::mma_f16_tmem_a(tmem + dcol, tmem + slot * kSlotCols + q * 8, bd, idesc, (uint32_t)(q & 1));
+      for (int j = 0; j < kTokens; ++j) {
+        acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
+        acc[j] = fmaf(sc.y, __uint_as_float(d[16 + j]), acc[j]);
+      }
+    };
+#pragma unroll
+    for (int p = 0; p < kPrefetch; ++p)
+      if (p < nst) load(p, ring[p], sring[p]);
+    for (int i0 = 0; i0 < nst; i0 += kPrefetch) {
+#pragma unroll
+      for (int p = 0; p < kPrefetch; ++p) {
+        const int i = i0 + p;
+        if (i < nst) {
+          const uint4 w0 = ring[p][0], w1 = ring[p][1];
+          const float2 sc = make_float2(__half2float(sring[p][0]), __half2float(sring[p][1]));
+          if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], sring[p]);
+          uint32_t v[32];
+          dq16(w0, v);
+          dq16(w1, v + 16);
+          const int slot = i % kStages;
+          if (i >= kStages) {
+            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / kStages) - 1) & 1u, kWaitLimit))
+              ok = false;
+            tc::fence_after_sync();
+            drain(slot);   // stage i - kStages, in ascending order
           }
-          tc::mma_commit(tc::smem_u32(&mbar[slot]));
-          if (s == nst - 1) tc::mma_commit(tc::smem_u32(&mbar[kStages]));
+          scale_s[slot][t] = sc;
+          tc::tmem_st32(tmem + lane_base + slot * kSlotCols, v);
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[slot]));
         }
       }
     }
+    if (!tc::mbar_wait(tc::smem_u32(&final_bar), 0u, kWaitLimit)) ok = false;
+    tc::fence_after_sync();
+    for (int i = (nst > kStages ? nst - kStages : 0); i < nst; ++i) drain(i % kStages);
+  }
+  if (!ok && a.err) atomicExch(a.err, 4);
+
+  // ---- split-K: every split writes its partial sums; the last to arrive
+  // adds them in split order and runs the epilogue
+  if (ksplit > 1) {
+    float* mine = a.part + ((size_t)job * ksplit + ks) * (kTokens * 128);
+    if (t < kProducers) {
+#pragma unroll
+      for (int j = 0; j < kTokens; ++j)
+        if (j < ntok) mine[j * 128 + t] = acc[j];
+    }
+    __threadfence();
+    __syncthreads();
+    if (t == 0) {
+      const int prev = atomicAdd(&a.counters[job], 1);
+      flag_s = (prev == ksplit - 1);
+    }
+    __syncthreads();
+    if (!flag_s) {
+      tc::fence_before_sync();
+      __syncthreads();
+      if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+    __threadfence();
+    if (t < kProducers) {
+      const float* base = a.part + (size_t)job * ksplit * (kTokens * 128);
+#pragma unroll
+      for (int j = 0; j < kTokens; ++j) {
+        if (j < ntok) {
+          float s = 0.f;
+          for (int k2 = 0; k2 < ksplit; ++k2) s += __ldcg(base + ((size_t)k2 * kTokens + j) * 128 + t);
+          acc[j] = s;
+        }
+      }
+    }
+    if (t == 0) a.counters[job] = 0;
   }
 
-  // ---- drain the last stages, then the epilogue: lane t = weight row t
-  if (!tc::mbar_wait(tc::smem_u32(&mbar[kStages]), 0u, kWaitLimit)) ok = false;
-  tc::fence_after_sync();
-  for (int s = (nst > kStages ? nst - kStages : 0); s < nst; ++s) drain(s % kStages);
-  if (!ok && a.err) atomicExch(a.err, 4);
-  if (MODE == TC_DENSE) {
-    const size_t n = (size_t)tile * 128 + t;
+  // ---- epilogue: lane t = weight row t of the tile
+  if (t < kProducers) {
+    if (MODE == TC_DENSE) {
+      const size_t n = (size_t)tile * 128 + t;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j < ntok) {
-        const size_t m = row0 + j;
-        float v = acc[j];
-        if (a.Res) v += bf2f(a.Res[m * a.ldr + n]);
-        a.Y[m * a.ldy + n] = f2bf(v);
+      for (int j = 0; j < 16; ++j) {
+        if (j < ntok) {
+          const size_t m = row0 + j;
+          float v = acc[j];
+          if (a.Res) v += bf2f(a.Res[m * a.ldr + n]);
+          a.Y[m * a.ldy + n] = f2bf(v);
+        }
       }
-    }
-  } else if (MODE == TC_GATEUP) {
-    // rows interleave (gate f, up f): lanes 2i and 2i+1 hold the pair
-    const int f = tile * 64 + (t >> 1);
+    } else if (MODE == TC_GATEUP) {
+      // rows interleave (gate f, up f): lanes 2i and 2i+1 hold the pair
+      const int f = tile * 64 + (t >> 1);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float other = __shfl_xor_sync(0xffffffffu, acc[j], 1);
-      if (j < ntok && (t & 1) == 0) {
-        const float gv = acc[j], uv = other;
-        const float sv = gv / (1.f + expf(-gv));
-        a.act[(size_t)(row0 + j) * a.F + f] = f2bf(sv * uv);
+      for (int j = 0; j < 16; ++j) {
+        const float other = __shfl_xor_sync(0xffffffffu, acc[j], 1);
+        if (j < ntok && (t & 1) == 0) {
+          const float gv = acc[j], uv = other;
+          const float sv = gv / (1.f + expf(-gv));
+          a.act[(size_t)(row0 + j) * a.F + f] = f2bf(sv * uv);
+        }
       }
-    }
-  } else {
-    const size_t h = (size_t)tile * 128 + t;
+    } else {
+      const size_t h = (size_t)tile * 128 + t;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < ntok) a.out[(size_t)(row0 + j) * a.H + h] = acc[j];
+      for (int j = 0; j < 16; ++j)
+        if (j < ntok) a.out[(size_t)(row0 + j) * a.H + h] = acc[j];
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -316,12 +393,29 @@ __global__ void k_repack_tc(const uint8_t* src, const __half* ssrc, const uint8_
 
 template <int MODE>
 cudaError_t run_tc(const TcArgs& a, dim3 grid, cudaStream_t st) {
-  const size_t smem = (size_t)kTokens * a.K * 2;
+  const int ks = a.ksplit < 1 ? 1 : a.ksplit;
+  if ((a.K / kStageK) % ks != 0 || ks > kMaxSplit || (ks > 1 && (!a.part || !a.counters)))
+    return cudaErrorInvalidValue;
+  grid.x *= ks;
+  const size_t smem = (size_t)kTokens * (a.K / ks) * 2;
   k_w4_tc<MODE><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int tc_pick_ksplit(int jobs, int nst) {
+  // aim for at least ~2 CTAs per SM of the 152, with >= 4 stages per split
+  int best = 1;
+  for (int ks = 2; ks <= kMaxSplit; ++ks) {
+    if (nst % ks || nst / ks < 4) continue;
+    if ((long)jobs * best >= 300) break;
+    best = ks;
+  }
+  return best;
+}
+
+size_t tc_part_floats(int jobs, int ksplit) { return (size_t)jobs * ksplit * kTokens * 128; }
 
 bool tc_supports(int rows, int K, int g) {
   return rows > 0 && rows % 128 == 0 && K >= kStageK && K % kStageK == 0 && K <= 4096 &&

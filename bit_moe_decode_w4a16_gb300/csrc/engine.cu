@@ -143,7 +143,7 @@ DevCheck chk_of(bm_engine* e) { return DevCheck{e->d_err}; }
 
 // K split of a tensor-core launch of `jobs` (tile, token group, expert) jobs.
 void tc_split(bm_engine* e, TcArgs& t, int jobs) {
-  t.ksplit = tc_pick_ksplit(jobs, t.K / 64);
+  t.ksplit = tc_pick_ksplit(jobs, t.K / 32);
   t.part = e->tc_part;
   t.counters = e->tc_counters;
 }
@@ -157,7 +157,7 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
     const int tg = (B + 15) / 16, max_u = B * c.top_k < c.experts ? B * c.top_k : c.experts;
     const int jobs[4] = {(qkv_rows / 128) * tg, (H / 128) * tg, (2 * c.ffn / 128) * tg * max_u,
                          (H / 128) * tg * max_u};
-    const int nst[4] = {H / 64, qd / 64, H / 64, c.ffn / 64};
+    const int nst[4] = {H / 32, qd / 32, H / 32, c.ffn / 32};
     for (int i = 0; i < 4; ++i) {
       const size_t j = jobs[i];
       *max_jobs = j > *max_jobs ? j : *max_jobs;
@@ -244,9 +244,17 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
       if ((err = launch_moe(ma, mb, s, &n, mark)) != cudaSuccess) return err;
     }
   }
-  if ((err = launch_lm_head(e->lm_head, c.vocab, H, e->x, e->has_final_norm ? e->final_norm_buf : nullptr,
-                            c.rms_eps, e->logits, B, s)) != cudaSuccess)
+  const bf16* final_nw = e->has_final_norm ? e->final_norm_buf : nullptr;
+  if (tc && c.vocab % 128 == 0) {
+    TcArgs tl{};
+    tl.W = reinterpret_cast<const uint8_t*>(e->lm_head); tl.rows = c.vocab; tl.K = H; tl.g = c.group;
+    tl.X = e->x; tl.ldx = H; tl.ntok = B; tl.do_norm = 1; tl.norm_w = final_nw; tl.eps = c.rms_eps;
+    tl.out = e->logits; tl.ksplit = 1; tl.err = e->d_err;
+    if ((err = launch_lm_tc(tl, s)) != cudaSuccess) return err;
+  } else if ((err = launch_lm_head(e->lm_head, c.vocab, H, e->x, final_nw, c.rms_eps, e->logits, B, s)) !=
+             cudaSuccess) {
     return err;
+  }
   mark(KT_LM_HEAD);
   ++n;
   if ((err = launch_argmax(e->logits, c.vocab, B, e->d_next, e->arena.len, e->d_slots, 1, s)) != cudaSuccess)

@@ -123,6 +123,10 @@ cudaError_t launch_repack_tc(const uint8_t* W, const __half* S, const uint8_t* W
 cudaError_t launch_w4_tc_dense(const TcArgs& a, cudaStream_t st);
 cudaError_t launch_w4_tc_gateup(const TcArgs& a, int max_u, int max_tok, cudaStream_t st);
 cudaError_t launch_w4_tc_down(const TcArgs& a, int max_u, int max_tok, cudaStream_t st);
+// Output projection on the tensor cores: W = bf16 [rows][K] row-major (no
+// repack), X = final hidden state (RMSNorm fused, bf16), out = fp32 logits
+// [ntok][rows].  rows % 128 == 0.
+cudaError_t launch_lm_tc(const TcArgs& a, cudaStream_t st);
 cudaError_t init_tc_attributes();
 
 // ---------------------------------------------------------------- attention

@@ -1,31 +1,33 @@
-// Tensor-core (tcgen05) W4A16 projections: dense Y = X·Wᵀ and the grouped
-// expert gate/up and down GEMMs.
+// Tensor-core (tcgen05) projections of the decode step: the dense W4A16
+// projections, the grouped expert gate/up and down GEMMs, and the bf16
+// output projection.
 //
 // A CTA owns a job: a tile of 128 weight rows, up to 16 tokens (M = 128
 // weight rows x N = 16 tokens: the large dimension on the MMA's M) and a
 // range of K (the whole K, or 1/ksplit of it when there are too few jobs to
-// fill the GPU).  Warps 0-3 are producers: thread t streams the packed int4
-// of row t, turns each code into the exact fp16 integer q - 8 and writes it
-// with tcgen05.st into TMEM lane t, where it is the MMA's A operand.  Warp 4
-// issues the MMAs.  The tokens' activations (fp16) sit in shared memory as
-// the B operand.  Each 64-wide K stage accumulates into its own fp32 TMEM
-// region (one per 32-wide half, so a region never spans two int4 groups):
-// the products q * x are exact in fp32, and the producers apply the fp32
-// group scale when they drain the region, so weights are never rounded.
+// fill the GPU).  Warps 0-3 are producers: thread t streams weight row t and
+// writes it with tcgen05.st into TMEM lane t, where it is the MMA's A
+// operand — for int4 weights each code becomes the exact fp16 integer q - 8;
+// bf16 weights are stored as they are.  Warp 4 issues the MMAs.  The tokens'
+// activations sit in shared memory as the B operand (fp16, or bf16 for the
+// output projection).
 //
-// Three stages rotate through TMEM, with two mbarriers each: `full` (the four
-// producer warps arrive once their A columns are written) and `done`
-// (tcgen05.commit arrives once the stage's MMAs finish).  Before rewriting a
-// stage the producers wait on its `done`, drain its accumulator, then write.
-// There is no CTA-wide barrier in the K loop.
+// K advances in stages of 32 (16 TMEM columns of A).  Four stages rotate
+// through TMEM with two mbarriers each: `full` (the four producer warps
+// arrive once their A columns are written) and `done` (tcgen05.commit
+// arrives once the stage's MMAs finish); before rewriting a stage the
+// producers wait on its `done`.  There is no CTA-wide barrier in the K loop.
+// For int4 weights every stage accumulates into its own fp32 TMEM region
+// (a stage never spans two groups): the products q * x are exact in fp32,
+// and the producers apply the fp32 group scale when they drain the region,
+// so the weights are never rounded.  A row's result is the sum over stages,
+// in ascending K, of scale x (exact group sum); with a K split, the CTA that
+// arrives last adds the splits' partials in split order.  Nothing depends on
+// the other tokens of the tile.
 //
-// A row's result is the sum over stages, in ascending K, of scale x (exact
-// group sum); with a K split, the CTA that arrives last sums the splits'
-// partials in split order.  Nothing depends on the other tokens of the tile.
-//
-// Weight layout ("tc layout", written once by the repack kernel): for tile
-// t, stage s (64 K) and half h (32 K): 128 rows x 16 bytes, row-contiguous,
-// so a warp's loads of one half are 512 contiguous bytes.  Inside each 32-bit
+// Int4 weight layout ("tc layout", written once by the repack kernel): for
+// tile t and 32-wide K chunk c: 128 rows x 16 bytes, row-contiguous, so a
+// warp's loads of one chunk are 512 contiguous bytes.  Inside each 32-bit
 // word the 8 codes are ordered (k0 k2 k4 k6 k1 k3 k5 k7), so one
 // (w >> 4i) & 0x000F000F | 0x64006400 yields the fp16 pair (1024 + u_2i,
 // 1024 + u_2i+1) of one TMEM column.  Scales: [tile][K/g][128 rows] fp16.
@@ -39,11 +41,10 @@ namespace {
 constexpr int kProducers = 128;
 constexpr int kThreads = kProducers + 32;   // + the MMA warp
 constexpr int kTokens = 16;                 // MMA N
-constexpr int kStageK = 64;                 // K per stage: A 32 columns, D 2 x 16 columns
-constexpr int kStages = 3;                  // stages in TMEM
-constexpr int kSlotCols = 64;
-constexpr uint32_t kTmemCols = 256;
-constexpr int kPrefetch = 6;                // stages of weights in flight per producer thread
+constexpr int kStageK = 32;                 // K per stage: 16 TMEM columns of A
+constexpr int kSlots = 4;                   // stages resident in TMEM
+constexpr int kDBase = 64;                  // accumulator columns start here
+constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kMaxSplit = 8;
 
@@ -55,25 +56,19 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t w, int i) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// 16 packed bytes (32 codes) -> 16 TMEM columns of fp16 pairs.
-__device__ __forceinline__ void dq16(const uint4 w, uint32_t* out) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out[q * 4 + i] = dq_pair(ws[q], i);
-}
-
-enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2 };
+enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2, TC_LM = 3 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
+  constexpr bool LM = MODE == TC_LM;
+  constexpr int kPrefetch = LM ? 4 : 8;   // stages of weights in flight per producer thread
+  constexpr int kVec = LM ? 4 : 1;        // 16-byte loads per thread per stage
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ __align__(8) uint64_t done_bar[kStages];
+  __shared__ __align__(8) uint64_t full_bar[kSlots];
+  __shared__ __align__(8) uint64_t done_bar[kSlots];
   __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
-  __shared__ float2 scale_s[kStages][kProducers];   // group scales of the stage in each slot
+  __shared__ float scale_s[kSlots][kProducers];   // group scale of the stage in each slot
   __shared__ int flag_s;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -86,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
   const uint8_t* W = a.W;
   const __half* S = a.S;
   int ntok, row0 = 0;   // tokens of this CTA; first pair / row index
-  if (MODE == TC_DENSE) {
+  if (MODE == TC_DENSE || LM) {
     ntok = min(kTokens, a.ntok - tg * kTokens);
     row0 = tg * kTokens;
   } else {
@@ -111,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     tc::tmem_relinquish();
   }
   if (t == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), kProducers / 32);
       tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
     }
@@ -120,10 +115,11 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     flag_s = 0;
   }
 
-  // ---- activations (this split's K range) -> shared memory, fp16,
-  // no-swizzle K-major core matrices.  Warp w stages rows w, w+5, ...; a
-  // lane's chunks of a row are loaded together before they are used.  With
-  // the fused RMSNorm the whole row is read for its mean square.
+  // ---- activations (this split's K range) -> shared memory, no-swizzle
+  // K-major core matrices of 8 rows x 16 bytes.  Warp w stages rows w,
+  // w+5, ...; a lane loads 4 chunks at a time before using them.  With the
+  // fused RMSNorm the whole row is read first for its mean square.
+  const bool do_norm = (MODE == TC_DENSE || LM) && a.do_norm;
   const int nk8 = Kc / 8;
   const uint32_t sbo = (uint32_t)nk8 * 128u;   // bytes between the two 8-row groups
   constexpr int kWarps = kThreads / 32;
@@ -137,54 +133,60 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
     else x = a.X + (size_t)(row0 + r) * a.ldx;
     float rinv = 1.f;
-    if (MODE == TC_DENSE && a.do_norm) {
-      constexpr int kMaxAll = 4096 / 8 / 32;
+    if (do_norm) {
       float ss = 0.f;
-      uint4 raw[kMaxAll];
+      for (int j0 = lane; j0 < K / 8; j0 += 128) {
+        uint4 raw[4];
 #pragma unroll
-      for (int i = 0; i < kMaxAll; ++i)
-        if (lane + 32 * i < K / 8) raw[i] = *reinterpret_cast<const uint4*>(x + (lane + 32 * i) * 8);
+        for (int i = 0; i < 4; ++i)
+          if (j0 + 32 * i < K / 8) raw[i] = *reinterpret_cast<const uint4*>(x + (j0 + 32 * i) * 8);
 #pragma unroll
-      for (int i = 0; i < kMaxAll; ++i) {
-        if (lane + 32 * i < K / 8) {
-          const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        for (int i = 0; i < 4; ++i) {
+          if (j0 + 32 * i < K / 8) {
+            const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
-            ss = fmaf(v0, v0, ss);
-            ss = fmaf(v1, v1, ss);
+            for (int q = 0; q < 4; ++q) {
+              const float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
+              ss = fmaf(v0, v0, ss);
+              ss = fmaf(v1, v1, ss);
+            }
           }
         }
       }
       ss = warp_sum(ss);
       rinv = 1.0f / sqrtf(ss / (float)K + a.eps);
     }
-    constexpr int kMaxChunks = 4096 / 8 / 32;
-    uint4 raw[kMaxChunks];
     const bf16* xk = x + k_begin;
+    for (int j0 = lane; j0 < nk8; j0 += 128) {
+      uint4 raw[4];
 #pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i)
-      if (lane + 32 * i < nk8) raw[i] = *reinterpret_cast<const uint4*>(xk + (lane + 32 * i) * 8);
+      for (int i = 0; i < 4; ++i)
+        if (j0 + 32 * i < nk8) raw[i] = *reinterpret_cast<const uint4*>(xk + (j0 + 32 * i) * 8);
 #pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i) {
-      const int j = lane + 32 * i;
-      if (j < nk8) {
-        const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        uint32_t o[4];
+      for (int i = 0; i < 4; ++i) {
+        const int j = j0 + 32 * i;
+        if (j < nk8) {
+          const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
-          if (MODE == TC_DENSE && a.do_norm) {
-            const int k = k_begin + j * 8 + 2 * q;
-            const float w0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
-            const float w1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
-            v0 = round_bf16(v0 * rinv * w0);
-            v1 = round_bf16(v1 * rinv * w1);
+          for (int q = 0; q < 4; ++q) {
+            float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
+            if (do_norm) {
+              const int k = k_begin + j * 8 + 2 * q;
+              const float w0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
+              const float w1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
+              v0 = round_bf16(v0 * rinv * w0);
+              v1 = round_bf16(v1 * rinv * w1);
+            }
+            if (LM) {
+              o[q] = (__float_as_uint(v0) >> 16) | (__float_as_uint(v1) & 0xFFFF0000u);   // exact: already bf16
+            } else {
+              __half2 h = __floats2half2_rn(v0, v1);
+              o[q] = *reinterpret_cast<uint32_t*>(&h);
+            }
           }
-          __half2 h = __floats2half2_rn(v0, v1);
-          o[q] = *reinterpret_cast<uint32_t*>(&h);
+          *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
@@ -202,16 +204,17 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     // ---------------- MMA warp: one elected lane issues, the others idle
     if (lane == 0) {
       const uint32_t b_base = tc::smem_u32(smem);
-      const uint32_t idesc = tc::idesc_f16_f32(128, kTokens);
+      const uint32_t idesc = LM ? tc::idesc_bf16_f32(128, kTokens) : tc::idesc_f16_f32(128, kTokens);
       for (int i = 0; i < nst; ++i) {
-        const int slot = i % kStages;
-        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), (uint32_t)(i / kStages) & 1u, kWaitLimit)) ok = false;
+        const int slot = i % kSlots;
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), (uint32_t)(i / kSlots) & 1u, kWaitLimit)) ok = false;
         tc::fence_after_sync();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(i * 4 + q) * 256u, 128u, sbo);
-          const uint32_t dcol = slot * kSlotCols + 32 + (q >> 1) * 16;
-          tc::mma_f16_tmem_a(tmem + dcol, tmem + slot * kSlotCols + q * 8, bd, idesc, (uint32_t)(q & 1));
+        for (int q = 0; q < 2; ++q) {
+          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(i * 2 + q) * 256u, 128u, sbo);
+          const uint32_t dcol = LM ? kDBase : kDBase + slot * 16;
+          const uint32_t accum = LM ? (uint32_t)(i > 0 || q > 0) : (uint32_t)q;
+          tc::mma_f16_tmem_a(tmem + dcol, tmem + slot * 16 + q * 8, bd, idesc, accum);
         }
         tc::mma_commit(tc::smem_u32(&done_bar[slot]));
       }
@@ -221,29 +224,29 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
   } else {
     // ---------------- producers: thread t owns weight row t / TMEM lane t
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int ng = K / a.g;
-    const uint8_t* wt = W + ((size_t)tile * nst_all * 2) * 2048 + (size_t)t * 16;
-    const __half* st_ = S + (size_t)tile * ng * 128 + t;
-    uint4 ring[kPrefetch][2];
-    __half sring[kPrefetch][2];
-    auto load = [&](int i, uint4 (&w)[2], __half (&sc)[2]) {
-      const int s = s_begin + i;
-      w[0] = ldg_nc_v4(wt + (size_t)(s * 2) * 2048);
-      w[1] = ldg_nc_v4(wt + (size_t)(s * 2 + 1) * 2048);
-      sc[0] = st_[(size_t)((s * kStageK) / a.g) * 128];
-      sc[1] = st_[(size_t)((s * kStageK + 32) / a.g) * 128];
-    };
-    // acc += scale_lo * D_lo + scale_hi * D_hi of the stage held in `slot`
-    auto drain = [&](int slot) {
-      uint32_t d[32];
-      tc::tmem_ld32(tmem + lane_base + slot * kSlotCols + 32, d);
-      tc::tmem_wait_ld();
-      const float2 sc = scale_s[slot][t];
+    const int ng = LM ? 1 : K / a.g;
+    const uint8_t* wt = LM ? W + ((size_t)tile * 128 + t) * (size_t)K * 2 + (size_t)k_begin * 2
+                           : W + (size_t)tile * nst_all * 2048 + (size_t)s_begin * 2048 + (size_t)t * 16;
+    const __half* st_ = LM ? nullptr : S + (size_t)tile * ng * 128 + t;
+    uint4 ring[kPrefetch][kVec];
+    __half sring[kPrefetch];
+    auto load = [&](int i, uint4 (&w)[kVec], __half& sc) {
+      if (LM) {
 #pragma unroll
-      for (int j = 0; j < kTokens; ++j) {
-        acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
-        acc[j] = fmaf(sc.y, __uint_as_float(d[16 + j]), acc[j]);
+        for (int v = 0; v < kVec; ++v) w[v] = ldg_nc_v4(wt + (size_t)i * 64 + v * 16);
+      } else {
+        w[0] = ldg_nc_v4(wt + (size_t)i * 2048);
+        sc = st_[(size_t)(((s_begin + i) * kStageK) / a.g) * 128];
       }
+    };
+    // acc += scale * D of the stage held in `slot`
+    auto drain = [&](int slot) {
+      uint32_t d[16];
+      tc::tmem_ld16(tmem + lane_base + kDBase + slot * 16, d);
+      tc::tmem_wait_ld();
+      const float sc = scale_s[slot][t];
+#pragma unroll
+      for (int j = 0; j < kTokens; ++j) acc[j] = fmaf(sc, __uint_as_float(d[j]), acc[j]);
     };
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p)
@@ -253,21 +256,32 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
       for (int p = 0; p < kPrefetch; ++p) {
         const int i = i0 + p;
         if (i < nst) {
-          const uint4 w0 = ring[p][0], w1 = ring[p][1];
-          const float2 sc = make_float2(__half2float(sring[p][0]), __half2float(sring[p][1]));
+          uint32_t v[16];
+          float sc = 0.f;
+          if (LM) {
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) {
+              v[4 * q] = ring[p][q].x; v[4 * q + 1] = ring[p][q].y;
+              v[4 * q + 2] = ring[p][q].z; v[4 * q + 3] = ring[p][q].w;
+            }
+          } else {
+            const uint32_t ws[4] = {ring[p][0].x, ring[p][0].y, ring[p][0].z, ring[p][0].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) v[q * 4 + c] = dq_pair(ws[q], c);
+            sc = __half2float(sring[p]);
+          }
           if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], sring[p]);
-          uint32_t v[32];
-          dq16(w0, v);
-          dq16(w1, v + 16);
-          const int slot = i % kStages;
-          if (i >= kStages) {
-            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / kStages) - 1) & 1u, kWaitLimit))
+          const int slot = i % kSlots;
+          if (i >= kSlots) {
+            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / kSlots) - 1) & 1u, kWaitLimit))
               ok = false;
             tc::fence_after_sync();
-            drain(slot);   // stage i - kStages, in ascending order
+            if (!LM) drain(slot);   // stage i - kSlots, in ascending order
           }
-          scale_s[slot][t] = sc;
-          tc::tmem_st32(tmem + lane_base + slot * kSlotCols, v);
+          if (!LM) scale_s[slot][t] = sc;
+          tc::tmem_st16(tmem + lane_base + slot * 16, v);
           tc::tmem_wait_st();
           tc::fence_before_sync();
           __syncwarp();
@@ -277,7 +291,15 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
     }
     if (!tc::mbar_wait(tc::smem_u32(&final_bar), 0u, kWaitLimit)) ok = false;
     tc::fence_after_sync();
-    for (int i = (nst > kStages ? nst - kStages : 0); i < nst; ++i) drain(i % kStages);
+    if (LM) {
+      uint32_t d[16];
+      tc::tmem_ld16(tmem + lane_base + kDBase, d);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < kTokens; ++j) acc[j] = __uint_as_float(d[j]);
+    } else {
+      for (int i = (nst > kSlots ? nst - kSlots : 0); i < nst; ++i) drain(i % kSlots);
+    }
   }
   if (!ok && a.err) atomicExch(a.err, 4);
 
@@ -343,11 +365,16 @@ __global__ void __launch_bounds__(kThreads) k_w4_tc(TcArgs a) {
           a.act[(size_t)(row0 + j) * a.F + f] = f2bf(sv * uv);
         }
       }
-    } else {
+    } else if (MODE == TC_DOWN) {
       const size_t h = (size_t)tile * 128 + t;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         if (j < ntok) a.out[(size_t)(row0 + j) * a.H + h] = acc[j];
+    } else {
+      const size_t v = (size_t)tile * 128 + t;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < ntok) a.out[(size_t)(row0 + j) * a.rows + v] = acc[j];
     }
   }
   tc::fence_before_sync();
@@ -379,8 +406,8 @@ __global__ void k_repack_tc(const uint8_t* src, const __half* ssrc, const uint8_
       }
       o[q] = r;
     }
-    const int tile = R >> 7, rr = R & 127, st = c >> 1, h = c & 1;
-    uint8_t* d = dst + ((((size_t)tile * (K / kStageK) + st) * 2 + h) * 128 + rr) * 16;
+    const int tile = R >> 7, rr = R & 127;
+    uint8_t* d = dst + (((size_t)tile * nch + c) * 128 + rr) * 16;
     *reinterpret_cast<uint4*>(d) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   const int ng = K / g;
@@ -398,6 +425,7 @@ cudaError_t run_tc(const TcArgs& a, dim3 grid, cudaStream_t st) {
     return cudaErrorInvalidValue;
   grid.x *= ks;
   const size_t smem = (size_t)kTokens * (a.K / ks) * 2;
+  if (smem > (size_t)kTokens * 4096 * 2) return cudaErrorInvalidValue;
   k_w4_tc<MODE><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -405,10 +433,10 @@ cudaError_t run_tc(const TcArgs& a, dim3 grid, cudaStream_t st) {
 }  // namespace
 
 int tc_pick_ksplit(int jobs, int nst) {
-  // aim for at least ~2 CTAs per SM of the 152, with >= 4 stages per split
+  // aim for at least ~2 CTAs per SM of the 152, with >= 8 stages per split
   int best = 1;
   for (int ks = 2; ks <= kMaxSplit; ++ks) {
-    if (nst % ks || nst / ks < 4) continue;
+    if (nst % ks || nst / ks < 8) continue;
     if ((long)jobs * best >= 300) break;
     best = ks;
   }
@@ -444,13 +472,26 @@ cudaError_t launch_w4_tc_down(const TcArgs& a, int max_u, int max_tok, cudaStrea
   return run_tc<TC_DOWN>(a, grid, st);
 }
 
+cudaError_t launch_lm_tc(const TcArgs& a, cudaStream_t st) {
+  if (a.rows % 128 || a.K % kStageK) return cudaErrorInvalidValue;
+  dim3 grid(a.rows / 128, (a.ntok + kTokens - 1) / kTokens, 1);
+  return run_tc<TC_LM>(a, grid, st);
+}
+
+template <int MODE>
+cudaError_t set_tc_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(k_w4_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokens * 4096 * 2);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_w4_tc<MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 cudaError_t init_tc_attributes() {
-  const int bytes = kTokens * 4096 * 2;
-  cudaError_t e = cudaFuncSetAttribute(k_w4_tc<TC_DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_w4_tc<TC_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_w4_tc<TC_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = set_tc_attrs<TC_DENSE>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_GATEUP>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_DOWN>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_LM>();
   return e;
 }
 

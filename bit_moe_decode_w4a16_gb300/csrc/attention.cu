@@ -87,11 +87,15 @@ __device__ __forceinline__ size_t part_index(int b, int h, int c, int qh, int ma
   return (((size_t)b * qh + h) * max_chunks + c) * (size_t)(d + 2);
 }
 
-// blockDim.x == kAttnChunk == 128 threads; d <= 128.
+// blockDim.x == kAttnChunk == 128 threads; D = head_dim (64 or 128).
+// Scores: thread t takes position j0 + t; its whole K row is loaded up front.
+// p·V: thread t takes dimension t of every q head of the group; the V rows
+// of the chunk are read in order, 8 positions per batch of loads.
+template <int D>
 __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int layer, const int32_t* slots,
                                                           const bf16* q, int qh, float* part, int max_chunks,
                                                           DevCheck chk) {
-  __shared__ float qs[kMaxGroup][128];
+  __shared__ float qs[kMaxGroup][D];
   __shared__ float ps[kMaxGroup][kAttnChunk];
   __shared__ float red[kMaxGroup][kAttnChunk / 32];
   __shared__ float stat[kMaxGroup][2];
@@ -102,34 +106,41 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
   if (L < 1 || L > ar.cap) { if (c == 0 && kh == 0 && threadIdx.x == 0) chk.fail(2); return; }
   const int j0 = c * kAttnChunk;
   if (j0 >= L) return;
-  const int d = ar.d, G = qh / ar.kvh, t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const float scale = 1.0f / sqrtf((float)d);
-  for (int idx = t; idx < G * d; idx += blockDim.x) {
-    const int g = idx / d, i = idx - g * d;
-    qs[g][i] = bf2f(q[((size_t)b * qh + kh * G + g) * d + i]);
+  const int G = qh / ar.kvh, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const float scale = 1.0f / sqrtf((float)D);
+  for (int idx = t; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D, i = idx - g * D;
+    qs[g][i] = bf2f(q[((size_t)b * qh + kh * G + g) * D + i]);
   }
-  __syncthreads();
-  const size_t base = layer * ar.layer_stride() + slot * ar.slot_stride() + (size_t)kh * ar.cap * d;
+  const size_t base = layer * ar.layer_stride() + slot * ar.slot_stride() + (size_t)kh * ar.cap * D;
   const bf16* Kb = ar.K + base;
   const bf16* Vb = ar.V + base;
   const int j = j0 + t;
+  constexpr int kVecs = D / 8;
+  uint4 kr[kVecs];
+  if (j < L) {
+    const uint4* src = reinterpret_cast<const uint4*>(Kb + (size_t)j * D);
+#pragma unroll
+    for (int i = 0; i < kVecs; ++i) kr[i] = src[i];
+  }
+  __syncthreads();
   float sc[kMaxGroup];
 #pragma unroll
   for (int g = 0; g < kMaxGroup; ++g) sc[g] = 0.f;
   if (j < L) {
-    const uint4* kr = reinterpret_cast<const uint4*>(Kb + (size_t)j * d);
-    for (int i8 = 0; i8 < d / 8; ++i8) {
-      const uint4 kv = kr[i8];
-      const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
-      const float k4 = bf_lo(kv.z), k5 = bf_hi(kv.z), k6 = bf_lo(kv.w), k7 = bf_hi(kv.w);
+#pragma unroll
+    for (int i = 0; i < kVecs; ++i) {
+      const float k0 = bf_lo(kr[i].x), k1 = bf_hi(kr[i].x), k2 = bf_lo(kr[i].y), k3 = bf_hi(kr[i].y);
+      const float k4 = bf_lo(kr[i].z), k5 = bf_hi(kr[i].z), k6 = bf_lo(kr[i].w), k7 = bf_hi(kr[i].w);
 #pragma unroll
       for (int g = 0; g < kMaxGroup; ++g) {
         if (g < G) {
-          const float* qq = &qs[g][i8 * 8];
-          float a = sc[g];
-          a = fmaf(qq[0], k0, a); a = fmaf(qq[1], k1, a); a = fmaf(qq[2], k2, a); a = fmaf(qq[3], k3, a);
-          a = fmaf(qq[4], k4, a); a = fmaf(qq[5], k5, a); a = fmaf(qq[6], k6, a); a = fmaf(qq[7], k7, a);
-          sc[g] = a;
+          const float* qq = &qs[g][i * 8];
+          float acc = sc[g];
+          acc = fmaf(qq[0], k0, acc); acc = fmaf(qq[1], k1, acc); acc = fmaf(qq[2], k2, acc);
+          acc = fmaf(qq[3], k3, acc); acc = fmaf(qq[4], k4, acc); acc = fmaf(qq[5], k5, acc);
+          acc = fmaf(qq[6], k6, acc); acc = fmaf(qq[7], k7, acc);
+          sc[g] = acc;
         }
       }
     }
@@ -165,26 +176,33 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
     stat[t][1] = l;
   }
   __syncthreads();
-  // p·V: thread t owns dimension t of every head of the group.
   const int n = min(kAttnChunk, L - j0);
-  if (t < d) {
+  if (t < D) {
     float o[kMaxGroup];
 #pragma unroll
     for (int g = 0; g < kMaxGroup; ++g) o[g] = 0.f;
-    for (int jj = 0; jj < n; ++jj) {
-      const float v = bf2f(Vb[(size_t)(j0 + jj) * d + t]);
+    const bf16* vcol = Vb + (size_t)j0 * D + t;
+    for (int jj0 = 0; jj0 < n; jj0 += 8) {
+      float vv[8];
 #pragma unroll
-      for (int g = 0; g < kMaxGroup; ++g)
-        if (g < G) o[g] = fmaf(ps[g][jj], v, o[g]);
+      for (int u = 0; u < 8; ++u) vv[u] = (jj0 + u < n) ? bf2f(vcol[(size_t)(jj0 + u) * D]) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (jj0 + u < n) {
+#pragma unroll
+          for (int g = 0; g < kMaxGroup; ++g)
+            if (g < G) o[g] = fmaf(ps[g][jj0 + u], vv[u], o[g]);
+        }
+      }
     }
 #pragma unroll
     for (int g = 0; g < kMaxGroup; ++g) {
       if (g >= G) break;
-      float* rec = part + part_index(b, kh * G + g, c, qh, max_chunks, d);
+      float* rec = part + part_index(b, kh * G + g, c, qh, max_chunks, D);
       rec[t] = o[g];
       if (t == 0) {
-        rec[d] = stat[g][0];
-        rec[d + 1] = stat[g][1];
+        rec[D] = stat[g][0];
+        rec[D + 1] = stat[g][1];
       }
     }
   }
@@ -237,7 +255,9 @@ cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slot
   if (ar.d > 128 || ar.d % 8 != 0 || qh % ar.kvh != 0 || qh / ar.kvh > kMaxGroup) return cudaErrorInvalidValue;
   const int max_chunks = (ar.cap + kAttnChunk - 1) / kAttnChunk;
   dim3 g1(max_chunks, ar.kvh, B);
-  k_attn_part<<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
+  if (ar.d == 128) k_attn_part<128><<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
+  else if (ar.d == 64) k_attn_part<64><<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
+  else return cudaErrorInvalidValue;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark(KT_ATTN_PART);

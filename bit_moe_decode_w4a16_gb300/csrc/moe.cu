@@ -30,45 +30,69 @@ namespace {
 constexpr int kRouterWarps = 8;
 constexpr int kMaxPairs = 1024;   // B * k handled by the single-CTA sort
 
+// Router logits.  Grid (ceil(E / kRouterExperts), B): a CTA takes one token
+// and kRouterExperts experts.  It normalises the token's row itself (every
+// CTA of the token computes the same bf16 values in the same order; the CTAs
+// of expert block 0 also write them out for the expert GEMMs), keeps the row
+// in shared memory as fp32, and each warp computes the dot products of its
+// experts with all of a router row's loads in flight.
+constexpr int kRouterExperts = 32;
+
 __global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
-  extern __shared__ float rinv_s[];   // [B]
+  extern __shared__ float xs[];        // [H] normalised row
+  __shared__ float red[kRouterWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (a.do_norm) {
-    for (int t = warp; t < a.B; t += kRouterWarps) {
-      const float r = row_rinv(a.x + (size_t)t * a.H, a.H, a.eps, lane);
-      if (lane == 0) rinv_s[t] = r;
-    }
-    __syncthreads();
-    if (blockIdx.x == 0) {
-      for (int i = threadIdx.x; i < a.B * a.H; i += blockDim.x) {
-        const int t = i / a.H, k = i - t * a.H;
-        const float w = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
-        b.xn[i] = f2bf(bf2f(a.x[i]) * rinv_s[t] * w);
-      }
+  const int tkn = blockIdx.y, H = a.H;
+  const bf16* x = a.x + (size_t)tkn * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x * 8; k < H; k += 256 * 8) {
+    const uint4 p = *reinterpret_cast<const uint4*>(x + k);
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float v0 = bf_lo(w[q]), v1 = bf_hi(w[q]);
+      xs[k + 2 * q] = v0;
+      xs[k + 2 * q + 1] = v1;
+      ss = fmaf(v0, v0, ss);
+      ss = fmaf(v1, v1, ss);
     }
   }
-  const int e = blockIdx.x * kRouterWarps + warp;
-  if (e >= a.E) return;
-  const float* wr = a.wr + (size_t)e * a.H;
-  for (int t = 0; t < a.B; ++t) {
-    const bf16* x = a.x + (size_t)t * a.H;
-    const float r = a.do_norm ? rinv_s[t] : 1.f;
+  if (a.do_norm) {
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < kRouterWarps; ++w) tot += red[w];
+    const float r = 1.0f / sqrtf(tot / (float)H + a.eps);
+    for (int k = threadIdx.x; k < H; k += 256) {
+      const float w = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
+      const bf16 v = f2bf(xs[k] * r * w);
+      xs[k] = bf2f(v);
+      if (blockIdx.x == 0) b.xn[(size_t)tkn * H + k] = v;
+    }
+  }
+  __syncthreads();
+  for (int ei = warp; ei < kRouterExperts; ei += kRouterWarps) {
+    const int e = blockIdx.x * kRouterExperts + ei;
+    if (e >= a.E) break;
+    const float* wr = a.wr + (size_t)e * H;
     float acc = 0.f;
-    for (int k = lane * 4; k < a.H; k += 128) {
-      const float4 w4 = *reinterpret_cast<const float4*>(wr + k);
-      const uint2 p = *reinterpret_cast<const uint2*>(x + k);
-      float x0 = bf_lo(p.x), x1 = bf_hi(p.x), x2 = bf_lo(p.y), x3 = bf_hi(p.y);
-      if (a.do_norm) {
-        const float n0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f, n1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
-        const float n2 = a.norm_w ? bf2f(a.norm_w[k + 2]) : 1.f, n3 = a.norm_w ? bf2f(a.norm_w[k + 3]) : 1.f;
-        x0 = round_bf16(x0 * r * n0); x1 = round_bf16(x1 * r * n1);
-        x2 = round_bf16(x2 * r * n2); x3 = round_bf16(x3 * r * n3);
+    for (int k0 = lane * 4; k0 < H; k0 += 128 * 4) {
+      float4 w4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (k0 + 128 * i < H) w4[i] = *reinterpret_cast<const float4*>(wr + k0 + 128 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = k0 + 128 * i;
+        if (k < H) {
+          acc = fmaf(xs[k], w4[i].x, acc); acc = fmaf(xs[k + 1], w4[i].y, acc);
+          acc = fmaf(xs[k + 2], w4[i].z, acc); acc = fmaf(xs[k + 3], w4[i].w, acc);
+        }
       }
-      acc = fmaf(x0, w4.x, acc); acc = fmaf(x1, w4.y, acc);
-      acc = fmaf(x2, w4.z, acc); acc = fmaf(x3, w4.w, acc);
     }
     acc = warp_sum(acc);
-    if (lane == 0) b.logits[(size_t)t * a.E + e] = acc;
+    if (lane == 0) b.logits[(size_t)tkn * a.E + e] = acc;
   }
 }
 
@@ -337,8 +361,8 @@ MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
 
 cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches, const Marker& mark) {
   if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
-  const int nblk = (a.E + kRouterWarps - 1) / kRouterWarps;
-  k_router<<<nblk, 256, sizeof(float) * a.B, st>>>(a, b);
+  const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
+  k_router<<<rgrid, 256, sizeof(float) * a.H, st>>>(a, b);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   mark(KT_ROUTER);
@@ -362,8 +386,8 @@ cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int*
 
 cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark) {
   if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
-  const int nblk = (a.E + kRouterWarps - 1) / kRouterWarps;
-  k_router<<<nblk, 256, sizeof(float) * a.B, st>>>(a, b);
+  const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
+  k_router<<<rgrid, 256, sizeof(float) * a.H, st>>>(a, b);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   mark(KT_ROUTER);

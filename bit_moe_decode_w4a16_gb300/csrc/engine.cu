@@ -143,7 +143,7 @@ DevCheck chk_of(bm_engine* e) { return DevCheck{e->d_err}; }
 
 // K split of a tensor-core launch of `jobs` (tile, token group, expert) jobs.
 void tc_split(bm_engine* e, TcArgs& t, int jobs) {
-  t.ksplit = tc_pick_ksplit(jobs, t.K / 32);
+  t.ksplit = tc_pick_ksplit(jobs, t.K / 64);
   t.part = e->tc_part;
   t.counters = e->tc_counters;
 }
@@ -157,7 +157,7 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
     const int tg = (B + 15) / 16, max_u = B * c.top_k < c.experts ? B * c.top_k : c.experts;
     const int jobs[4] = {(qkv_rows / 128) * tg, (H / 128) * tg, (2 * c.ffn / 128) * tg * max_u,
                          (H / 128) * tg * max_u};
-    const int nst[4] = {H / 32, qd / 32, H / 32, c.ffn / 32};
+    const int nst[4] = {H / 64, qd / 64, H / 64, c.ffn / 64};
     for (int i = 0; i < 4; ++i) {
       const size_t j = jobs[i];
       *max_jobs = j > *max_jobs ? j : *max_jobs;

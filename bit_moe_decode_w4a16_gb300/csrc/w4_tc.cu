@@ -12,16 +12,17 @@
 // activations sit in shared memory as the B operand (fp16, or bf16 for the
 // output projection).
 //
-// K advances in stages of 32 (16 TMEM columns of A).  Four stages rotate
-// through TMEM with two mbarriers each: `full` (the four producer warps
-// arrive once their A columns are written) and `done` (tcgen05.commit
-// arrives once the stage's MMAs finish); before rewriting a stage the
-// producers wait on its `done`.  There is no CTA-wide barrier in the K loop.
-// For int4 weights every stage accumulates into its own fp32 TMEM region
-// (a stage never spans two groups): the products q * x are exact in fp32,
-// and the producers apply the fp32 group scale when they drain the region,
-// so the weights are never rounded.  A row's result is the sum over stages,
-// in ascending K, of scale x (exact group sum); with a K split, the CTA that
+// K advances in stages of 64 (32 TMEM columns of A).  An MMA's completion
+// reaches its mbarrier about a microsecond after issue, so a CTA keeps
+// several stages resident in TMEM: each slot has `full` (the four producer
+// warps arrive once its A columns are written) and `done` (tcgen05.commit
+// arrives once its MMAs finish); before rewriting a slot the producers wait
+// on its `done`.  There is no CTA-wide barrier in the K loop.  For int4
+// weights each slot also holds the stage's own fp32 accumulator (one per
+// int4 group inside the stage): the products q * x are exact in fp32, and
+// the producers apply the fp32 group scale when they drain it, so the
+// weights are never rounded.  A row's result is the sum over stages, in
+// ascending K, of scale x (exact group sum); with a K split, the CTA that
 // arrives last adds the splits' partials in split order.  Nothing depends on
 // the other tokens of the tile.
 //
@@ -41,10 +42,10 @@ namespace {
 constexpr int kProducers = 128;
 constexpr int kThreads = kProducers + 32;   // + the MMA warp
 constexpr int kTokens = 16;                 // MMA N
-constexpr int kStageK = 32;                 // K per stage: 16 TMEM columns of A
-constexpr int kSlots = 4;                   // stages resident in TMEM
-constexpr int kDBase = 64;                  // accumulator columns start here
-constexpr uint32_t kTmemCols = 128;
+constexpr int kStageK = 64;                 // K per stage: 32 TMEM columns of A
+constexpr uint32_t kTmemCols = 256;
+constexpr int kMaxSlots = 6;
+constexpr int kLmSlots = 6;                 // output projection: A-only slots, one accumulator
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kMaxSplit = 8;
 
@@ -56,19 +57,27 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t w, int i) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ void dq16(const uint4 w, uint32_t* out) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) out[q * 4 + c] = dq_pair(ws[q], c);
+}
+
 enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2, TC_LM = 3 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   constexpr bool LM = MODE == TC_LM;
-  constexpr int kPrefetch = LM ? 4 : 8;   // stages of weights in flight per producer thread
-  constexpr int kVec = LM ? 4 : 1;        // 16-byte loads per thread per stage
+  constexpr int kPrefetch = LM ? 3 : 6;   // stages of weights in flight per producer thread
+  constexpr int kVec = LM ? 8 : 2;        // 16-byte loads per thread per stage
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full_bar[kSlots];
-  __shared__ __align__(8) uint64_t done_bar[kSlots];
+  __shared__ __align__(8) uint64_t full_bar[kMaxSlots];
+  __shared__ __align__(8) uint64_t done_bar[kMaxSlots];
   __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
-  __shared__ float scale_s[kSlots][kProducers];   // group scale of the stage in each slot
+  __shared__ float2 scale_s[kMaxSlots][kProducers];   // group scales of the stage in each slot
   __shared__ int flag_s;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -99,6 +108,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
   const int nst = nst_all / ksplit;          // stages of this split
   const int s_begin = ks * nst;
   const int k_begin = s_begin * kStageK, Kc = nst * kStageK;
+  // TMEM columns: int4 slots are [A 32 | D 16] (g >= 64) or [A 32 | D 2x16]
+  // (g == 32, two groups per stage); the output projection has A-only slots
+  // and one accumulator after them.
+  const bool two_groups = !LM && a.g == 32;
+  const int dcols = LM ? 0 : (two_groups ? 32 : 16);
+  const int slot_cols = 32 + dcols;
+  const int nslots = LM ? kLmSlots : (two_groups ? 4 : 5);
+  const int lm_dcol = kLmSlots * 32;
 
   // ---- TMEM and barriers
   if (warp == 0) {
@@ -106,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
     tc::tmem_relinquish();
   }
   if (t == 0) {
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < nslots; ++i) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), kProducers / 32);
       tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
     }
@@ -206,15 +223,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
       const uint32_t b_base = tc::smem_u32(smem);
       const uint32_t idesc = LM ? tc::idesc_bf16_f32(128, kTokens) : tc::idesc_f16_f32(128, kTokens);
       for (int i = 0; i < nst; ++i) {
-        const int slot = i % kSlots;
-        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), (uint32_t)(i / kSlots) & 1u, kWaitLimit)) ok = false;
+        const int slot = i % nslots;
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), (uint32_t)(i / nslots) & 1u, kWaitLimit)) ok = false;
         tc::fence_after_sync();
+        const uint32_t acol = slot * slot_cols;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(i * 2 + q) * 256u, 128u, sbo);
-          const uint32_t dcol = LM ? kDBase : kDBase + slot * 16;
-          const uint32_t accum = LM ? (uint32_t)(i > 0 || q > 0) : (uint32_t)q;
-          tc::mma_f16_tmem_a(tmem + dcol, tmem + slot * 16 + q * 8, bd, idesc, accum);
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)(i * 4 + q) * 256u, 128u, sbo);
+          uint32_t dcol, accum;
+          if (LM) {
+            dcol = lm_dcol;
+            accum = (uint32_t)(i > 0 || q > 0);
+          } else if (two_groups) {
+            dcol = acol + 32 + (q >> 1) * 16;
+            accum = (uint32_t)(q & 1);
+          } else {
+            dcol = acol + 32;
+            accum = (uint32_t)(q > 0);
+          }
+          tc::mma_f16_tmem_a(tmem + dcol, tmem + acol + q * 8, bd, idesc, accum);
         }
         tc::mma_commit(tc::smem_u32(&done_bar[slot]));
       }
@@ -226,27 +253,36 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int ng = LM ? 1 : K / a.g;
     const uint8_t* wt = LM ? W + ((size_t)tile * 128 + t) * (size_t)K * 2 + (size_t)k_begin * 2
-                           : W + (size_t)tile * nst_all * 2048 + (size_t)s_begin * 2048 + (size_t)t * 16;
+                           : W + (size_t)tile * (K / 32) * 2048 + (size_t)s_begin * 2 * 2048 + (size_t)t * 16;
     const __half* st_ = LM ? nullptr : S + (size_t)tile * ng * 128 + t;
     uint4 ring[kPrefetch][kVec];
-    __half sring[kPrefetch];
-    auto load = [&](int i, uint4 (&w)[kVec], __half& sc) {
+    __half2 sring[kPrefetch];
+    auto load = [&](int i, uint4 (&w)[kVec], __half2& sc) {
       if (LM) {
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) w[v] = ldg_nc_v4(wt + (size_t)i * 64 + v * 16);
+        for (int v = 0; v < kVec; ++v) w[v] = ldg_nc_v4(wt + (size_t)i * 128 + v * 16);
       } else {
-        w[0] = ldg_nc_v4(wt + (size_t)i * 2048);
-        sc = st_[(size_t)(((s_begin + i) * kStageK) / a.g) * 128];
+        w[0] = ldg_nc_v4(wt + (size_t)(2 * i) * 2048);
+        w[1] = ldg_nc_v4(wt + (size_t)(2 * i + 1) * 2048);
+        const int k0 = (s_begin + i) * kStageK;
+        sc = __halves2half2(st_[(size_t)(k0 / a.g) * 128], st_[(size_t)((k0 + 32) / a.g) * 128]);
       }
     };
-    // acc += scale * D of the stage held in `slot`
+    // acc += scale * D of the stage held in `slot` (two groups: two regions)
     auto drain = [&](int slot) {
+      const float2 sc = scale_s[slot][t];
+      const uint32_t dbase = tmem + lane_base + slot * slot_cols + 32;
       uint32_t d[16];
-      tc::tmem_ld16(tmem + lane_base + kDBase + slot * 16, d);
+      tc::tmem_ld16(dbase, d);
       tc::tmem_wait_ld();
-      const float sc = scale_s[slot][t];
 #pragma unroll
-      for (int j = 0; j < kTokens; ++j) acc[j] = fmaf(sc, __uint_as_float(d[j]), acc[j]);
+      for (int j = 0; j < kTokens; ++j) acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
+      if (two_groups) {
+        tc::tmem_ld16(dbase + 16, d);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < kTokens; ++j) acc[j] = fmaf(sc.y, __uint_as_float(d[j]), acc[j]);
+      }
     };
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p)
@@ -256,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
       for (int p = 0; p < kPrefetch; ++p) {
         const int i = i0 + p;
         if (i < nst) {
-          uint32_t v[16];
-          float sc = 0.f;
+          uint32_t v[32];
+          float2 sc = make_float2(0.f, 0.f);
           if (LM) {
 #pragma unroll
             for (int q = 0; q < kVec; ++q) {
@@ -265,23 +301,20 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
               v[4 * q + 2] = ring[p][q].z; v[4 * q + 3] = ring[p][q].w;
             }
           } else {
-            const uint32_t ws[4] = {ring[p][0].x, ring[p][0].y, ring[p][0].z, ring[p][0].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) v[q * 4 + c] = dq_pair(ws[q], c);
-            sc = __half2float(sring[p]);
+            dq16(ring[p][0], v);
+            dq16(ring[p][1], v + 16);
+            sc = __half22float2(sring[p]);
           }
           if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], sring[p]);
-          const int slot = i % kSlots;
-          if (i >= kSlots) {
-            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / kSlots) - 1) & 1u, kWaitLimit))
+          const int slot = i % nslots;
+          if (i >= nslots) {
+            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / nslots) - 1) & 1u, kWaitLimit))
               ok = false;
             tc::fence_after_sync();
-            if (!LM) drain(slot);   // stage i - kSlots, in ascending order
+            if (!LM) drain(slot);   // stage i - nslots, in ascending order
           }
           if (!LM) scale_s[slot][t] = sc;
-          tc::tmem_st16(tmem + lane_base + slot * 16, v);
+          tc::tmem_st32(tmem + lane_base + slot * slot_cols, v);
           tc::tmem_wait_st();
           tc::fence_before_sync();
           __syncwarp();
@@ -293,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_w4_tc(TcArgs a) {
     tc::fence_after_sync();
     if (LM) {
       uint32_t d[16];
-      tc::tmem_ld16(tmem + lane_base + kDBase, d);
+      tc::tmem_ld16(tmem + lane_base + lm_dcol, d);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < kTokens; ++j) acc[j] = __uint_as_float(d[j]);
     } else {
-      for (int i = (nst > kSlots ? nst - kSlots : 0); i < nst; ++i) drain(i % kSlots);
+      for (int i = (nst > nslots ? nst - nslots : 0); i < nst; ++i) drain(i % nslots);
     }
   }
   if (!ok && a.err) atomicExch(a.err, 4);
@@ -433,10 +466,10 @@ cudaError_t run_tc(const TcArgs& a, dim3 grid, cudaStream_t st) {
 }  // namespace
 
 int tc_pick_ksplit(int jobs, int nst) {
-  // aim for at least ~2 CTAs per SM of the 152, with >= 8 stages per split
+  // aim for at least ~2 CTAs per SM of the 152, with >= 4 stages per split
   int best = 1;
   for (int ks = 2; ks <= kMaxSplit; ++ks) {
-    if (nst % ks || nst / ks < 8) continue;
+    if (nst % ks || nst / ks < 4) continue;
     if ((long)jobs * best >= 300) break;
     best = ks;
   }

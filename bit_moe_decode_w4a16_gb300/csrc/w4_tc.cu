@@ -39,7 +39,7 @@ namespace bm {
 
 namespace {
 
-constexpr int kProducers = 128;
+constexpr int kProducers = 256;             // 8 warps: two per TMEM lane quarter
 constexpr int kThreads = kProducers + 32;   // + the MMA warp
 constexpr int kTokens = 16;                 // MMA N
 constexpr int kStageK = 64;                 // K per stage: 32 TMEM columns of A
@@ -70,8 +70,9 @@ enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2, TC_LM = 3 };
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   constexpr bool LM = MODE == TC_LM;
-  constexpr int kPrefetch = LM ? 3 : 6;   // stages of weights in flight per producer thread
-  constexpr int kVec = LM ? 8 : 2;        // 16-byte loads per thread per stage
+  constexpr int kPrefetch = LM ? 4 : 8;   // stages of weights in flight per producer thread
+  constexpr int kVec = LM ? 4 : 1;        // 16-byte loads per thread per stage (half a stage)
+  constexpr int kHalfTok = kTokens / 2;   // tokens drained by one of a row's two threads
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxSlots];
   __shared__ __align__(8) uint64_t done_bar[kMaxSlots];
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   }
   if (t == 0) {
     for (int i = 0; i < nslots; ++i) {
-      tc::mbar_init(tc::smem_u32(&full_bar[i]), kProducers / 32);
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), kProducers / 32);   // one arrive per producer warp
       tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
     }
     tc::mbar_init(tc::smem_u32(&final_bar), 1);
@@ -249,12 +250,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
     }
     __syncwarp();
   } else {
-    // ---------------- producers: thread t owns weight row t / TMEM lane t
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ---------------- producers: warps w and w + 4 share TMEM lane quarter
+    // w % 4 (weight rows 32 (w % 4) + lane); warp half h = w / 4 writes the
+    // h-th 32-wide half of each stage and drains tokens [8h, 8h + 8).
+    const int quarter = warp & 3, h = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int ng = LM ? 1 : K / a.g;
-    const uint8_t* wt = LM ? W + ((size_t)tile * 128 + t) * (size_t)K * 2 + (size_t)k_begin * 2
-                           : W + (size_t)tile * (K / 32) * 2048 + (size_t)s_begin * 2 * 2048 + (size_t)t * 16;
-    const __half* st_ = LM ? nullptr : S + (size_t)tile * ng * 128 + t;
+    const int gshift = 31 - __clz(a.g);
+    const uint8_t* wt = LM ? W + ((size_t)tile * 128 + row) * (size_t)K * 2 + (size_t)(k_begin + 32 * h) * 2
+                           : W + ((size_t)tile * (K / 32) + 2 * s_begin + h) * 2048 + (size_t)row * 16;
+    const __half* st_ = LM ? nullptr : S + (size_t)tile * ng * 128 + row;
     uint4 ring[kPrefetch][kVec];
     __half2 sring[kPrefetch];
     auto load = [&](int i, uint4 (&w)[kVec], __half2& sc) {
@@ -263,25 +269,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
         for (int v = 0; v < kVec; ++v) w[v] = ldg_nc_v4(wt + (size_t)i * 128 + v * 16);
       } else {
         w[0] = ldg_nc_v4(wt + (size_t)(2 * i) * 2048);
-        w[1] = ldg_nc_v4(wt + (size_t)(2 * i + 1) * 2048);
         const int k0 = (s_begin + i) * kStageK;
-        sc = __halves2half2(st_[(size_t)(k0 / a.g) * 128], st_[(size_t)((k0 + 32) / a.g) * 128]);
+        sc = __halves2half2(st_[(size_t)(k0 >> gshift) * 128], st_[(size_t)((k0 + 32) >> gshift) * 128]);
       }
     };
-    // acc += scale * D of the stage held in `slot` (two groups: two regions)
+    // acc[0..8) += scale * D of the stage held in `slot`, for this half's tokens
     auto drain = [&](int slot) {
       const float2 sc = scale_s[slot][t];
-      const uint32_t dbase = tmem + lane_base + slot * slot_cols + 32;
-      uint32_t d[16];
-      tc::tmem_ld16(dbase, d);
+      const uint32_t dbase = tmem + lane_base + slot * slot_cols + 32 + h * kHalfTok;
+      uint32_t d[8];
+      tc::tmem_ld8(dbase, d);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < kTokens; ++j) acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
+      for (int j = 0; j < kHalfTok; ++j) acc[j] = fmaf(sc.x, __uint_as_float(d[j]), acc[j]);
       if (two_groups) {
-        tc::tmem_ld16(dbase + 16, d);
+        tc::tmem_ld8(dbase + 16, d);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < kTokens; ++j) acc[j] = fmaf(sc.y, __uint_as_float(d[j]), acc[j]);
+        for (int j = 0; j < kHalfTok; ++j) acc[j] = fmaf(sc.y, __uint_as_float(d[j]), acc[j]);
       }
     };
 #pragma unroll
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
       for (int p = 0; p < kPrefetch; ++p) {
         const int i = i0 + p;
         if (i < nst) {
-          uint32_t v[32];
+          uint32_t v[16];
           float2 sc = make_float2(0.f, 0.f);
           if (LM) {
 #pragma unroll
@@ -302,7 +307,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
             }
           } else {
             dq16(ring[p][0], v);
-            dq16(ring[p][1], v + 16);
             sc = __half22float2(sring[p]);
           }
           if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], sring[p]);
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
             if (!LM) drain(slot);   // stage i - nslots, in ascending order
           }
           if (!LM) scale_s[slot][t] = sc;
-          tc::tmem_st32(tmem + lane_base + slot * slot_cols, v);
+          tc::tmem_st16(tmem + lane_base + slot * slot_cols + 16 * h, v);
           tc::tmem_wait_st();
           tc::fence_before_sync();
           __syncwarp();
@@ -325,25 +329,30 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
     if (!tc::mbar_wait(tc::smem_u32(&final_bar), 0u, kWaitLimit)) ok = false;
     tc::fence_after_sync();
     if (LM) {
-      uint32_t d[16];
-      tc::tmem_ld16(tmem + lane_base + lm_dcol, d);
+      uint32_t d[8];
+      tc::tmem_ld8(tmem + lane_base + lm_dcol + h * kHalfTok, d);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < kTokens; ++j) acc[j] = __uint_as_float(d[j]);
+      for (int j = 0; j < kHalfTok; ++j) acc[j] = __uint_as_float(d[j]);
     } else {
       for (int i = (nst > nslots ? nst - nslots : 0); i < nst; ++i) drain(i % nslots);
     }
   }
   if (!ok && a.err) atomicExch(a.err, 4);
 
+  // Producer thread t holds weight row `erow` of the tile and tokens
+  // [etok, etok + 8) in acc[0..8).
+  const int erow = (warp & 3) * 32 + lane, etok = (warp >> 2) * (kTokens / 2);
+  const bool producer = t < kProducers;
+
   // ---- split-K: every split writes its partial sums; the last to arrive
   // adds them in split order and runs the epilogue
   if (ksplit > 1) {
     float* mine = a.part + ((size_t)job * ksplit + ks) * (kTokens * 128);
-    if (t < kProducers) {
+    if (producer) {
 #pragma unroll
-      for (int j = 0; j < kTokens; ++j)
-        if (j < ntok) mine[j * 128 + t] = acc[j];
+      for (int j = 0; j < kTokens / 2; ++j)
+        if (etok + j < ntok) mine[(etok + j) * 128 + erow] = acc[j];
     }
     __threadfence();
     __syncthreads();
@@ -359,13 +368,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
       return;
     }
     __threadfence();
-    if (t < kProducers) {
+    if (producer) {
       const float* base = a.part + (size_t)job * ksplit * (kTokens * 128);
 #pragma unroll
-      for (int j = 0; j < kTokens; ++j) {
-        if (j < ntok) {
+      for (int j = 0; j < kTokens / 2; ++j) {
+        if (etok + j < ntok) {
           float s = 0.f;
-          for (int k2 = 0; k2 < ksplit; ++k2) s += __ldcg(base + ((size_t)k2 * kTokens + j) * 128 + t);
+          for (int k2 = 0; k2 < ksplit; ++k2) s += __ldcg(base + ((size_t)k2 * kTokens + etok + j) * 128 + erow);
           acc[j] = s;
         }
       }
@@ -373,14 +382,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
     if (t == 0) a.counters[job] = 0;
   }
 
-  // ---- epilogue: lane t = weight row t of the tile
-  if (t < kProducers) {
+  // ---- epilogue
+  if (producer) {
     if (MODE == TC_DENSE) {
-      const size_t n = (size_t)tile * 128 + t;
+      const size_t n = (size_t)tile * 128 + erow;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (j < ntok) {
-          const size_t m = row0 + j;
+      for (int j = 0; j < kTokens / 2; ++j) {
+        if (etok + j < ntok) {
+          const size_t m = row0 + etok + j;
           float v = acc[j];
           if (a.Res) v += bf2f(a.Res[m * a.ldr + n]);
           a.Y[m * a.ldy + n] = f2bf(v);
@@ -388,26 +397,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
       }
     } else if (MODE == TC_GATEUP) {
       // rows interleave (gate f, up f): lanes 2i and 2i+1 hold the pair
-      const int f = tile * 64 + (t >> 1);
+      const int f = tile * 64 + (erow >> 1);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kTokens / 2; ++j) {
         const float other = __shfl_xor_sync(0xffffffffu, acc[j], 1);
-        if (j < ntok && (t & 1) == 0) {
+        if (etok + j < ntok && (lane & 1) == 0) {
           const float gv = acc[j], uv = other;
           const float sv = gv / (1.f + expf(-gv));
-          a.act[(size_t)(row0 + j) * a.F + f] = f2bf(sv * uv);
+          a.act[(size_t)(row0 + etok + j) * a.F + f] = f2bf(sv * uv);
         }
       }
     } else if (MODE == TC_DOWN) {
-      const size_t h = (size_t)tile * 128 + t;
+      const size_t hh = (size_t)tile * 128 + erow;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < ntok) a.out[(size_t)(row0 + j) * a.H + h] = acc[j];
+      for (int j = 0; j < kTokens / 2; ++j)
+        if (etok + j < ntok) a.out[(size_t)(row0 + etok + j) * a.H + hh] = acc[j];
     } else {
-      const size_t v = (size_t)tile * 128 + t;
+      const size_t v = (size_t)tile * 128 + erow;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < ntok) a.out[(size_t)(row0 + j) * a.rows + v] = acc[j];
+      for (int j = 0; j < kTokens / 2; ++j)
+        if (etok + j < ntok) a.out[(size_t)(row0 + etok + j) * a.rows + v] = acc[j];
     }
   }
   tc::fence_before_sync();

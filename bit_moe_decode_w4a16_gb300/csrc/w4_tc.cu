@@ -70,7 +70,7 @@ enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2, TC_LM = 3 };
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   constexpr bool LM = MODE == TC_LM;
-  constexpr int kPrefetch = LM ? 4 : 8;   // stages of weights in flight per producer thread
+  constexpr int kPrefetch = LM ? 4 : 6;   // stages of weights in flight per producer thread
   constexpr int kVec = LM ? 4 : 1;        // 16-byte loads per thread per stage (half a stage)
   constexpr int kHalfTok = kTokens / 2;   // tokens drained by one of a row's two threads
   extern __shared__ __align__(128) unsigned char smem[];
@@ -134,24 +134,28 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   }
 
   // ---- activations (this split's K range) -> shared memory, no-swizzle
-  // K-major core matrices of 8 rows x 16 bytes.  Warp w stages rows w,
-  // w+5, ...; a lane loads 4 chunks at a time before using them.  With the
-  // fused RMSNorm the whole row is read first for its mean square.
+  // K-major core matrices of 8 rows x 16 bytes: element (r, k) of the CTA's
+  // 16 x Kc tile sits at byte ((r / 8) * Kc / 8 + k / 8) * 128 + (r % 8) * 16
+  // + (k % 8) * 2, i.e. 16-byte chunk L = ((r / 8) * Kc / 8 + k / 8) * 8 + r % 8.
+  // Thread t fills chunks t, t + kThreads, ... — consecutive threads,
+  // consecutive 16 bytes, no bank conflicts.  With the fused RMSNorm each
+  // row's mean square comes first (one warp per row, the whole K).
   const bool do_norm = (MODE == TC_DENSE || LM) && a.do_norm;
   const int nk8 = Kc / 8;
   const uint32_t sbo = (uint32_t)nk8 * 128u;   // bytes between the two 8-row groups
   constexpr int kWarps = kThreads / 32;
-  for (int r = warp; r < kTokens; r += kWarps) {
-    unsigned char* rowp = smem + (r >> 3) * sbo + (r & 7) * 16;
-    if (r >= ntok) {
-      for (int j = lane; j < nk8; j += 32) *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const bf16* x;
-    if (MODE == TC_GATEUP) x = a.X + (size_t)a.pair_token[row0 + r] * a.ldx;
-    else x = a.X + (size_t)(row0 + r) * a.ldx;
-    float rinv = 1.f;
-    if (do_norm) {
+  __shared__ float rinv_s[kTokens];
+  __shared__ const bf16* rowp_s[kTokens];
+  if (t < kTokens) {
+    const bf16* x = nullptr;
+    if (t < ntok) x = (MODE == TC_GATEUP) ? a.X + (size_t)a.pair_token[row0 + t] * a.ldx
+                                          : a.X + (size_t)(row0 + t) * a.ldx;
+    rowp_s[t] = x;
+  }
+  __syncthreads();
+  if (do_norm) {
+    for (int r = warp; r < ntok; r += kWarps) {
+      const bf16* x = rowp_s[r];
       float ss = 0.f;
       for (int j0 = lane; j0 < K / 8; j0 += 128) {
         uint4 raw[4];
@@ -172,38 +176,50 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
         }
       }
       ss = warp_sum(ss);
-      rinv = 1.0f / sqrtf(ss / (float)K + a.eps);
+      if (lane == 0) rinv_s[r] = 1.0f / sqrtf(ss / (float)K + a.eps);
     }
-    const bf16* xk = x + k_begin;
-    for (int j0 = lane; j0 < nk8; j0 += 128) {
+    __syncthreads();
+  }
+  {
+    const int nchunks = kTokens * nk8;
+    for (int L0 = t; L0 < nchunks; L0 += 4 * kThreads) {
       uint4 raw[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (j0 + 32 * i < nk8) raw[i] = *reinterpret_cast<const uint4*>(xk + (j0 + 32 * i) * 8);
+      for (int i = 0; i < 4; ++i) {
+        const int L = L0 + i * kThreads;
+        raw[i] = make_uint4(0, 0, 0, 0);
+        if (L < nchunks) {
+          const int r = (L / (nk8 * 8)) * 8 + (L & 7), j = (L >> 3) % nk8;
+          if (r < ntok) raw[i] = *reinterpret_cast<const uint4*>(rowp_s[r] + k_begin + j * 8);
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int j = j0 + 32 * i;
-        if (j < nk8) {
-          const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-          uint32_t o[4];
+        const int L = L0 + i * kThreads;
+        if (L < nchunks) {
+          const int r = (L / (nk8 * 8)) * 8 + (L & 7), j = (L >> 3) % nk8;
+          uint32_t o[4] = {0u, 0u, 0u, 0u};
+          if (r < ntok) {
+            const uint32_t rw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
-            if (do_norm) {
-              const int k = k_begin + j * 8 + 2 * q;
-              const float w0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
-              const float w1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
-              v0 = round_bf16(v0 * rinv * w0);
-              v1 = round_bf16(v1 * rinv * w1);
-            }
-            if (LM) {
-              o[q] = (__float_as_uint(v0) >> 16) | (__float_as_uint(v1) & 0xFFFF0000u);   // exact: already bf16
-            } else {
-              __half2 h = __floats2half2_rn(v0, v1);
-              o[q] = *reinterpret_cast<uint32_t*>(&h);
+            for (int q = 0; q < 4; ++q) {
+              float v0 = bf_lo(rw[q]), v1 = bf_hi(rw[q]);
+              if (do_norm) {
+                const int k = k_begin + j * 8 + 2 * q;
+                const float w0 = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
+                const float w1 = a.norm_w ? bf2f(a.norm_w[k + 1]) : 1.f;
+                v0 = round_bf16(v0 * rinv_s[r] * w0);
+                v1 = round_bf16(v1 * rinv_s[r] * w1);
+              }
+              if (LM) {
+                o[q] = (__float_as_uint(v0) >> 16) | (__float_as_uint(v1) & 0xFFFF0000u);   // exact: already bf16
+              } else {
+                __half2 hh = __floats2half2_rn(v0, v1);
+                o[q] = *reinterpret_cast<uint32_t*>(&hh);
+              }
             }
           }
-          *reinterpret_cast<uint4*>(rowp + j * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(smem + (size_t)L * 16) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
     }
@@ -261,16 +277,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
     const uint8_t* wt = LM ? W + ((size_t)tile * 128 + row) * (size_t)K * 2 + (size_t)(k_begin + 32 * h) * 2
                            : W + ((size_t)tile * (K / 32) + 2 * s_begin + h) * 2048 + (size_t)row * 16;
     const __half* st_ = LM ? nullptr : S + (size_t)tile * ng * 128 + row;
+    // The ring holds each stage's weights and scale(s) as loaded: nothing
+    // touches a loaded register before the stage comes round (kPrefetch
+    // stages later), so no load latency is exposed.
     uint4 ring[kPrefetch][kVec];
-    __half2 sring[kPrefetch];
-    auto load = [&](int i, uint4 (&w)[kVec], __half2& sc) {
+    __half slo[kPrefetch], shi[kPrefetch];
+    auto load = [&](int i, uint4 (&w)[kVec], __half& lo, __half& hi) {
       if (LM) {
 #pragma unroll
         for (int v = 0; v < kVec; ++v) w[v] = ldg_nc_v4(wt + (size_t)i * 128 + v * 16);
       } else {
         w[0] = ldg_nc_v4(wt + (size_t)(2 * i) * 2048);
         const int k0 = (s_begin + i) * kStageK;
-        sc = __halves2half2(st_[(size_t)(k0 >> gshift) * 128], st_[(size_t)((k0 + 32) >> gshift) * 128]);
+        lo = st_[(size_t)(k0 >> gshift) * 128];
+        if (two_groups) hi = st_[(size_t)((k0 + 32) >> gshift) * 128];
       }
     };
     // acc[0..8) += scale * D of the stage held in `slot`, for this half's tokens
@@ -291,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
     };
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p)
-      if (p < nst) load(p, ring[p], sring[p]);
+      if (p < nst) load(p, ring[p], slo[p], shi[p]);
     for (int i0 = 0; i0 < nst; i0 += kPrefetch) {
 #pragma unroll
       for (int p = 0; p < kPrefetch; ++p) {
@@ -307,9 +327,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
             }
           } else {
             dq16(ring[p][0], v);
-            sc = __half22float2(sring[p]);
+            sc.x = __half2float(slo[p]);
+            sc.y = two_groups ? __half2float(shi[p]) : sc.x;
           }
-          if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], sring[p]);
+          if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], slo[p], shi[p]);
           const int slot = i % nslots;
           if (i >= nslots) {
             if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / nslots) - 1) & 1u, kWaitLimit))

@@ -49,25 +49,37 @@ constexpr int kLmSlots = 6;                 // output projection: A-only slots, 
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kMaxSplit = 8;
 
-// (u_lo, u_hi) codes of one TMEM column -> the fp16 pair (u_lo - 8, u_hi - 8), exact.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w, int i) {
-  const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;   // (1024 + u_lo, 1024 + u_hi)
-  __half2 h = *reinterpret_cast<const __half2*>(&v);
-  h = __hsub2(h, __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));   // - 1032
-  return *reinterpret_cast<uint32_t*>(&h);
+// One packed word (codes ordered k0 k2 k4 k6 k1 k3 k5 k7) -> the four TMEM
+// columns of fp16 pairs (q_2i, q_2i+1), q = u - 8, exact.  Nibbles at bits
+// 0-3 / 16-19 become 1024 + u (minus 1032 gives q); nibbles at bits 4-7 /
+// 20-23 become 1024 + 16u, and (1024 + 16u) / 16 - 72 = u - 8 in one fma.
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t* out) {
+  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
+  const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));    // -72
+  const uint32_t w8 = w >> 8;
+  uint32_t v0 = (w & 0x000F000Fu) | 0x64006400u, v1 = (w & 0x00F000F0u) | 0x64006400u;
+  uint32_t v2 = (w8 & 0x000F000Fu) | 0x64006400u, v3 = (w8 & 0x00F000F0u) | 0x64006400u;
+  __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&v0), k1032);
+  __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&v1), k16th, km72);
+  __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&v2), k1032);
+  __half2 h3 = __hfma2(*reinterpret_cast<__half2*>(&v3), k16th, km72);
+  out[0] = *reinterpret_cast<uint32_t*>(&h0);
+  out[1] = *reinterpret_cast<uint32_t*>(&h1);
+  out[2] = *reinterpret_cast<uint32_t*>(&h2);
+  out[3] = *reinterpret_cast<uint32_t*>(&h3);
 }
 
 __device__ __forceinline__ void dq16(const uint4 w, uint32_t* out) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) out[q * 4 + c] = dq_pair(ws[q], c);
+  dq_word(w.x, out);
+  dq_word(w.y, out + 4);
+  dq_word(w.z, out + 8);
+  dq_word(w.w, out + 12);
 }
 
 enum TcMode { TC_DENSE = 0, TC_GATEUP = 1, TC_DOWN = 2, TC_LM = 3 };
 
-template <int MODE>
+template <int MODE, bool TWO_GROUPS>
 __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   constexpr bool LM = MODE == TC_LM;
   constexpr int kPrefetch = LM ? 4 : 6;   // stages of weights in flight per producer thread
@@ -112,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
   // TMEM columns: int4 slots are [A 32 | D 16] (g >= 64) or [A 32 | D 2x16]
   // (g == 32, two groups per stage); the output projection has A-only slots
   // and one accumulator after them.
-  const bool two_groups = !LM && a.g == 32;
-  const int dcols = LM ? 0 : (two_groups ? 32 : 16);
-  const int slot_cols = 32 + dcols;
-  const int nslots = LM ? kLmSlots : (two_groups ? 4 : 5);
-  const int lm_dcol = kLmSlots * 32;
+  constexpr bool two_groups = !LM && TWO_GROUPS;
+  constexpr int dcols = LM ? 0 : (two_groups ? 32 : 16);
+  constexpr int slot_cols = 32 + dcols;
+  constexpr int nslots = LM ? kLmSlots : (two_groups ? 4 : 5);
+  constexpr int lm_dcol = kLmSlots * 32;
 
   // ---- TMEM and barriers
   if (warp == 0) {
@@ -239,9 +251,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
     if (lane == 0) {
       const uint32_t b_base = tc::smem_u32(smem);
       const uint32_t idesc = LM ? tc::idesc_bf16_f32(128, kTokens) : tc::idesc_f16_f32(128, kTokens);
+      int slot = 0;
+      uint32_t phase = 0;
       for (int i = 0; i < nst; ++i) {
-        const int slot = i % nslots;
-        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), (uint32_t)(i / nslots) & 1u, kWaitLimit)) ok = false;
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[slot]), phase, kWaitLimit)) ok = false;
         tc::fence_after_sync();
         const uint32_t acol = slot * slot_cols;
 #pragma unroll
@@ -261,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
           tc::mma_f16_tmem_a(tmem + dcol, tmem + acol + q * 8, bd, idesc, accum);
         }
         tc::mma_commit(tc::smem_u32(&done_bar[slot]));
+        if (++slot == nslots) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
       tc::mma_commit(tc::smem_u32(&final_bar));
     }
@@ -312,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p)
       if (p < nst) load(p, ring[p], slo[p], shi[p]);
+    int slot = 0;
+    uint32_t phase = 0;   // parity of the `done` phase to wait for at this slot
     for (int i0 = 0; i0 < nst; i0 += kPrefetch) {
 #pragma unroll
       for (int p = 0; p < kPrefetch; ++p) {
@@ -331,10 +350,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
             sc.y = two_groups ? __half2float(shi[p]) : sc.x;
           }
           if (i + kPrefetch < nst) load(i + kPrefetch, ring[p], slo[p], shi[p]);
-          const int slot = i % nslots;
           if (i >= nslots) {
-            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), (uint32_t)((i / nslots) - 1) & 1u, kWaitLimit))
-              ok = false;
+            if (!tc::mbar_wait(tc::smem_u32(&done_bar[slot]), phase, kWaitLimit)) ok = false;
             tc::fence_after_sync();
             if (!LM) drain(slot);   // stage i - nslots, in ascending order
           }
@@ -344,6 +361,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_w4_tc(TcArgs a) {
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[slot]));
+          if (++slot == nslots) {
+            slot = 0;
+            if (i >= nslots) phase ^= 1u;
+          }
         }
       }
     }
@@ -483,13 +504,15 @@ __global__ void k_repack_tc(const uint8_t* src, const __half* ssrc, const uint8_
 
 template <int MODE>
 cudaError_t run_tc(const TcArgs& a, dim3 grid, cudaStream_t st) {
+  const bool two = MODE != TC_LM && a.g == 32;
   const int ks = a.ksplit < 1 ? 1 : a.ksplit;
   if ((a.K / kStageK) % ks != 0 || ks > kMaxSplit || (ks > 1 && (!a.part || !a.counters)))
     return cudaErrorInvalidValue;
   grid.x *= ks;
   const size_t smem = (size_t)kTokens * (a.K / ks) * 2;
   if (smem > (size_t)kTokens * 4096 * 2) return cudaErrorInvalidValue;
-  k_w4_tc<MODE><<<grid, kThreads, smem, st>>>(a);
+  if (two) k_w4_tc<MODE, true><<<grid, kThreads, smem, st>>>(a);
+  else k_w4_tc<MODE, false><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -541,20 +564,24 @@ cudaError_t launch_lm_tc(const TcArgs& a, cudaStream_t st) {
   return run_tc<TC_LM>(a, grid, st);
 }
 
-template <int MODE>
+template <int MODE, bool TWO>
 cudaError_t set_tc_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(k_w4_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokens * 4096 * 2);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_w4_tc<MODE, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokens * 4096 * 2);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_w4_tc<MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(k_w4_tc<MODE, TWO>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
 cudaError_t init_tc_attributes() {
-  cudaError_t e = set_tc_attrs<TC_DENSE>();
-  if (e == cudaSuccess) e = set_tc_attrs<TC_GATEUP>();
-  if (e == cudaSuccess) e = set_tc_attrs<TC_DOWN>();
-  if (e == cudaSuccess) e = set_tc_attrs<TC_LM>();
+  cudaError_t e = set_tc_attrs<TC_DENSE, false>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_DENSE, true>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_GATEUP, false>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_GATEUP, true>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_DOWN, false>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_DOWN, true>();
+  if (e == cudaSuccess) e = set_tc_attrs<TC_LM, false>();
   return e;
 }
 

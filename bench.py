@@ -328,7 +328,7 @@ def run_ours(args, dist, world, rank, local):
                    "kv_len_mean_at_start": round(sum(lens) / len(lens), 1),
                    "l2": "inputs larger than L2: ~14.6 GB of weights read per step",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
-                   "kernel_family": "tc" if bm.bm_engine_kernel_family(e) == 2 else "simt"},
+                   "kernel_family": {1: "simt", 2: "tc", 3: "mma"}.get(bm.bm_engine_kernel_family(e), "?")},
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": int(launches),
         "graph_launches_per_step": (st1["graph_launches"] - st0["graph_launches"]) / (args.steps + args.warmup),
         "roofline": roof,

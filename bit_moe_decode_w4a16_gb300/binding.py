@@ -20,7 +20,7 @@ STATUS_NAMES = {
     4: "BM_ERR_SLOT_FREE", 5: "BM_ERR_CUDA", 6: "BM_ERR_OOM", 7: "BM_ERR_NOT_READY",
     8: "BM_ERR_DEVICE_CHECK", 9: "BM_ERR_UNSUPPORTED",
 }
-POLICY_AUTO, POLICY_SIMT, POLICY_TC = 0, 1, 2
+POLICY_AUTO, POLICY_SIMT, POLICY_TC, POLICY_MMA = 0, 1, 2, 3
 
 
 class BitMoeError(RuntimeError):
@@ -94,6 +94,8 @@ def lib():
             "bm_moe_workspace_bytes": ([I, I, I, I, I], SZ),
             "bm_w4_repack_tc": ([V, V, I, I, I, V, V, V], S),
             "w4_gemm_batched_tc": ([V, V, V, V, V, I, I, I, I, V], S),
+            "bm_w4_repack_mma": ([V, V, I, I, I, V, V, V], S),
+            "w4_gemm_batched_mma": ([V, V, V, V, V, I, I, I, I, V], S),
             "moe_grouped_w4": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V, SZ, V], S),
             "moe_grouped_w4_noalloc": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V], S),
             "bm_moe_noalloc_max_bytes": ([], SZ),
@@ -247,6 +249,14 @@ def bm_w4_repack_tc(W, S, N, K, g, Wtc, Stc, stream=None):
 
 def w4_gemm_batched_tc(Wtc, Stc, X, Y, R, M, N, K, g, stream=None):
     _check(lib().w4_gemm_batched_tc(ptr(Wtc), ptr(Stc), ptr(X), ptr(Y), ptr(R), M, N, K, g, stream_handle(stream)))
+
+
+def bm_w4_repack_mma(W, S, N, K, g, Wm, Sm, stream=None):
+    _check(lib().bm_w4_repack_mma(ptr(W), ptr(S), N, K, g, ptr(Wm), ptr(Sm), stream_handle(stream)))
+
+
+def w4_gemm_batched_mma(Wm, Sm, X, Y, R, M, N, K, g, stream=None):
+    _check(lib().w4_gemm_batched_mma(ptr(Wm), ptr(Sm), ptr(X), ptr(Y), ptr(R), M, N, K, g, stream_handle(stream)))
 
 
 def bm_moe_workspace_bytes(B, experts, top_k, hidden, ffn):

@@ -87,10 +87,20 @@ __device__ __forceinline__ size_t part_index(int b, int h, int c, int qh, int ma
   return (((size_t)b * qh + h) * max_chunks + c) * (size_t)(d + 2);
 }
 
-// blockDim.x == kAttnChunk == 128 threads; D = head_dim (64 or 128).
-// Scores: thread t takes position j0 + t; its whole K row is loaded up front.
-// p·V: thread t takes dimension t of every q head of the group; the V rows
-// of the chunk are read in order, 8 positions per batch of loads.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// blockDim.x == kAttnChunk == 128 threads; D = head_dim (64 or 128).  Grid
+// (kv head, stream, chunk): the chunks past a stream's length exit at once
+// and sit at the end of the launch order.
+// The chunk's V rows are copied to shared memory asynchronously while the
+// scores are computed.  Scores: thread t takes position j0 + t, its whole K
+// row loaded up front.  p.V: thread t takes dimension t of every q head of
+// the group, positions in ascending order.
 template <int D>
 __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int layer, const int32_t* slots,
                                                           const bf16* q, int qh, float* part, int max_chunks,
@@ -99,24 +109,31 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
   __shared__ float ps[kMaxGroup][kAttnChunk];
   __shared__ float red[kMaxGroup][kAttnChunk / 32];
   __shared__ float stat[kMaxGroup][2];
-  const int c = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  __shared__ __align__(16) bf16 vs[kAttnChunk][D];
+  const int kh = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
   const int slot = slots[b];
   if (slot < 0 || slot >= ar.S) { if (c == 0 && kh == 0 && threadIdx.x == 0) chk.fail(1); return; }
   const int L = ar.len[slot] + 1;   // committed prefix + this step's position
   if (L < 1 || L > ar.cap) { if (c == 0 && kh == 0 && threadIdx.x == 0) chk.fail(2); return; }
   const int j0 = c * kAttnChunk;
   if (j0 >= L) return;
+  const int n = min(kAttnChunk, L - j0);
   const int G = qh / ar.kvh, t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const float scale = 1.0f / sqrtf((float)D);
+  const size_t base = layer * ar.layer_stride() + slot * ar.slot_stride() + (size_t)kh * ar.cap * D;
+  const bf16* Kb = ar.K + base;
+  const bf16* Vb = ar.V + base;
+  constexpr int kVecs = D / 8;
+  for (int i = t; i < n * kVecs; i += kAttnChunk) {
+    const int r = i / kVecs, v8 = i - r * kVecs;
+    cp_async16(&vs[r][v8 * 8], Vb + (size_t)(j0 + r) * D + v8 * 8);
+  }
+  cp_async_commit();
   for (int idx = t; idx < G * D; idx += blockDim.x) {
     const int g = idx / D, i = idx - g * D;
     qs[g][i] = bf2f(q[((size_t)b * qh + kh * G + g) * D + i]);
   }
-  const size_t base = layer * ar.layer_stride() + slot * ar.slot_stride() + (size_t)kh * ar.cap * D;
-  const bf16* Kb = ar.K + base;
-  const bf16* Vb = ar.V + base;
   const int j = j0 + t;
-  constexpr int kVecs = D / 8;
   uint4 kr[kVecs];
   if (j < L) {
     const uint4* src = reinterpret_cast<const uint4*>(Kb + (size_t)j * D);
@@ -169,6 +186,7 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
     const float sum = warp_sum(p);
     if (lane == 0) red[g][warp] = sum;
   }
+  cp_async_wait_all();
   __syncthreads();
   if (t < G) {
     float l = 0.f;
@@ -176,24 +194,15 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
     stat[t][1] = l;
   }
   __syncthreads();
-  const int n = min(kAttnChunk, L - j0);
   if (t < D) {
     float o[kMaxGroup];
 #pragma unroll
     for (int g = 0; g < kMaxGroup; ++g) o[g] = 0.f;
-    const bf16* vcol = Vb + (size_t)j0 * D + t;
-    for (int jj0 = 0; jj0 < n; jj0 += 8) {
-      float vv[8];
+    for (int jj = 0; jj < n; ++jj) {
+      const float vv = bf2f(vs[jj][t]);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) vv[u] = (jj0 + u < n) ? bf2f(vcol[(size_t)(jj0 + u) * D]) : 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (jj0 + u < n) {
-#pragma unroll
-          for (int g = 0; g < kMaxGroup; ++g)
-            if (g < G) o[g] = fmaf(ps[g][jj0 + u], vv[u], o[g]);
-        }
-      }
+      for (int g = 0; g < kMaxGroup; ++g)
+        if (g < G) o[g] = fmaf(ps[g][jj], vv, o[g]);
     }
 #pragma unroll
     for (int g = 0; g < kMaxGroup; ++g) {
@@ -208,22 +217,48 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
   }
 }
 
+// One CTA per (q head, stream): the chunks' (m, l) go to shared memory in
+// parallel, then thread t merges dimension t over the chunks in ascending
+// order with eight chunks' loads in flight at a time.
+constexpr int kMaxChunksSmem = 1024;
+
 __global__ void k_attn_combine(AttnArena ar, const int32_t* slots, const float* part, int qh, int max_chunks,
                                bf16* out) {
+  __shared__ float ml_s[kMaxChunksSmem][2];
+  __shared__ float M_s;
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x, d = ar.d;
   const int slot = slots[b];
   if (slot < 0 || slot >= ar.S) return;
   const int L = ar.len[slot] + 1;
   if (L < 1 || L > ar.cap) return;
   const int nc = (L + kAttnChunk - 1) / kAttnChunk;
-  float M = -FLT_MAX;
-  for (int c = 0; c < nc; ++c) M = fmaxf(M, part[part_index(b, h, c, qh, max_chunks, d) + d]);
-  float den = 0.f, acc = 0.f;
-  for (int c = 0; c < nc; ++c) {
+  for (int c = t; c < nc; c += blockDim.x) {
     const float* rec = part + part_index(b, h, c, qh, max_chunks, d);
-    const float w = expf(rec[d] - M);
-    den = fmaf(rec[d + 1], w, den);
-    if (t < d) acc = fmaf(rec[t], w, acc);
+    ml_s[c][0] = rec[d];
+    ml_s[c][1] = rec[d + 1];
+  }
+  __syncthreads();
+  if (t == 0) {
+    float M = -FLT_MAX;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, ml_s[c][0]);
+    M_s = M;
+  }
+  __syncthreads();
+  const float M = M_s;
+  float den = 0.f, acc = 0.f;
+  for (int c0 = 0; c0 < nc; c0 += 8) {
+    float o[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      o[u] = (t < d && c0 + u < nc) ? part[part_index(b, h, c0 + u, qh, max_chunks, d) + t] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (c0 + u < nc) {
+        const float w = expf(ml_s[c0 + u][0] - M);
+        den = fmaf(ml_s[c0 + u][1], w, den);
+        acc = fmaf(o[u], w, acc);
+      }
+    }
   }
   if (t < d) out[((size_t)b * qh + h) * d + t] = f2bf(acc / den);
 }
@@ -254,7 +289,8 @@ cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slot
                              const Marker& mark) {
   if (ar.d > 128 || ar.d % 8 != 0 || qh % ar.kvh != 0 || qh / ar.kvh > kMaxGroup) return cudaErrorInvalidValue;
   const int max_chunks = (ar.cap + kAttnChunk - 1) / kAttnChunk;
-  dim3 g1(max_chunks, ar.kvh, B);
+  if (max_chunks > kMaxChunksSmem) return cudaErrorInvalidValue;
+  dim3 g1(ar.kvh, B, max_chunks);
   if (ar.d == 128) k_attn_part<128><<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
   else if (ar.d == 64) k_attn_part<64><<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
   else return cudaErrorInvalidValue;

@@ -59,6 +59,19 @@ __device__ __forceinline__ float group_sum(float v) {
   return v;
 }
 
+// 1 / sqrt(S / n + eps), S = the CTA-wide sum of the threads' partials ss,
+// added in a fixed order (each warp's butterfly, then the warps in ascending
+// order).  Every thread returns the same value.  red: >= 32 floats of shared
+// memory, not reused by the caller until the next __syncthreads.
+__device__ __forceinline__ float block_rms_inv(float ss, int n, float eps, float* red) {
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+  return 1.0f / sqrtf(tot / (float)n + eps);
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

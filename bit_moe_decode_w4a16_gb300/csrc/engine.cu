@@ -54,6 +54,7 @@ bm_status ensure_attributes() {
   BM_CUDA(init_moe_attributes(), "kernel attributes (experts)");
   BM_CUDA(init_misc_attributes(), "kernel attributes (lm_head)");
   BM_CUDA(init_tc_attributes(), "kernel attributes (tensor-core projections)");
+  BM_CUDA(init_mma_attributes(), "kernel attributes (warp-MMA projections)");
   g_attr_devices.insert(dev);
   return BM_OK;
 }
@@ -111,6 +112,9 @@ struct bm_engine {
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   bf16 *x = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr;
+  bf16* xn = nullptr;                      // RMSNorm of x for the next projection (warp-MMA family)
+  unsigned long long* lm_keys = nullptr;   // fused argmax keys [max_streams], zero between launches
+  unsigned int* lm_counter = nullptr;
   float* attn_part = nullptr;
   void* moe_ws = nullptr;
   float* logits = nullptr;
@@ -167,8 +171,81 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
   }
 }
 
+// The step on the warp-MMA family.  Every RMSNorm is computed by the kernel
+// that produces its input row (embedding, router, combine), so the
+// projections read ready activations: embed+norm, then per layer QKV,
+// rope+append, attention (2), o_proj+residual, router, top-k+sort, gate/up,
+// down, combine+norm; then lm_head with the argmax fused.
+cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark) {
+  const bm_config& c = e->cfg;
+  const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
+  cudaError_t err;
+  int n = 0;
+  auto attn_nw = [&](int l) -> const bf16* { return e->L[l].has_attn_norm ? e->L[l].attn_norm_buf : nullptr; };
+  auto u32 = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
+  if ((err = launch_embed_norm(e->embed, c.vocab, H, e->d_tokens, e->x, attn_nw(0), c.rms_eps, e->xn, B,
+                               chk_of(e), s)) != cudaSuccess)
+    return err;
+  mark(KT_EMBED);
+  ++n;
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerW& w = e->L[l];
+    MmaArgs m1{};
+    m1.W = w.wqkv; m1.S = u32(w.wqkv_s); m1.rows = e->qkv_rows; m1.K = H; m1.g = g;
+    m1.X = e->xn; m1.ldx = H; m1.ntok = B; m1.Y = e->qkv; m1.ldy = e->qkv_rows;
+    if ((err = launch_w4_mma_dense(m1, s)) != cudaSuccess) return err;
+    mark(KT_QKV);
+    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
+                                  chk_of(e), s)) != cudaSuccess)
+      return err;
+    mark(KT_ROPE_APPEND);
+    n += 2;
+    if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
+                                &n, mark)) != cudaSuccess)
+      return err;
+    MmaArgs m2{};
+    m2.W = w.wo; m2.S = u32(w.wo_s); m2.rows = H; m2.K = qd; m2.g = g;
+    m2.X = e->attn; m2.ldx = qd; m2.ntok = B; m2.Res = e->x; m2.ldr = H; m2.Y = e->h; m2.ldy = H;
+    if ((err = launch_w4_mma_dense(m2, s)) != cudaSuccess) return err;
+    mark(KT_OPROJ);
+    MoeArgs ma{B, c.experts, c.top_k, H, F, g, c.renorm_topk,
+               w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
+               e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l};
+    const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, F);
+    if ((err = launch_moe_route(ma, mb, s, mark)) != cudaSuccess) return err;
+    MmaArgs m3{};
+    m3.W = w.wg; m3.S = u32(w.wg_s); m3.rows = 2 * F; m3.K = H; m3.g = g; m3.X = mb.xn; m3.ldx = H;
+    m3.pair_token = mb.pair_token; m3.n_jobs = mb.n_jobs; m3.jobs = mb.jobs;
+    m3.max_jobs = moe_max_jobs(B, c.experts, c.top_k);
+    m3.w_expert_stride = (size_t)2 * F * H / 2; m3.s_expert_stride = (size_t)F * (H / g);
+    m3.act = mb.act; m3.F = F;
+    if ((err = launch_w4_mma_gateup(m3, s)) != cudaSuccess) return err;
+    mark(KT_GATEUP);
+    MmaArgs m4{};
+    m4.W = w.wd; m4.S = u32(w.wd_s); m4.rows = H; m4.K = F; m4.g = g; m4.X = mb.act; m4.ldx = F;
+    m4.pair_token = mb.pair_token; m4.n_jobs = mb.n_jobs; m4.jobs = mb.jobs; m4.max_jobs = m3.max_jobs;
+    m4.w_expert_stride = (size_t)H * F / 2; m4.s_expert_stride = (size_t)H * (F / g) / 2;
+    m4.out = mb.out; m4.H = H;
+    if ((err = launch_w4_mma_down(m4, s)) != cudaSuccess) return err;
+    mark(KT_DOWN);
+    const bf16* next_nw = l + 1 < c.layers ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
+    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, s, mark)) != cudaSuccess) return err;
+    n += 6;   // o_proj, router, top-k + sort, gate/up, down, combine
+  }
+  LmArgs la{};
+  la.W = e->lm_head; la.V = c.vocab; la.K = H; la.X = e->xn; la.B = B; la.logits = e->logits;
+  la.next = e->d_next; la.len = e->arena.len; la.slots = e->d_slots; la.advance = 1;
+  la.keys = e->lm_keys; la.counter = e->lm_counter;
+  if ((err = launch_lm_mma(la, s)) != cudaSuccess) return err;
+  mark(KT_LM_HEAD);
+  ++n;
+  if (launches) *launches = n;
+  return cudaSuccess;
+}
+
 // Enqueue one decode step for B streams reading e->d_slots / e->d_tokens.
 cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark = Marker()) {
+  if (e->family == BM_POLICY_MMA) return enqueue_step_mma(e, B, s, launches, mark);
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim;
   const bool tc = e->family == BM_POLICY_TC;
@@ -308,6 +385,13 @@ bool tc_shapes_ok(const bm_config& c) {
          tc_supports(2 * c.ffn, c.hidden, c.group) && tc_supports(c.hidden, c.ffn, c.group);
 }
 
+bool mma_shapes_ok(const bm_config& c) {
+  const int qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim, qd = c.q_heads * c.head_dim;
+  return mma_supports(qkv_rows, c.hidden, c.group) && mma_supports(c.hidden, qd, c.group) &&
+         mma_supports(2 * c.ffn, c.hidden, c.group) && mma_supports(c.hidden, c.ffn, c.group) &&
+         c.ffn % 16 == 0 && lm_mma_supports(c.vocab, c.hidden, 1) && c.hidden <= 8192;
+}
+
 bm_status check_config(const bm_config& c) {
   auto bad = [](const std::string& m) { return set_error(BM_ERR_INVALID_ARG, "bm_engine_create: " + m); };
   if (c.hidden <= 0 || c.hidden % 32 != 0) return bad("hidden must be a positive multiple of 32");
@@ -323,11 +407,14 @@ bm_status check_config(const bm_config& c) {
   if (c.vocab < 1 || c.layers < 1) return bad("vocab and layers must be >= 1");
   if (c.max_streams < 1 || c.max_streams > 64) return bad("max_streams must be in [1, 64]");
   if (c.max_streams * c.top_k > 1024) return bad("max_streams * top_k must be <= 1024");
-  if (c.ctx_cap < 1) return bad("ctx_cap must be >= 1");
+  if (c.ctx_cap < 1 || c.ctx_cap > 131072) return bad("ctx_cap must be in [1, 131072]");
   if (!(c.rope_base > 0.f) || !(c.rms_eps >= 0.f)) return bad("rope_base > 0 and rms_eps >= 0 required");
   if (!simt_supports_k(c.hidden) || !simt_supports_k(c.ffn) || !simt_supports_k(c.q_heads * c.head_dim))
     return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: a reduction length has no kernel shape in this build");
-  if (c.kernel_policy < 0 || c.kernel_policy > 2) return bad("unknown kernel_policy");
+  if (c.kernel_policy < 0 || c.kernel_policy > 3) return bad("unknown kernel_policy");
+  if (c.kernel_policy == BM_POLICY_MMA && !mma_shapes_ok(c))
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: shapes outside the warp-MMA family (rows multiples "
+                                         "of 32, reduction lengths multiples of 128 up to 4096, vocab % 16 == 0)");
   if (c.kernel_policy == BM_POLICY_TC && !tc_shapes_ok(c))
     return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: shapes outside the tensor-core family (rows must be "
                                          "multiples of 128, reduction lengths multiples of 64 up to 4096)");
@@ -380,7 +467,10 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   cudaGetDevice(&e->device);
   // The family is fixed for the engine's life, never chosen per step, so a
   // stream's bytes never depend on the batch it is decoded in.
-  e->family = (c.kernel_policy == BM_POLICY_SIMT || !tc_shapes_ok(c)) ? BM_POLICY_SIMT : BM_POLICY_TC;
+  if (c.kernel_policy == BM_POLICY_SIMT) e->family = BM_POLICY_SIMT;
+  else if (c.kernel_policy == BM_POLICY_TC) e->family = BM_POLICY_TC;
+  else if (mma_shapes_ok(c)) e->family = BM_POLICY_MMA;
+  else e->family = tc_shapes_ok(c) ? BM_POLICY_TC : BM_POLICY_SIMT;
   e->qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim;
   const int H = c.hidden, E = c.experts, F = c.ffn, g = c.group, qd = c.q_heads * c.head_dim;
   const size_t S = c.max_streams;
@@ -455,7 +545,8 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
              s_part = take(attn_partial_floats(c.max_streams, c.q_heads, c.ctx_cap, c.head_dim) * 4),
              s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
              s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
-             s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4);
+             s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4), s_xn = take(S * H * 2),
+             s_keys = take(S * 8), s_cnt = take(4);
   size_t tc_jobs = 0, tc_floats = 0;
   if (e->family == BM_POLICY_TC) tc_workspace(c, e->qkv_rows, &tc_jobs, &tc_floats);
   const Part s_tcp = take(tc_floats * 4), s_tcc = take(tc_jobs * 4);
@@ -476,6 +567,9 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   e->d_slots_aux = reinterpret_cast<int32_t*>(sb + s_sa.off);
   e->d_err = reinterpret_cast<int*>(sb + s_err.off);
   e->d_u_log = reinterpret_cast<int32_t*>(sb + s_ulog.off);
+  e->xn = reinterpret_cast<bf16*>(sb + s_xn.off);
+  e->lm_keys = reinterpret_cast<unsigned long long*>(sb + s_keys.off);
+  e->lm_counter = reinterpret_cast<unsigned int*>(sb + s_cnt.off);
   e->tc_part = tc_floats ? reinterpret_cast<float*>(sb + s_tcp.off) : nullptr;
   e->tc_counters = tc_jobs ? reinterpret_cast<int*>(sb + s_tcc.off) : nullptr;
   BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");
@@ -499,7 +593,8 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
                "bitmoe: engine on device %d: weights %.3f GB, KV arena %.3f GB (%d layers x %d slots x %d "
                "positions x %d kv heads x %d), scratch %.1f MB, kernel family %s\n",
                e->device, e->wbytes / 1e9, e->arena_bytes / 1e9, c.layers, c.max_streams, c.ctx_cap, c.kv_heads,
-               c.head_dim, e->scratch_bytes / 1e6, e->family == BM_POLICY_TC ? "tc" : "simt");
+               c.head_dim, e->scratch_bytes / 1e6,
+               e->family == BM_POLICY_MMA ? "mma" : (e->family == BM_POLICY_TC ? "tc" : "simt"));
   *out = guard.release();
   return bm::ok();
 }
@@ -524,7 +619,22 @@ bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w
   auto cp = [&](void* dst, const void* src, size_t bytes) {
     return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s);
   };
-  if (e->family == BM_POLICY_TC) {
+  if (e->family == BM_POLICY_MMA) {
+    // repack into the warp-MMA layout; F % 8 == 0, so tile T of the whole
+    // gate/up bank is gate rows 8T..8T+7 then the same up rows, all of one
+    // expert, and expert x's tiles start at row 2xF
+    auto h = [](const uint16_t* p) { return reinterpret_cast<const __half*>(p); };
+    auto u32 = [](__half* p) { return reinterpret_cast<uint32_t*>(p); };
+    BM_CUDA(launch_repack_mma(w->wqkv, h(w->wqkv_s), nullptr, nullptr, e->qkv_rows, H, g, d.wqkv, u32(d.wqkv_s), s),
+            "set_layer wqkv repack");
+    BM_CUDA(launch_repack_mma(w->wo, h(w->wo_s), nullptr, nullptr, H, qd, g, d.wo, u32(d.wo_s), s),
+            "set_layer wo repack");
+    BM_CUDA(launch_repack_mma(w->wg, h(w->wg_s), w->wu, h(w->wu_s), 2 * E * F, H, g, d.wg, u32(d.wg_s), s),
+            "set_layer gate/up repack");
+    BM_CUDA(launch_repack_mma(w->wd, h(w->wd_s), nullptr, nullptr, E * H, F, g, d.wd, u32(d.wd_s), s),
+            "set_layer down repack");
+    BM_CUDA(cp(d.wr, w->wr, (size_t)E * H * 4), "set_layer router");
+  } else if (e->family == BM_POLICY_TC) {
     // repack into the tensor-core layout; the gate and up banks interleave
     // row by row (row 2f = gate f, row 2f+1 = up f) so a TMEM lane pair holds
     // both halves of one SiLU(g)*u
@@ -907,6 +1017,34 @@ bm_status bm_w4_repack_tc(const uint8_t* W, const uint16_t* S, int N, int K, int
   BM_CUDA(launch_repack_tc(W, reinterpret_cast<const __half*>(S), nullptr, nullptr, N, K, g, Wtc,
                            reinterpret_cast<__half*>(Stc), static_cast<cudaStream_t>(stream)),
           "bm_w4_repack_tc launch");
+  return bm::ok();
+}
+
+bm_status bm_w4_repack_mma(const uint8_t* W, const uint16_t* S, int N, int K, int g, uint8_t* Wm, uint32_t* Sm,
+                           void* stream) {
+  if (!W || !S || !Wm || !Sm) return set_error(BM_ERR_INVALID_ARG, "bm_w4_repack_mma: null pointer");
+  if (!mma_supports(N, K, g))
+    return set_error(BM_ERR_INVALID_ARG, "bm_w4_repack_mma: need N % 32 == 0, K % 128 == 0, K <= 4096, "
+                                         "g in {32, 64, 128}, K % g == 0");
+  BM_CUDA(launch_repack_mma(W, reinterpret_cast<const __half*>(S), nullptr, nullptr, N, K, g, Wm, Sm,
+                            static_cast<cudaStream_t>(stream)),
+          "bm_w4_repack_mma launch");
+  return bm::ok();
+}
+
+bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint16_t* X, uint16_t* Y,
+                              const uint16_t* R, int M, int N, int K, int g, void* stream) {
+  if (!Wm || !Sm || !X || !Y) return set_error(BM_ERR_INVALID_ARG, "w4_gemm_batched_mma: null pointer");
+  if (M < 1 || !mma_supports(N, K, g))
+    return set_error(BM_ERR_INVALID_ARG, "w4_gemm_batched_mma: need M >= 1, N % 32 == 0, K % 128 == 0, "
+                                         "K <= 4096, g in {32, 64, 128}, K % g == 0");
+  bm_status st = ensure_attributes();
+  if (st != BM_OK) return st;
+  MmaArgs a{};
+  a.W = Wm; a.S = Sm; a.rows = N; a.K = K; a.g = g;
+  a.X = reinterpret_cast<const bf16*>(X); a.ldx = K; a.ntok = M;
+  a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
+  BM_CUDA(launch_w4_mma_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched_mma launch");
   return bm::ok();
 }
 

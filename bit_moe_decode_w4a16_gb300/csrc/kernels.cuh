@@ -53,11 +53,19 @@ struct MoeBufs {
   int32_t* active_off;  // [E+1]
   int32_t* pair_token;  // [B*k] token of the p-th pair in expert order
   int32_t* pos_of;      // [B*k] sorted position of pair (b, r) = b*k + r
+  // work list of the warp-MMA expert kernels, in expert order: job j =
+  // e | first << 9 | n << 21 is the n (<= 8) sorted pairs first.. of expert e
+  int32_t* n_jobs;      // [1]
+  int32_t* jobs;        // [moe_max_jobs(B, E, k)]
   bf16* act;            // [B*k][F]
   float* out;           // [B*k][H]
 };
 size_t moe_scratch_bytes(int B, int E, int k, int H, int F);
 MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F);
+// Upper bound of the job count: sum over active experts of ceil(count / 8)
+// <= min(E, B k) + B k / 8.
+int moe_max_jobs(int B, int E, int k);
+constexpr int kJobTokens = 8;
 
 struct MoeArgs {
   int B, E, k, H, F, g, renorm;
@@ -80,6 +88,10 @@ cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int*
 // combine (1 launch) on their own, for the tensor-core expert path.
 cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
 cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
+// The combine with the next RMSNorm fused: also xn[b] = RMSNorm(y[b]) * nw
+// (nw null = ones; a.eps).  H <= 8192.
+cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, bf16* xn, cudaStream_t st,
+                                    const Marker& mark);
 
 // ---------------------------------------------------------------- tensor-core W4A16
 struct TcArgs {
@@ -129,6 +141,62 @@ cudaError_t launch_w4_tc_down(const TcArgs& a, int max_u, int max_tok, cudaStrea
 cudaError_t launch_lm_tc(const TcArgs& a, cudaStream_t st);
 cudaError_t init_tc_attributes();
 
+// ---------------------------------------------------------------- warp-MMA W4A16
+struct MmaArgs {
+  const uint8_t* W;          // mma layout (whole bank for experts)
+  const uint32_t* S;         // [tiles][K/g][8] fp16 pairs
+  int rows, K, g;            // rows of one matrix (one expert for the banks)
+  const bf16* X;             // activations (already normalised where the op needs it)
+  int ldx;
+  int ntok;                  // dense: number of activation rows
+  const bf16* Res;           // dense: residual [ntok][ldr] or null
+  int ldr;
+  bf16* Y;                   // dense output [ntok][ldy]
+  int ldy;
+  const int32_t* pair_token; // experts: token of each sorted pair
+  const int32_t* n_jobs;     // experts: routing work list
+  const int32_t* jobs;
+  int max_jobs;              // grid bound of the expert launches
+  size_t w_expert_stride;    // bytes of one expert's matrix
+  size_t s_expert_stride;    // 32-bit words of one expert's scales
+  bf16* act;                 // gate/up output [pairs][F]
+  int F;
+  float* out;                // down output [pairs][H]
+  int H;
+  int ks;                    // set by the launchers
+};
+// Shape support of the warp-MMA kernels: rows % 32 == 0, K % 128 == 0,
+// K <= 4096, g in {32, 64, 128}.
+bool mma_supports(int rows, int K, int g);
+// Canonical [rows][K/2] (+ scales) -> mma layout; with W2/S2 the 16-row
+// tiles hold 8 rows of W then the same 8 rows of W2 (gate/up banks).
+cudaError_t launch_repack_mma(const uint8_t* W, const __half* S, const uint8_t* W2, const __half* S2, int rows,
+                              int K, int g, uint8_t* Wm, uint32_t* Sm, cudaStream_t st);
+cudaError_t launch_w4_mma_dense(MmaArgs a, cudaStream_t st);
+cudaError_t launch_w4_mma_gateup(MmaArgs a, cudaStream_t st);
+cudaError_t launch_w4_mma_down(MmaArgs a, cudaStream_t st);
+// Output projection + greedy argmax: logits[b][v] = x[b] . W[v] (bf16 W
+// [V][K] row-major, x already normalised, fp32 out), next[b] = argmax_v
+// (ties: lowest v, NaN never wins) and len[slots[b]] += advance, in one
+// launch.  keys [B] (u64) and counter [1] are zero before the launch and left
+// zero after it.
+struct LmArgs {
+  const bf16* W;
+  int V, K;
+  const bf16* X;
+  int B;
+  float* logits;
+  int32_t* next;
+  int32_t* len;
+  const int32_t* slots;
+  int advance;
+  unsigned long long* keys;
+  unsigned int* counter;
+};
+cudaError_t launch_lm_mma(const LmArgs& a, cudaStream_t st);
+bool lm_mma_supports(int V, int K, int B);
+cudaError_t init_mma_attributes();
+
 // ---------------------------------------------------------------- attention
 struct AttnArena {
   bf16* K;        // [layers][S][kvh][cap][d]
@@ -157,6 +225,9 @@ cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st);
 // ---------------------------------------------------------------- model glue
 cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, int B,
                          DevCheck chk, cudaStream_t st);
+// The embedding rows and their RMSNorm: xn[b] = bf16(x[b] * rinv * nw).
+cudaError_t launch_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, const bf16* nw,
+                              float eps, bf16* xn, int B, DevCheck chk, cudaStream_t st);
 // logits[b][v] = RMSNorm(x[b]) . W[v] (bf16 weights, fp32 out).
 cudaError_t launch_lm_head(const bf16* W, int V, int H, const bf16* x, const bf16* norm_w, float eps,
                            float* logits, int B, cudaStream_t st);

@@ -22,6 +22,27 @@ __global__ void k_embed(const bf16* table, int V, int H, const int32_t* tokens, 
   for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
 }
 
+// One CTA per token: x = the embedding row, xn = bf16(x * rinv * nw).
+__global__ void __launch_bounds__(256) k_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x,
+                                                    const bf16* nw, float eps, bf16* xn, DevCheck chk) {
+  __shared__ float red[32];
+  const int b = blockIdx.x;
+  int tok = tokens[b];
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) chk.fail(3);
+    tok = -1;
+  }
+  float ss = 0.f;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    const bf16 v = tok >= 0 ? table[(size_t)tok * H + h] : f2bf(0.f);
+    x[(size_t)b * H + h] = v;
+    ss = fmaf(bf2f(v), bf2f(v), ss);
+  }
+  const float r = block_rms_inv(ss, H, eps, red);
+  for (int h = threadIdx.x; h < H; h += blockDim.x)
+    xn[(size_t)b * H + h] = f2bf(bf2f(x[(size_t)b * H + h]) * r * (nw ? bf2f(nw[h]) : 1.f));
+}
+
 // logits[m][v] = sum_k xn[m][k] * W[v][k]; a lane group of LPR lanes owns two
 // vocab rows; each lane owns CPL chunks of 32 consecutive k (64 bytes).
 // Order per element: ascending k within a chunk, ascending chunk per lane,
@@ -172,6 +193,12 @@ cudaError_t run_lm(const bf16* W, int V, int H, const bf16* x, const bf16* nw, f
 cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, int B, DevCheck chk,
                          cudaStream_t st) {
   k_embed<<<B, 256, 0, st>>>(table, V, H, tokens, x, chk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, const bf16* nw,
+                              float eps, bf16* xn, int B, DevCheck chk, cudaStream_t st) {
+  k_embed_norm<<<B, 256, 0, st>>>(table, V, H, tokens, x, nw, eps, xn, chk);
   return cudaGetLastError();
 }
 

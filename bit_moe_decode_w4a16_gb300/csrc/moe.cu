@@ -36,7 +36,7 @@ constexpr int kMaxPairs = 1024;   // B * k handled by the single-CTA sort
 // of expert block 0 also write them out for the expert GEMMs), keeps the row
 // in shared memory as fp32, and each warp computes the dot products of its
 // experts with all of a router row's loads in flight.
-constexpr int kRouterExperts = 32;
+constexpr int kRouterExperts = kRouterWarps;   // one expert per warp
 
 __global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
   extern __shared__ float xs[];        // [H] normalised row
@@ -77,13 +77,14 @@ __global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
     if (e >= a.E) break;
     const float* wr = a.wr + (size_t)e * H;
     float acc = 0.f;
-    for (int k0 = lane * 4; k0 < H; k0 += 128 * 4) {
-      float4 w4[4];
+    // up to 16 float4 per lane (the whole row for H <= 2048) in flight at once
+    for (int k0 = lane * 4; k0 < H; k0 += 16 * 128) {
+      float4 w4[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 16; ++i)
         if (k0 + 128 * i < H) w4[i] = *reinterpret_cast<const float4*>(wr + k0 + 128 * i);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const int k = k0 + 128 * i;
         if (k < H) {
           acc = fmaf(xs[k], w4[i].x, acc); acc = fmaf(xs[k + 1], w4[i].y, acc);
@@ -164,21 +165,44 @@ __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
     cnt_s[e] = c;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0, u = 0;
-    for (int e = 0; e < E; ++e) {
-      off_s[e] = acc;
-      if (cnt_s[e] > 0) {
-        b.active_e[u] = e;
-        b.active_off[u] = acc;
-        ++u;
+  // warp 0: exclusive scans over the experts (ascending id) of the pair
+  // counts, the active flags and the job counts, 32 experts at a time
+  if (warp == 0) {
+    int run_off = 0, run_u = 0, run_j = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? cnt_s[e] : 0, act = c > 0, nj = (c + kJobTokens - 1) / kJobTokens;
+      int ic = c, ia = act, ij = nj;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int c2 = __shfl_up_sync(0xffffffffu, ic, o), a2 = __shfl_up_sync(0xffffffffu, ia, o),
+                  j2 = __shfl_up_sync(0xffffffffu, ij, o);
+        if (lane >= o) { ic += c2; ia += a2; ij += j2; }
       }
-      acc += cnt_s[e];
+      if (e < E) {
+        const int off = run_off + ic - c, u = run_u + ia - act, j0 = run_j + ij - nj;
+        off_s[e] = off;
+        if (act) {
+          b.active_e[u] = e;
+          b.active_off[u] = off;
+          // one self-contained word per job: expert | first pair << 9 | tokens << 21
+          for (int g = 0; g < nj; ++g) {
+            const int n = min(kJobTokens, c - g * kJobTokens);
+            b.jobs[j0 + g] = e | ((off + g * kJobTokens) << 9) | (n << 21);
+          }
+        }
+      }
+      run_off += __shfl_sync(0xffffffffu, ic, 31);
+      run_u += __shfl_sync(0xffffffffu, ia, 31);
+      run_j += __shfl_sync(0xffffffffu, ij, 31);
     }
-    off_s[E] = acc;
-    b.active_off[u] = acc;
-    *b.n_active = u;
-    if (a.u_log) *a.u_log = u;
+    if (lane == 0) {
+      off_s[E] = run_off;
+      b.active_off[run_u] = run_off;
+      *b.n_active = run_u;
+      *b.n_jobs = run_j;
+      if (a.u_log) *a.u_log = run_u;
+    }
   }
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
@@ -272,15 +296,68 @@ __global__ void __launch_bounds__(kSimtThreads) k_down(MoeArgs a, MoeBufs b) {
 }
 
 __global__ void __launch_bounds__(256) k_combine(MoeArgs a, MoeBufs b) {
+  __shared__ float w_s[16];
+  __shared__ int pos_s[16];
   const int t = blockIdx.x;
+  if (threadIdx.x < a.k) {
+    w_s[threadIdx.x] = b.topk_w[t * a.k + threadIdx.x];
+    pos_s[threadIdx.x] = b.pos_of[t * a.k + threadIdx.x];
+  }
+  __syncthreads();
   for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+    float ov[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) ov[r] = r < a.k ? b.out[(size_t)pos_s[r] * a.H + h] : 0.f;
     float acc = 0.f;
-    for (int r = 0; r < a.k; ++r) {
-      const int pos = b.pos_of[t * a.k + r];
-      acc = fmaf(b.topk_w[t * a.k + r], b.out[(size_t)pos * a.H + h], acc);
-    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < a.k) acc = fmaf(w_s[r], ov[r], acc);
     const float res = a.res ? bf2f(a.res[(size_t)t * a.H + h]) : 0.f;
     a.y[(size_t)t * a.H + h] = f2bf(res + acc);
+  }
+}
+
+// The combine followed by the next RMSNorm of the same row: y as in
+// k_combine, then xn = bf16(y * rinv * nw) with rinv from the bf16 values of
+// y.  One CTA per token; H <= 256 * kCombineMaxPer.
+constexpr int kCombineMaxPer = 32;
+
+__global__ void __launch_bounds__(256) k_combine_norm(MoeArgs a, MoeBufs b, const bf16* nw, bf16* xn) {
+  __shared__ float red[32];
+  __shared__ float w_s[16];
+  __shared__ int pos_s[16];
+  const int t = blockIdx.x, H = a.H;
+  if (threadIdx.x < a.k) {
+    w_s[threadIdx.x] = b.topk_w[t * a.k + threadIdx.x];
+    pos_s[threadIdx.x] = b.pos_of[t * a.k + threadIdx.x];
+  }
+  __syncthreads();
+  float yv[kCombineMaxPer];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCombineMaxPer; ++i) {
+    const int h = threadIdx.x + 256 * i;
+    yv[i] = 0.f;
+    if (h < H) {
+      float ov[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) ov[r] = r < a.k ? b.out[(size_t)pos_s[r] * H + h] : 0.f;
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (r < a.k) acc = fmaf(w_s[r], ov[r], acc);
+      const float res = a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
+      const bf16 y = f2bf(res + acc);
+      a.y[(size_t)t * H + h] = y;
+      yv[i] = bf2f(y);
+      ss = fmaf(yv[i], yv[i], ss);
+    }
+  }
+  const float r = block_rms_inv(ss, H, a.eps, red);
+#pragma unroll
+  for (int i = 0; i < kCombineMaxPer; ++i) {
+    const int h = threadIdx.x + 256 * i;
+    if (h < H) xn[(size_t)t * H + h] = f2bf(yv[i] * r * (nw ? bf2f(nw[h]) : 1.f));
   }
 }
 
@@ -337,7 +414,13 @@ size_t moe_scratch_bytes(int B, int E, int k, int H, int F) {
   return align_up(sizeof(float) * B * E) + align_up(sizeof(int32_t) * P) + align_up(sizeof(float) * P) +
          align_up(sizeof(bf16) * B * H) + align_up(sizeof(int32_t)) + align_up(sizeof(int32_t) * E) +
          align_up(sizeof(int32_t) * (E + 1)) + align_up(sizeof(int32_t) * P) + align_up(sizeof(int32_t) * P) +
+         align_up(sizeof(int32_t)) + align_up(sizeof(int32_t) * moe_max_jobs(B, E, k)) +
          align_up(sizeof(bf16) * P * F) + align_up(sizeof(float) * P * H);
+}
+
+int moe_max_jobs(int B, int E, int k) {
+  const int P = B * k;
+  return (P < E ? P : E) + P / kJobTokens;
 }
 
 MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
@@ -354,9 +437,20 @@ MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
   b.active_off = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
   b.pair_token = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
   b.pos_of = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
+  b.n_jobs = reinterpret_cast<int32_t*>(take(sizeof(int32_t)));
+  b.jobs = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * moe_max_jobs(B, E, k)));
   b.act = reinterpret_cast<bf16*>(take(sizeof(bf16) * P * F));
   b.out = reinterpret_cast<float*>(take(sizeof(float) * P * H));
   return b;
+}
+
+cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, bf16* xn, cudaStream_t st,
+                                    const Marker& mark) {
+  if (a.H > 256 * kCombineMaxPer || a.k > 16) return cudaErrorInvalidValue;
+  k_combine_norm<<<a.B, 256, 0, st>>>(a, b, nw, xn);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) mark(KT_COMBINE);
+  return err;
 }
 
 cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches, const Marker& mark) {

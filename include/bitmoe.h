@@ -59,12 +59,17 @@ typedef enum bm_status {
 /* Kernel family of the dense and expert projections.  Chosen once per engine,
  * never per step, so that a stream's bytes never depend on the batch it runs
  * in ([KV-slot isolation] follow-up update: one reduction order for solo and
- * batched).  AUTO picks the family measured fastest for the engine's
- * max_streams.  SIMT = CUDA-core W4A16 GEMV; TC = tcgen05 tensor cores. */
+ * batched).  SIMT = CUDA-core W4A16 GEMV; TC = tcgen05 tensor cores
+ * (tensor memory accumulators); MMA = warp-level tensor-core instruction
+ * (mma.sync m16n8k16, bf16) with every RMSNorm computed by the kernel that
+ * writes its input row and the greedy argmax fused into the output
+ * projection.  AUTO picks MMA when the shapes allow it (measured fastest at
+ * every decode batch size), else TC, else SIMT. */
 typedef enum bm_kernel_policy {
   BM_POLICY_AUTO = 0,
   BM_POLICY_SIMT = 1,
-  BM_POLICY_TC = 2
+  BM_POLICY_TC = 2,
+  BM_POLICY_MMA = 3
 } bm_kernel_policy;
 
 /* Model geometry and engine limits. */
@@ -176,7 +181,7 @@ bm_status bm_engine_sync(bm_engine* e, void* stream);
 /* Counters and standing memory. */
 bm_status bm_engine_stats(const bm_engine* e, bm_stats* out);
 
-/* The kernel family this engine resolved its policy to (SIMT or TC). */
+/* The kernel family this engine resolved its policy to (SIMT, TC or MMA). */
 int bm_engine_kernel_family(const bm_engine* e);
 
 /* ---------------------------------------------------------------- slots
@@ -257,11 +262,36 @@ bm_status bm_w4_repack_tc(const uint8_t* W, const uint16_t* S, int N, int K, int
 
 /* The batched W4A16 GEMM of w4_gemm_batched on the tensor cores (tcgen05,
  * fp16 operands, fp32 accumulation in tensor memory), with weights in the
- * layout of bm_w4_repack_tc.  Each weight is dequantized to fp16 as
- * fp16((q - 8) * scale) before the MMA.  Weight bytes are read from HBM once
- * per group of 16 rows of X.  Shapes as bm_w4_repack_tc, M >= 1. */
+ * layout of bm_w4_repack_tc.  Each int4 code enters the MMA as the exact
+ * fp16 integer q - 8 and each activation as fp16(x); the per-stage fp32 sums
+ * are multiplied by the fp32 group scale.  Weight bytes are read from HBM
+ * once per group of 16 rows of X.  Shapes as bm_w4_repack_tc, M >= 1. */
 bm_status w4_gemm_batched_tc(const uint8_t* Wtc, const uint16_t* Stc, const uint16_t* X, uint16_t* Y,
                              const uint16_t* R, int M, int N, int K, int g, void* stream);
+
+/* Repack canonical int4 weights W [N][K/2] and scales S [N][K/g] (DEVICE)
+ * into the layout consumed by w4_gemm_batched_mma: Wm (N*K/2 bytes) and Sm
+ * (N*K/(2g) 32-bit words), both DEVICE, caller-owned.  Layout: for each tile
+ * of 16 rows and each 64-wide K chunk, 32 lane slots of 16 bytes; slot
+ * (g = lane / 4, t = lane % 4) holds, for MMA step s = 0..3 of the chunk, the
+ * codes of rows 16T+g and 16T+g+8 at k = 64c + 32(s/2) + 8t + 4(s%2) + 0..3
+ * (nibbles: r0 k0, r1 k0, r0 k2, r1 k2, r0 k1, r1 k1, r0 k3, r1 k3); scales
+ * [N/16][K/g][8] words, word p = the fp16 scales of rows 16T+p and 16T+p+8.
+ * Errors: BM_ERR_INVALID_ARG unless N % 32 == 0, K % 128 == 0, K <= 4096,
+ * g in {32, 64, 128}, K % g == 0. */
+bm_status bm_w4_repack_mma(const uint8_t* W, const uint16_t* S, int N, int K, int g, uint8_t* Wm,
+                           uint32_t* Sm, void* stream);
+
+/* The batched W4A16 GEMM of w4_gemm_batched on the warp-level tensor-core
+ * instruction (mma.sync m16n8k16, bf16 operands, fp32 accumulation), weights
+ * in the layout of bm_w4_repack_mma.  Each int4 code enters the MMA as the
+ * exact bf16 integer q - 8 and each activation as itself; the fp32 sum of a
+ * scale group is multiplied by the group's fp32 scale.  A weight byte is
+ * read from HBM once per group of 32 rows of X.  The summation order of an
+ * output depends only on (N, K, g), so a row's result does not depend on M
+ * or on the other rows.  Shapes as bm_w4_repack_mma, M >= 1. */
+bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint16_t* X, uint16_t* Y,
+                              const uint16_t* R, int M, int N, int K, int g, void* stream);
 
 /* Bytes of DEVICE workspace moe_grouped_w4 needs for B tokens. */
 size_t bm_moe_workspace_bytes(int B, int experts, int top_k, int hidden, int ffn);

@@ -2,8 +2,8 @@
 // the RMSNorm of X fused into the activation staging.
 //
 // Every packed weight byte is read from HBM once per launch, whatever M is
-// (the batched 4-bit GEMM of the batched-serving page, §1: "each packed-int4
-// dense weight is read once across the B rows"); the weights of a warp's
+// (the batched 4-bit GEMM of the batched-serving page, §1: one read of each
+// packed dense weight serves all B rows); the weights of a warp's
 // rows stay in registers while the CTA walks the activation rows in tiles
 // of up to four.
 #include "kernels.cuh"

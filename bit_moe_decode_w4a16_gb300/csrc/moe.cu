@@ -1,6 +1,6 @@
-// Grouped int4 expert op of B tokens (the batched-serving page, §1: "the
-// selected experts of all B streams are dispatched as one grouped
-// sparse-expert operation against the device-resident expert bank").
+// Grouped int4 expert op of B tokens (the batched-serving page, §1: the
+// experts chosen for all B streams run as one grouped operation over the
+// expert bank that stays resident on the device).
 //
 //   1. k_router      fp32 router logits of every token (RMSNorm fused; CTA 0
 //                    also writes the normed input for the experts)

@@ -16,9 +16,9 @@
 //   lane sum   = sum over the lane's chunks, ascending c, of scale * chunk sum
 //   result     = butterfly sum of the LPR lane sums (xor 16, 8, 4, 2, 1)
 // LPR and CPL depend on K only, so a stream's bytes do not depend on the
-// batch it runs in (the "row-independent" batched GEMM of the
-// batched-serving page, §3, and one reduction order for solo and batched as
-// in the KV-slot isolation page's follow-up update).
+// batch it runs in (each row of the batched GEMM is computed on its own, as
+// on the batched-serving page, §3, with one reduction order for solo and
+// batched as in the KV-slot isolation page's follow-up update).
 #pragma once
 
 #include "common.cuh"

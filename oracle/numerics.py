@@ -2,11 +2,11 @@
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
-[Batched serving, §1 Contribution and §3 Results] stores every linear weight
-as "packed-int4" and runs 16-bit activations ("W4A16" in the path's name).
-[KV-slot isolation, follow-up update] says the batched and single-stream
-dense projections share "identical dequantization", i.e. dequantization is a
-fixed function of the stored codes and scales.  The pages print neither the
+[Batched serving, §1 Contribution and §3 Results] keeps every linear weight
+as packed 4-bit codes and computes with 16-bit activations (W4A16).
+[KV-slot isolation, follow-up update] has the batched and single-stream
+dense projections dequantize the same way, so dequantization is a fixed
+function of the stored codes and scales.  The pages print neither the
 code nor the packing, so these readings are taken:
 
 * int4 code: symmetric per-group quantization.  For a group of g consecutive

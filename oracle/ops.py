@@ -17,11 +17,11 @@ from .numerics import dequant_w4
 def w4_gemm(X, packed, scales, K, g):
     """Y = X · Wᵀ with W the dequantized int4 weight, fp64 accumulation.
 
-    [Batched serving, §1 Contribution]: the dense projections "run as a
-    single batched 4-bit GEMM so each packed-int4 dense weight is read once
-    across the B rows"; [Batched serving, §3 Results]: "the batched GEMM row
-    math is row-independent".  X is [M][K] (bf16 values as float64), the
-    result is [M][N] float64 (unrounded).
+    [Batched serving, §1 Contribution]: each dense projection is one batched
+    4-bit GEMM over the B rows, so its packed weights are read once per step;
+    [Batched serving, §3 Results]: each row's result is computed independently
+    of the other rows.  X is [M][K] (bf16 values as float64), the result is
+    [M][N] float64 (unrounded).
     """
     W = dequant_w4(packed, scales, K, g)
     X = np.asarray(X, dtype=np.float64)
@@ -109,8 +109,8 @@ def silu(x):
 def route_topk(xn, Wr, k, renorm=True):
     """Top-k expert routing of each token.
 
-    [Batched serving, §1 Contribution] routes each stream to its "selected
-    experts"; the router's form is not printed.  Reading: logits = xn · Wrᵀ
+    [Batched serving, §1 Contribution] sends each stream to the experts its
+    router selects; the router's form is not printed.  Reading: logits = xn · Wrᵀ
     (Wr fp32 [E][H]), p = softmax(logits) over all E experts, the k experts of
     largest p are selected (equal p: lower expert id first), and their weights
     are p renormalised to sum to one (or left as p when renorm is False).

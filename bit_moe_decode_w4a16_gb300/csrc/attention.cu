@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
 constexpr int kMaxChunksSmem = 1024;
 
 __global__ void k_attn_combine(AttnArena ar, const int32_t* slots, const float* part, int qh, int max_chunks,
-                               bf16* out) {
+                               void* out, int out_f16) {
   __shared__ float ml_s[kMaxChunksSmem][2];
   __shared__ float M_s;
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x, d = ar.d;
@@ -260,7 +260,11 @@ __global__ void k_attn_combine(AttnArena ar, const int32_t* slots, const float* 
       }
     }
   }
-  if (t < d) out[((size_t)b * qh + h) * d + t] = f2bf(acc / den);
+  if (t < d) {
+    const size_t o = ((size_t)b * qh + h) * d + t;
+    if (out_f16) static_cast<__half*>(out)[o] = __float2half_rn(round_bf16(acc / den));
+    else static_cast<bf16*>(out)[o] = f2bf(acc / den);
+  }
 }
 
 __global__ void k_set_len(int32_t* len, int slot, int value) { len[slot] = value; }
@@ -284,9 +288,9 @@ cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slot
   return cudaGetLastError();
 }
 
-cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q, bf16* out,
+cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q, void* out,
                              int qh, int B, float* partials, DevCheck chk, cudaStream_t st, int* launches,
-                             const Marker& mark) {
+                             const Marker& mark, int out_f16) {
   if (ar.d > 128 || ar.d % 8 != 0 || qh % ar.kvh != 0 || qh / ar.kvh > kMaxGroup) return cudaErrorInvalidValue;
   const int max_chunks = (ar.cap + kAttnChunk - 1) / kAttnChunk;
   if (max_chunks > kMaxChunksSmem) return cudaErrorInvalidValue;
@@ -298,7 +302,7 @@ cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slot
   if (e != cudaSuccess) return e;
   mark(KT_ATTN_PART);
   dim3 g2(qh, B);
-  k_attn_combine<<<g2, 128, 0, st>>>(ar, slots, partials, qh, max_chunks, out);
+  k_attn_combine<<<g2, 128, 0, st>>>(ar, slots, partials, qh, max_chunks, out, out_f16);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   mark(KT_ATTN_COMBINE);
   if (launches) *launches += 2;

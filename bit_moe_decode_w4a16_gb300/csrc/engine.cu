@@ -183,7 +183,8 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
   int n = 0;
   auto attn_nw = [&](int l) -> const bf16* { return e->L[l].has_attn_norm ? e->L[l].attn_norm_buf : nullptr; };
   auto u32 = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
-  if ((err = launch_embed_norm(e->embed, c.vocab, H, e->d_tokens, e->x, attn_nw(0), c.rms_eps, e->xn, B,
+  __half* xn16 = reinterpret_cast<__half*>(e->xn);
+  if ((err = launch_embed_norm(e->embed, c.vocab, H, e->d_tokens, e->x, attn_nw(0), c.rms_eps, xn16, B,
                                chk_of(e), s)) != cudaSuccess)
     return err;
   mark(KT_EMBED);
@@ -192,7 +193,7 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     const LayerW& w = e->L[l];
     MmaArgs m1{};
     m1.W = w.wqkv; m1.S = u32(w.wqkv_s); m1.rows = e->qkv_rows; m1.K = H; m1.g = g;
-    m1.X = e->xn; m1.ldx = H; m1.ntok = B; m1.Y = e->qkv; m1.ldy = e->qkv_rows;
+    m1.X = xn16; m1.ldx = H; m1.ntok = B; m1.Y = e->qkv; m1.ldy = e->qkv_rows;
     if ((err = launch_w4_mma_dense(m1, s)) != cudaSuccess) return err;
     mark(KT_QKV);
     if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
@@ -201,7 +202,7 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     mark(KT_ROPE_APPEND);
     n += 2;
     if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
-                                &n, mark)) != cudaSuccess)
+                                &n, mark, 1)) != cudaSuccess)
       return err;
     MmaArgs m2{};
     m2.W = w.wo; m2.S = u32(w.wo_s); m2.rows = H; m2.K = qd; m2.g = g;
@@ -210,7 +211,7 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     mark(KT_OPROJ);
     MoeArgs ma{B, c.experts, c.top_k, H, F, g, c.renorm_topk,
                w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
-               e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l};
+               e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l, 1};
     const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, F);
     if ((err = launch_moe_route(ma, mb, s, mark)) != cudaSuccess) return err;
     MmaArgs m3{};
@@ -218,18 +219,20 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     m3.pair_token = mb.pair_token; m3.n_jobs = mb.n_jobs; m3.jobs = mb.jobs;
     m3.max_jobs = moe_max_jobs(B, c.experts, c.top_k);
     m3.w_expert_stride = (size_t)2 * F * H / 2; m3.s_expert_stride = (size_t)F * (H / g);
-    m3.act = mb.act; m3.F = F;
+    m3.act16 = reinterpret_cast<__half*>(mb.act); m3.F = F; m3.err = e->d_err;
     if ((err = launch_w4_mma_gateup(m3, s)) != cudaSuccess) return err;
     mark(KT_GATEUP);
     MmaArgs m4{};
     m4.W = w.wd; m4.S = u32(w.wd_s); m4.rows = H; m4.K = F; m4.g = g; m4.X = mb.act; m4.ldx = F;
     m4.pair_token = mb.pair_token; m4.n_jobs = mb.n_jobs; m4.jobs = mb.jobs; m4.max_jobs = m3.max_jobs;
     m4.w_expert_stride = (size_t)H * F / 2; m4.s_expert_stride = (size_t)H * (F / g) / 2;
-    m4.out = mb.out; m4.H = H;
+    m4.out = mb.out; m4.H = H; m4.err = e->d_err;
     if ((err = launch_w4_mma_down(m4, s)) != cudaSuccess) return err;
     mark(KT_DOWN);
-    const bf16* next_nw = l + 1 < c.layers ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
-    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, s, mark)) != cudaSuccess) return err;
+    // the next layer's QKV reads fp16; the output projection reads bf16
+    const bool last = l + 1 == c.layers;
+    const bf16* next_nw = !last ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
+    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, last ? 0 : 1, s, mark)) != cudaSuccess) return err;
     n += 6;   // o_proj, router, top-k + sort, gate/up, down, combine
   }
   LmArgs la{};
@@ -1042,7 +1045,7 @@ bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint1
   if (st != BM_OK) return st;
   MmaArgs a{};
   a.W = Wm; a.S = Sm; a.rows = N; a.K = K; a.g = g;
-  a.X = reinterpret_cast<const bf16*>(X); a.ldx = K; a.ntok = M;
+  a.X = X; a.ldx = K; a.ntok = M; a.x_bf16 = 1;
   a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
   BM_CUDA(launch_w4_mma_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched_mma launch");
   return bm::ok();

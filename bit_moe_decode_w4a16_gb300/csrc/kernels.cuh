@@ -80,6 +80,7 @@ struct MoeArgs {
   const bf16* res;                 // [B][H] residual or null
   bf16* y;                         // [B][H]
   int32_t* u_log;                  // if set, the number of active experts is also written here
+  int xn_f16;                      // the router writes bufs.xn as fp16 (warp-MMA experts)
 };
 // Router logits + top-k + sort, gate/up, down, combine: 5 launches.
 cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches,
@@ -89,9 +90,10 @@ cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int*
 cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
 cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
 // The combine with the next RMSNorm fused: also xn[b] = RMSNorm(y[b]) * nw
-// (nw null = ones; a.eps).  H <= 8192.
-cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, bf16* xn, cudaStream_t st,
-                                    const Marker& mark);
+// (nw null = ones; a.eps), rounded to bf16 and stored as fp16 (xn_f16) or
+// bf16.  H <= 8192.
+cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
+                                    cudaStream_t st, const Marker& mark);
 
 // ---------------------------------------------------------------- tensor-core W4A16
 struct TcArgs {
@@ -146,7 +148,7 @@ struct MmaArgs {
   const uint8_t* W;          // mma layout (whole bank for experts)
   const uint32_t* S;         // [tiles][K/g][8] fp16 pairs
   int rows, K, g;            // rows of one matrix (one expert for the banks)
-  const bf16* X;             // activations (already normalised where the op needs it)
+  const void* X;             // activations, fp16 (bf16 for the standalone GEMM), normalised where needed
   int ldx;
   int ntok;                  // dense: number of activation rows
   const bf16* Res;           // dense: residual [ntok][ldr] or null
@@ -159,10 +161,12 @@ struct MmaArgs {
   int max_jobs;              // grid bound of the expert launches
   size_t w_expert_stride;    // bytes of one expert's matrix
   size_t s_expert_stride;    // 32-bit words of one expert's scales
-  bf16* act;                 // gate/up output [pairs][F]
+  __half* act16;             // gate/up output [pairs][F], bf16-rounded values in fp16
   int F;
   float* out;                // down output [pairs][H]
   int H;
+  int* err;                  // device error flag or null
+  int x_bf16;                // dense only: X holds bf16 values (converted on load) instead of fp16
   int ks;                    // set by the launchers
 };
 // Shape support of the warp-MMA kernels: rows % 32 == 0, K % 128 == 0,
@@ -217,17 +221,19 @@ cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* sl
 cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* k,
                              const bf16* v, int B, DevCheck chk, cudaStream_t st);
 // Split-K attention over positions 0..len[slot] (inclusive) and the combine.
+// out is bf16, or fp16 holding the same bf16-rounded values when out_f16.
 cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q,
-                             bf16* out, int qh, int B, float* partials, DevCheck chk,
-                             cudaStream_t st, int* launches, const Marker& mark = Marker());
+                             void* out, int qh, int B, float* partials, DevCheck chk,
+                             cudaStream_t st, int* launches, const Marker& mark = Marker(), int out_f16 = 0);
 cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st);
 
 // ---------------------------------------------------------------- model glue
 cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, int B,
                          DevCheck chk, cudaStream_t st);
-// The embedding rows and their RMSNorm: xn[b] = bf16(x[b] * rinv * nw).
+// The embedding rows and their RMSNorm: xn[b] = bf16(x[b] * rinv * nw),
+// stored as fp16.
 cudaError_t launch_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, const bf16* nw,
-                              float eps, bf16* xn, int B, DevCheck chk, cudaStream_t st);
+                              float eps, __half* xn, int B, DevCheck chk, cudaStream_t st);
 // logits[b][v] = RMSNorm(x[b]) . W[v] (bf16 weights, fp32 out).
 cudaError_t launch_lm_head(const bf16* W, int V, int H, const bf16* x, const bf16* norm_w, float eps,
                            float* logits, int B, cudaStream_t st);

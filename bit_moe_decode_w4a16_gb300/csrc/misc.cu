@@ -24,7 +24,7 @@ __global__ void k_embed(const bf16* table, int V, int H, const int32_t* tokens, 
 
 // One CTA per token: x = the embedding row, xn = bf16(x * rinv * nw).
 __global__ void __launch_bounds__(256) k_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x,
-                                                    const bf16* nw, float eps, bf16* xn, DevCheck chk) {
+                                                    const bf16* nw, float eps, __half* xn, DevCheck chk) {
   __shared__ float red[32];
   const int b = blockIdx.x;
   int tok = tokens[b];
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256) k_embed_norm(const bf16* table, int V, in
   }
   const float r = block_rms_inv(ss, H, eps, red);
   for (int h = threadIdx.x; h < H; h += blockDim.x)
-    xn[(size_t)b * H + h] = f2bf(bf2f(x[(size_t)b * H + h]) * r * (nw ? bf2f(nw[h]) : 1.f));
+    xn[(size_t)b * H + h] = __float2half_rn(round_bf16(bf2f(x[(size_t)b * H + h]) * r * (nw ? bf2f(nw[h]) : 1.f)));
 }
 
 // logits[m][v] = sum_k xn[m][k] * W[v][k]; a lane group of LPR lanes owns two
@@ -197,7 +197,7 @@ cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens,
 }
 
 cudaError_t launch_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, const bf16* nw,
-                              float eps, bf16* xn, int B, DevCheck chk, cudaStream_t st) {
+                              float eps, __half* xn, int B, DevCheck chk, cudaStream_t st) {
   k_embed_norm<<<B, 256, 0, st>>>(table, V, H, tokens, x, nw, eps, xn, chk);
   return cudaGetLastError();
 }

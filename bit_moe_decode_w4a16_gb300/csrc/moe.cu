@@ -68,7 +68,10 @@ __global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
       const float w = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
       const bf16 v = f2bf(xs[k] * r * w);
       xs[k] = bf2f(v);
-      if (blockIdx.x == 0) b.xn[(size_t)tkn * H + k] = v;
+      if (blockIdx.x == 0) {
+        if (a.xn_f16) reinterpret_cast<__half*>(b.xn)[(size_t)tkn * H + k] = __float2half_rn(bf2f(v));
+        else b.xn[(size_t)tkn * H + k] = v;
+      }
     }
   }
   __syncthreads();
@@ -319,45 +322,44 @@ __global__ void __launch_bounds__(256) k_combine(MoeArgs a, MoeBufs b) {
 
 // The combine followed by the next RMSNorm of the same row: y as in
 // k_combine, then xn = bf16(y * rinv * nw) with rinv from the bf16 values of
-// y.  One CTA per token; H <= 256 * kCombineMaxPer.
-constexpr int kCombineMaxPer = 32;
+// y.  One CTA of kCombineThreads per token (H <= kCombineMaxH, the row kept
+// in shared memory); each thread issues the k loads of an element at once.
+constexpr int kCombineThreads = 1024, kCombineMaxH = 8192;
 
-__global__ void __launch_bounds__(256) k_combine_norm(MoeArgs a, MoeBufs b, const bf16* nw, bf16* xn) {
+__global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, MoeBufs b, const bf16* __restrict__ nw,
+                                                                  void* __restrict__ xn, int xn_f16) {
   __shared__ float red[32];
   __shared__ float w_s[16];
   __shared__ int pos_s[16];
+  __shared__ float ys[kCombineMaxH];
   const int t = blockIdx.x, H = a.H;
   if (threadIdx.x < a.k) {
     w_s[threadIdx.x] = b.topk_w[t * a.k + threadIdx.x];
     pos_s[threadIdx.x] = b.pos_of[t * a.k + threadIdx.x];
   }
   __syncthreads();
-  float yv[kCombineMaxPer];
+  const float* __restrict__ outp = b.out;
+  const int kk = a.k;
   float ss = 0.f;
+  for (int h = threadIdx.x; h < H; h += kCombineThreads) {
+    float ov[16];
 #pragma unroll
-  for (int i = 0; i < kCombineMaxPer; ++i) {
-    const int h = threadIdx.x + 256 * i;
-    yv[i] = 0.f;
-    if (h < H) {
-      float ov[16];
+    for (int r = 0; r < 16; ++r) ov[r] = r < kk ? __ldg(outp + (size_t)pos_s[r] * H + h) : 0.f;
+    const float res = a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
+    float acc = 0.f;
 #pragma unroll
-      for (int r = 0; r < 16; ++r) ov[r] = r < a.k ? b.out[(size_t)pos_s[r] * H + h] : 0.f;
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < 16; ++r)
-        if (r < a.k) acc = fmaf(w_s[r], ov[r], acc);
-      const float res = a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
-      const bf16 y = f2bf(res + acc);
-      a.y[(size_t)t * H + h] = y;
-      yv[i] = bf2f(y);
-      ss = fmaf(yv[i], yv[i], ss);
-    }
+    for (int r = 0; r < 16; ++r)
+      if (r < kk) acc = fmaf(w_s[r], ov[r], acc);
+    const bf16 y = f2bf(res + acc);
+    a.y[(size_t)t * H + h] = y;
+    ys[h] = bf2f(y);
+    ss = fmaf(ys[h], ys[h], ss);
   }
   const float r = block_rms_inv(ss, H, a.eps, red);
-#pragma unroll
-  for (int i = 0; i < kCombineMaxPer; ++i) {
-    const int h = threadIdx.x + 256 * i;
-    if (h < H) xn[(size_t)t * H + h] = f2bf(yv[i] * r * (nw ? bf2f(nw[h]) : 1.f));
+  for (int h = threadIdx.x; h < H; h += kCombineThreads) {
+    const float v = round_bf16(ys[h] * r * (nw ? bf2f(nw[h]) : 1.f));
+    if (xn_f16) static_cast<__half*>(xn)[(size_t)t * H + h] = __float2half_rn(v);
+    else static_cast<bf16*>(xn)[(size_t)t * H + h] = f2bf(v);
   }
 }
 
@@ -444,10 +446,10 @@ MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
   return b;
 }
 
-cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, bf16* xn, cudaStream_t st,
-                                    const Marker& mark) {
-  if (a.H > 256 * kCombineMaxPer || a.k > 16) return cudaErrorInvalidValue;
-  k_combine_norm<<<a.B, 256, 0, st>>>(a, b, nw, xn);
+cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
+                                    cudaStream_t st, const Marker& mark) {
+  if (a.H > kCombineMaxH || a.k > 16) return cudaErrorInvalidValue;
+  k_combine_norm<<<a.B, kCombineThreads, 0, st>>>(a, b, nw, xn, xn_f16);
   cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess) mark(KT_COMBINE);
   return err;

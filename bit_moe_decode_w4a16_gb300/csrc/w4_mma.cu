@@ -62,7 +62,8 @@ template <int MODE, int NT, int CPW, int G>
 cudaError_t run(const MmaArgs& a, const Shape& sh, dim3 grid, cudaStream_t st) {
   const int threads = 32 * sh.ks * sh.rtp;
   const size_t smem = (size_t)sh.ks * sh.rtp * 2 * NT * 4 * 32 * sizeof(float);
-  k_w4_mma<MODE, NT, CPW, G><<<grid, threads, smem, st>>>(a);
+  if (a.x_bf16) k_w4_mma<MODE, NT, CPW, G, true><<<grid, threads, smem, st>>>(a);
+  else k_w4_mma<MODE, NT, CPW, G, false><<<grid, threads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -235,8 +236,12 @@ cudaError_t run_lm(const LmArgs& a, cudaStream_t st) {
 
 template <int MODE, int NT, int CPW, int G>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(k_w4_mma<MODE, NT, CPW, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kMaxWarps * 2 * NT * 4 * 32 * (int)sizeof(float));
+  const int bytes = kMaxWarps * 2 * NT * 4 * 32 * (int)sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_w4_mma<MODE, NT, CPW, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_w4_mma<MODE, NT, CPW, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
 }
 
 }  // namespace

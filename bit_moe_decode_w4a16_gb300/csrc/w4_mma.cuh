@@ -1,6 +1,16 @@
-// Warp-level tensor-core W4A16 projections (mma.sync m16n8k16, bf16 x bf16
+// Warp-level tensor-core W4A16 projections (mma.sync m16n8k16, fp16 x fp16
 // -> fp32) for the decode step: the dense projections and the grouped expert
 // gate/up and down GEMMs.
+//
+// Operands.  The MMA runs on fp16: every activation this family consumes is
+// written as fp16 by the kernel that produces it (a bf16 value converts to
+// fp16 exactly inside fp16's range), and each code enters as a biased fp16
+// integer from the packed word: the nibbles of rows r0 become (1024 + u)
+// (low nibble of a byte, magic 0x6400) and those of rows r1 (64 + u) (high
+// nibble, magic 0x5400: 64 has an ulp of 1/16, so the nibble at bits 4-7
+// adds exactly u); one HSUB2 each (1032, 72) leaves the exact code q = u - 8.
+// That is 5 integer and 4 fp16 ops per 8 codes, on two different pipes.
+// Products q x are exact in fp32.
 //
 // Why this instruction.  A decode projection streams its int4 weights once
 // per step against at most a few dozen tokens, so it is bound by HBM, and the
@@ -20,8 +30,7 @@
 // fixed-order sum whatever the batch holds:
 //     y = sum over ks (ascending) of [ sum over the warp's scale groups
 //         (ascending K) of scale x (exact group sum of q x) ]
-// where the group sum is accumulated in fp32 by the MMA (products q x of an
-// int4 code and a bf16 activation are exact in fp32).
+// where the group sum is accumulated in fp32 by the MMA.
 //
 // Int4 layout ("mma layout", written once by the repack kernel): for 16-row
 // tile T and 64-wide chunk c, 32 lanes x 16 bytes; lane (g = lane / 4,
@@ -31,9 +40,9 @@
 // with base = 64c + 32b + 8t + 4(s % 2), the word's nibbles 0..7 are
 //     W[r0][base], W[r1][base], W[r0][base+2], W[r1][base+2],
 //     W[r0][base+1], W[r1][base+1], W[r0][base+3], W[r1][base+3]
-// (r0 = 16T + g, r1 = r0 + 8).  (w >> 4i) & 0x000F000F | 0x43004300 is then
-// the bf16 pair (128 + u) of fragment register i, and subtracting 136 gives
-// the exact codes q = u - 8.  Scales: [T][K/g][8] words, word p = fp16
+// (r0 = 16T + g, r1 = r0 + 8): fragment registers a0, a1 are the masks
+// 0x000F000F and 0x00F000F0 of the word, a2, a3 the same masks of word >> 8.
+// Scales: [T][K/g][8] words, word p = fp16
 // scales of rows (16T + p, 16T + p + 8).  Expert gate/up banks interleave
 // by 8 inside a tile: rows 0-7 are gate rows 8T..8T+7, rows 8-15 the up
 // rows of the same features, so one thread holds both halves of a SiLU pair.
@@ -57,18 +66,37 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One packed word -> the four A-fragment registers (bf16 pairs of exact q).
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One packed word -> the four A-fragment registers: fp16 pairs of the exact
+// codes q, rows r0 in a0, a2 and rows r1 in a1, a3.
 __device__ __forceinline__ void dq_word(uint32_t w, uint32_t (&a)[4]) {
-  constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;   // bf16 128.0 in both halves
-  const uint32_t v[4] = {(w & kMask) | kMagic, ((w >> 4) & kMask) | kMagic, ((w >> 8) & kMask) | kMagic,
-                         ((w >> 12) & kMask) | kMagic};
-  const uint32_t off_bits = 0x43084308u;   // bf16 136.0 in both halves
-  const __nv_bfloat162 off = *reinterpret_cast<const __nv_bfloat162*>(&off_bits);
+  const uint32_t w8 = w >> 8;
+  const uint32_t v[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
+                         (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x54005400u};
+  const uint32_t lo_bits = 0x64086408u, hi_bits = 0x54805480u;   // fp16 1032, 72
+  const __half2 lo = *reinterpret_cast<const __half2*>(&lo_bits), hi = *reinterpret_cast<const __half2*>(&hi_bits);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v[i]), off);
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v[i]), (i & 1) ? hi : lo);
     a[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
+}
+
+// bf16 pair -> fp16 pair (exact inside fp16's range).
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t p) {
+  const float lo = __uint_as_float(p << 16), hi = __uint_as_float(p & 0xFFFF0000u);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 bf8_to_h8(uint4 v) {
+  return make_uint4(bf2_to_h2(v.x), bf2_to_h2(v.y), bf2_to_h2(v.z), bf2_to_h2(v.w));
 }
 
 __device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
@@ -85,7 +113,7 @@ __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ush
 // The projection kernel.  Grid: x = row block (RTP x 32 rows), y = token
 // group (dense, 8 * NT tokens each) or routing job (experts: one expert and
 // up to 8 of its sorted tokens).  Block: KS * RTP warps.
-template <int MODE, int NT, int CPW, int G>
+template <int MODE, int NT, int CPW, int G, bool XBF = false>
 __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
   extern __shared__ float red[];   // [KS][RTP][2][NT][4][32]
   constexpr int kSpg = G / 16;                           // k-steps per scale group
@@ -145,7 +173,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
     const bf16* p = nullptr;
     if (tk < ntok) {
       const int row = MODE == GATEUP ? a.pair_token[tok0 + tk] : tok0 + tk;
-      p = a.X + (size_t)row * a.ldx + (lane & 3) * 8;
+      p = reinterpret_cast<const bf16*>(a.X) + (size_t)row * a.ldx + (lane & 3) * 8;
     }
     xr[nt] = p;
   }
@@ -153,8 +181,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int b = 0; b < 2; ++b)
-        dst[nt][b] = xr[nt] ? *reinterpret_cast<const uint4*>(xr[nt] + c * kChunkK + 32 * b) : make_uint4(0, 0, 0, 0);
+      for (int b = 0; b < 2; ++b) {
+        uint4 v = xr[nt] ? *reinterpret_cast<const uint4*>(xr[nt] + c * kChunkK + 32 * b) : make_uint4(0, 0, 0, 0);
+        if (XBF) v = bf8_to_h8(v);
+        dst[nt][b] = v;
+      }
   };
 
   float acc[2][NT][4];
@@ -187,7 +218,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
           }
           const uint4& xv = xb[j & 1][nt][s >> 1];
           const uint32_t b0 = (s & 1) ? xv.z : xv.x, b1 = (s & 1) ? xv.w : xv.y;
-          mma_bf16(tmp[rt][nt], af, b0, b1);
+          mma_f16(tmp[rt][nt], af, b0, b1);
           if ((gs + 1) % kSpg == 0) {
             const uint32_t sw = sv[j][rt][G >= kChunkK ? 0 : (s * 16) / G];
             const float slo = half_lo(sw), shi = half_hi(sw);
@@ -237,9 +268,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
       a.Y[m * a.ldy + r0] = f2bf(y0);
       a.Y[m * a.ldy + r1] = f2bf(y1);
     } else if (MODE == GATEUP) {
+      // the activation is rounded to bf16 (the path's 16-bit activations) and
+      // stored as the same value in fp16 for the down projection's MMA
       const int f = tile * 8 + (l >> 2);
       const float sv0 = v0 / (1.f + expf(-v0));
-      a.act[m * a.F + f] = f2bf(sv0 * v1);
+      a.act16[m * a.F + f] = __float2half_rn(round_bf16(sv0 * v1));
     } else {
       a.out[m * a.H + r0] = v0;
       a.out[m * a.H + r1] = v1;

@@ -25,7 +25,7 @@ namespace {
 constexpr int kMaxGroup = 8;   // q heads per kv head handled by one CTA
 
 __global__ void k_rope_append(AttnArena ar, int layer, const int32_t* slots, const bf16* qkv, int ld_qkv,
-                              int qh, const double* theta, bf16* qout, DevCheck chk) {
+                              int qh, const float2* rope, bf16* qout, DevCheck chk) {
   extern __shared__ float cs[];   // [d/2] cos, [d/2] sin
   const int b = blockIdx.x;
   const int slot = slots[b];
@@ -34,10 +34,9 @@ __global__ void k_rope_append(AttnArena ar, int layer, const int32_t* slots, con
   if (pos < 0 || pos >= ar.cap) { if (threadIdx.x == 0) chk.fail(2); return; }
   const int d = ar.d, half = d / 2;
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    double sn, cn;
-    sincos((double)pos * theta[i], &sn, &cn);
-    cs[i] = (float)cn;
-    cs[half + i] = (float)sn;
+    const float2 v = rope[(size_t)pos * half + i];
+    cs[i] = v.x;
+    cs[half + i] = v.y;
   }
   __syncthreads();
   const bf16* row = qkv + (size_t)b * ld_qkv;
@@ -277,8 +276,8 @@ size_t attn_partial_floats(int B, int qh, int cap, int d) {
 }
 
 cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* qkv, int ld_qkv,
-                               int qh, const double* theta, bf16* qout, int B, DevCheck chk, cudaStream_t st) {
-  k_rope_append<<<B, 256, sizeof(float) * ar.d, st>>>(ar, layer, slots, qkv, ld_qkv, qh, theta, qout, chk);
+                               int qh, const float2* rope, bf16* qout, int B, DevCheck chk, cudaStream_t st) {
+  k_rope_append<<<B, 256, sizeof(float) * ar.d, st>>>(ar, layer, slots, qkv, ld_qkv, qh, rope, qout, chk);
   return cudaGetLastError();
 }
 

@@ -107,7 +107,7 @@ struct bm_engine {
   AttnArena arena{};
   void* arena_mem = nullptr;
   size_t arena_bytes = 0;
-  double* d_theta = nullptr;
+  float2* d_rope = nullptr;   // [ctx_cap][d/2] (cos, sin) of pos * theta_i
   // scratch
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -115,6 +115,7 @@ struct bm_engine {
   bf16* xn = nullptr;                      // RMSNorm of x for the next projection (warp-MMA family)
   unsigned long long* lm_keys = nullptr;   // fused argmax keys [max_streams], zero between launches
   unsigned int* lm_counter = nullptr;
+  unsigned int* route_cnt = nullptr;       // fused routing arrival counters [max_streams + 1], zero between launches
   float* attn_part = nullptr;
   void* moe_ws = nullptr;
   float* logits = nullptr;
@@ -174,8 +175,9 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
 // The step on the warp-MMA family.  Every RMSNorm is computed by the kernel
 // that produces its input row (embedding, router, combine), so the
 // projections read ready activations: embed+norm, then per layer QKV,
-// rope+append, attention (2), o_proj+residual, router, top-k+sort, gate/up,
-// down, combine+norm; then lm_head with the argmax fused.
+// rope+append, attention (2), o_proj+residual, routing (router, top-k and
+// sort in one launch), gate/up, down, combine+norm; then lm_head with the
+// argmax fused.
 cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark) {
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
@@ -196,7 +198,7 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     m1.X = xn16; m1.ldx = H; m1.ntok = B; m1.Y = e->qkv; m1.ldy = e->qkv_rows;
     if ((err = launch_w4_mma_dense(m1, s)) != cudaSuccess) return err;
     mark(KT_QKV);
-    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
+    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope, e->q, B,
                                   chk_of(e), s)) != cudaSuccess)
       return err;
     mark(KT_ROPE_APPEND);
@@ -213,7 +215,8 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
                w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
                e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l, 1};
     const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, F);
-    if ((err = launch_moe_route(ma, mb, s, mark)) != cudaSuccess) return err;
+    if ((err = launch_moe_route_fused(ma, mb, e->route_cnt, e->route_cnt + c.max_streams, s, mark)) != cudaSuccess)
+      return err;
     MmaArgs m3{};
     m3.W = w.wg; m3.S = u32(w.wg_s); m3.rows = 2 * F; m3.K = H; m3.g = g; m3.X = mb.xn; m3.ldx = H;
     m3.pair_token = mb.pair_token; m3.n_jobs = mb.n_jobs; m3.jobs = mb.jobs;
@@ -233,7 +236,7 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     const bool last = l + 1 == c.layers;
     const bf16* next_nw = !last ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
     if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, last ? 0 : 1, s, mark)) != cudaSuccess) return err;
-    n += 6;   // o_proj, router, top-k + sort, gate/up, down, combine
+    n += 5;   // o_proj, routing, gate/up, down, combine
   }
   LmArgs la{};
   la.W = e->lm_head; la.V = c.vocab; la.K = H; la.X = e->xn; la.B = B; la.logits = e->logits;
@@ -274,7 +277,7 @@ cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, con
     }
     mark(KT_QKV);
     ++n;
-    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_theta, e->q, B,
+    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope, e->q, B,
                                   chk_of(e), s)) != cudaSuccess)
       return err;
     mark(KT_ROPE_APPEND);
@@ -526,18 +529,27 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   AttnArena& ar = e->arena;
   ar.layers = c.layers; ar.S = c.max_streams; ar.kvh = c.kv_heads; ar.cap = c.ctx_cap; ar.d = c.head_dim;
   const size_t kv_elems = (size_t)c.layers * ar.layer_stride();
-  e->arena_bytes = al(kv_elems * 2) * 2 + al(S * 4) + al((size_t)c.head_dim / 2 * sizeof(double));
+  const size_t rope_elems = (size_t)c.ctx_cap * (c.head_dim / 2);
+  e->arena_bytes = al(kv_elems * 2) * 2 + al(S * 4) + al(rope_elems * sizeof(float2));
   BM_CUDA(cudaMalloc(&e->arena_mem, e->arena_bytes), "KV arena allocation");
   char* am = static_cast<char*>(e->arena_mem);
   ar.K = reinterpret_cast<bf16*>(am);
   ar.V = reinterpret_cast<bf16*>(am + al(kv_elems * 2));
   ar.len = reinterpret_cast<int32_t*>(am + 2 * al(kv_elems * 2));
-  e->d_theta = reinterpret_cast<double*>(am + 2 * al(kv_elems * 2) + al(S * 4));
+  e->d_rope = reinterpret_cast<float2*>(am + 2 * al(kv_elems * 2) + al(S * 4));
   BM_CUDA(cudaMemset(ar.len, 0, S * 4), "arena length reset");
   {
-    std::vector<double> theta(c.head_dim / 2);
-    for (int i = 0; i < c.head_dim / 2; ++i) theta[i] = std::pow((double)c.rope_base, -2.0 * i / c.head_dim);
-    BM_CUDA(cudaMemcpy(e->d_theta, theta.data(), theta.size() * sizeof(double), cudaMemcpyHostToDevice),
+    // cos / sin of pos * theta_i, theta_i = base^(-2i/d), in double, stored as float
+    const int half = c.head_dim / 2;
+    std::vector<double> theta(half);
+    for (int i = 0; i < half; ++i) theta[i] = std::pow((double)c.rope_base, -2.0 * i / c.head_dim);
+    std::vector<float2> tab(rope_elems);
+    for (int p = 0; p < c.ctx_cap; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * theta[i];
+        tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    BM_CUDA(cudaMemcpy(e->d_rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice),
             "rope table upload");
   }
 
@@ -549,7 +561,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
              s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
              s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
              s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4), s_xn = take(S * H * 2),
-             s_keys = take(S * 8), s_cnt = take(4);
+             s_keys = take(S * 8), s_cnt = take(4), s_rcnt = take((S + 1) * 4);
   size_t tc_jobs = 0, tc_floats = 0;
   if (e->family == BM_POLICY_TC) tc_workspace(c, e->qkv_rows, &tc_jobs, &tc_floats);
   const Part s_tcp = take(tc_floats * 4), s_tcc = take(tc_jobs * 4);
@@ -573,6 +585,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   e->xn = reinterpret_cast<bf16*>(sb + s_xn.off);
   e->lm_keys = reinterpret_cast<unsigned long long*>(sb + s_keys.off);
   e->lm_counter = reinterpret_cast<unsigned int*>(sb + s_cnt.off);
+  e->route_cnt = reinterpret_cast<unsigned int*>(sb + s_rcnt.off);
   e->tc_part = tc_floats ? reinterpret_cast<float*>(sb + s_tcp.off) : nullptr;
   e->tc_counters = tc_jobs ? reinterpret_cast<int*>(sb + s_tcc.off) : nullptr;
   BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");

@@ -89,6 +89,10 @@ cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int*
 // combine (1 launch) on their own, for the tensor-core expert path.
 cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
 cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark);
+// Router + top-k + sort in one launch (the same results as launch_moe_route).
+// tok_cnt [B] and all_cnt [1] are zero before the launch and left zero.
+cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned int* tok_cnt, unsigned int* all_cnt,
+                                  cudaStream_t st, const Marker& mark);
 // The combine with the next RMSNorm fused: also xn[b] = RMSNorm(y[b]) * nw
 // (nw null = ones; a.eps), rounded to bf16 and stored as fp16 (xn_f16) or
 // bf16.  H <= 8192.
@@ -215,7 +219,7 @@ size_t attn_partial_floats(int B, int qh, int cap, int d);
 
 // RoPE on q and k at pos = len[slot], q -> qout [B][qh][d], k,v -> arena.
 cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* qkv,
-                               int ld_qkv, int qh, const double* theta, bf16* qout, int B,
+                               int ld_qkv, int qh, const float2* rope, bf16* qout, int B,
                                DevCheck chk, cudaStream_t st);
 // Plain append of already-rotated k, v ([B][kvh][d]) at pos = len[slot].
 cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* k,

@@ -38,8 +38,8 @@ constexpr int kMaxPairs = 1024;   // B * k handled by the single-CTA sort
 // experts with all of a router row's loads in flight.
 constexpr int kRouterExperts = kRouterWarps;   // one expert per warp
 
-__global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
-  extern __shared__ float xs[];        // [H] normalised row
+// The router logits of one token and kRouterExperts experts (one CTA).
+__device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, float* xs) {
   __shared__ float red[kRouterWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tkn = blockIdx.y, H = a.H;
@@ -100,67 +100,79 @@ __global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
   }
 }
 
-__global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
-  __shared__ int ids_s[kMaxPairs];
-  __shared__ int cnt_s[256];
-  __shared__ int off_s[257];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const int E = a.E, k = a.k, P = a.B * a.k;
-  for (int t = warp; t < a.B; t += nwarps) {
-    const float* lg = b.logits + (size_t)t * E;
-    // A NaN logit ranks as -inf; every token still gets k distinct valid ids.
-    float v[8];
-    bool taken[8];
+__global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
+  extern __shared__ float xs[];        // [H] normalised row
+  router_cta(a, b, xs);
+}
+
+// Softmax top-k of token t by one warp (ties: lower expert id; a NaN logit
+// ranks as -inf, and every token still gets k distinct valid ids); writes
+// topk_ids / topk_w of the token and, if ids_out, the ids there too.  With
+// `cg` the logits are read through L2 (they were written by other CTAs of the
+// same launch).
+__device__ __forceinline__ void topk_warp(const MoeArgs& a, const MoeBufs& b, int t, bool cg, int* ids_out) {
+  const int lane = threadIdx.x & 31, E = a.E, k = a.k;
+  const float* lg = b.logits + (size_t)t * E;
+  float v[8];
+  bool taken[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    const float x = e < E ? (cg ? __ldcg(lg + e) : lg[e]) : -INFINITY;
+    v[i] = isnan(x) ? -INFINITY : x;
+    taken[i] = e >= E;
+  }
+  float lmax = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) lmax = fmaxf(lmax, v[i]);
+  lmax = warp_max(lmax);
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) z += taken[i] ? 0.f : expf(v[i] - lmax);
+  z = warp_sum(z);
+  float sel_v[16];
+  int sel_e[16];
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      const float x = e < E ? lg[e] : -INFINITY;
-      v[i] = isnan(x) ? -INFINITY : x;
-      taken[i] = e >= E;
+      if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
     }
-    float lmax = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lmax = fmaxf(lmax, v[i]);
-    lmax = warp_max(lmax);
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) z += taken[i] ? 0.f : expf(v[i] - lmax);
-    z = warp_sum(z);
-    float sel_v[16];
-    int sel_e[16];
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      sel_v[r] = bv;
-      sel_e[r] = be;   // k <= E, so an untaken id always exists
-      if ((be & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i == (be >> 5)) taken[i] = true;
-      }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
     }
-    if (lane == 0) {
-      float ex[16], sum = 0.f;
-      for (int r = 0; r < k; ++r) { ex[r] = expf(sel_v[r] - lmax); sum += ex[r]; }
-      const float den = a.renorm ? sum : z;
-      for (int r = 0; r < k; ++r) {
-        b.topk_ids[t * k + r] = sel_e[r];
-        b.topk_w[t * k + r] = ex[r] / den;
-        ids_s[t * k + r] = sel_e[r];
-      }
+    sel_v[r] = bv;
+    sel_e[r] = be;   // k <= E, so an untaken id always exists
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i == (be >> 5)) taken[i] = true;
     }
   }
+  if (lane == 0) {
+    float ex[16], sum = 0.f;
+    for (int r = 0; r < k; ++r) { ex[r] = expf(sel_v[r] - lmax); sum += ex[r]; }
+    const float den = a.renorm ? sum : z;
+    for (int r = 0; r < k; ++r) {
+      b.topk_ids[t * k + r] = sel_e[r];
+      b.topk_w[t * k + r] = ex[r] / den;
+      if (ids_out) ids_out[t * k + r] = sel_e[r];
+    }
+  }
+}
+
+// Stable counting sort of the P = B k (token, rank) pairs by expert, the
+// list of active experts and the job list, by the whole CTA from ids_s
+// (shared memory, pair p = b k + r).  Every reduction has a fixed order.
+__device__ __forceinline__ void group_pairs(const MoeArgs& a, const MoeBufs& b, const int* ids_s, int* cnt_s,
+                                            int* off_s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, k = a.k, P = a.B * a.k;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
@@ -216,6 +228,51 @@ __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
     b.pair_token[pos] = p / k;
     b.pos_of[p] = pos;
   }
+}
+
+__global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
+  __shared__ int ids_s[kMaxPairs];
+  __shared__ int cnt_s[256];
+  __shared__ int off_s[257];
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int t = warp; t < a.B; t += nwarps) topk_warp(a, b, t, false, ids_s);
+  group_pairs(a, b, ids_s, cnt_s, off_s);
+}
+
+// Router, top-k and grouping in one launch.  Every CTA computes its
+// experts' logits for one token; the CTA that finishes a token last (per-token
+// arrival counter) runs the token's top-k; the CTA that finishes the last
+// token (a second counter) sorts the pairs and writes the job list.  Stores
+// are made visible with __threadfence before each arrival, and the late
+// readers load through L2.  The counters are zero before the launch and are
+// left zero.  The result is the same as k_router + k_topk_sort.
+__global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsigned int* tok_cnt,
+                                                     unsigned int* all_cnt) {
+  extern __shared__ float xs[];        // [H] normalised row
+  __shared__ int ids_s[kMaxPairs];
+  __shared__ int cnt_s[256];
+  __shared__ int off_s[257];
+  __shared__ int flag_s;
+  const int tkn = blockIdx.y, warp = threadIdx.x >> 5;
+  router_cta(a, b, xs);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) flag_s = atomicAdd(&tok_cnt[tkn], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!flag_s) return;
+  __threadfence();
+  if (warp == 0) topk_warp(a, b, tkn, true, nullptr);
+  if (threadIdx.x == 0) tok_cnt[tkn] = 0u;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) flag_s = atomicAdd(all_cnt, 1u) == gridDim.y - 1;
+  __syncthreads();
+  if (!flag_s) return;
+  __threadfence();
+  const int P = a.B * a.k;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) ids_s[p] = __ldcg(b.topk_ids + p);
+  group_pairs(a, b, ids_s, cnt_s, off_s);
+  if (threadIdx.x == 0) *all_cnt = 0u;
 }
 
 // Gate/up: a lane group computes rows f of W_g[e] and W_u[e] together.
@@ -491,6 +548,16 @@ cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   mark(KT_TOPK_SORT);
   return cudaSuccess;
+}
+
+cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned int* tok_cnt, unsigned int* all_cnt,
+                                  cudaStream_t st, const Marker& mark) {
+  if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16 || !tok_cnt || !all_cnt) return cudaErrorInvalidValue;
+  const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
+  k_route_fused<<<rgrid, 256, sizeof(float) * a.H, st>>>(a, b, tok_cnt, all_cnt);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) mark(KT_ROUTER);
+  return err;
 }
 
 cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark) {

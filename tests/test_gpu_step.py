@@ -106,8 +106,9 @@ def test_graph_count_paths_and_determinism(bm, policy):
         st1 = bm.bm_engine_stats(e)
         assert st1["graph_launches"] - st0["graph_launches"] == 4     # one launch per step
         assert st1["graph_captures"] == 2                             # one graph per distinct B
-        # embed, 10 per layer, lm_head (+ argmax unless fused into it)
-        assert st1["kernels_per_step"] == 1 + 10 * layers + (1 if policy == MMA else 2)
+        # embed, 10 per layer (9: routing in one launch), lm_head (+ argmax unless fused into it)
+        want = 1 + 9 * layers + 1 if policy == MMA else 1 + 10 * layers + 2
+        assert st1["kernels_per_step"] == want
         # device-resident tokens and outputs take the same path
         bm.decode_step(e, s1, dev_toks, nxt_dev)
         bm.decode_step(e2, s2, torch.tensor(toks, dtype=torch.int32), torch.empty(3, dtype=torch.int32))

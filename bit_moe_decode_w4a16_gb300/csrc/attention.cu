@@ -27,6 +27,7 @@ constexpr int kMaxGroup = 8;   // q heads per kv head handled by one CTA
 __global__ void k_rope_append(AttnArena ar, int layer, const int32_t* slots, const bf16* qkv, int ld_qkv,
                               int qh, const float2* rope, bf16* qout, DevCheck chk) {
   extern __shared__ float cs[];   // [d/2] cos, [d/2] sin
+  pdl_wait();
   const int b = blockIdx.x;
   const int slot = slots[b];
   if (slot < 0 || slot >= ar.S) { if (threadIdx.x == 0) chk.fail(1); return; }
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kAttnChunk) k_attn_part(AttnArena ar, int laye
   __shared__ float red[kMaxGroup][kAttnChunk / 32];
   __shared__ float stat[kMaxGroup][2];
   __shared__ __align__(16) bf16 vs[kAttnChunk][D];
+  pdl_wait();
   const int kh = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
   const int slot = slots[b];
   if (slot < 0 || slot >= ar.S) { if (c == 0 && kh == 0 && threadIdx.x == 0) chk.fail(1); return; }
@@ -225,6 +227,7 @@ __global__ void k_attn_combine(AttnArena ar, const int32_t* slots, const float* 
                                void* out, int out_f16) {
   __shared__ float ml_s[kMaxChunksSmem][2];
   __shared__ float M_s;
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x, d = ar.d;
   const int slot = slots[b];
   if (slot < 0 || slot >= ar.S) return;
@@ -276,9 +279,10 @@ size_t attn_partial_floats(int B, int qh, int cap, int d) {
 }
 
 cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* qkv, int ld_qkv,
-                               int qh, const float2* rope, bf16* qout, int B, DevCheck chk, cudaStream_t st) {
-  k_rope_append<<<B, 256, sizeof(float) * ar.d, st>>>(ar, layer, slots, qkv, ld_qkv, qh, rope, qout, chk);
-  return cudaGetLastError();
+                               int qh, const float2* rope, bf16* qout, int B, DevCheck chk, cudaStream_t st,
+                               bool pdl) {
+  return launch_k(pdl, k_rope_append, dim3(B), dim3(256), sizeof(float) * ar.d, st, ar, layer, slots, qkv, ld_qkv, qh,
+                  rope, qout, chk);
 }
 
 cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* k, const bf16* v,
@@ -289,20 +293,24 @@ cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slot
 
 cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q, void* out,
                              int qh, int B, float* partials, DevCheck chk, cudaStream_t st, int* launches,
-                             const Marker& mark, int out_f16) {
+                             const Marker& mark, int out_f16, bool pdl) {
   if (ar.d > 128 || ar.d % 8 != 0 || qh % ar.kvh != 0 || qh / ar.kvh > kMaxGroup) return cudaErrorInvalidValue;
   const int max_chunks = (ar.cap + kAttnChunk - 1) / kAttnChunk;
   if (max_chunks > kMaxChunksSmem) return cudaErrorInvalidValue;
   dim3 g1(ar.kvh, B, max_chunks);
-  if (ar.d == 128) k_attn_part<128><<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
-  else if (ar.d == 64) k_attn_part<64><<<g1, kAttnChunk, 0, st>>>(ar, layer, slots, q, qh, partials, max_chunks, chk);
-  else return cudaErrorInvalidValue;
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (ar.d == 128)
+    e = launch_k(pdl, k_attn_part<128>, g1, dim3(kAttnChunk), 0, st, ar, layer, slots, q, qh, partials, max_chunks, chk);
+  else if (ar.d == 64)
+    e = launch_k(pdl, k_attn_part<64>, g1, dim3(kAttnChunk), 0, st, ar, layer, slots, q, qh, partials, max_chunks, chk);
+  else
+    return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   mark(KT_ATTN_PART);
   dim3 g2(qh, B);
-  k_attn_combine<<<g2, 128, 0, st>>>(ar, slots, partials, qh, max_chunks, out, out_f16);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_k(pdl, k_attn_combine, g2, dim3(128), 0, st, ar, slots, (const float*)partials, qh, max_chunks, out,
+                    out_f16)) != cudaSuccess)
+    return e;
   mark(KT_ATTN_COMBINE);
   if (launches) *launches += 2;
   return cudaSuccess;

@@ -1,0 +1,336 @@
+// Fused decode attention of the warp-MMA family: RoPE of q and of the new k,
+// the append of the new k and v to the stream's slot, split-K attention over
+// 128-position chunks on the tensor cores, and the ordered merge of a
+// stream's chunks, in one persistent launch.
+//
+// Work items are (stream, kv head, chunk); each CTA reads the slot lengths
+// once, enumerates only the chunks that exist and walks them with a stride of
+// the grid, so no CTA is spent on positions past a stream's length.  For one
+// item the CTA:
+//   - rotates the kv group's G query heads (rotate-half, cos/sin of the
+//     position from the table) into shared memory as bf16, and on the chunk
+//     that holds the new position also rotates the new k and writes k and v
+//     to the arena at that position (before any of the chunk is read);
+//   - copies the chunk's V rows to shared memory asynchronously;
+//   - computes S = Q K^T with mma.sync m16n8k16 (bf16): the G heads on M
+//     (rows past G are zero), 8 positions per n-tile on N, the head dimension
+//     on K.  Inside each 32-wide block of d a lane takes the 8 consecutive
+//     elements 8t..8t+7 of both q and its K row (the same permutation of the
+//     reduction on both operands), so K rows are read straight from memory
+//     as 16-byte loads;
+//   - takes the chunk's softmax statistics (max m, sum l of exp(s - m)) per
+//     head over its 4 warps in a fixed order;
+//   - computes O = P V in fp16 (P reused from the score registers as the A
+//     operand, V through ldmatrix.trans and converted from bf16 exactly),
+//     warp w over its 32 positions, and adds the 4 warps' partials in warp
+//     order;
+//   - writes the chunk's record (o, m, l) and, if it is the last chunk of its
+//     (stream, kv head) to finish (arrival counter), merges all of that
+//     stream's chunks in ascending order: M = max m_c, den = sum l_c e^(m_c - M),
+//     out = (sum o_c e^(m_c - M)) / den, rounded to bf16 and stored as fp16.
+// A stream's result depends only on its own length and data.
+#include <float.h>
+
+#include "kernels.cuh"
+#include "w4_mma.cuh"
+
+namespace bm {
+
+namespace {
+
+constexpr int kWarpsA = 4;
+constexpr int kMaxBatch = 64;
+
+__device__ __forceinline__ size_t rec_index(int b, int h, int c, int qh, int max_chunks, int d) {
+  return (((size_t)b * qh + h) * max_chunks + c) * (size_t)(d + 2);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+template <int D>
+struct AttnSmem {
+  static constexpr int kVS = D + 8;   // padded V row: conflict-free ldmatrix
+  union {
+    bf16 vs[kAttnChunk][kVS];          // V rows of the chunk
+    float ored[kWarpsA][8][D];         // per-warp partial O (after the V reads)
+  } u;
+  bf16 qs[8][D];                       // rotated q of the kv group
+  float cs[D];                         // cos | sin at the new position
+  float red_m[kWarpsA][8], red_l[kWarpsA][8];
+  float stat_m[8], stat_l[8];
+  float mm[8][kMaxMergeChunks], ww[8][kMaxMergeChunks];   // merge: chunk maxima, then weights
+  float mden[8];
+  int slot[kMaxBatch], nc[kMaxBatch], pre[kMaxBatch + 1];
+  int last;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
+  __shared__ __align__(16) AttnSmem<D> sm;
+  constexpr int kVS = AttnSmem<D>::kVS;
+  pdl_wait();
+  const AttnArena& ar = a.ar;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int kvh = ar.kvh, G = a.qh / kvh, B = a.B, half = D / 2;
+  const float scale = 1.0f / sqrtf((float)D);
+
+  // ---- slots, chunk counts and the item prefix (chunk-major within a stream)
+  for (int b = tid; b < B; b += blockDim.x) {
+    const int slot = a.slots[b];
+    int nc = 0;
+    if (slot < 0 || slot >= ar.S) {
+      if (blockIdx.x == 0) a.chk.fail(1);
+    } else {
+      const int L = ar.len[slot] + 1;
+      if (L < 1 || L > ar.cap) {
+        if (blockIdx.x == 0) a.chk.fail(2);
+      } else {
+        nc = (L + kAttnChunk - 1) / kAttnChunk;
+      }
+    }
+    sm.slot[b] = slot;
+    sm.nc[b] = nc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    sm.pre[0] = 0;
+    for (int b = 0; b < B; ++b) sm.pre[b + 1] = sm.pre[b] + sm.nc[b] * kvh;
+  }
+  __syncthreads();
+  const int total = sm.pre[B];
+
+  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    int b = 0;
+    while (sm.pre[b + 1] <= it) ++b;
+    const int r = it - sm.pre[b], kh = r % kvh, c = r / kvh;
+    const int slot = sm.slot[b], nc = sm.nc[b];
+    const int pos = ar.len[slot], L = pos + 1;
+    const int j0 = c * kAttnChunk, n = min(kAttnChunk, L - j0);
+    const bool last_chunk = c == nc - 1;
+    const bf16* row = a.qkv + (size_t)b * a.ld_qkv;
+    const size_t base = (size_t)a.layer * ar.layer_stride() + (size_t)slot * ar.slot_stride() + (size_t)kh * ar.cap * D;
+    bf16* Kb = ar.K + base;
+    bf16* Vb = ar.V + base;
+
+    // ---- RoPE of q (and of the new k, with the append, on the last chunk)
+    for (int i = tid; i < half; i += blockDim.x) {
+      const float2 v = a.rope[(size_t)pos * half + i];
+      sm.cs[i] = v.x;
+      sm.cs[half + i] = v.y;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 8 * half; idx += blockDim.x) {
+      const int h = idx / half, i = idx - h * half;
+      bf16 y0 = f2bf(0.f), y1 = f2bf(0.f);
+      if (h < G) {
+        const bf16* src = row + (size_t)(kh * G + h) * D;
+        const float x0 = bf2f(src[i]), x1 = bf2f(src[i + half]), cc = sm.cs[i], ss = sm.cs[half + i];
+        y0 = f2bf(x0 * cc - x1 * ss);
+        y1 = f2bf(x1 * cc + x0 * ss);
+      }
+      sm.qs[h][i] = y0;
+      sm.qs[h][i + half] = y1;
+    }
+    if (last_chunk) {
+      const bf16* ksrc = row + (size_t)(a.qh + kh) * D;
+      const bf16* vsrc = row + (size_t)(a.qh + kvh + kh) * D;
+      for (int i = tid; i < half; i += blockDim.x) {
+        const float x0 = bf2f(ksrc[i]), x1 = bf2f(ksrc[i + half]), cc = sm.cs[i], ss = sm.cs[half + i];
+        Kb[(size_t)pos * D + i] = f2bf(x0 * cc - x1 * ss);
+        Kb[(size_t)pos * D + i + half] = f2bf(x1 * cc + x0 * ss);
+      }
+      for (int i = tid; i < D; i += blockDim.x) Vb[(size_t)pos * D + i] = vsrc[i];
+      __threadfence();
+    }
+    __syncthreads();
+
+    // ---- V rows -> shared memory (async); rows past n are zeroed (P is 0 there)
+    constexpr int kV8 = D / 8;
+    for (int i = tid; i < kAttnChunk * kV8; i += blockDim.x) {
+      const int rr = i / kV8, v8 = i - rr * kV8;
+      if (rr < n) cp_async16(&sm.u.vs[rr][v8 * 8], Vb + (size_t)(j0 + rr) * D + v8 * 8);
+      else *reinterpret_cast<uint4*>(&sm.u.vs[rr][v8 * 8]) = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
+    // ---- scores: warp w takes positions [32w, 32w + 32): 4 n-tiles of 8
+    constexpr int kBlk = D / 32;
+    uint32_t qa[kBlk][4];
+#pragma unroll
+    for (int blk = 0; blk < kBlk; ++blk) {
+      const uint4 q4 = *reinterpret_cast<const uint4*>(&sm.qs[g][32 * blk + 8 * t]);
+      qa[blk][0] = q4.x; qa[blk][1] = q4.y; qa[blk][2] = q4.z; qa[blk][3] = q4.w;
+    }
+    float s[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s[nt][q] = 0.f;
+      const int p = 32 * warp + 8 * nt + g;   // this lane's B column (a position of the chunk)
+      uint4 kb[kBlk];
+#pragma unroll
+      for (int blk = 0; blk < kBlk; ++blk)
+        kb[blk] = p < n ? __ldcg(reinterpret_cast<const uint4*>(Kb + (size_t)(j0 + p) * D + 32 * blk + 8 * t))
+                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int blk = 0; blk < kBlk; ++blk) {
+        const uint32_t a0[4] = {qa[blk][0], 0u, qa[blk][1], 0u};
+        const uint32_t a1[4] = {qa[blk][2], 0u, qa[blk][3], 0u};
+        mma::mma_bf16(s[nt], a0, kb[blk].x, kb[blk].y);
+        mma::mma_bf16(s[nt], a1, kb[blk].z, kb[blk].w);
+      }
+    }
+    // s[nt][0..1] = S[head g][position 32w + 8nt + 2t (+1)]; rows g + 8 (c2, c3) are padding
+    float mx = -FLT_MAX;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int p = 32 * warp + 8 * nt + 2 * t + j;
+        s[nt][j] = p < n ? s[nt][j] * scale : -FLT_MAX;
+        mx = fmaxf(mx, s[nt][j]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (t == 0) sm.red_m[warp][g] = mx;
+    __syncthreads();
+    if (tid < 8) {
+      float m = sm.red_m[0][tid];
+      for (int w = 1; w < kWarpsA; ++w) m = fmaxf(m, sm.red_m[w][tid]);
+      sm.stat_m[tid] = m;
+    }
+    __syncthreads();
+    const float mrow = sm.stat_m[g];
+    float ls = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int p = 32 * warp + 8 * nt + 2 * t + j;
+        s[nt][j] = p < n ? expf(s[nt][j] - mrow) : 0.f;
+        ls += s[nt][j];
+      }
+    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    if (t == 0) sm.red_l[warp][g] = ls;
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (tid < 8) {
+      float l = 0.f;
+      for (int w = 0; w < kWarpsA; ++w) l += sm.red_l[w][tid];
+      sm.stat_l[tid] = l;
+    }
+
+    // ---- O = P V over the warp's 32 positions (2 k-steps of 16)
+    constexpr int kNT = D / 8;
+    float o[kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[nt][q] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t pa[4] = {pack_f16(s[2 * kk][0], s[2 * kk][1]), 0u, pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                              0u};
+      const int vrow = 32 * warp + 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int dt = 0; dt < kNT / 2; ++dt) {
+        uint32_t vb[4];
+        ldsm_x4_trans(vb, static_cast<uint32_t>(__cvta_generic_to_shared(&sm.u.vs[vrow][16 * dt + (lane >> 4) * 8])));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) vb[q] = mma::bf2_to_h2(vb[q]);   // exact: V is bf16 inside fp16's range
+        mma::mma_f16(o[2 * dt], pa, vb[0], vb[1]);
+        mma::mma_f16(o[2 * dt + 1], pa, vb[2], vb[3]);
+      }
+    }
+    __syncthreads();   // all V reads are done: the union now holds the partial O
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      sm.u.ored[warp][g][8 * nt + 2 * t] = o[nt][0];
+      sm.u.ored[warp][g][8 * nt + 2 * t + 1] = o[nt][1];
+    }
+    __syncthreads();
+
+    // ---- the chunk's record: o (warps added in order), m, l
+    for (int idx = tid; idx < G * D; idx += blockDim.x) {
+      const int h = idx / D, d = idx - h * D;
+      float v = 0.f;
+      for (int w = 0; w < kWarpsA; ++w) v += sm.u.ored[w][h][d];
+      a.part[rec_index(b, kh * G + h, c, a.qh, a.max_chunks, D) + d] = v;
+    }
+    if (tid < G) {
+      float* rec = a.part + rec_index(b, kh * G + tid, c, a.qh, a.max_chunks, D);
+      rec[D] = sm.stat_m[tid];
+      rec[D + 1] = sm.stat_l[tid];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.last = atomicAdd(&a.counters[b * kvh + kh], 1u) == (unsigned)(nc - 1);
+    __syncthreads();
+    if (sm.last) {
+      // ---- merge the stream's chunks for this kv group, ascending chunk order
+      __threadfence();
+      for (int idx = tid; idx < G * nc; idx += blockDim.x) {
+        const int h = idx / nc, cc = idx - h * nc;
+        sm.mm[h][cc] = __ldcg(a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D) + D);
+      }
+      __syncthreads();
+      if (tid < G) {
+        float M = -FLT_MAX;
+        for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, sm.mm[tid][cc]);
+        float den = 0.f;
+        for (int cc = 0; cc < nc; ++cc) {
+          const float w = expf(sm.mm[tid][cc] - M);
+          sm.ww[tid][cc] = w;
+          den = fmaf(__ldcg(a.part + rec_index(b, kh * G + tid, cc, a.qh, a.max_chunks, D) + D + 1), w, den);
+        }
+        sm.mden[tid] = den;
+      }
+      __syncthreads();
+      for (int idx = tid; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx - h * D;
+        float acc = 0.f;
+        for (int cc = 0; cc < nc; ++cc)
+          acc = fmaf(__ldcg(a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D) + d), sm.ww[h][cc], acc);
+        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(acc / sm.mden[h]));
+      }
+      if (tid == 0) a.counters[b * kvh + kh] = 0u;
+    }
+    __syncthreads();   // shared memory is reused by the next item
+  }
+}
+
+}  // namespace
+
+bool attention_fused_supports(const AttnArena& ar, int qh) {
+  return (ar.d == 64 || ar.d == 128) && qh % ar.kvh == 0 && qh / ar.kvh <= 8 &&
+         (ar.cap + kAttnChunk - 1) / kAttnChunk <= kMaxMergeChunks;
+}
+
+cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool pdl) {
+  if (!attention_fused_supports(a.ar, a.qh) || a.B < 1 || a.B > kMaxBatch || !a.counters) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 132;
+  const long items = (long)a.B * a.ar.kvh * a.max_chunks;
+  const long cap = (long)sms * 4;
+  const dim3 grid((unsigned)(items < cap ? items : cap));
+  if (a.ar.d == 128) return launch_k(pdl, k_attn_fused<128>, grid, dim3(kWarpsA * 32), 0, st, a);
+  return launch_k(pdl, k_attn_fused<64>, grid, dim3(kWarpsA * 32), 0, st, a);
+}
+
+}  // namespace bm

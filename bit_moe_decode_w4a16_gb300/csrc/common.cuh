@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace bm {
 
 using bf16 = __nv_bfloat16;
@@ -20,6 +22,32 @@ struct DevCheck {
     if (flag) atomicExch(flag, code);
   }
 };
+
+// Programmatic dependent launch.  A kernel launched with launch_k(pdl=true)
+// may start while the previous kernel of the stream is finishing: it calls
+// pdl_wait() before touching anything that kernel (or any earlier one)
+// writes, and pdl_trigger() to let the next kernel start early.  Both are
+// no-ops when the kernel was launched the ordinary way.  Every kernel of a
+// PDL chain calls pdl_wait() before it writes memory or exits, so the chain
+// stays ordered end to end.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ float bf2f(bf16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ bf16 f2bf(float v) { return __float2bfloat16_rn(v); }

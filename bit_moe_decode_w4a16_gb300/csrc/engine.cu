@@ -116,6 +116,7 @@ struct bm_engine {
   unsigned long long* lm_keys = nullptr;   // fused argmax keys [max_streams], zero between launches
   unsigned int* lm_counter = nullptr;
   unsigned int* route_cnt = nullptr;       // fused routing arrival counters [max_streams + 1], zero between launches
+  unsigned int* attn_cnt = nullptr;        // fused attention arrival counters [max_streams * kv_heads], zero between launches
   float* attn_part = nullptr;
   void* moe_ws = nullptr;
   float* logits = nullptr;
@@ -175,19 +176,22 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
 // The step on the warp-MMA family.  Every RMSNorm is computed by the kernel
 // that produces its input row (embedding, router, combine), so the
 // projections read ready activations: embed+norm, then per layer QKV,
-// rope+append, attention (2), o_proj+residual, routing (router, top-k and
-// sort in one launch), gate/up, down, combine+norm; then lm_head with the
-// argmax fused.
+// attention (RoPE, append, chunks and merge in one launch), o_proj+residual,
+// routing (router, top-k and sort in one launch), gate/up, down,
+// combine+norm; then lm_head with the argmax fused.
 cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark) {
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
   cudaError_t err;
   int n = 0;
+  // kernels overlap their launch with the previous kernel's tail, except
+  // under the per-kernel profiler, whose events sit between the launches
+  const bool pdl = !mark.fn;
   auto attn_nw = [&](int l) -> const bf16* { return e->L[l].has_attn_norm ? e->L[l].attn_norm_buf : nullptr; };
   auto u32 = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
   __half* xn16 = reinterpret_cast<__half*>(e->xn);
   if ((err = launch_embed_norm(e->embed, c.vocab, H, e->d_tokens, e->x, attn_nw(0), c.rms_eps, xn16, B,
-                               chk_of(e), s)) != cudaSuccess)
+                               chk_of(e), s, pdl)) != cudaSuccess)
     return err;
   mark(KT_EMBED);
   ++n;
@@ -195,53 +199,64 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     const LayerW& w = e->L[l];
     MmaArgs m1{};
     m1.W = w.wqkv; m1.S = u32(w.wqkv_s); m1.rows = e->qkv_rows; m1.K = H; m1.g = g;
-    m1.X = xn16; m1.ldx = H; m1.ntok = B; m1.Y = e->qkv; m1.ldy = e->qkv_rows;
+    m1.X = xn16; m1.ldx = H; m1.ntok = B; m1.Y = e->qkv; m1.ldy = e->qkv_rows; m1.pdl = pdl;
     if ((err = launch_w4_mma_dense(m1, s)) != cudaSuccess) return err;
     mark(KT_QKV);
-    if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope, e->q, B,
-                                  chk_of(e), s)) != cudaSuccess)
-      return err;
-    mark(KT_ROPE_APPEND);
-    n += 2;
-    if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
-                                &n, mark, 1)) != cudaSuccess)
-      return err;
+    ++n;
+    if (attention_fused_supports(e->arena, c.q_heads)) {
+      AttnFusedArgs fa{e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope,
+                       reinterpret_cast<__half*>(e->attn), e->attn_part,
+                       (c.ctx_cap + kAttnChunk - 1) / kAttnChunk, e->attn_cnt, B, chk_of(e)};
+      if ((err = launch_attention_fused(fa, s, pdl)) != cudaSuccess) return err;
+      mark(KT_ATTN_PART);
+      ++n;
+    } else {
+      if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope, e->q, B,
+                                    chk_of(e), s, pdl)) != cudaSuccess)
+        return err;
+      mark(KT_ROPE_APPEND);
+      ++n;
+      if ((err = launch_attention(e->arena, l, e->d_slots, e->q, e->attn, c.q_heads, B, e->attn_part, chk_of(e), s,
+                                  &n, mark, 1, pdl)) != cudaSuccess)
+        return err;
+    }
     MmaArgs m2{};
     m2.W = w.wo; m2.S = u32(w.wo_s); m2.rows = H; m2.K = qd; m2.g = g;
-    m2.X = e->attn; m2.ldx = qd; m2.ntok = B; m2.Res = e->x; m2.ldr = H; m2.Y = e->h; m2.ldy = H;
+    m2.X = e->attn; m2.ldx = qd; m2.ntok = B; m2.Res = e->x; m2.ldr = H; m2.Y = e->h; m2.ldy = H; m2.pdl = pdl;
     if ((err = launch_w4_mma_dense(m2, s)) != cudaSuccess) return err;
     mark(KT_OPROJ);
     MoeArgs ma{B, c.experts, c.top_k, H, F, g, c.renorm_topk,
                w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
                e->h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->h, e->x, e->d_u_log + l, 1};
     const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, F);
-    if ((err = launch_moe_route_fused(ma, mb, e->route_cnt, e->route_cnt + c.max_streams, s, mark)) != cudaSuccess)
+    if ((err = launch_moe_route_fused(ma, mb, e->route_cnt, e->route_cnt + c.max_streams, s, mark, pdl)) !=
+        cudaSuccess)
       return err;
     MmaArgs m3{};
     m3.W = w.wg; m3.S = u32(w.wg_s); m3.rows = 2 * F; m3.K = H; m3.g = g; m3.X = mb.xn; m3.ldx = H;
     m3.pair_token = mb.pair_token; m3.n_jobs = mb.n_jobs; m3.jobs = mb.jobs;
     m3.max_jobs = moe_max_jobs(B, c.experts, c.top_k);
     m3.w_expert_stride = (size_t)2 * F * H / 2; m3.s_expert_stride = (size_t)F * (H / g);
-    m3.act16 = reinterpret_cast<__half*>(mb.act); m3.F = F; m3.err = e->d_err;
+    m3.act16 = reinterpret_cast<__half*>(mb.act); m3.F = F; m3.err = e->d_err; m3.pdl = pdl;
     if ((err = launch_w4_mma_gateup(m3, s)) != cudaSuccess) return err;
     mark(KT_GATEUP);
     MmaArgs m4{};
     m4.W = w.wd; m4.S = u32(w.wd_s); m4.rows = H; m4.K = F; m4.g = g; m4.X = mb.act; m4.ldx = F;
     m4.pair_token = mb.pair_token; m4.n_jobs = mb.n_jobs; m4.jobs = mb.jobs; m4.max_jobs = m3.max_jobs;
     m4.w_expert_stride = (size_t)H * F / 2; m4.s_expert_stride = (size_t)H * (F / g) / 2;
-    m4.out = mb.out; m4.H = H; m4.err = e->d_err;
+    m4.out = mb.out; m4.H = H; m4.err = e->d_err; m4.pdl = pdl;
     if ((err = launch_w4_mma_down(m4, s)) != cudaSuccess) return err;
     mark(KT_DOWN);
     // the next layer's QKV reads fp16; the output projection reads bf16
     const bool last = l + 1 == c.layers;
     const bf16* next_nw = !last ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
-    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, last ? 0 : 1, s, mark)) != cudaSuccess) return err;
+    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, last ? 0 : 1, s, mark, pdl)) != cudaSuccess) return err;
     n += 5;   // o_proj, routing, gate/up, down, combine
   }
   LmArgs la{};
   la.W = e->lm_head; la.V = c.vocab; la.K = H; la.X = e->xn; la.B = B; la.logits = e->logits;
   la.next = e->d_next; la.len = e->arena.len; la.slots = e->d_slots; la.advance = 1;
-  la.keys = e->lm_keys; la.counter = e->lm_counter;
+  la.keys = e->lm_keys; la.counter = e->lm_counter; la.pdl = pdl;
   if ((err = launch_lm_mma(la, s)) != cudaSuccess) return err;
   mark(KT_LM_HEAD);
   ++n;
@@ -561,7 +576,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
              s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
              s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
              s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4), s_xn = take(S * H * 2),
-             s_keys = take(S * 8), s_cnt = take(4), s_rcnt = take((S + 1) * 4);
+             s_keys = take(S * 8), s_cnt = take(4), s_rcnt = take((S + 1) * 4), s_acnt = take(S * c.kv_heads * 4);
   size_t tc_jobs = 0, tc_floats = 0;
   if (e->family == BM_POLICY_TC) tc_workspace(c, e->qkv_rows, &tc_jobs, &tc_floats);
   const Part s_tcp = take(tc_floats * 4), s_tcc = take(tc_jobs * 4);
@@ -586,6 +601,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   e->lm_keys = reinterpret_cast<unsigned long long*>(sb + s_keys.off);
   e->lm_counter = reinterpret_cast<unsigned int*>(sb + s_cnt.off);
   e->route_cnt = reinterpret_cast<unsigned int*>(sb + s_rcnt.off);
+  e->attn_cnt = reinterpret_cast<unsigned int*>(sb + s_acnt.off);
   e->tc_part = tc_floats ? reinterpret_cast<float*>(sb + s_tcp.off) : nullptr;
   e->tc_counters = tc_jobs ? reinterpret_cast<int*>(sb + s_tcc.off) : nullptr;
   BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");

@@ -92,12 +92,12 @@ cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t 
 // Router + top-k + sort in one launch (the same results as launch_moe_route).
 // tok_cnt [B] and all_cnt [1] are zero before the launch and left zero.
 cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned int* tok_cnt, unsigned int* all_cnt,
-                                  cudaStream_t st, const Marker& mark);
+                                  cudaStream_t st, const Marker& mark, bool pdl = false);
 // The combine with the next RMSNorm fused: also xn[b] = RMSNorm(y[b]) * nw
 // (nw null = ones; a.eps), rounded to bf16 and stored as fp16 (xn_f16) or
 // bf16.  H <= 8192.
 cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
-                                    cudaStream_t st, const Marker& mark);
+                                    cudaStream_t st, const Marker& mark, bool pdl = false);
 
 // ---------------------------------------------------------------- tensor-core W4A16
 struct TcArgs {
@@ -171,6 +171,7 @@ struct MmaArgs {
   int H;
   int* err;                  // device error flag or null
   int x_bf16;                // dense only: X holds bf16 values (converted on load) instead of fp16
+  int pdl;                   // launch with programmatic dependent launch
   int ks;                    // set by the launchers
 };
 // Shape support of the warp-MMA kernels: rows % 32 == 0, K % 128 == 0,
@@ -200,6 +201,7 @@ struct LmArgs {
   int advance;
   unsigned long long* keys;
   unsigned int* counter;
+  int pdl;                   // launch with programmatic dependent launch
 };
 cudaError_t launch_lm_mma(const LmArgs& a, cudaStream_t st);
 bool lm_mma_supports(int V, int K, int B);
@@ -220,7 +222,7 @@ size_t attn_partial_floats(int B, int qh, int cap, int d);
 // RoPE on q and k at pos = len[slot], q -> qout [B][qh][d], k,v -> arena.
 cudaError_t launch_rope_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* qkv,
                                int ld_qkv, int qh, const float2* rope, bf16* qout, int B,
-                               DevCheck chk, cudaStream_t st);
+                               DevCheck chk, cudaStream_t st, bool pdl = false);
 // Plain append of already-rotated k, v ([B][kvh][d]) at pos = len[slot].
 cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slots, const bf16* k,
                              const bf16* v, int B, DevCheck chk, cudaStream_t st);
@@ -228,8 +230,32 @@ cudaError_t launch_kv_append(const AttnArena& ar, int layer, const int32_t* slot
 // out is bf16, or fp16 holding the same bf16-rounded values when out_f16.
 cudaError_t launch_attention(const AttnArena& ar, int layer, const int32_t* slots, const bf16* q,
                              void* out, int qh, int B, float* partials, DevCheck chk,
-                             cudaStream_t st, int* launches, const Marker& mark = Marker(), int out_f16 = 0);
+                             cudaStream_t st, int* launches, const Marker& mark = Marker(), int out_f16 = 0,
+                             bool pdl = false);
 cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st);
+
+// RoPE + append + attention + merge in one launch (warp-MMA family).  q, k
+// and v come straight from the QKV projection's rows; out is fp16 holding
+// bf16-rounded values [B][qh][d]; counters [B * kvh] are zero before the
+// launch and left zero.  Needs d in {64, 128}, qh / kvh <= 8 and at most
+// kMaxMergeChunks chunks per stream.
+constexpr int kMaxMergeChunks = 64;
+struct AttnFusedArgs {
+  AttnArena ar;
+  int layer;
+  const int32_t* slots;
+  const bf16* qkv;
+  int ld_qkv, qh;
+  const float2* rope;   // [cap][d/2] (cos, sin)
+  __half* out;
+  float* part;          // chunk records, as attn_partial_floats
+  int max_chunks;
+  unsigned int* counters;
+  int B;
+  DevCheck chk;
+};
+bool attention_fused_supports(const AttnArena& ar, int qh);
+cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool pdl = false);
 
 // ---------------------------------------------------------------- model glue
 cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, int B,
@@ -237,7 +263,7 @@ cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens,
 // The embedding rows and their RMSNorm: xn[b] = bf16(x[b] * rinv * nw),
 // stored as fp16.
 cudaError_t launch_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, const bf16* nw,
-                              float eps, __half* xn, int B, DevCheck chk, cudaStream_t st);
+                              float eps, __half* xn, int B, DevCheck chk, cudaStream_t st, bool pdl = false);
 // logits[b][v] = RMSNorm(x[b]) . W[v] (bf16 weights, fp32 out).
 cudaError_t launch_lm_head(const bf16* W, int V, int H, const bf16* x, const bf16* norm_w, float eps,
                            float* logits, int B, cudaStream_t st);

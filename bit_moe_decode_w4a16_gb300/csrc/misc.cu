@@ -26,6 +26,7 @@ __global__ void k_embed(const bf16* table, int V, int H, const int32_t* tokens, 
 __global__ void __launch_bounds__(256) k_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x,
                                                     const bf16* nw, float eps, __half* xn, DevCheck chk) {
   __shared__ float red[32];
+  pdl_wait();
   const int b = blockIdx.x;
   int tok = tokens[b];
   if (tok < 0 || tok >= V) {
@@ -197,9 +198,8 @@ cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens,
 }
 
 cudaError_t launch_embed_norm(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, const bf16* nw,
-                              float eps, __half* xn, int B, DevCheck chk, cudaStream_t st) {
-  k_embed_norm<<<B, 256, 0, st>>>(table, V, H, tokens, x, nw, eps, xn, chk);
-  return cudaGetLastError();
+                              float eps, __half* xn, int B, DevCheck chk, cudaStream_t st, bool pdl) {
+  return launch_k(pdl, k_embed_norm, dim3(B), dim3(256), 0, st, table, V, H, tokens, x, nw, eps, xn, chk);
 }
 
 cudaError_t launch_lm_head(const bf16* W, int V, int H, const bf16* x, const bf16* norm_w, float eps,

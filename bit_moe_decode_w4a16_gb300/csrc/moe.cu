@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsig
   __shared__ int cnt_s[256];
   __shared__ int off_s[257];
   __shared__ int flag_s;
+  pdl_wait();
   const int tkn = blockIdx.y, warp = threadIdx.x >> 5;
   router_cta(a, b, xs);
   __threadfence();
@@ -389,6 +390,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
   __shared__ float w_s[16];
   __shared__ int pos_s[16];
   __shared__ float ys[kCombineMaxH];
+  pdl_wait();
   const int t = blockIdx.x, H = a.H;
   if (threadIdx.x < a.k) {
     w_s[threadIdx.x] = b.topk_w[t * a.k + threadIdx.x];
@@ -504,10 +506,9 @@ MoeBufs moe_carve(void* ws, int B, int E, int k, int H, int F) {
 }
 
 cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
-                                    cudaStream_t st, const Marker& mark) {
+                                    cudaStream_t st, const Marker& mark, bool pdl) {
   if (a.H > kCombineMaxH || a.k > 16) return cudaErrorInvalidValue;
-  k_combine_norm<<<a.B, kCombineThreads, 0, st>>>(a, b, nw, xn, xn_f16);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_k(pdl, k_combine_norm, dim3(a.B), dim3(kCombineThreads), 0, st, a, b, nw, xn, xn_f16);
   if (err == cudaSuccess) mark(KT_COMBINE);
   return err;
 }
@@ -551,11 +552,10 @@ cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st
 }
 
 cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned int* tok_cnt, unsigned int* all_cnt,
-                                  cudaStream_t st, const Marker& mark) {
+                                  cudaStream_t st, const Marker& mark, bool pdl) {
   if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16 || !tok_cnt || !all_cnt) return cudaErrorInvalidValue;
   const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
-  k_route_fused<<<rgrid, 256, sizeof(float) * a.H, st>>>(a, b, tok_cnt, all_cnt);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_k(pdl, k_route_fused, rgrid, dim3(256), sizeof(float) * a.H, st, a, b, tok_cnt, all_cnt);
   if (err == cudaSuccess) mark(KT_ROUTER);
   return err;
 }

@@ -62,9 +62,8 @@ template <int MODE, int NT, int CPW, int G>
 cudaError_t run(const MmaArgs& a, const Shape& sh, dim3 grid, cudaStream_t st) {
   const int threads = 32 * sh.ks * sh.rtp;
   const size_t smem = (size_t)sh.ks * sh.rtp * 2 * NT * 4 * 32 * sizeof(float);
-  if (a.x_bf16) k_w4_mma<MODE, NT, CPW, G, true><<<grid, threads, smem, st>>>(a);
-  else k_w4_mma<MODE, NT, CPW, G, false><<<grid, threads, smem, st>>>(a);
-  return cudaGetLastError();
+  if (a.x_bf16) return launch_k(a.pdl != 0, k_w4_mma<MODE, NT, CPW, G, true>, grid, dim3(threads), smem, st, a);
+  return launch_k(a.pdl != 0, k_w4_mma<MODE, NT, CPW, G, false>, grid, dim3(threads), smem, st, a);
 }
 
 template <int NT>
@@ -116,6 +115,7 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[rt][nt][c] = 0.f;
 
+  bool waited = false;
   if (active) {
     const bf16* wr[RT][2];
 #pragma unroll
@@ -156,7 +156,20 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
             mma_bf16(acc[rt][nt], af, hi ? x[nt][b].z : x[nt][b].x, hi ? x[nt][b].w : x[nt][b].y);
         }
     };
-    load(wa, xa, 0);
+    // the first chunk's weights do not depend on the previous kernel
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) wa[rt][h][b] = ldg_nc_v4(wr[rt][h] + 32 * b);
+    pdl_wait();
+    waited = true;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        xa[nt][b] = xr[nt] ? *reinterpret_cast<const uint4*>(xr[nt] + 32 * b) : make_uint4(0, 0, 0, 0);
     for (int c = 0; c < NC; c += 2) {
       if (c + 1 < NC) load(wb, xb, c + 1);
       compute(wa, xa);
@@ -178,6 +191,7 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
         }
   }
 
+  if (!waited) pdl_wait();
   // ---- argmax: per token, the largest (value, lowest row) of this warp,
   // then of the CTA, then one atomicMax per token and CTA
 #pragma unroll
@@ -230,8 +244,7 @@ template <int NT, int RT>
 cudaError_t run_lm(const LmArgs& a, cudaStream_t st) {
   const int rows_per_cta = kLmWarps * RT * 16;
   const dim3 grid((a.V + rows_per_cta - 1) / rows_per_cta, (a.B + 8 * NT - 1) / (8 * NT));
-  k_lm_mma<NT, RT><<<grid, kLmWarps * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(a.pdl != 0, k_lm_mma<NT, RT>, grid, dim3(kLmWarps * 32), 0, st, a);
 }
 
 template <int MODE, int NT, int CPW, int G>

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
   const int KS = a.ks, RTP = (blockDim.x >> 5) / KS;
   const int ks = warp % KS, rtp = warp / KS;
 
+  if (MODE != DENSE) pdl_wait();   // the job list comes from the previous kernel
   const uint8_t* W = a.W;
   const uint32_t* S = a.S;
   int ntok, tok0;
@@ -164,6 +165,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
         const int grp = G >= kChunkK ? ((c0 + j) * kChunkK) / G : (c0 + j) * kSpc + q;
         sv[j][rt][q] = ldg_nc_u32(S + ((size_t)(T0 + rt) * NG + grp) * 8 + (lane >> 2));
       }
+
+  // dense: the weights above do not depend on the previous kernel
+  if (MODE == DENSE) pdl_wait();
 
   // ---- activation rows of the lane's B-fragment column (token g of each n-tile)
   const bf16* xr[NT];

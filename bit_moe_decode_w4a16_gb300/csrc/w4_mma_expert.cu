@@ -60,8 +60,7 @@ cudaError_t run_staged(const MmaArgs& a, const StagedGeom& geo, cudaStream_t st)
   const long items = (long)a.max_jobs * geo.nrb;
   const long cap = (long)sm_count() * per_sm;
   const int grid = (int)(items < cap ? items : cap);
-  k_w4_mma_staged<MODE, CPW, G><<<grid, threads, smem, st>>>(a, geo);
-  return cudaGetLastError();
+  return launch_k(a.pdl != 0, k_w4_mma_staged<MODE, CPW, G>, dim3(grid), dim3(threads), smem, st, a, geo);
 }
 
 template <int MODE, int CPW, int G>
@@ -70,8 +69,7 @@ cudaError_t run(const MmaArgs& a, const Shape& sh, cudaStream_t st) {
   if (geo.ns >= 2) return run_staged<MODE, CPW, G>(a, geo, st);
   const dim3 grid(a.rows / (32 * sh.rtp), a.max_jobs);
   const size_t smem = (size_t)sh.ks * sh.rtp * 2 * 4 * 32 * sizeof(float);
-  k_w4_mma<MODE, 1, CPW, G><<<grid, 32 * sh.ks * sh.rtp, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(a.pdl != 0, k_w4_mma<MODE, 1, CPW, G, false>, grid, dim3(32 * sh.ks * sh.rtp), smem, st, a);
 }
 
 template <int MODE>

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NW = geo.nw, RTP = geo.rtp, KS = NW / RTP;
   const int NC = a.K / kChunkK, NG = a.K / G;
+  pdl_wait();
   // this CTA's items: a contiguous, balanced share of (job, row block) in
   // job order, so consecutive items of a CTA read the same activation rows
   const int n_items = *a.n_jobs * geo.nrb;

@@ -518,14 +518,14 @@ cudaError_t run_tc(const TcArgs& a, dim3 grid, cudaStream_t st) {
 
 }  // namespace
 
-int tc_pick_ksplit(int jobs, int nst) {
-  // aim for at least ~2 CTAs per SM of the 152, with >= 4 stages per split
+int tc_pick_ksplit(int /*jobs*/, int nst) {
+  // The split fixes the order in which a row's partial sums are added, so it
+  // depends on the reduction length only, never on how many jobs (streams,
+  // active experts) share the launch: the largest split <= kMaxSplit that
+  // leaves >= 4 stages per split.
   int best = 1;
-  for (int ks = 2; ks <= kMaxSplit; ++ks) {
-    if (nst % ks || nst / ks < 4) continue;
-    if ((long)jobs * best >= 300) break;
-    best = ks;
-  }
+  for (int ks = 2; ks <= kMaxSplit; ++ks)
+    if (nst % ks == 0 && nst / ks >= 4) best = ks;
   return best;
 }
 

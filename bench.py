@@ -14,6 +14,8 @@ on a bounded sample of the same workload instead.
 """
 
 import argparse
+import glob
+import hashlib
 import json
 import os
 import subprocess
@@ -170,6 +172,25 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu record
+    (profiles/dram_traffic.json), or None if there is none or the kernel
+    sources changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "bit_moe_decode_w4a16_gb300", "csrc", "*"))):
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("csrc_sha256"):
+        return None
+    return rec.get("bytes_per_launch", {}).get(kernel)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -293,7 +314,7 @@ def run_ours(args, dist, world, rank, local):
         p = prof[dom]
         achieved = p["bytes"] / (p["ms"] / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(dom),
                 "algorithmic_bytes_per_launch": round(p["bytes"] / p["launches"]),
                 "peak_source": f"{peak_kind} hbm_gbs (copy)"}
     step_bytes = sum(p["bytes"] for p in prof.values()) / max(1, args.profile_steps)

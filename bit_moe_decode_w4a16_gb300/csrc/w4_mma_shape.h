@@ -22,7 +22,7 @@ inline bool mma_shape_ok(int rows, int K, int g) {
 inline Shape mma_shape(int rows, int K, int /*g*/, int groups = 0, int min_ctas = 0) {
   Shape s;
   const int nc = K / 64;                          // even: K % 128 == 0
-  s.cpw = (nc % 4 == 0 && nc >= 16) ? 4 : 2;      // 256 or 128 of K per warp
+  s.cpw = nc % 4 == 0 ? 4 : 2;                    // 256 or 128 of K per warp
   s.ks = nc / s.cpw;                              // <= 16 for K <= 4096
   s.rtp = 1;
   while (s.rtp * 2 * s.ks <= 16 && rows % (32 * s.rtp * 2) == 0 &&

@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--max-streams", type=int, default=0,
+                    help="slots of the engine's KV arena (default: the workload's 32, or --batch if larger; at most 64)")
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--sweep", default="1,2,4,8,16,32", help="B values for the sweep ('' to skip)")
     ap.add_argument("--sweep-steps", type=int, default=10)
@@ -254,6 +256,7 @@ def run_ours(args, dist, world, rank, local):
     bm.build()
     cfg = dict(synth.CONFIGS[WORKLOAD])
     B = args.batch
+    cfg["max_streams"] = max(args.max_streams or cfg["max_streams"], B)
     e, t_build = build_model(bm, cfg, args.layers, cfg["max_streams"], args.policy)
     slots, last, lens = prefill(bm, e, cfg, B, args.layers, args.prefill)
     stream = torch.cuda.current_stream()

@@ -15,10 +15,10 @@
 //
 // Consumer warp (rtp, ks) reads its two tiles' A fragments and scales for
 // chunks [ks*CPW, +CPW) and the B fragments of the 8 token rows from the
-// stage, then the KS partial sums meet in shared memory and are added in ks
-// order, exactly as in k_w4_mma.  After the partials are written the
-// consumers release the stage (`empty` mbarrier) and the producer refills it
-// with item n+NS.  Every mbarrier wait is bounded; a wait that gives up sets
+// stage into registers and releases the stage at once (`empty` mbarrier, one
+// arrival per consumer warp), so the producer refills it with item n+NS while
+// the warps compute; the KS partial sums meet in shared memory and are added
+// in ks order, exactly as in k_w4_mma.  Every mbarrier wait is bounded; a wait that gives up sets
 // the error flag and the CTA stops consuming (the remaining waits stay
 // bounded), so a fault in the pipeline cannot hang the GPU.
 #pragma once
@@ -64,7 +64,7 @@ struct ItemInfo {
 };
 
 template <int MODE, int CPW, int G>
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs a, StagedGeom geo) {
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaArgs a, StagedGeom geo) {
   constexpr int kSpg = G / 16;
   constexpr int kSpc = G >= kChunkK ? 1 : kChunkK / G;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
   if (threadIdx.x == 0) {
     for (int i = 0; i < geo.ns; ++i) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), 1);
-      tc::mbar_init(tc::smem_u32(&empty_bar[i]), 1);
+      tc::mbar_init(tc::smem_u32(&empty_bar[i]), NW);   // one arrival per consumer warp
     }
     tc::fence_mbar_init();
     abort_s = 0;
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
   if (warp == NW) {
     // ---------------- producer: one lane issues every copy
     if (lane == 0) {
+      int cur_j = -1, cur_e = 0, cur_tok0 = 0, cur_ntok = 0, cur_row[kJobTokens];
       for (int n = 0; n < count; ++n) {
         const int it = first + n, s = n % geo.ns;
         if (n >= geo.ns) {
@@ -107,14 +108,21 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
           tc::fence_proxy_async_smem();
         }
         const int j = it / geo.nrb, rb = it - j * geo.nrb;
-        const int job = a.jobs[j];
-        const int e = job & 0x1FF, tok0 = (job >> 9) & 0xFFF, ntok = (job >> 21) & 0x1F;
+        if (j != cur_j) {   // consecutive items of a CTA mostly share their job: decode it once
+          cur_j = j;
+          const int job = a.jobs[j];
+          cur_e = job & 0x1FF;
+          cur_tok0 = (job >> 9) & 0xFFF;
+          cur_ntok = (job >> 21) & 0x1F;
+          for (int r = 0; r < kJobTokens; ++r)
+            cur_row[r] = r < cur_ntok ? (MODE == GATEUP ? a.pair_token[cur_tok0 + r] : cur_tok0 + r) : -1;
+        }
+        const int e = cur_e, tok0 = cur_tok0, ntok = cur_ntok;
         ItemInfo& inf = info_s[s];
         inf.tok0 = tok0;
         inf.ntok = ntok;
         inf.rb = rb;
-        for (int r = 0; r < kJobTokens; ++r)
-          inf.row[r] = r < ntok ? (MODE == GATEUP ? a.pair_token[tok0 + r] : tok0 + r) : -1;
+        for (int r = 0; r < kJobTokens; ++r) inf.row[r] = cur_row[r];
         const uint32_t base = tc::smem_u32(smem + (size_t)s * geo.stage);
         const uint32_t bar = tc::smem_u32(&full_bar[s]);
         const uint32_t x_bytes = (uint32_t)a.K * 2u;
@@ -151,6 +159,28 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
     const uint32_t* ss = reinterpret_cast<const uint32_t*>(st + geo.w_bytes);
     // rows past ntok hold stale bytes: they only feed MMA columns that are never stored
     const unsigned char* xrow = st + geo.w_bytes + geo.s_bytes + (size_t)(lane >> 2) * geo.x_stride + (lane & 3) * 16;
+    // this warp's operands of the item -> registers, then the stage is released
+    // at once, so its refill overlaps the warp's MMAs
+    uint4 wreg[CPW][2], xreg[CPW][2];
+    uint32_t sreg[CPW][2][kSpc];
+#pragma unroll
+    for (int j = 0; j < CPW; ++j) {
+      const int c = c0 + j;
+      xreg[j][0] = *reinterpret_cast<const uint4*>(xrow + (size_t)c * kChunkK * 2);
+      xreg[j][1] = *reinterpret_cast<const uint4*>(xrow + (size_t)c * kChunkK * 2 + 64);
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt) {
+        const int lt = rtp * 2 + rt;
+        wreg[j][rt] = ws[(lt * NC + c) * 32 + lane];
+#pragma unroll
+        for (int q = 0; q < kSpc; ++q) {
+          const int grp = G >= kChunkK ? (c * kChunkK) / G : c * kSpc + q;
+          sreg[j][rt][q] = ss[(lt * NG + grp) * 8 + (lane >> 2)];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty_bar[s]));
     float acc[2][4], tmp[2][4];
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt)
@@ -158,19 +188,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
       for (int c = 0; c < 4; ++c) acc[rt][c] = 0.f;
 #pragma unroll
     for (int j = 0; j < CPW; ++j) {
-      const int c = c0 + j;
-      const uint4 xv0 = *reinterpret_cast<const uint4*>(xrow + (size_t)c * kChunkK * 2);
-      const uint4 xv1 = *reinterpret_cast<const uint4*>(xrow + (size_t)c * kChunkK * 2 + 64);
+      const uint4 xv0 = xreg[j][0], xv1 = xreg[j][1];
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt) {
-        const int lt = rtp * 2 + rt;
-        const uint4 wv = ws[(lt * NC + c) * 32 + lane];
-        uint32_t sw[kSpc];
-#pragma unroll
-        for (int q = 0; q < kSpc; ++q) {
-          const int grp = G >= kChunkK ? (c * kChunkK) / G : c * kSpc + q;
-          sw[q] = ss[(lt * NG + grp) * 8 + (lane >> 2)];
-        }
+        const uint4 wv = wreg[j][rt];
+        const uint32_t(&sw)[kSpc] = sreg[j][rt];
         const uint32_t wwords[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
         for (int st4 = 0; st4 < 4; ++st4) {
@@ -199,8 +221,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32) k_w4_mma_staged(MmaArgs 
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) red[((((ks * RTP + rtp) * 2 + rt) * 4 + c) * 32) + lane] = acc[rt][c];
-    consumer_sync(nthreads);   // every consumer is done with stage s and the partials are in
-    if (threadIdx.x == 0) tc::mbar_arrive(tc::smem_u32(&empty_bar[s]));
+    consumer_sync(nthreads);   // the partials are in
 
     // epilogue: unit (rp, rt, j, lane) -> rows (g, g + 8), token 2t + j;
     // partials in ks order

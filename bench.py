@@ -47,9 +47,11 @@ def parse():
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--policy", type=int, default=0)
-    ap.add_argument("--prefill", default="decode", choices=["decode", "kv"],
-                    help="decode: prompts through decode_step (teacher-forced); kv: seed synthetic K/V of the "
-                         "same lengths (faster start, for profiler runs)")
+    ap.add_argument("--prefill", default="prompt", choices=["prompt", "decode", "kv"],
+                    help="prompt: prompts through kv_slot_prefill; decode: through decode_step (teacher-forced); "
+                         "kv: seed synthetic K/V of the same lengths (faster start, for profiler runs)")
+    ap.add_argument("--prefill-steps", type=int, default=5,
+                    help="timed ingestions of one longest-workload prompt (0 to skip)")
     return ap.parse_args()
 
 
@@ -88,10 +90,11 @@ class Dist:
             self.pg.destroy_process_group()
 
 
-def timed_region(step, sync, dist, steps, warmup, new_event=None, device="cpu"):
+def timed_region(step, sync, dist, steps, warmup, new_event=None, device="cpu", label="timed"):
     """W untimed steps, then exactly K steps bracketed by barrier + sync on
     both sides; returns the max over ranks of the elapsed seconds.  With
-    ``new_event`` (CUDA), the device time between two events is used."""
+    ``new_event`` (CUDA), the device time between two events is used, inside
+    an NVTX range named ``label``."""
     for _ in range(warmup):
         step()
     sync()
@@ -100,7 +103,7 @@ def timed_region(step, sync, dist, steps, warmup, new_event=None, device="cpu"):
     if new_event:
         import torch
         t0, t1 = new_event(), new_event()
-        torch.cuda.nvtx.range_push("timed")
+        torch.cuda.nvtx.range_push(label)
         t0.record()
         for _ in range(steps):
             step()
@@ -216,9 +219,10 @@ def build_model(bm, cfg, layers, max_streams, policy):
 
 
 def prefill(bm, e, cfg, B, layers, mode="decode"):
-    """Join B streams with empty slots and feed their prompts through
-    decode_step, teacher-forced; returns (slots, next device tokens).  With
-    mode "kv" the slots are seeded with synthetic K/V of the same lengths."""
+    """Join B streams with empty slots and feed their prompts (kv_slot_prefill,
+    or decode_step teacher-forced with mode "decode": the same bytes); returns
+    (slots, next device tokens, lengths).  With mode "kv" the slots are
+    seeded with synthetic K/V of the same lengths."""
     import torch
     import synth
     lens = synth.prompt_lengths(B, cfg["prompt"][0], cfg["prompt"][1], synth.seed_of(WORKLOAD, "prompt_lens"))
@@ -234,6 +238,11 @@ def prefill(bm, e, cfg, B, layers, mode="decode"):
     empty = torch.empty((layers, cfg["kv_heads"], 0, cfg["head_dim"]), dtype=torch.bfloat16, device="cuda")
     slots = [bm.kv_slot_seed(e, empty, empty, 0) for _ in range(B)]
     last = torch.zeros(B, dtype=torch.int32, device="cuda")
+    if mode == "prompt":
+        for i, s in enumerate(slots):
+            bm.kv_slot_prefill(e, s, torch.tensor(prompts[i], dtype=torch.int32, device="cuda"), last[i:i + 1])
+        torch.cuda.synchronize()
+        return slots, last, lens
     scratch = torch.empty(B, dtype=torch.int32, device="cuda")
     for t in range(max(lens)):
         idx = [i for i in range(B) if t < lens[i]]
@@ -337,8 +346,30 @@ def run_ours(args, dist, world, rank, local):
                 c1, n1 = n1, c1
 
             d = timed_region(sstep, torch.cuda.synchronize, dist, args.sweep_steps, 3,
-                             new_event=lambda: torch.cuda.Event(enable_timing=True), device="cuda")
+                             new_event=lambda: torch.cuda.Event(enable_timing=True), device="cuda",
+                             label="sweep_timed")
             sweep[str(b)] = round(world * b * args.sweep_steps / d, 1)
+    # prompt ingestion: one prompt of the workload's longest length into a
+    # fresh slot per step (blocks of max_streams rows)
+    pf = None
+    if args.prefill_steps > 0:
+        P = cfg["prompt"][1]
+        ptoks = synth.tokens(WORKLOAD, "prefill_bench", P, cfg["vocab"], device="cuda")
+        one = torch.empty(1, dtype=torch.int32, device="cuda")
+        empty = torch.empty((args.layers, cfg["kv_heads"], 0, cfg["head_dim"]), dtype=torch.bfloat16, device="cuda")
+        bm.kv_slot_release(e, slots[0])
+
+        def pstep():
+            s = bm.kv_slot_seed(e, empty, empty, 0)
+            bm.kv_slot_prefill(e, s, ptoks, one, None, stream)
+            bm.kv_slot_release(e, s)
+
+        d = timed_region(pstep, torch.cuda.synchronize, dist, args.prefill_steps, 3,
+                         new_event=lambda: torch.cuda.Event(enable_timing=True), device="cuda",
+                         label="prefill_timed")
+        pf = {"prompt_tokens": P, "block_rows": cfg["max_streams"], "steps": args.prefill_steps,
+              "ms_per_prompt": round(1e3 * d / args.prefill_steps, 3),
+              "tok_s": round(world * P * args.prefill_steps / d, 1)}
     stats = bm.bm_engine_stats(e)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -348,7 +379,7 @@ def run_ours(args, dist, world, rank, local):
         "config": {"workload": "full 48-layer 30B-class MoE decode (hidden 2048, 32/4 heads x 128, 128 experts "
                                "top-8, FFN 768, vocab 151936), one decode_step of B streams per step",
                    "global_batch": B, "layers": args.layers, "ctx_cap": cfg["ctx_cap"],
-                   "prompt_lens": f"U[{cfg['prompt'][0]},{cfg['prompt'][1]}] prefilled teacher-forced",
+                   "prompt_lens": f"U[{cfg['prompt'][0]},{cfg['prompt'][1]}] ingested before timing ({args.prefill})",
                    "kv_len_mean_at_start": round(sum(lens) / len(lens), 1),
                    "l2": "inputs larger than L2: ~14.6 GB of weights read per step",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
@@ -358,7 +389,7 @@ def run_ours(args, dist, world, rank, local):
         "roofline": roof,
         "step_algorithmic_GB": round(step_bytes / 1e9, 3),
         "step_GB_per_s": round(step_bytes / (dt / args.steps) / 1e9, 1),
-        "kernels": kernels, "sweep_tok_s": sweep,
+        "kernels": kernels, "sweep_tok_s": sweep, "prefill": pf,
         "weight_GB": round(stats["weight_bytes"] / 1e9, 3), "arena_GB": round(stats["arena_bytes"] / 1e9, 3),
         "setup_s": round(t_build, 1),
     }

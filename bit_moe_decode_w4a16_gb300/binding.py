@@ -100,6 +100,7 @@ def lib():
             "moe_grouped_w4_noalloc": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V], S),
             "bm_moe_noalloc_max_bytes": ([], SZ),
             "decode_step": ([V, I, V, V, V, V, V], S),
+            "kv_slot_prefill": ([V, I, I, V, V, V, V], S),
             "bm_engine_profile_step": ([V, I, V, V, V, ctypes.POINTER(bm_kernel_profile), I, PI, V], S),
             "bm_w4_quantize": ([V, I, I, I, V, V, V], S),
             "bm_slot_map_create": ([I, I, ctypes.POINTER(V)], S),
@@ -289,6 +290,12 @@ def decode_step(e, slots, tokens, next_tokens, logits=None, stream=None):
     arr = _i32_array(slots)
     _check(lib().decode_step(e, len(slots), ctypes.addressof(arr), ptr(tokens), ptr(next_tokens), ptr(logits),
                              stream_handle(stream)))
+
+
+def kv_slot_prefill(e, slot, tokens, next_token, logits=None, stream=None):
+    """tokens: host or device int32 [n]; next_token: host or device int32 [1]."""
+    _check(lib().kv_slot_prefill(e, int(slot), int(tokens.numel()), ptr(tokens), ptr(next_token), ptr(logits),
+                                 stream_handle(stream)))
 
 
 def bm_engine_profile_step(e, slots, tokens, next_tokens, stream=None):

@@ -29,6 +29,13 @@
 //     stream's chunks in ascending order: M = max m_c, den = sum l_c e^(m_c - M),
 //     out = (sum o_c e^(m_c - M)) / den, rounded to bf16 and stored as fp16.
 // A stream's result depends only on its own length and data.
+//
+// Prompt ingestion runs the same kernel over rows that all belong to one
+// slot: row b sits at position len + b and attends causally to positions
+// 0..len + b.  The rows' rotated k and v are written by k_append_rows first
+// (a row reads positions that other rows of the launch produce), and the
+// kernel then skips its own append; a row's arithmetic is that of a decode
+// step at the same position, so both paths leave the same bytes.
 #include <float.h>
 
 #include "kernels.cuh"
@@ -59,6 +66,18 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// Rotate-half RoPE of one pair (x0 = x[i], x1 = x[i + d/2]) with explicit
+// roundings, so every kernel that rotates k produces the same bits.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, bf16& y0, bf16& y1) {
+  y0 = f2bf(__fmaf_rn(x0, c, -__fmul_rn(x1, s)));
+  y1 = f2bf(__fmaf_rn(x1, c, __fmul_rn(x0, s)));
+}
+
+// Position of row b: the slot's length, plus b for the rows of a prompt.
+__device__ __forceinline__ int row_position(const AttnFusedArgs& a, int b, int slot) {
+  return a.ar.len[slot] + (a.prefill ? b : 0);
 }
 
 template <int D>
@@ -95,7 +114,7 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     if (slot < 0 || slot >= ar.S) {
       if (blockIdx.x == 0) a.chk.fail(1);
     } else {
-      const int L = ar.len[slot] + 1;
+      const int L = row_position(a, b, slot) + 1;
       if (L < 1 || L > ar.cap) {
         if (blockIdx.x == 0) a.chk.fail(2);
       } else {
@@ -118,7 +137,7 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     while (sm.pre[b + 1] <= it) ++b;
     const int r = it - sm.pre[b], kh = r % kvh, c = r / kvh;
     const int slot = sm.slot[b], nc = sm.nc[b];
-    const int pos = ar.len[slot], L = pos + 1;
+    const int pos = row_position(a, b, slot), L = pos + 1;
     const int j0 = c * kAttnChunk, n = min(kAttnChunk, L - j0);
     const bool last_chunk = c == nc - 1;
     const bf16* row = a.qkv + (size_t)b * a.ld_qkv;
@@ -138,21 +157,17 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
       bf16 y0 = f2bf(0.f), y1 = f2bf(0.f);
       if (h < G) {
         const bf16* src = row + (size_t)(kh * G + h) * D;
-        const float x0 = bf2f(src[i]), x1 = bf2f(src[i + half]), cc = sm.cs[i], ss = sm.cs[half + i];
-        y0 = f2bf(x0 * cc - x1 * ss);
-        y1 = f2bf(x1 * cc + x0 * ss);
+        rope_pair(bf2f(src[i]), bf2f(src[i + half]), sm.cs[i], sm.cs[half + i], y0, y1);
       }
       sm.qs[h][i] = y0;
       sm.qs[h][i + half] = y1;
     }
-    if (last_chunk) {
+    if (last_chunk && !a.prefill) {
       const bf16* ksrc = row + (size_t)(a.qh + kh) * D;
       const bf16* vsrc = row + (size_t)(a.qh + kvh + kh) * D;
-      for (int i = tid; i < half; i += blockDim.x) {
-        const float x0 = bf2f(ksrc[i]), x1 = bf2f(ksrc[i + half]), cc = sm.cs[i], ss = sm.cs[half + i];
-        Kb[(size_t)pos * D + i] = f2bf(x0 * cc - x1 * ss);
-        Kb[(size_t)pos * D + i + half] = f2bf(x1 * cc + x0 * ss);
-      }
+      for (int i = tid; i < half; i += blockDim.x)
+        rope_pair(bf2f(ksrc[i]), bf2f(ksrc[i + half]), sm.cs[i], sm.cs[half + i], Kb[(size_t)pos * D + i],
+                  Kb[(size_t)pos * D + i + half]);
       for (int i = tid; i < D; i += blockDim.x) Vb[(size_t)pos * D + i] = vsrc[i];
       __threadfence();
     }
@@ -314,6 +329,35 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
   }
 }
 
+// Rotated k and v of every row to the arena at the row's position: one CTA
+// per (row, kv head).
+template <int D>
+__global__ void __launch_bounds__(64) k_append_rows(AttnFusedArgs a) {
+  pdl_wait();
+  const AttnArena& ar = a.ar;
+  const int b = blockIdx.x, kh = blockIdx.y, half = D / 2;
+  const int slot = a.slots[b];
+  if (slot < 0 || slot >= ar.S) {
+    if (threadIdx.x == 0) a.chk.fail(1);
+    return;
+  }
+  const int pos = row_position(a, b, slot);
+  if (pos < 0 || pos >= ar.cap) {
+    if (threadIdx.x == 0) a.chk.fail(2);
+    return;
+  }
+  const bf16* row = a.qkv + (size_t)b * a.ld_qkv;
+  const bf16* ksrc = row + (size_t)(a.qh + kh) * D;
+  const bf16* vsrc = row + (size_t)(a.qh + ar.kvh + kh) * D;
+  const size_t base = (size_t)a.layer * ar.layer_stride() + (size_t)slot * ar.slot_stride() +
+                      (size_t)kh * ar.cap * D + (size_t)pos * D;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const float2 cs = a.rope[(size_t)pos * half + i];
+    rope_pair(bf2f(ksrc[i]), bf2f(ksrc[i + half]), cs.x, cs.y, ar.K[base + i], ar.K[base + i + half]);
+  }
+  for (int i = threadIdx.x; i < D; i += blockDim.x) ar.V[base + i] = vsrc[i];
+}
+
 }  // namespace
 
 bool attention_fused_supports(const AttnArena& ar, int qh) {
@@ -331,6 +375,13 @@ cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool
   const dim3 grid((unsigned)(items < cap ? items : cap));
   if (a.ar.d == 128) return launch_k(pdl, k_attn_fused<128>, grid, dim3(kWarpsA * 32), 0, st, a);
   return launch_k(pdl, k_attn_fused<64>, grid, dim3(kWarpsA * 32), 0, st, a);
+}
+
+cudaError_t launch_append_rows(const AttnFusedArgs& a, cudaStream_t st, bool pdl) {
+  if (!attention_fused_supports(a.ar, a.qh) || a.B < 1 || a.B > kMaxBatch) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)a.B, (unsigned)a.ar.kvh);
+  if (a.ar.d == 128) return launch_k(pdl, k_append_rows<128>, grid, dim3(64), 0, st, a);
+  return launch_k(pdl, k_append_rows<64>, grid, dim3(64), 0, st, a);
 }
 
 }  // namespace bm

@@ -136,7 +136,8 @@ struct bm_engine {
   int* tc_counters = nullptr;   // split-K arrival counters (zero between launches)
   std::vector<cudaEvent_t> prof_events;
   cudaStream_t cap_stream = nullptr;
-  std::map<int, cudaGraphExec_t> graphs;
+  std::map<int, cudaGraphExec_t> graphs;   // decode graphs by B; prompt blocks under negative keys
+  std::map<int, int> graph_kernels;         // kernels in each graph
   bm_stats st{};
 
   bm_engine(const bm_config& c) : cfg(c), slots(c.max_streams, c.ctx_cap) {}
@@ -179,7 +180,15 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
 // attention (RoPE, append, chunks and merge in one launch), o_proj+residual,
 // routing (router, top-k and sort in one launch), gate/up, down,
 // combine+norm; then lm_head with the argmax fused.
-cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark) {
+// Prompt blocks (`prompt` 1, or 2 for the last block of a prompt) run the
+// same kernels over B rows of one slot at positions len .. len + B - 1: the
+// rows' k and v go to the arena first, attention takes each row's own
+// position, and the length advances by B.  Only the last block's last row
+// reaches the output projection.
+enum PromptBlock { kDecode = 0, kPromptBlock = 1, kPromptLast = 2 };
+
+cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark,
+                             int prompt = kDecode) {
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
   cudaError_t err;
@@ -206,11 +215,18 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     if (attention_fused_supports(e->arena, c.q_heads)) {
       AttnFusedArgs fa{e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope,
                        reinterpret_cast<__half*>(e->attn), e->attn_part,
-                       (c.ctx_cap + kAttnChunk - 1) / kAttnChunk, e->attn_cnt, B, chk_of(e)};
+                       (c.ctx_cap + kAttnChunk - 1) / kAttnChunk, e->attn_cnt, B, chk_of(e),
+                       prompt != kDecode ? 1 : 0};
+      if (prompt != kDecode) {
+        if ((err = launch_append_rows(fa, s, pdl)) != cudaSuccess) return err;
+        mark(KT_ROPE_APPEND);
+        ++n;
+      }
       if ((err = launch_attention_fused(fa, s, pdl)) != cudaSuccess) return err;
       mark(KT_ATTN_PART);
       ++n;
     } else {
+      if (prompt != kDecode) return cudaErrorNotSupported;
       if ((err = launch_rope_append(e->arena, l, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope, e->q, B,
                                     chk_of(e), s, pdl)) != cudaSuccess)
         return err;
@@ -253,10 +269,22 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
     if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->xn, last ? 0 : 1, s, mark, pdl)) != cudaSuccess) return err;
     n += 5;   // o_proj, routing, gate/up, down, combine
   }
+  if (prompt == kPromptBlock) {
+    // the slot's length moves past the block (row 0 of d_slots is the slot)
+    if ((err = launch_advance(e->arena.len, e->d_slots, 1, s, B)) != cudaSuccess) return err;
+    ++n;
+    if (launches) *launches = n;
+    return cudaSuccess;
+  }
   LmArgs la{};
   la.W = e->lm_head; la.V = c.vocab; la.K = H; la.X = e->xn; la.B = B; la.logits = e->logits;
   la.next = e->d_next; la.len = e->arena.len; la.slots = e->d_slots; la.advance = 1;
   la.keys = e->lm_keys; la.counter = e->lm_counter; la.pdl = pdl;
+  if (prompt == kPromptLast) {
+    la.X = e->xn + (size_t)(B - 1) * H;
+    la.B = 1;
+    la.advance = B;
+  }
   if ((err = launch_lm_mma(la, s)) != cudaSuccess) return err;
   mark(KT_LM_HEAD);
   ++n;
@@ -265,8 +293,10 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
 }
 
 // Enqueue one decode step for B streams reading e->d_slots / e->d_tokens.
-cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark = Marker()) {
-  if (e->family == BM_POLICY_MMA) return enqueue_step_mma(e, B, s, launches, mark);
+cudaError_t enqueue_step(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark = Marker(),
+                         int prompt = kDecode) {
+  if (e->family == BM_POLICY_MMA) return enqueue_step_mma(e, B, s, launches, mark, prompt);
+  if (prompt != kDecode) return cudaErrorNotSupported;
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim;
   const bool tc = e->family == BM_POLICY_TC;
@@ -862,6 +892,8 @@ namespace {
 // Checks shared by decode_step and bm_engine_profile_step, then the upload of
 // slot ids and tokens into the step's static device inputs (through the next
 // entry of the pinned staging ring).
+bm_status stage_inputs(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, cudaStream_t s);
+
 bm_status prepare_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, int32_t* next_tokens,
                        cudaStream_t s, const char* who) {
   if (!e || !slots || !tokens || !next_tokens) return set_error(BM_ERR_INVALID_ARG, std::string(who) + ": null argument");
@@ -872,7 +904,13 @@ bm_status prepare_step(bm_engine* e, int B, const int32_t* slots, const int32_t*
   std::string err;
   const bm_status st = e->slots.check_batch(slots, B, &err);
   if (st != BM_OK) return set_error(st, std::string(who) + ": " + err);
-  const size_t S = c.max_streams;
+  return stage_inputs(e, B, slots, tokens, s);
+}
+
+// Copy B slot ids (host) and B tokens (host or device) to e->d_slots and
+// e->d_tokens through the pinned staging ring.
+bm_status stage_inputs(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens, cudaStream_t s) {
+  const size_t S = e->cfg.max_streams;
   const int slot = e->ring_pos;
   e->ring_pos = (e->ring_pos + 1) % bm_engine::kStageRing;
   int32_t* stage = e->h_stage + 2 * S * slot;
@@ -886,6 +924,44 @@ bm_status prepare_step(bm_engine* e, int B, const int32_t* slots, const int32_t*
     BM_CUDA(cudaMemcpyAsync(e->d_tokens, stage + S, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s), "token upload");
   }
   BM_CUDA(cudaEventRecord(e->ev_ring[slot], s), "staging event");
+  return BM_OK;
+}
+
+// Enqueue one step (or prompt block) of B rows from e->d_slots / e->d_tokens:
+// through the cached CUDA graph of (B, prompt) when graphs are on, else
+// eagerly.  *n_out = the kernels it launches.
+bm_status run_step(bm_engine* e, int B, int prompt, cudaStream_t s, int* n_out, const char* who) {
+  int n = 0;
+  if (e->cfg.use_graph) {
+    const int key = prompt == kDecode ? B : -(4 * B + prompt);   // prompt graphs under negative keys
+    auto it = e->graphs.find(key);
+    if (it == e->graphs.end()) {
+      cudaGraph_t graph = nullptr;
+      BM_CUDA(cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal), "graph capture begin");
+      const cudaError_t ce = enqueue_step(e, B, e->cap_stream, &n, Marker(), prompt);
+      const cudaError_t ee = cudaStreamEndCapture(e->cap_stream, &graph);
+      if (ce != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return set_error(BM_ERR_CUDA, std::string(who) + " capture: " + cudaGetErrorString(ce));
+      }
+      BM_CUDA(ee, "graph capture end");
+      cudaGraphExec_t exec = nullptr;
+      const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      BM_CUDA(ie, "graph instantiate");
+      it = e->graphs.emplace(key, exec).first;
+      e->graph_kernels[key] = n;
+      e->st.graph_captures += 1;
+    }
+    BM_CUDA(cudaGraphLaunch(it->second, s), "graph launch");
+    e->st.graph_launches += 1;
+    n = e->graph_kernels[key];
+  } else {
+    const cudaError_t ce = enqueue_step(e, B, s, &n, Marker(), prompt);
+    if (ce != cudaSuccess) return set_error(BM_ERR_CUDA, std::string(who) + " launch: " + cudaGetErrorString(ce));
+  }
+  e->st.kernel_launches += n;
+  *n_out = n;
   return BM_OK;
 }
 
@@ -925,33 +1001,8 @@ bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* 
   bm_status st = prepare_step(e, B, slots, tokens, next_tokens, s, "decode_step");
   if (st != BM_OK) return st;
   int n = 0;
-  if (c.use_graph) {
-    auto it = e->graphs.find(B);
-    if (it == e->graphs.end()) {
-      cudaGraph_t graph = nullptr;
-      BM_CUDA(cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal), "graph capture begin");
-      const cudaError_t ce = enqueue_step(e, B, e->cap_stream, &n);
-      const cudaError_t ee = cudaStreamEndCapture(e->cap_stream, &graph);
-      if (ce != cudaSuccess) {
-        if (graph) cudaGraphDestroy(graph);
-        return set_error(BM_ERR_CUDA, std::string("decode_step capture: ") + cudaGetErrorString(ce));
-      }
-      BM_CUDA(ee, "graph capture end");
-      cudaGraphExec_t exec = nullptr;
-      const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
-      cudaGraphDestroy(graph);
-      BM_CUDA(ie, "graph instantiate");
-      it = e->graphs.emplace(B, exec).first;
-      e->st.graph_captures += 1;
-      e->st.kernels_per_step = n;
-    }
-    BM_CUDA(cudaGraphLaunch(it->second, s), "graph launch");
-    e->st.graph_launches += 1;
-  } else {
-    BM_CUDA(enqueue_step(e, B, s, &n), "decode_step launch");
-    e->st.kernels_per_step = n;
-  }
-  e->st.kernel_launches += e->st.kernels_per_step;
+  if ((st = run_step(e, B, kDecode, s, &n, "decode_step")) != BM_OK) return st;
+  e->st.kernels_per_step = n;
   BM_CUDA(cudaMemcpyAsync(next_tokens, e->d_next, sizeof(int32_t) * B, cudaMemcpyDefault, s), "next token copy");
   if (logits)
     BM_CUDA(cudaMemcpyAsync(logits, e->logits, sizeof(float) * B * (size_t)c.vocab, cudaMemcpyDefault, s),
@@ -959,6 +1010,41 @@ bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* 
   e->slots.advance(slots, B);
   e->st.steps += 1;
   e->st.tokens += B;
+  return bm::ok();
+}
+
+bm_status kv_slot_prefill(bm_engine* e, int slot, int n_tokens, const int32_t* tokens, int32_t* next_token,
+                          float* logits, void* stream) {
+  if (!e || !tokens || !next_token) return set_error(BM_ERR_INVALID_ARG, "kv_slot_prefill: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_tokens < 1) return set_error(BM_ERR_INVALID_ARG, "kv_slot_prefill: n_tokens must be >= 1");
+  if (slot < 0 || slot >= c.max_streams) return set_error(BM_ERR_INVALID_ARG, "kv_slot_prefill: slot out of range");
+  if (!e->slots.active(slot)) return set_error(BM_ERR_SLOT_FREE, "kv_slot_prefill: slot is not active");
+  if (!e->emb_set) return set_error(BM_ERR_NOT_READY, "kv_slot_prefill: embeddings not set");
+  for (int l = 0; l < c.layers; ++l)
+    if (!e->L[l].set) return set_error(BM_ERR_NOT_READY, "kv_slot_prefill: layer " + std::to_string(l) + " not set");
+  if (e->family != BM_POLICY_MMA || !attention_fused_supports(e->arena, c.q_heads))
+    return set_error(BM_ERR_UNSUPPORTED, "kv_slot_prefill: needs the warp-MMA kernel family and fused attention");
+  if ((long)e->slots.length(slot) + n_tokens > c.ctx_cap)
+    return set_error(BM_ERR_CTX_CAP, "kv_slot_prefill: the prompt does not fit the context cap");
+  const int T = c.max_streams;
+  std::vector<int32_t> rows(T, slot);
+  for (int i = 0; i < n_tokens; i += T) {
+    const int b = n_tokens - i < T ? n_tokens - i : T;
+    const int32_t* tok = tokens + i;
+    bm_status st = stage_inputs(e, b, rows.data(), tok, s);
+    if (st != BM_OK) return st;
+    int n = 0;
+    if ((st = run_step(e, b, i + b == n_tokens ? kPromptLast : kPromptBlock, s, &n, "kv_slot_prefill")) != BM_OK)
+      return st;
+  }
+  BM_CUDA(cudaMemcpyAsync(next_token, e->d_next, sizeof(int32_t), cudaMemcpyDefault, s), "next token copy");
+  if (logits)
+    BM_CUDA(cudaMemcpyAsync(logits, e->logits, sizeof(float) * (size_t)c.vocab, cudaMemcpyDefault, s), "logits copy");
+  e->slots.advance_by(slot, n_tokens);
+  e->st.tokens += n_tokens;
   return bm::ok();
 }
 

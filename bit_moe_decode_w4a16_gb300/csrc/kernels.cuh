@@ -253,9 +253,13 @@ struct AttnFusedArgs {
   unsigned int* counters;
   int B;
   DevCheck chk;
+  int prefill;          // rows of one slot at positions len + b; k/v appended beforehand
 };
 bool attention_fused_supports(const AttnArena& ar, int qh);
 cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool pdl = false);
+// Rotated k and v of each row b to the arena at the row's position (len of
+// its slot, plus b when a.prefill): the prompt path's append.
+cudaError_t launch_append_rows(const AttnFusedArgs& a, cudaStream_t st, bool pdl = false);
 
 // ---------------------------------------------------------------- model glue
 cudaError_t launch_embed(const bf16* table, int V, int H, const int32_t* tokens, bf16* x, int B,
@@ -270,7 +274,8 @@ cudaError_t launch_lm_head(const bf16* W, int V, int H, const bf16* x, const bf1
 // next[b] = argmax_v logits[b][v] (ties: lowest v); len[slots[b]] += advance.
 cudaError_t launch_argmax(const float* logits, int V, int B, int32_t* next, int32_t* len,
                           const int32_t* slots, int advance, cudaStream_t st);
-cudaError_t launch_advance(int32_t* len, const int32_t* slots, int B, cudaStream_t st);
+// len[slots[b]] += by for b < B (slots distinct).
+cudaError_t launch_advance(int32_t* len, const int32_t* slots, int B, cudaStream_t st, int by = 1);
 cudaError_t launch_quantize(const float* W, int N, int K, int g, uint8_t* packed, __half* scales,
                             cudaStream_t st);
 

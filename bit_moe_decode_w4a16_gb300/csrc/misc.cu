@@ -145,9 +145,9 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int
   }
 }
 
-__global__ void k_advance(int32_t* len, const int32_t* slots, int B) {
+__global__ void k_advance(int32_t* len, const int32_t* slots, int B, int by) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) len[slots[b]] += 1;
+  if (b < B) len[slots[b]] += by;
 }
 
 // One thread per (row, group of g).
@@ -217,8 +217,8 @@ cudaError_t launch_argmax(const float* logits, int V, int B, int32_t* next, int3
   return cudaGetLastError();
 }
 
-cudaError_t launch_advance(int32_t* len, const int32_t* slots, int B, cudaStream_t st) {
-  k_advance<<<(B + 127) / 128, 128, 0, st>>>(len, slots, B);
+cudaError_t launch_advance(int32_t* len, const int32_t* slots, int B, cudaStream_t st, int by) {
+  k_advance<<<(B + 127) / 128, 128, 0, st>>>(len, slots, B, by);
   return cudaGetLastError();
 }
 

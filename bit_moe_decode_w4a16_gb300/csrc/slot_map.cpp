@@ -87,6 +87,8 @@ void SlotMap::advance(const int32_t* slots, int B) {
   for (int i = 0; i < B; ++i) len_[slots[i]] += 1;
 }
 
+void SlotMap::advance_by(int slot, int n) { len_[slot] += n; }
+
 }  // namespace bm
 
 // ------------------------------------------------------------------ C ABI

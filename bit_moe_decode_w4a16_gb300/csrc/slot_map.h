@@ -34,6 +34,8 @@ class SlotMap {
   // Slot ids in range, distinct, active, with room for one more position.
   bm_status check_batch(const int32_t* slots, int B, std::string* err) const;
   void advance(const int32_t* slots, int B);
+  // A prompt of n positions written into an active slot.
+  void advance_by(int slot, int n);
 
  private:
   int cap_;

@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     const unsigned long long key = atomicExch(a.keys + b, 0ull);
     a.next[b] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-    if (a.advance) a.len[a.slots[b]] += 1;
+    if (a.advance) a.len[a.slots[b]] += a.advance;
   }
   if (threadIdx.x == 0) *a.counter = 0u;
 }

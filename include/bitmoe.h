@@ -351,6 +351,26 @@ size_t bm_moe_noalloc_max_bytes(void);
 bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens,
                       int32_t* next_tokens, float* logits, void* stream);
 
+/* Prompt ingestion into an active slot ([KV-slot isolation] §1: a stream's
+ * K/V is written once when it joins, then grows one position per decode
+ * step): the n_tokens prompt tokens go to positions len .. len + n_tokens - 1
+ * of `slot`, each layer's rotated k and v are written there, and the slot's
+ * length advances by n_tokens.  The prompt runs in blocks of up to
+ * max_streams rows through the decode kernels (one CUDA graph per block
+ * shape with use_graph); row j of a block attends causally to positions
+ * 0..len + j.  Every row is computed exactly as a decode step at its
+ * position, so the arena bytes, logits and next token equal those of
+ * n_tokens single-stream decode_step calls fed the same tokens.
+ * tokens: int32 [n_tokens], HOST or DEVICE; next_token: int32 [1], HOST or
+ * DEVICE, the greedy argmax after the last prompt token; logits: DEVICE fp32
+ * [V] of that position, or NULL.
+ * Errors: BM_ERR_INVALID_ARG (NULL, n_tokens < 1, slot out of range),
+ * BM_ERR_SLOT_FREE, BM_ERR_CTX_CAP (len + n_tokens > ctx_cap; nothing is
+ * written), BM_ERR_NOT_READY, BM_ERR_UNSUPPORTED (an engine not on the
+ * warp-MMA kernel family), BM_ERR_CUDA. */
+bm_status kv_slot_prefill(bm_engine* e, int slot, int n_tokens, const int32_t* tokens,
+                          int32_t* next_token, float* logits, void* stream);
+
 /* decode_step run without the graph, with a CUDA event recorded after every
  * kernel launch on `stream`, then synchronised.  Same arguments and the same
  * effect on slots and outputs as decode_step (logits are not returned).  Fills

@@ -40,7 +40,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 from .numerics import bf16_round, dequant_w4, from_bf16_bits
-from .ops import rmsnorm, rope_rotate_half, slot_attention, route_topk, silu, rowwise
+from .ops import rmsnorm, rope_rotate_half, slot_attention, causal_block_attention, route_topk, silu, rowwise
 
 
 @dataclass
@@ -143,6 +143,16 @@ class OracleKV:
         Vl = np.concatenate([Vl[:, :pos], np.asarray(v, np.float64)[:, None]], axis=1)
         self.K[slot][layer], self.V[slot][layer] = Kl, Vl
 
+    def write_block(self, layer, slot, k, v):
+        """Place a prompt's k, v ([P][kvh][d]) at positions length .. length+P-1."""
+        pos = self.map.length[slot]
+        k = np.asarray(k, np.float64).transpose(1, 0, 2)
+        v = np.asarray(v, np.float64).transpose(1, 0, 2)
+        Kl, Vl = self.K[slot][layer], self.V[slot][layer]
+        assert Kl.shape[1] in (pos, pos + k.shape[1])
+        self.K[slot][layer] = np.concatenate([Kl[:, :pos], k], axis=1)
+        self.V[slot][layer] = np.concatenate([Vl[:, :pos], v], axis=1)
+
     def view(self, layer, slot, count):
         return self.K[slot][layer][:, :count], self.V[slot][layer][:, :count]
 
@@ -178,6 +188,18 @@ def decoder_layer(cfg, lw, x, slots, kv, layer, trace=None):
         kv.write_pending(layer, slot, k_rot, v[b])
         Kc, Vc = kv.view(layer, slot, pos + 1)
         o[b] = _round(slot_attention(q_rot[b], Kc, Vc)).reshape(-1)
+    y = _after_attention(cfg, lw, x, o, trace)
+    if trace is not None:
+        trace.update(dict(xn=xn, qkv=qkv, q_rot=q_rot, attn=o))
+    return y
+
+
+def _after_attention(cfg, lw, x, o, trace=None):
+    """The rest of a decoder layer, row by row: output projection with the
+    residual, RMSNorm, top-k routing, the selected experts, and the weighted
+    combine with the residual (x, o: bf16 values [B][H], [B][qh*d])."""
+    H, qh, d, g = cfg.hidden, cfg.q_heads, cfg.head_dim, cfg.group
+    B = x.shape[0]
     Wo = dequant_w4(lw["wo"][0], lw["wo"][1], qh * d, g)
     h = _round(x + rowwise(Wo, o))
     hn = _round(rmsnorm(h, lw.get("ffn_norm"), cfg.eps))
@@ -205,8 +227,34 @@ def decoder_layer(cfg, lw, x, slots, kv, layer, trace=None):
             acc = acc + w[b, r] * out
         y[b] = _round(h[b] + acc)
     if trace is not None:
-        trace.update(dict(xn=xn, qkv=qkv, q_rot=q_rot, attn=o, h=h, hn=hn,
-                          ids=ids, w=w, expert_out=outs_all, y=y))
+        trace.update(dict(h=h, hn=hn, ids=ids, w=w, expert_out=outs_all, y=y))
+    return y
+
+
+def prefill_layer(cfg, lw, x, slot, kv, layer, trace=None):
+    """One decoder layer over the P prompt rows of one stream (bf16 values
+    [P][H]); row i sits at position start + i, start = the slot's length.
+    Same arithmetic as ``decoder_layer`` for every row; the attention is the
+    causal block form over the slot."""
+    H, qh, kvh, d, g = cfg.hidden, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.group
+    x = np.asarray(x, dtype=np.float64)
+    P = x.shape[0]
+    start = kv.map.length[slot]
+    xn = _round(rmsnorm(x, lw.get("attn_norm"), cfg.eps))
+    Wqkv = dequant_w4(lw["wqkv"][0], lw["wqkv"][1], H, g)
+    qkv = _round(rowwise(Wqkv, xn))
+    q = qkv[:, : qh * d].reshape(P, qh, d)
+    k = qkv[:, qh * d: (qh + kvh) * d].reshape(P, kvh, d)
+    v = qkv[:, (qh + kvh) * d:].reshape(P, kvh, d)
+    pos = start + np.arange(P)
+    q_rot = _round(rope_rotate_half(q, pos, cfg.rope_base))
+    k_rot = _round(rope_rotate_half(k, pos, cfg.rope_base))
+    kv.write_block(layer, slot, k_rot, v)
+    Kc, Vc = kv.view(layer, slot, start + P)
+    o = _round(causal_block_attention(q_rot, Kc, Vc, start)).reshape(P, qh * d)
+    y = _after_attention(cfg, lw, x, o, trace)
+    if trace is not None:
+        trace.update(dict(xn=xn, qkv=qkv, q_rot=q_rot, attn=o))
     return y
 
 
@@ -241,3 +289,33 @@ def model_step(cfg, weights, kv, slots, tokens, traces=None):
     nxt = np.argmax(logits, axis=1).astype(np.int32)
     kv.map.advance(list(slots))
     return logits, nxt
+
+
+def model_prefill(cfg, weights, kv, slot, tokens, traces=None):
+    """Prompt ingestion for one active stream; returns (logits [V], next id)
+    of the position after the prompt.
+
+    The P tokens take positions start .. start+P-1 (start = the slot's
+    length); every layer writes their K/V into the slot
+    ([KV-slot isolation, §1 Contribution]: the stream's K/V is written once,
+    at join, then extended by decode), and the length advances by P.  Only
+    the last row reaches the output projection.  Rejected (ValueError) when
+    the slot is free or the prompt does not fit the context cap.
+    """
+    P = len(tokens)
+    if P < 1:
+        raise ValueError("empty prompt")
+    if not kv.map.active[slot]:
+        raise ValueError("slot is free")
+    if kv.map.length[slot] + P > kv.map.ctx_cap:
+        raise ValueError("context cap")
+    x = np.stack([np.asarray(weights["embed_row"](int(t)), np.float64) for t in tokens])
+    for layer, lw in enumerate(weights["layers"]):
+        tr = {} if traces is not None else None
+        x = prefill_layer(cfg, lw, x, slot, kv, layer, tr)
+        if traces is not None:
+            traces.append(tr)
+    xf = _round(rmsnorm(x[-1:], weights.get("final_norm"), cfg.eps))
+    logits = lm_head_logits(xf, weights["lm_head_bits"])[0]
+    kv.map.length[slot] += P
+    return logits, int(np.argmax(logits))

@@ -100,6 +100,36 @@ def slot_attention(q, K, V):
     return out
 
 
+def causal_block_attention(Q, K, V, start):
+    """Causal grouped-query attention of a block of P consecutive queries.
+
+    Q: [P][qh][d], the queries of positions start .. start+P-1; K, V:
+    [kvh][start+P][d], the slot's positions with the block's own keys
+    already in place.  Query row i may see positions 0..start+i: the score
+    matrix of each head is formed whole, entries j > start+i are set to -inf
+    before a row-wise softmax (max subtracted), and O = P V.  This is the
+    decode attention of ``slot_attention`` applied to every row of a prompt
+    at once ([KV-slot isolation, §1 Contribution]: a stream's K/V grows one
+    position per token, so row i's keys are those of its own prefix).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    P, qh, d = Q.shape
+    kvh, L, _ = K.shape
+    assert L == start + P and qh % kvh == 0
+    group = qh // kvh
+    visible = np.arange(L)[None, :] <= (start + np.arange(P))[:, None]   # [P][L]
+    out = np.empty((P, qh, d), dtype=np.float64)
+    for h in range(qh):
+        kv = h // group
+        S = (Q[:, h, :] @ K[kv].T) / math.sqrt(d)
+        S = np.where(visible, S, -np.inf)
+        E = np.exp(S - S.max(axis=1, keepdims=True))
+        out[:, h, :] = (E / E.sum(axis=1, keepdims=True)) @ V[kv]
+    return out
+
+
 def silu(x):
     """SiLU(x) = x / (1 + exp(-x))."""
     x = np.asarray(x, dtype=np.float64)

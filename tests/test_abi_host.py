@@ -78,6 +78,11 @@ def test_argument_checks_without_gpu():
         bm.moe_grouped_w4(w, 1, None, 1, None, None, 4, 1, need - 1)
     assert "workspace" in ei.value.message
     assert bm.last_error() != ""
+    # prompt ingestion checks its arguments before any device work
+    toks = (ctypes.c_int32 * 2)(1, 2)
+    nxt = (ctypes.c_int32 * 1)()
+    st = bm.lib().kv_slot_prefill(None, 0, 2, ctypes.addressof(toks), ctypes.addressof(nxt), None, None)
+    assert st == 1 and "kv_slot_prefill" in bm.last_error()
 
 
 def test_slot_map_lifecycle_and_errors():

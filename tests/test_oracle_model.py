@@ -71,6 +71,50 @@ def test_seeded_prefix_equals_decoded_prefix(model):
     np.testing.assert_array_equal(last_a, last_b)
 
 
+def test_prefill_equals_token_by_token_decode(model):
+    # Ingesting a prompt in one block (causal block attention over the slot)
+    # leaves the same K/V, length and last-position logits as feeding the
+    # prompt one decode step at a time: the definition a prompt has.
+    cfg, w = model
+    toks = [3, 99, 1024, 7, 3000, 42, 5, 4095, 17]
+    L0 = 17
+    kv_a = _kv(cfg)
+    sa = kv_a.seed(*_prefix(0, L0))
+    logits_a, nxt_a = oracle.model_prefill(cfg, w, kv_a, sa, toks)
+    kv_b = _kv(cfg)
+    sb = kv_b.seed(*_prefix(0, L0))
+    for t in toks:
+        logits_b, ids_b = oracle.model_step(cfg, w, kv_b, [sb], [t])
+    np.testing.assert_allclose(logits_a, logits_b[0], rtol=0, atol=1e-9)
+    assert nxt_a == int(ids_b[0])
+    assert kv_a.map.length[sa] == kv_b.map.length[sb] == L0 + len(toks)
+    for l in range(LAYERS):
+        np.testing.assert_allclose(kv_a.K[sa][l], kv_b.K[sb][l], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(kv_a.V[sa][l], kv_b.V[sb][l], rtol=0, atol=1e-12)
+    # the prefix seeded at join is untouched
+    K0, V0 = _prefix(0, L0)
+    np.testing.assert_array_equal(kv_a.K[sa][1][:, :L0], K0[1])
+
+
+def test_prefill_from_empty_slot_and_rejections(model):
+    cfg, w = model
+    kv = _kv(cfg)
+    empty = np.zeros((LAYERS, cfg.kv_heads, 0, cfg.head_dim))
+    s = kv.seed(empty, empty)
+    logits, nxt = oracle.model_prefill(cfg, w, kv, s, [11])
+    kv2 = _kv(cfg)
+    s2 = kv2.seed(empty, empty)
+    ref, ids = oracle.model_step(cfg, w, kv2, [s2], [11])
+    np.testing.assert_allclose(logits, ref[0], rtol=0, atol=1e-9)
+    with pytest.raises(ValueError):
+        oracle.model_prefill(cfg, w, kv, s, [])
+    with pytest.raises(ValueError):
+        oracle.model_prefill(cfg, w, kv, s, [1] * cfg.ctx_cap)     # 1 + cap > cap
+    kv.release(s)
+    with pytest.raises(ValueError):
+        oracle.model_prefill(cfg, w, kv, s, [1])
+
+
 def test_slot_map_lifecycle_errors():
     m = oracle.OracleSlotMap(2, 16)
     with pytest.raises(ValueError):

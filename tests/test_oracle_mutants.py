@@ -86,6 +86,36 @@ def _attn_gqa_modulo(q, K, V):
     return out
 
 
+def _causal_strict(Q, K, V, start):
+    # wrong mask: a row does not see its own position
+    Q, K, V = (np.asarray(a, np.float64) for a in (Q, K, V))
+    P, qh, d = Q.shape
+    L = K.shape[1]
+    vis = np.arange(L)[None, :] < (start + np.arange(P))[:, None]
+    out = np.zeros((P, qh, d))
+    for h in range(qh):
+        kv = h // (qh // K.shape[0])
+        S = np.where(vis, Q[:, h] @ K[kv].T / math.sqrt(d), -np.inf)
+        E = np.nan_to_num(np.exp(S - S.max(1, keepdims=True)))
+        out[:, h] = E / np.maximum(E.sum(1, keepdims=True), 1e-300) @ V[kv]
+    return out
+
+
+def _causal_no_offset(Q, K, V, start):
+    # wrong mask: row i sees positions 0..i, ignoring the prefix length
+    Q, K, V = (np.asarray(a, np.float64) for a in (Q, K, V))
+    P, qh, d = Q.shape
+    L = K.shape[1]
+    vis = np.arange(L)[None, :] <= np.arange(P)[:, None]
+    out = np.zeros((P, qh, d))
+    for h in range(qh):
+        kv = h // (qh // K.shape[0])
+        S = np.where(vis, Q[:, h] @ K[kv].T / math.sqrt(d), -np.inf)
+        E = np.exp(S - S.max(1, keepdims=True))
+        out[:, h] = E / E.sum(1, keepdims=True) @ V[kv]
+    return out
+
+
 def _route_ties_high(xn, Wr, k, renorm=True):
     logits = np.asarray(xn, np.float64) @ np.asarray(Wr, np.float64).T
     p = np.exp(logits - logits.max(1, keepdims=True))
@@ -140,6 +170,10 @@ MUTANTS = [
      [to.test_attention_hand_value, to.test_attention_brute_force_and_gqa_map]),
     ("gqa map", [(oracle, "slot_attention")], _attn_gqa_modulo,
      [to.test_attention_special_cases, to.test_attention_brute_force_and_gqa_map]),
+    ("causal mask strict", [(oracle, "causal_block_attention")], _causal_strict,
+     [to.test_causal_block_attention_brute_force_and_causality]),
+    ("causal mask offset", [(oracle, "causal_block_attention")], _causal_no_offset,
+     [to.test_causal_block_attention_brute_force_and_causality]),
     ("router ties", [(oracle, "route_topk")], _route_ties_high,
      [to.test_router_hand_values]),
     ("router renorm", [(oracle, "route_topk")], _route_no_renorm,

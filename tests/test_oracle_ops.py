@@ -160,6 +160,36 @@ def test_attention_brute_force_and_gqa_map():
     np.testing.assert_allclose(oracle.slot_attention(q, K[:, perm], V[:, perm]), out, rtol=1e-12)
 
 
+def test_causal_block_attention_brute_force_and_causality():
+    rng = np.random.default_rng(17)
+    qh, kvh, d, start, P = 8, 2, 16, 5, 4
+    Q = rng.standard_normal((P, qh, d))
+    K = rng.standard_normal((kvh, start + P, d))
+    V = rng.standard_normal((kvh, start + P, d))
+    out = oracle.causal_block_attention(Q, K, V, start)
+    for i in range(P):              # row i: softmax over positions 0..start+i only
+        n = start + i + 1
+        for h in range(qh):
+            kv = h // (qh // kvh)
+            s = [sum(Q[i][h][t] * K[kv][j][t] for t in range(d)) / math.sqrt(d) for j in range(n)]
+            m = max(s)
+            e = [math.exp(v - m) for v in s]
+            z = sum(e)
+            o = [sum(e[j] / z * V[kv][j][t] for j in range(n)) for t in range(d)]
+            np.testing.assert_allclose(out[i][h], o, rtol=1e-12)
+    # positions past start + 1 are invisible to rows 0 and 1, visible to rows 2 and 3
+    K2, V2 = K.copy(), V.copy()
+    K2[:, start + 2:] = rng.standard_normal((kvh, P - 2, d))
+    V2[:, start + 2:] = rng.standard_normal((kvh, P - 2, d))
+    out2 = oracle.causal_block_attention(Q, K2, V2, start)
+    np.testing.assert_array_equal(out2[:2], out[:2])
+    assert np.abs(out2[2:] - out[2:]).min() > 0
+    # an empty prefix and one query: the one visible position, o = V0
+    o1 = oracle.causal_block_attention(Q[:1], K[:, :1], V[:, :1], 0)
+    for h in range(qh):
+        np.testing.assert_array_equal(o1[0][h], V[h // 4, 0])
+
+
 # ---------------------------------------------------------------- routing
 
 def test_router_hand_values():

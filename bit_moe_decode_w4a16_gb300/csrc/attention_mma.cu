@@ -7,11 +7,15 @@
 // once, enumerates only the chunks that exist and walks them with a stride of
 // the grid, so no CTA is spent on positions past a stream's length.  For one
 // item the CTA:
+//   - issues all of the item's loads before any arithmetic: the chunk's V rows
+//     to shared memory (cp.async), the lane's K rows to registers, the
+//     rotation table entries, q and the new k / v;
 //   - rotates the kv group's G query heads (rotate-half, cos/sin of the
-//     position from the table) into shared memory as bf16, and on the chunk
-//     that holds the new position also rotates the new k and writes k and v
-//     to the arena at that position (before any of the chunk is read);
-//   - copies the chunk's V rows to shared memory asynchronously;
+//     position from the table) into shared memory as bf16; on the chunk that
+//     holds a decode row's new position it also rotates the new k, writes k
+//     and v to the arena at that position, and uses the rotated k (and v
+//     straight from the row) for that position instead of the arena, so the
+//     chunk never waits for its own append;
 //   - computes S = Q K^T with mma.sync m16n8k16 (bf16): the G heads on M
 //     (rows past G are zero), 8 positions per n-tile on N, the head dimension
 //     on K.  Inside each 32-wide block of d a lane takes the 8 consecutive
@@ -24,10 +28,12 @@
 //     operand, V through ldmatrix.trans and converted from bf16 exactly),
 //     warp w over its 32 positions, and adds the 4 warps' partials in warp
 //     order;
-//   - writes the chunk's record (o, m, l) and, if it is the last chunk of its
+//   - a stream of one chunk writes o / l directly; otherwise the CTA writes
+//     the chunk's record (o, m, l) and, if it is the last chunk of its
 //     (stream, kv head) to finish (arrival counter), merges all of that
 //     stream's chunks in ascending order: M = max m_c, den = sum l_c e^(m_c - M),
-//     out = (sum o_c e^(m_c - M)) / den, rounded to bf16 and stored as fp16.
+//     out = (sum o_c e^(m_c - M)) / den, rounded to bf16 and stored as fp16
+//     (with one chunk the weight is e^0 = 1 and both ways give the same bits).
 // A stream's result depends only on its own length and data.
 //
 // Prompt ingestion runs the same kernel over rows that all belong to one
@@ -88,12 +94,12 @@ struct AttnSmem {
     float ored[kWarpsA][8][D];         // per-warp partial O (after the V reads)
   } u;
   bf16 qs[8][D];                       // rotated q of the kv group
-  float cs[D];                         // cos | sin at the new position
+  bf16 knew[D];                        // rotated k of a decode row's new position
   float red_m[kWarpsA][8], red_l[kWarpsA][8];
   float stat_m[8], stat_l[8];
-  float mm[8][kMaxMergeChunks], ww[8][kMaxMergeChunks];   // merge: chunk maxima, then weights
+  float mm[8][kMaxMergeChunks], ll[8][kMaxMergeChunks], ww[8][kMaxMergeChunks];   // merge: m, l, weights
   float mden[8];
-  int slot[kMaxBatch], nc[kMaxBatch], pre[kMaxBatch + 1];
+  int slot[kMaxBatch], nc[kMaxBatch], pos[kMaxBatch], pre[kMaxBatch + 1];
   int last;
 };
 
@@ -101,28 +107,32 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
   __shared__ __align__(16) AttnSmem<D> sm;
   constexpr int kVS = AttnSmem<D>::kVS;
+  constexpr int kBlk = D / 32;
+  constexpr int kV8 = D / 8;
+  constexpr int kNT = D / 8;
   pdl_wait();
   const AttnArena& ar = a.ar;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int kvh = ar.kvh, G = a.qh / kvh, B = a.B, half = D / 2;
   const float scale = 1.0f / sqrtf((float)D);
 
-  // ---- slots, chunk counts and the item prefix (chunk-major within a stream)
+  // ---- slots, positions, chunk counts and the item prefix (chunk-major within a stream)
   for (int b = tid; b < B; b += blockDim.x) {
     const int slot = a.slots[b];
-    int nc = 0;
+    int nc = 0, pos = 0;
     if (slot < 0 || slot >= ar.S) {
       if (blockIdx.x == 0) a.chk.fail(1);
     } else {
-      const int L = row_position(a, b, slot) + 1;
-      if (L < 1 || L > ar.cap) {
+      pos = row_position(a, b, slot);
+      if (pos < 0 || pos + 1 > ar.cap) {
         if (blockIdx.x == 0) a.chk.fail(2);
       } else {
-        nc = (L + kAttnChunk - 1) / kAttnChunk;
+        nc = (pos + kAttnChunk) / kAttnChunk;
       }
     }
     sm.slot[b] = slot;
     sm.nc[b] = nc;
+    sm.pos[b] = pos;
   }
   __syncthreads();
   if (tid == 0) {
@@ -136,54 +146,76 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     int b = 0;
     while (sm.pre[b + 1] <= it) ++b;
     const int r = it - sm.pre[b], kh = r % kvh, c = r / kvh;
-    const int slot = sm.slot[b], nc = sm.nc[b];
-    const int pos = row_position(a, b, slot), L = pos + 1;
+    const int slot = sm.slot[b], nc = sm.nc[b], pos = sm.pos[b], L = pos + 1;
     const int j0 = c * kAttnChunk, n = min(kAttnChunk, L - j0);
     const bool last_chunk = c == nc - 1;
+    // on the chunk that holds a decode row's new position, k and v of that
+    // position come from this row's qkv (rotated here), not from the arena
+    const bool own_new = last_chunk && !a.prefill;
+    const int p_new = own_new ? pos - j0 : -1;
     const bf16* row = a.qkv + (size_t)b * a.ld_qkv;
+    const bf16* ksrc = row + (size_t)(a.qh + kh) * D;
+    const bf16* vsrc = row + (size_t)(a.qh + kvh + kh) * D;
     const size_t base = (size_t)a.layer * ar.layer_stride() + (size_t)slot * ar.slot_stride() + (size_t)kh * ar.cap * D;
     bf16* Kb = ar.K + base;
     bf16* Vb = ar.V + base;
 
-    // ---- RoPE of q (and of the new k, with the append, on the last chunk)
-    for (int i = tid; i < half; i += blockDim.x) {
-      const float2 v = a.rope[(size_t)pos * half + i];
-      sm.cs[i] = v.x;
-      sm.cs[half + i] = v.y;
+    // ---- every load of the item at once: V rows (async, to shared memory),
+    // the lane's K rows, the rotation table, q and the new k / v
+    for (int i = tid; i < kAttnChunk * kV8; i += blockDim.x) {
+      const int rr = i / kV8, v8 = i - rr * kV8;
+      if (rr == p_new) cp_async16(&sm.u.vs[rr][v8 * 8], vsrc + v8 * 8);
+      else if (rr < n) cp_async16(&sm.u.vs[rr][v8 * 8], Vb + (size_t)(j0 + rr) * D + v8 * 8);
+      else *reinterpret_cast<uint4*>(&sm.u.vs[rr][v8 * 8]) = make_uint4(0, 0, 0, 0);
     }
-    __syncthreads();
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    uint4 kb[4][kBlk];   // this lane's B column of n-tile nt: position 32w + 8nt + g
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int p = 32 * warp + 8 * nt + g;
+#pragma unroll
+      for (int blk = 0; blk < kBlk; ++blk)
+        kb[nt][blk] = p < n && p != p_new
+                          ? __ldcg(reinterpret_cast<const uint4*>(Kb + (size_t)(j0 + p) * D + 32 * blk + 8 * t))
+                          : make_uint4(0, 0, 0, 0);
+    }
+
+    // ---- RoPE of the kv group's q heads (and of the new k, with its append)
+    const float2* cs = a.rope + (size_t)pos * half;
     for (int idx = tid; idx < 8 * half; idx += blockDim.x) {
       const int h = idx / half, i = idx - h * half;
       bf16 y0 = f2bf(0.f), y1 = f2bf(0.f);
       if (h < G) {
         const bf16* src = row + (size_t)(kh * G + h) * D;
-        rope_pair(bf2f(src[i]), bf2f(src[i + half]), sm.cs[i], sm.cs[half + i], y0, y1);
+        const float2 v = cs[i];
+        rope_pair(bf2f(src[i]), bf2f(src[i + half]), v.x, v.y, y0, y1);
       }
       sm.qs[h][i] = y0;
       sm.qs[h][i + half] = y1;
     }
-    if (last_chunk && !a.prefill) {
-      const bf16* ksrc = row + (size_t)(a.qh + kh) * D;
-      const bf16* vsrc = row + (size_t)(a.qh + kvh + kh) * D;
-      for (int i = tid; i < half; i += blockDim.x)
-        rope_pair(bf2f(ksrc[i]), bf2f(ksrc[i + half]), sm.cs[i], sm.cs[half + i], Kb[(size_t)pos * D + i],
-                  Kb[(size_t)pos * D + i + half]);
+    if (own_new) {
+      for (int i = tid; i < half; i += blockDim.x) {
+        const float2 v = cs[i];
+        bf16 y0, y1;
+        rope_pair(bf2f(ksrc[i]), bf2f(ksrc[i + half]), v.x, v.y, y0, y1);
+        sm.knew[i] = y0;
+        sm.knew[i + half] = y1;
+        Kb[(size_t)pos * D + i] = y0;
+        Kb[(size_t)pos * D + i + half] = y1;
+      }
       for (int i = tid; i < D; i += blockDim.x) Vb[(size_t)pos * D + i] = vsrc[i];
-      __threadfence();
     }
     __syncthreads();
-
-    // ---- V rows -> shared memory (async); rows past n are zeroed (P is 0 there)
-    constexpr int kV8 = D / 8;
-    for (int i = tid; i < kAttnChunk * kV8; i += blockDim.x) {
-      const int rr = i / kV8, v8 = i - rr * kV8;
-      if (rr < n) cp_async16(&sm.u.vs[rr][v8 * 8], Vb + (size_t)(j0 + rr) * D + v8 * 8);
-      else *reinterpret_cast<uint4*>(&sm.u.vs[rr][v8 * 8]) = make_uint4(0, 0, 0, 0);
+    if (own_new) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+        if (32 * warp + 8 * nt + g == p_new) {
+#pragma unroll
+          for (int blk = 0; blk < kBlk; ++blk) kb[nt][blk] = *reinterpret_cast<const uint4*>(&sm.knew[32 * blk + 8 * t]);
+        }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
 
     // ---- scores: warp w takes positions [32w, 32w + 32): 4 n-tiles of 8
-    constexpr int kBlk = D / 32;
     uint32_t qa[kBlk][4];
 #pragma unroll
     for (int blk = 0; blk < kBlk; ++blk) {
@@ -195,18 +227,12 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) s[nt][q] = 0.f;
-      const int p = 32 * warp + 8 * nt + g;   // this lane's B column (a position of the chunk)
-      uint4 kb[kBlk];
-#pragma unroll
-      for (int blk = 0; blk < kBlk; ++blk)
-        kb[blk] = p < n ? __ldcg(reinterpret_cast<const uint4*>(Kb + (size_t)(j0 + p) * D + 32 * blk + 8 * t))
-                        : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int blk = 0; blk < kBlk; ++blk) {
         const uint32_t a0[4] = {qa[blk][0], 0u, qa[blk][1], 0u};
         const uint32_t a1[4] = {qa[blk][2], 0u, qa[blk][3], 0u};
-        mma::mma_bf16(s[nt], a0, kb[blk].x, kb[blk].y);
-        mma::mma_bf16(s[nt], a1, kb[blk].z, kb[blk].w);
+        mma::mma_bf16(s[nt], a0, kb[nt][blk].x, kb[nt][blk].y);
+        mma::mma_bf16(s[nt], a1, kb[nt][blk].z, kb[nt][blk].w);
       }
     }
     // s[nt][0..1] = S[head g][position 32w + 8nt + 2t (+1)]; rows g + 8 (c2, c3) are padding
@@ -251,7 +277,6 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     }
 
     // ---- O = P V over the warp's 32 positions (2 k-steps of 16)
-    constexpr int kNT = D / 8;
     float o[kNT][4];
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt)
@@ -280,6 +305,19 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     }
     __syncthreads();
 
+    if (nc == 1) {
+      // ---- one chunk: its record is the result (the merge of one chunk has
+      // weight exp(0) = 1, so o / l is the merge's value bit for bit)
+      for (int idx = tid; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx - h * D;
+        float v = 0.f;
+        for (int w = 0; w < kWarpsA; ++w) v += sm.u.ored[w][h][d];
+        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(v / sm.stat_l[h]));
+      }
+      __syncthreads();
+      continue;
+    }
+
     // ---- the chunk's record: o (warps added in order), m, l
     for (int idx = tid; idx < G * D; idx += blockDim.x) {
       const int h = idx / D, d = idx - h * D;
@@ -301,7 +339,9 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
       __threadfence();
       for (int idx = tid; idx < G * nc; idx += blockDim.x) {
         const int h = idx / nc, cc = idx - h * nc;
-        sm.mm[h][cc] = __ldcg(a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D) + D);
+        const float* rec = a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D);
+        sm.mm[h][cc] = __ldcg(rec + D);
+        sm.ll[h][cc] = __ldcg(rec + D + 1);
       }
       __syncthreads();
       if (tid < G) {
@@ -311,7 +351,7 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
         for (int cc = 0; cc < nc; ++cc) {
           const float w = expf(sm.mm[tid][cc] - M);
           sm.ww[tid][cc] = w;
-          den = fmaf(__ldcg(a.part + rec_index(b, kh * G + tid, cc, a.qh, a.max_chunks, D) + D + 1), w, den);
+          den = fmaf(sm.ll[tid][cc], w, den);
         }
         sm.mden[tid] = den;
       }

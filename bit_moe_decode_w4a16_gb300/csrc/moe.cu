@@ -31,18 +31,48 @@ constexpr int kRouterWarps = 8;
 constexpr int kMaxPairs = 1024;   // B * k handled by the single-CTA sort
 
 // Router logits.  Grid (ceil(E / kRouterExperts), B): a CTA takes one token
-// and kRouterExperts experts.  It normalises the token's row itself (every
-// CTA of the token computes the same bf16 values in the same order; the CTAs
-// of expert block 0 also write them out for the expert GEMMs), keeps the row
-// in shared memory as fp32, and each warp computes the dot products of its
-// experts with all of a router row's loads in flight.
-constexpr int kRouterExperts = kRouterWarps;   // one expert per warp
+// and kRouterExperts experts, two per warp.  Each warp issues the loads of
+// its first router row before anything else (the router weights do not
+// depend on the previous kernel, so they go out before the dependency wait),
+// then the CTA normalises the token's row itself (every CTA of the token
+// computes the same bf16 values in the same order; the CTAs of expert block 0
+// also write them out for the expert GEMMs) and keeps it in shared memory as
+// fp32.  A warp's dot product takes the row in 128-float strips, lane l
+// holding elements 4l..4l+3 of each strip, in a fixed order.
+constexpr int kRouterExperts = 2 * kRouterWarps;
+constexpr int kRouterStrips = 16;   // 16 x 128 = 2048 floats of a router row per pass
 
-// The router logits of one token and kRouterExperts experts (one CTA).
+__device__ __forceinline__ void router_load(const float* wr, int H, int k0, float4 (&w4)[kRouterStrips]) {
+#pragma unroll
+  for (int i = 0; i < kRouterStrips; ++i)
+    if (k0 + 128 * i < H) w4[i] = __ldg(reinterpret_cast<const float4*>(wr + k0 + 128 * i));
+}
+
+__device__ __forceinline__ float router_fma(const float* xs, int H, int k0, const float4 (&w4)[kRouterStrips],
+                                            float acc) {
+#pragma unroll
+  for (int i = 0; i < kRouterStrips; ++i) {
+    const int k = k0 + 128 * i;
+    if (k < H) {
+      const float4 x = *reinterpret_cast<const float4*>(xs + k);
+      acc = fmaf(x.x, w4[i].x, acc); acc = fmaf(x.y, w4[i].y, acc);
+      acc = fmaf(x.z, w4[i].z, acc); acc = fmaf(x.w, w4[i].w, acc);
+    }
+  }
+  return acc;
+}
+
+// The router logits of one token and kRouterExperts experts (one CTA); the
+// dependency wait of a programmatic launch is taken inside, after the
+// weight prefetch.
 __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, float* xs) {
   __shared__ float red[kRouterWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tkn = blockIdx.y, H = a.H;
+  float4 w4[kRouterStrips];
+  const int e_first = blockIdx.x * kRouterExperts + warp;
+  if (e_first < a.E) router_load(a.wr + (size_t)e_first * H, H, lane * 4, w4);
+  pdl_wait();
   const bf16* x = a.x + (size_t)tkn * H;
   float ss = 0.f;
   for (int k = threadIdx.x * 8; k < H; k += 256 * 8) {
@@ -80,20 +110,9 @@ __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, f
     if (e >= a.E) break;
     const float* wr = a.wr + (size_t)e * H;
     float acc = 0.f;
-    // up to 16 float4 per lane (the whole row for H <= 2048) in flight at once
-    for (int k0 = lane * 4; k0 < H; k0 += 16 * 128) {
-      float4 w4[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (k0 + 128 * i < H) w4[i] = *reinterpret_cast<const float4*>(wr + k0 + 128 * i);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int k = k0 + 128 * i;
-        if (k < H) {
-          acc = fmaf(xs[k], w4[i].x, acc); acc = fmaf(xs[k + 1], w4[i].y, acc);
-          acc = fmaf(xs[k + 2], w4[i].z, acc); acc = fmaf(xs[k + 3], w4[i].w, acc);
-        }
-      }
+    for (int k0 = lane * 4; k0 < H; k0 += kRouterStrips * 128) {
+      if (ei != warp || k0 != lane * 4) router_load(wr, H, k0, w4);
+      acc = router_fma(xs, H, k0, w4, acc);
     }
     acc = warp_sum(acc);
     if (lane == 0) b.logits[(size_t)tkn * a.E + e] = acc;
@@ -101,7 +120,7 @@ __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, f
 }
 
 __global__ void __launch_bounds__(256) k_router(MoeArgs a, MoeBufs b) {
-  extern __shared__ float xs[];        // [H] normalised row
+  extern __shared__ __align__(16) float xs[];   // [H] normalised row
   router_cta(a, b, xs);
 }
 
@@ -168,16 +187,32 @@ __device__ __forceinline__ void topk_warp(const MoeArgs& a, const MoeBufs& b, in
 
 // Stable counting sort of the P = B k (token, rank) pairs by expert, the
 // list of active experts and the job list, by the whole CTA from ids_s
-// (shared memory, pair p = b k + r).  Every reduction has a fixed order.
+// (shared memory, pair p = b k + r).  Warp 0 walks the pairs 32 at a time in
+// order: lanes holding the same expert find each other (match), a pair's
+// rank among its expert's pairs is the expert's running count plus the
+// same-expert lanes below it, and the group's lowest lane adds the group to
+// the running count.  Then exclusive scans over the experts give the
+// offsets.  Every result is a count, so it does not depend on timing.
 __device__ __forceinline__ void group_pairs(const MoeArgs& a, const MoeBufs& b, const int* ids_s, int* cnt_s,
-                                            int* off_s) {
+                                            int* off_s, int* rank_s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, P = a.B * a.k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int p = 0; p < P; ++p) c += (ids_s[p] == e);
-    cnt_s[e] = c;
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + lane;
+      const int e = p < P ? ids_s[p] : -1 - lane;   // past the end: a value no other lane holds
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int before = p < P ? cnt_s[e] : 0;
+      __syncwarp();   // every lane has read its expert's count before any is updated
+      if (p < P) {
+        rank_s[p] = before + __popc(same & lt);
+        if ((same & lt) == 0u) cnt_s[e] = before + __popc(same);
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
   // warp 0: exclusive scans over the experts (ascending id) of the pair
@@ -221,10 +256,7 @@ __device__ __forceinline__ void group_pairs(const MoeArgs& a, const MoeBufs& b, 
   }
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int e = ids_s[p];
-    int rank = 0;
-    for (int q = 0; q < p; ++q) rank += (ids_s[q] == e);
-    const int pos = off_s[e] + rank;
+    const int pos = off_s[ids_s[p]] + rank_s[p];
     b.pair_token[pos] = p / k;
     b.pos_of[p] = pos;
   }
@@ -232,11 +264,13 @@ __device__ __forceinline__ void group_pairs(const MoeArgs& a, const MoeBufs& b, 
 
 __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
   __shared__ int ids_s[kMaxPairs];
+  __shared__ int rank_s[kMaxPairs];
   __shared__ int cnt_s[256];
   __shared__ int off_s[257];
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int t = warp; t < a.B; t += nwarps) topk_warp(a, b, t, false, ids_s);
-  group_pairs(a, b, ids_s, cnt_s, off_s);
+  __syncthreads();
+  group_pairs(a, b, ids_s, cnt_s, off_s, rank_s);
 }
 
 // Router, top-k and grouping in one launch.  Every CTA computes its
@@ -248,14 +282,14 @@ __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
 // left zero.  The result is the same as k_router + k_topk_sort.
 __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsigned int* tok_cnt,
                                                      unsigned int* all_cnt) {
-  extern __shared__ float xs[];        // [H] normalised row
+  extern __shared__ __align__(16) float xs[];   // [H] normalised row
   __shared__ int ids_s[kMaxPairs];
+  __shared__ int rank_s[kMaxPairs];
   __shared__ int cnt_s[256];
   __shared__ int off_s[257];
   __shared__ int flag_s;
-  pdl_wait();
   const int tkn = blockIdx.y, warp = threadIdx.x >> 5;
-  router_cta(a, b, xs);
+  router_cta(a, b, xs);   // takes the dependency wait after its weight prefetch
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) flag_s = atomicAdd(&tok_cnt[tkn], 1u) == gridDim.x - 1;
@@ -272,7 +306,8 @@ __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsig
   __threadfence();
   const int P = a.B * a.k;
   for (int p = threadIdx.x; p < P; p += blockDim.x) ids_s[p] = __ldcg(b.topk_ids + p);
-  group_pairs(a, b, ids_s, cnt_s, off_s);
+  __syncthreads();
+  group_pairs(a, b, ids_s, cnt_s, off_s, rank_s);
   if (threadIdx.x == 0) *all_cnt = 0u;
 }
 

@@ -91,12 +91,13 @@ __device__ __forceinline__ uint32_t ord_key(float v) {
 constexpr int kLmWarps = 8;
 
 // A warp owns RT 16-row tiles of W and the whole K, walking it in chunks of
-// 64 with the next chunk's loads in flight; the same K permutation as the
+// 64 with the next chunk's weight loads in flight (two CTAs per SM for the
+// wider variants, so enough weight bytes are in flight per SM); the same K permutation as the
 // int4 layout lets each lane's A and B fragments of a 32-wide block be 16
 // consecutive bytes of a row, so W is read in its plain row-major form.
 // Each logit is one fp32 sum over K in a fixed order.
 template <int NT, int RT>
-__global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
+__global__ void __launch_bounds__(kLmWarps * 32, NT * RT >= 2 ? 2 : 1) k_lm_mma(LmArgs a) {
   __shared__ unsigned long long best_s[kLmWarps][32];
   __shared__ int last_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,21 +129,25 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
       const int tk = nt * 8 + g;
       xr[nt] = tk < ntok ? a.X + (size_t)(tok0 + tk) * K + 8 * t : nullptr;
     }
-    uint4 wa[RT][2][2], wb[RT][2][2], xa[NT][2], xb[NT][2];
-    auto load = [&](uint4 (&w)[RT][2][2], uint4 (&x)[NT][2], int c) {
+    // weights: two chunks in flight per warp; activations (the same rows for
+    // every warp of the CTA, so mostly L1 hits) are loaded right before use
+    uint4 wa[RT][2][2], wb[RT][2][2], xf[NT][2];
+    auto loadw = [&](uint4 (&w)[RT][2][2], int c) {
 #pragma unroll
       for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int b = 0; b < 2; ++b) w[rt][h][b] = ldg_nc_v4(wr[rt][h] + c * kChunkK + 32 * b);
+    };
+    auto loadx = [&](int c) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int b = 0; b < 2; ++b)
-          x[nt][b] = xr[nt] ? *reinterpret_cast<const uint4*>(xr[nt] + c * kChunkK + 32 * b) : make_uint4(0, 0, 0, 0);
+          xf[nt][b] = xr[nt] ? *reinterpret_cast<const uint4*>(xr[nt] + c * kChunkK + 32 * b) : make_uint4(0, 0, 0, 0);
     };
-    auto compute = [&](const uint4 (&w)[RT][2][2], const uint4 (&x)[NT][2]) {
+    auto compute = [&](const uint4 (&w)[RT][2][2]) {
 #pragma unroll
       for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
@@ -153,29 +158,22 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lm_mma(LmArgs a) {
                                   hi ? w[rt][0][b].w : w[rt][0][b].y, hi ? w[rt][1][b].w : w[rt][1][b].y};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma_bf16(acc[rt][nt], af, hi ? x[nt][b].z : x[nt][b].x, hi ? x[nt][b].w : x[nt][b].y);
+            mma_bf16(acc[rt][nt], af, hi ? xf[nt][b].z : xf[nt][b].x, hi ? xf[nt][b].w : xf[nt][b].y);
         }
     };
-    // the first chunk's weights do not depend on the previous kernel
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int b = 0; b < 2; ++b) wa[rt][h][b] = ldg_nc_v4(wr[rt][h] + 32 * b);
+    // the first two chunks' weights do not depend on the previous kernel
+    loadw(wa, 0);
+    if (NC > 1) loadw(wb, 1);
     pdl_wait();
     waited = true;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-        xa[nt][b] = xr[nt] ? *reinterpret_cast<const uint4*>(xr[nt] + 32 * b) : make_uint4(0, 0, 0, 0);
     for (int c = 0; c < NC; c += 2) {
-      if (c + 1 < NC) load(wb, xb, c + 1);
-      compute(wa, xa);
+      loadx(c);
+      compute(wa);
+      if (c + 2 < NC) loadw(wa, c + 2);
       if (c + 1 < NC) {
-        if (c + 2 < NC) load(wa, xa, c + 2);
-        compute(wb, xb);
+        loadx(c + 1);
+        compute(wb);
+        if (c + 3 < NC) loadw(wb, c + 3);
       }
     }
     // logits: acc[rt][nt][c] is row row0 + 16 rt + g (+8 for c >= 2), token nt * 8 + 2t + (c & 1)

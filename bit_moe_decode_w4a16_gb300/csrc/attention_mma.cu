@@ -23,10 +23,10 @@
 //     reduction on both operands), so K rows are read straight from memory
 //     as 16-byte loads;
 //   - takes the chunk's softmax statistics (max m, sum l of exp(s - m)) per
-//     head over its 4 warps in a fixed order;
+//     head over its 8 warps in a fixed order;
 //   - computes O = P V in fp16 (P reused from the score registers as the A
 //     operand, V through ldmatrix.trans and converted from bf16 exactly),
-//     warp w over its 32 positions, and adds the 4 warps' partials in warp
+//     warp w over its 16 positions, and adds the 8 warps' partials in warp
 //     order;
 //   - a stream of one chunk writes o / l directly; otherwise the CTA writes
 //     the chunk's record (o, m, l) and, if it is the last chunk of its
@@ -51,7 +51,7 @@ namespace bm {
 
 namespace {
 
-constexpr int kWarpsA = 4;
+constexpr int kWarpsA = 8;   // a warp takes 16 of a chunk's 128 positions
 constexpr int kMaxBatch = 64;
 
 __device__ __forceinline__ size_t rec_index(int b, int h, int c, int qh, int max_chunks, int d) {
@@ -104,7 +104,7 @@ struct AttnSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
+__global__ void __launch_bounds__(kWarpsA * 32, 3) k_attn_fused(AttnFusedArgs a) {
   __shared__ __align__(16) AttnSmem<D> sm;
   constexpr int kVS = AttnSmem<D>::kVS;
   constexpr int kBlk = D / 32;
@@ -169,10 +169,10 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
       else *reinterpret_cast<uint4*>(&sm.u.vs[rr][v8 * 8]) = make_uint4(0, 0, 0, 0);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    uint4 kb[4][kBlk];   // this lane's B column of n-tile nt: position 32w + 8nt + g
+    uint4 kb[2][kBlk];   // this lane's B column of n-tile nt: position 16w + 8nt + g
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int p = 32 * warp + 8 * nt + g;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int p = 16 * warp + 8 * nt + g;
 #pragma unroll
       for (int blk = 0; blk < kBlk; ++blk)
         kb[nt][blk] = p < n && p != p_new
@@ -208,23 +208,23 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     __syncthreads();
     if (own_new) {
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-        if (32 * warp + 8 * nt + g == p_new) {
+      for (int nt = 0; nt < 2; ++nt)
+        if (16 * warp + 8 * nt + g == p_new) {
 #pragma unroll
           for (int blk = 0; blk < kBlk; ++blk) kb[nt][blk] = *reinterpret_cast<const uint4*>(&sm.knew[32 * blk + 8 * t]);
         }
     }
 
-    // ---- scores: warp w takes positions [32w, 32w + 32): 4 n-tiles of 8
+    // ---- scores: warp w takes positions [16w, 16w + 16): 2 n-tiles of 8
     uint32_t qa[kBlk][4];
 #pragma unroll
     for (int blk = 0; blk < kBlk; ++blk) {
       const uint4 q4 = *reinterpret_cast<const uint4*>(&sm.qs[g][32 * blk + 8 * t]);
       qa[blk][0] = q4.x; qa[blk][1] = q4.y; qa[blk][2] = q4.z; qa[blk][3] = q4.w;
     }
-    float s[4][4];
+    float s[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) s[nt][q] = 0.f;
 #pragma unroll
@@ -235,13 +235,13 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
         mma::mma_bf16(s[nt], a1, kb[nt][blk].z, kb[nt][blk].w);
       }
     }
-    // s[nt][0..1] = S[head g][position 32w + 8nt + 2t (+1)]; rows g + 8 (c2, c3) are padding
+    // s[nt][0..1] = S[head g][position 16w + 8nt + 2t (+1)]; rows g + 8 (c2, c3) are padding
     float mx = -FLT_MAX;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int p = 32 * warp + 8 * nt + 2 * t + j;
+        const int p = 16 * warp + 8 * nt + 2 * t + j;
         s[nt][j] = p < n ? s[nt][j] * scale : -FLT_MAX;
         mx = fmaxf(mx, s[nt][j]);
       }
@@ -258,10 +258,10 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
     const float mrow = sm.stat_m[g];
     float ls = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int p = 32 * warp + 8 * nt + 2 * t + j;
+        const int p = 16 * warp + 8 * nt + 2 * t + j;
         s[nt][j] = p < n ? expf(s[nt][j] - mrow) : 0.f;
         ls += s[nt][j];
       }
@@ -276,17 +276,15 @@ __global__ void __launch_bounds__(kWarpsA * 32) k_attn_fused(AttnFusedArgs a) {
       sm.stat_l[tid] = l;
     }
 
-    // ---- O = P V over the warp's 32 positions (2 k-steps of 16)
+    // ---- O = P V over the warp's 16 positions (one k-step)
     float o[kNT][4];
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
       for (int q = 0; q < 4; ++q) o[nt][q] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t pa[4] = {pack_f16(s[2 * kk][0], s[2 * kk][1]), 0u, pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                              0u};
-      const int vrow = 32 * warp + 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+    {
+      const uint32_t pa[4] = {pack_f16(s[0][0], s[0][1]), 0u, pack_f16(s[1][0], s[1][1]), 0u};
+      const int vrow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int dt = 0; dt < kNT / 2; ++dt) {
         uint32_t vb[4];
@@ -411,7 +409,7 @@ cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 132;
   const long items = (long)a.B * a.ar.kvh * a.max_chunks;
-  const long cap = (long)sms * 4;
+  const long cap = (long)sms * 3;   // resident CTAs per SM
   const dim3 grid((unsigned)(items < cap ? items : cap));
   if (a.ar.d == 128) return launch_k(pdl, k_attn_fused<128>, grid, dim3(kWarpsA * 32), 0, st, a);
   return launch_k(pdl, k_attn_fused<64>, grid, dim3(kWarpsA * 32), 0, st, a);

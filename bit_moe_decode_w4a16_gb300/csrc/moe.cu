@@ -152,6 +152,9 @@ __device__ __forceinline__ void topk_warp(const MoeArgs& a, const MoeBufs& b, in
   float sel_v[16];
   int sel_e[16];
   for (int r = 0; r < k; ++r) {
+    // the lane's best untaken (value, lowest id), then the warp's: the
+    // largest order key of the value, and among the lanes holding it the
+    // lowest id (-0 and +0 share a key, so they tie, as under ==)
     float bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
@@ -159,12 +162,11 @@ __device__ __forceinline__ void topk_warp(const MoeArgs& a, const MoeBufs& b, in
       const int e = lane + 32 * i;
       if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-    }
+    const uint32_t u = __float_as_uint(bv == 0.f ? 0.f : bv);
+    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    be = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)be : 0x7fffffffu);
+    bv = __shfl_sync(0xffffffffu, bv, be & 31);
     sel_v[r] = bv;
     sel_e[r] = be;   // k <= E, so an untaken id always exists
     if ((be & 31) == lane) {
@@ -222,13 +224,16 @@ __device__ __forceinline__ void group_pairs(const MoeArgs& a, const MoeBufs& b, 
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
       const int c = e < E ? cnt_s[e] : 0, act = c > 0, nj = (c + kJobTokens - 1) / kJobTokens;
-      int ic = c, ia = act, ij = nj;
+      // one inclusive scan of the three counts packed in a word: over 32
+      // experts the pair count stays below 2^11, the active count below
+      // 2^6 and the job count below 2^8, so the fields never carry
+      uint32_t packed = (uint32_t)c | ((uint32_t)act << 11) | ((uint32_t)nj << 17);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int c2 = __shfl_up_sync(0xffffffffu, ic, o), a2 = __shfl_up_sync(0xffffffffu, ia, o),
-                  j2 = __shfl_up_sync(0xffffffffu, ij, o);
-        if (lane >= o) { ic += c2; ia += a2; ij += j2; }
+        const uint32_t p2 = __shfl_up_sync(0xffffffffu, packed, o);
+        if (lane >= o) packed += p2;
       }
+      const int ic = (int)(packed & 0x7FFu), ia = (int)((packed >> 11) & 0x3Fu), ij = (int)(packed >> 17);
       if (e < E) {
         const int off = run_off + ic - c, u = run_u + ia - act, j0 = run_j + ij - nj;
         off_s[e] = off;

@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--max-streams", type=int, default=0,
-                    help="slots of the engine's KV arena (default: the workload's 32, or --batch if larger; at most 64)")
+                    help="slots of the engine's KV arena (default: the workload's 32, or --batch if larger; at most 128)")
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--sweep", default="1,2,4,8,16,32", help="B values for the sweep ('' to skip)")
     ap.add_argument("--sweep-steps", type=int, default=10)

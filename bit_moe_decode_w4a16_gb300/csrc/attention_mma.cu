@@ -52,7 +52,7 @@ namespace bm {
 namespace {
 
 constexpr int kWarpsA = 8;   // a warp takes 16 of a chunk's 128 positions
-constexpr int kMaxBatch = 64;
+constexpr int kMaxBatch = 128;
 
 __device__ __forceinline__ size_t rec_index(int b, int h, int c, int qh, int max_chunks, int d) {
   return (((size_t)b * qh + h) * max_chunks + c) * (size_t)(d + 2);

@@ -456,7 +456,9 @@ bm_status check_config(const bm_config& c) {
   if (c.hidden % c.group || c.ffn % c.group || (c.q_heads * c.head_dim) % c.group)
     return bad("every reduction length must be a multiple of group");
   if (c.vocab < 1 || c.layers < 1) return bad("vocab and layers must be >= 1");
-  if (c.max_streams < 1 || c.max_streams > 64) return bad("max_streams must be in [1, 64]");
+  if (c.max_streams < 1 || c.max_streams > 128) return bad("max_streams must be in [1, 128]");
+  if (c.max_streams > 64 && !(c.kernel_policy == BM_POLICY_MMA || (c.kernel_policy == BM_POLICY_AUTO && mma_shapes_ok(c))))
+    return bad("max_streams above 64 needs the warp-MMA kernel family");
   if (c.max_streams * c.top_k > 1024) return bad("max_streams * top_k must be <= 1024");
   if (c.ctx_cap < 1 || c.ctx_cap > 131072) return bad("ctx_cap must be in [1, 131072]");
   if (!(c.rope_base > 0.f) || !(c.rms_eps >= 0.f)) return bad("rope_base > 0 and rms_eps >= 0 required");

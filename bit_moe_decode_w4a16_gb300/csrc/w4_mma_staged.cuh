@@ -43,8 +43,8 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                "l"(src), "r"(bytes), "r"(mbar)
                : "memory");
 }
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+__device__ __forceinline__ void consumer_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 struct StagedGeom {
@@ -146,12 +146,19 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
   // of tiles 2 rtp and 2 rtp + 1 of the item
   const int ks = warp % KS, rtp = warp / KS;
   const int c0 = ks * CPW;
-  const int nthreads = NW * 32;
+  // consumer groups: the row pairs rtp = grp, grp + NGRP, ... share a named
+  // barrier and their own epilogue, so the groups' compute and epilogue
+  // phases drift apart instead of running in lockstep
+  const int NGRP = RTP < 8 ? RTP : 8;
+  const int grp = rtp % NGRP, per_grp = RTP / NGRP;
+  const int gthreads = per_grp * KS * 32;
+  const int gtid = ((rtp / NGRP) * KS + ks) * 32 + lane;
+  const int bar_id = 1 + grp;
   int n = 0;
   for (; n < count; ++n) {
     const int s = n % geo.ns;
     if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), (n / geo.ns) & 1, kStagedWaitLimit)) abort_s = 1;
-    consumer_sync(nthreads);
+    consumer_sync(bar_id, gthreads);
     if (abort_s) break;
     const int tok0 = info_s[s].tok0, ntok = info_s[s].ntok, rb = info_s[s].rb;
     const unsigned char* st = smem + (size_t)s * geo.stage;
@@ -221,12 +228,12 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) red[((((ks * RTP + rtp) * 2 + rt) * 4 + c) * 32) + lane] = acc[rt][c];
-    consumer_sync(nthreads);   // the partials are in
+    consumer_sync(bar_id, gthreads);   // the group's partials are in
 
-    // epilogue: unit (rp, rt, j, lane) -> rows (g, g + 8), token 2t + j;
-    // partials in ks order
-    for (int uix = threadIdx.x; uix < RTP * 128; uix += nthreads) {
-      const int l = uix & 31, jj = (uix >> 5) & 1, rt = (uix >> 6) & 1, rp = uix >> 7;
+    // epilogue of the group's row pairs: unit (rp, rt, j, lane) -> rows
+    // (g, g + 8), token 2t + j; partials in ks order
+    for (int uix = gtid; uix < per_grp * 128; uix += gthreads) {
+      const int l = uix & 31, jj = (uix >> 5) & 1, rt = (uix >> 6) & 1, rp = grp + NGRP * (uix >> 7);
       const int token = 2 * (l & 3) + jj;
       if (token >= ntok) continue;
       float v0 = 0.f, v1 = 0.f;
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
         a.out[m * a.H + r0 + 8] = v1;
       }
     }
-    consumer_sync(nthreads);   // the partials are read before the next item overwrites them
+    consumer_sync(bar_id, gthreads);   // the partials are read before the next item overwrites them
   }
   if (abort_s) {
     if (threadIdx.x == 0 && a.err) atomicExch(a.err, 5);

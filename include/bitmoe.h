@@ -86,7 +86,7 @@ typedef struct bm_config {
   int layers;        /* decoder layers                                        */
   float rope_base;   /* RoPE base (rotate-half pairing)                       */
   float rms_eps;     /* RMSNorm epsilon                                       */
-  int max_streams;   /* slots in the KV arena (<= 64)                         */
+  int max_streams;   /* slots in the KV arena (<= 64; <= 128 on the MMA family) */
   int ctx_cap;       /* positions per slot                                    */
   int renorm_topk;   /* 1: top-k weights renormalised to sum to one           */
   int kernel_policy; /* bm_kernel_policy                                      */

@@ -61,6 +61,15 @@ def test_argument_checks_without_gpu():
     cfg.update(group=32, top_k=9)
     with pytest.raises(bm.BitMoeError):
         bm.bm_engine_create(cfg)
+    cfg.update(top_k=2, max_streams=129)
+    with pytest.raises(bm.BitMoeError) as ei:
+        bm.bm_engine_create(cfg)
+    assert ei.value.status == 1 and "max_streams" in ei.value.message
+    cfg.update(max_streams=100, kernel_policy=1)      # above 64 only on the warp-MMA family
+    with pytest.raises(bm.BitMoeError) as ei:
+        bm.bm_engine_create(cfg)
+    assert ei.value.status == 1 and "warp-MMA" in ei.value.message
+    cfg.update(max_streams=2, kernel_policy=0)
     # the dense op rejects bad shapes before touching the device
     for (M, N, K, g) in [(0, 8, 64, 32), (1, 8, 48, 32), (1, 8, 64, 48), (1, 0, 64, 32)]:
         with pytest.raises(bm.BitMoeError) as ei:

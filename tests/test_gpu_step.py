@@ -278,3 +278,34 @@ def test_long_context_step(bm, policy):
             bm.kv_slot_release(e, s)
     finally:
         bm.bm_engine_destroy(e)
+
+
+def test_wide_batch_128_streams(bm):
+    # 128 streams in one step (the warp-MMA family's widest arena): sampled
+    # rows against the oracle and against the same streams stepped alone.
+    layers, S, cap = 2, 128, 64
+    lens = [int(x) for x in synth.randint(1, cap - 1, (S,), synth.seed_of(NAME, "wide_lens"), "cpu")]
+    toks = [int(t) for t in synth.tokens(NAME, "wide", S, CFG["vocab"])]
+    e = build_engine(NAME, CFG, layers, max_streams=S, ctx_cap=cap, policy=MMA, gen_device="cpu")
+    try:
+        assert bm.bm_engine_kernel_family(e) == MMA
+        slots = [seed_stream(e, NAME, CFG, i, L, layers, gen_device="cpu") for i, L in enumerate(lens)]
+        nxt, logits = _step(bm, e, slots, toks, CFG["vocab"])
+        sample = [0, 1, 37, 64, 100, 127]
+        ocfg = oracle_config(CFG, layers=layers, max_streams=len(sample), ctx_cap=cap)
+        ow = oracle_weights(NAME, CFG, layers)
+        kv = _oracle_kv(ocfg, layers)
+        oslots = [kv.seed(*_prefix_np(i, lens[i], layers)) for i in sample]
+        ref, _ = oracle.model_step(ocfg, ow, kv, oslots, [toks[i] for i in sample])
+        err, _ = assert_close_rows(logits[sample], ref, max_abs=logit_bound(layers), what="128-stream step",
+                                   bf16_out=False)
+        check_greedy(nxt[sample], ref, err)
+        for i in sample:
+            bm.kv_slot_release(e, slots[i])
+        for i in sample:
+            s = seed_stream(e, NAME, CFG, i, lens[i], layers, gen_device="cpu")
+            n1, l1 = _step(bm, e, [s], [toks[i]], CFG["vocab"])
+            assert torch.equal(l1[0], logits[i]) and n1[0] == nxt[i], f"stream {i}: solo bytes differ"
+            bm.kv_slot_release(e, s)
+    finally:
+        bm.bm_engine_destroy(e)

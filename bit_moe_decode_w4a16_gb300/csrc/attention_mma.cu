@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kWarpsA * 32, 3) k_attn_fused(AttnFusedArgs a)
   constexpr int kV8 = D / 8;
   constexpr int kNT = D / 8;
   pdl_wait();
+  pdl_trigger();   // the grid is at most one wave: the output projection may start its weight loads
   const AttnArena& ar = a.ar;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int kvh = ar.kvh, G = a.qh / kvh, B = a.B, half = D / 2;

@@ -29,7 +29,10 @@ struct DevCheck {
 // writes, and pdl_trigger() to let the next kernel start early.  Both are
 // no-ops when the kernel was launched the ordinary way.  Every kernel of a
 // PDL chain calls pdl_wait() before it writes memory or exits, so the chain
-// stays ordered end to end.
+// stays ordered end to end.  Only kernels whose whole grid is resident at
+// once trigger, right after their own wait: their dependents' CTAs then fill
+// the free slots and run their weight loads (which no kernel writes) before
+// their own wait, without holding slots the triggering grid still needs.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256) k_embed_norm(const bf16* table, int V, in
                                                     const bf16* nw, float eps, __half* xn, DevCheck chk) {
   __shared__ float red[32];
   pdl_wait();
+  pdl_trigger();   // one wave: the next projection may start its weight loads
   const int b = blockIdx.x;
   int tok = tokens[b];
   if (tok < 0 || tok >= V) {

@@ -431,6 +431,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
   __shared__ int pos_s[16];
   __shared__ float ys[kCombineMaxH];
   pdl_wait();
+  pdl_trigger();   // one wave (a CTA per token): the next projection may start its weight loads
   const int t = blockIdx.x, H = a.H;
   if (threadIdx.x < a.k) {
     w_s[threadIdx.x] = b.topk_w[t * a.k + threadIdx.x];

@@ -167,7 +167,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
       }
 
   // dense: the weights above do not depend on the previous kernel
-  if (MODE == DENSE) pdl_wait();
+  if (MODE == DENSE) {
+    pdl_wait();
+    // one token group is one wave (at most two CTAs per SM): the next kernel
+    // may start its own weight loads; wider launches keep their slots
+    if (gridDim.y == 1) pdl_trigger();
+  }
 
   // ---- activation rows of the lane's B-fragment column (token g of each n-tile)
   const bf16* xr[NT];

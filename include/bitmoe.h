@@ -367,7 +367,9 @@ bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* 
  * Errors: BM_ERR_INVALID_ARG (NULL, n_tokens < 1, slot out of range),
  * BM_ERR_SLOT_FREE, BM_ERR_CTX_CAP (len + n_tokens > ctx_cap; nothing is
  * written), BM_ERR_NOT_READY, BM_ERR_UNSUPPORTED (an engine not on the
- * warp-MMA kernel family), BM_ERR_CUDA. */
+ * warp-MMA kernel family), BM_ERR_CUDA.  The argument errors leave the slot
+ * untouched; after BM_ERR_CUDA the slot's contents and length are undefined
+ * and the caller releases it. */
 bm_status kv_slot_prefill(bm_engine* e, int slot, int n_tokens, const int32_t* tokens,
                           int32_t* next_token, float* logits, void* stream);
 

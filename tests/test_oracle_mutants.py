@@ -198,3 +198,57 @@ def test_pins_catch_mutant(monkeypatch, name, targets, mutant, pins):
         except AssertionError:
             failed += 1
     assert failed >= 1, f"no pin caught the planted mistake: {name}"
+
+
+# ---------------------------------------------------------------- prompt ingestion (model level)
+
+def _prefill_layer_positions_from_zero(cfg, lw, x, slot, kv, layer, trace=None):
+    # wrong: the prompt's rows are rotated at 0..P-1, ignoring the slot's prefix
+    import oracle.model as om
+    H, qh, kvh, d, g = cfg.hidden, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.group
+    x = np.asarray(x, dtype=np.float64)
+    P = x.shape[0]
+    start = kv.map.length[slot]
+    xn = om._round(om.rmsnorm(x, lw.get("attn_norm"), cfg.eps))
+    qkv = om._round(om.rowwise(om.dequant_w4(lw["wqkv"][0], lw["wqkv"][1], H, g), xn))
+    q = qkv[:, : qh * d].reshape(P, qh, d)
+    k = qkv[:, qh * d: (qh + kvh) * d].reshape(P, kvh, d)
+    v = qkv[:, (qh + kvh) * d:].reshape(P, kvh, d)
+    pos = np.arange(P)
+    q_rot = om._round(om.rope_rotate_half(q, pos, cfg.rope_base))
+    k_rot = om._round(om.rope_rotate_half(k, pos, cfg.rope_base))
+    kv.write_block(layer, slot, k_rot, v)
+    Kc, Vc = kv.view(layer, slot, start + P)
+    o = om._round(om.causal_block_attention(q_rot, Kc, Vc, start)).reshape(P, qh * d)
+    return om._after_attention(cfg, lw, x, o, trace)
+
+
+def _block_attention_unmasked(Q, K, V, start):
+    # wrong: every row of the prompt sees the whole block (no causal mask)
+    Q, K, V = (np.asarray(a, np.float64) for a in (Q, K, V))
+    P, qh, d = Q.shape
+    out = np.empty((P, qh, d))
+    for h in range(qh):
+        kv = h // (qh // K.shape[0])
+        S = Q[:, h] @ K[kv].T / math.sqrt(d)
+        E = np.exp(S - S.max(1, keepdims=True))
+        out[:, h] = E / E.sum(1, keepdims=True) @ V[kv]
+    return out
+
+
+PREFILL_MUTANTS = [
+    ("prompt positions from zero", "prefill_layer", _prefill_layer_positions_from_zero),
+    ("prompt attention unmasked", "causal_block_attention", _block_attention_unmasked),
+]
+
+
+@pytest.mark.parametrize("name,attr,mutant", PREFILL_MUTANTS, ids=[m[0] for m in PREFILL_MUTANTS])
+def test_decode_equivalence_catches_prefill_mutant(monkeypatch, name, attr, mutant):
+    import oracle.model as om
+    import test_oracle_model as tmod
+    cfg = tmod.oracle_config(tmod.CFG, layers=tmod.LAYERS, max_streams=6, ctx_cap=128)
+    w = tmod.oracle_weights(tmod.NAME, tmod.CFG, tmod.LAYERS)
+    tmod.test_prefill_equals_token_by_token_decode((cfg, w))   # the pin holds on the oracle as written
+    monkeypatch.setattr(om, attr, mutant)
+    with pytest.raises(AssertionError):
+        tmod.test_prefill_equals_token_by_token_decode((cfg, w))

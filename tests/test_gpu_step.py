@@ -309,3 +309,38 @@ def test_wide_batch_128_streams(bm):
             bm.kv_slot_release(e, s)
     finally:
         bm.bm_engine_destroy(e)
+
+
+def test_full_size_step_solo_equals_batched(bm):
+    # The benchmarked configuration itself: 48 layers of the 30B-class shape,
+    # vocab 151936, 32 slots of 4096 positions, 32 streams with prefixes of the
+    # workload's length mix, one graph launch per step.  The oracle cannot run
+    # 48 full-width layers in test time, so the check is a property that holds
+    # at any size: sampled streams stepped alone in fresh slots reproduce their
+    # batched rows byte for byte (two steps, so the appended K/V is reused),
+    # and every output is finite and in range.
+    name = "full_model"
+    cfg = dict(synth.CONFIGS[name])
+    layers, S, cap = cfg["layers"], cfg["max_streams"], cfg["ctx_cap"]
+    lens = synth.prompt_lengths(S, cfg["prompt"][0], cfg["prompt"][1], synth.seed_of(name, "prompt_lens"))
+    toks = [[int(t) for t in synth.tokens(name, f"full_size_step{k}", S, cfg["vocab"])] for k in range(2)]
+    e = build_engine(name, cfg, layers, max_streams=S, ctx_cap=cap, policy=MMA, gen_device="cuda")
+    try:
+        assert bm.bm_engine_kernel_family(e) == MMA
+        slots = [seed_stream(e, name, cfg, i, L, layers) for i, L in enumerate(lens)]
+        batched = [_step(bm, e, slots, toks[k], cfg["vocab"]) for k in range(2)]
+        for nxt, logits in batched:
+            assert torch.isfinite(logits).all()
+            assert ((nxt >= 0) & (nxt < cfg["vocab"])).all()
+        sample = [0, 13, 31]
+        for i in sample:
+            bm.kv_slot_release(e, slots[i])
+        for i in sample:
+            s = seed_stream(e, name, cfg, i, lens[i], layers)
+            for k in range(2):
+                n1, l1 = _step(bm, e, [s], [toks[k][i]], cfg["vocab"])
+                assert torch.equal(l1[0], batched[k][1][i]) and n1[0] == batched[k][0][i], \
+                    f"stream {i}, step {k}: solo bytes differ from the 32-stream batch"
+            bm.kv_slot_release(e, s)
+    finally:
+        bm.bm_engine_destroy(e)

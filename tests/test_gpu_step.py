@@ -229,16 +229,16 @@ def test_step_at_full_width(bm, policy, layers):
         bm.bm_engine_destroy(e)
 
 
-@pytest.mark.parametrize("policy", [MMA, TC], ids=["mma", "tc"])
-def test_long_context_step(bm, policy):
+@pytest.mark.parametrize("policy,cap", [(MMA, 4096), (TC, 4096), (MMA, 8192)], ids=["mma", "tc", "mma_cap8192"])
+def test_long_context_step(bm, policy, cap):
     # One layer of the 30B-class shape with context lengths on chunk
-    # boundaries (127, 128, 129) and at the cap (4095 -> the new token is
-    # position 4095 of a 4096-position slot): the split-K chunks, their merge
-    # and the append at the last position, against the oracle.
+    # boundaries (127, 128, 129) and at the cap (cap - 1 -> the new token is
+    # the last position of the slot; at 8192 the merge takes its largest
+    # count, 64 chunks): the split-K chunks, their merge and the append at the
+    # last position, against the oracle.
     cfg = dict(synth.CONFIGS["full_model"])
     cfg["vocab"] = 4096
     layers = 1
-    cap = 4096
     e = build_engine("long_ctx", cfg, layers, max_streams=4, ctx_cap=cap, policy=policy, gen_device="cpu")
     try:
         lens = [127, 128, 129, cap - 1]

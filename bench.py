@@ -196,6 +196,25 @@ def measured_traffic(kernel):
     return rec.get("bytes_per_launch", {}).get(kernel)
 
 
+def int4_bytes(rows, K, g):
+    """Bytes of a packed int4 matrix [rows][K] with one fp16 scale per group of g."""
+    return rows * K // 2 + rows * (K // g) * 2
+
+
+def weight_roofline_tok_s(cfg, layers, B, peak_gbs):
+    """Decode tok/s if one step only streamed its weights at peak_gbs: per layer
+    the dense projections, the fp32 router and the expected number of active
+    experts under uniform routing, E (1 - (1 - k/E)^B); once per step the bf16
+    output projection."""
+    H, F, E, k, g = cfg["hidden"], cfg["ffn"], cfg["experts"], cfg["top_k"], cfg["group"]
+    qd, kvd = cfg["q_heads"] * cfg["head_dim"], cfg["kv_heads"] * cfg["head_dim"]
+    dense = int4_bytes(qd + 2 * kvd, H, g) + int4_bytes(H, qd, g)
+    expert = int4_bytes(2 * F, H, g) + int4_bytes(H, F, g)
+    active = E * (1.0 - (1.0 - k / E) ** B)
+    step = layers * (dense + E * H * 4 + active * expert) + cfg["vocab"] * H * 2
+    return B * peak_gbs * 1e9 / step
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -370,6 +389,14 @@ def run_ours(args, dist, world, rank, local):
         pf = {"prompt_tokens": P, "block_rows": cfg["max_streams"], "steps": args.prefill_steps,
               "ms_per_prompt": round(1e3 * d / args.prefill_steps, 3),
               "tok_s": round(world * P * args.prefill_steps / d, 1)}
+    # each measured B against the weight-bytes roofline at the measured copy bandwidth
+    sweep_roof = {}
+    try:
+        for b_str, v in sweep.items():
+            roof_b = weight_roofline_tok_s(cfg, args.layers, int(b_str), peak) * world
+            sweep_roof[b_str] = {"roof_tok_s": round(roof_b, 1), "frac": round(v / roof_b, 4)}
+    except Exception:   # a reporting extra: never lose the measured line over it
+        sweep_roof = None
     stats = bm.bm_engine_stats(e)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -389,7 +416,7 @@ def run_ours(args, dist, world, rank, local):
         "roofline": roof,
         "step_algorithmic_GB": round(step_bytes / 1e9, 3),
         "step_GB_per_s": round(step_bytes / (dt / args.steps) / 1e9, 1),
-        "kernels": kernels, "sweep_tok_s": sweep, "prefill": pf,
+        "kernels": kernels, "sweep_tok_s": sweep, "sweep_weight_roofline": sweep_roof, "prefill": pf,
         "weight_GB": round(stats["weight_bytes"] / 1e9, 3), "arena_GB": round(stats["arena_bytes"] / 1e9, 3),
         "setup_s": round(t_build, 1),
     }

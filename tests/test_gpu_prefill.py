@@ -81,11 +81,20 @@ def _oracle_prefill(name, cfg, layers, cap, stream, L0, toks, max_streams=4):
 def _check_against_decode_and_oracle(bm, e, name, cfg, layers, cap, L0, toks, what):
     V = cfg["vocab"]
     P = len(toks)
+    # a bystander stream whose slot neither the prompt nor the decode steps may touch
+    L_by = 23
+    s_by = _seed(bm, e, name, cfg, 3, L_by, layers)
+    by_before = [_read(bm, e, cfg, l, s_by, L_by) for l in range(layers)]
     sa = _seed(bm, e, name, cfg, 0, L0, layers)
     sb = _seed(bm, e, name, cfg, 0, L0, layers)
     nxt_a, logits_a = _prefill(bm, e, sa, toks, V)
     nxt_b, logits_b = _decode_prompt(bm, e, sb, toks, V)
     assert bm.kv_slot_length(e, sa) == bm.kv_slot_length(e, sb) == L0 + P
+    assert bm.kv_slot_length(e, s_by) == L_by
+    for l in range(layers):
+        Kx, Vx = _read(bm, e, cfg, l, s_by, L_by)
+        assert torch.equal(Kx, by_before[l][0]) and torch.equal(Vx, by_before[l][1]), f"{what}: bystander slot changed"
+    bm.kv_slot_release(e, s_by)
     # byte identity with teacher-forced decode
     assert torch.equal(logits_a, logits_b), f"{what}: prompt logits differ from decode bytes"
     assert nxt_a == nxt_b

@@ -7,7 +7,7 @@ byte identity (arena, logits, next id, length) with feeding the same prompt
 through single-stream decode steps; blocks with a ragged tail, a prompt that
 crosses a 128-position attention chunk, an empty prefix, the graph path
 against the eager path with its launch count, a decode step after the
-prompt, and the argument checks."""
+prompt, a bystander slot left byte-identical, and the argument checks."""
 
 import numpy as np
 import pytest

@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -20,3 +21,25 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The measured error of every GPU-vs-oracle comparison of the session."""
+    import parity
+    rec = parity.RECORD
+    if not rec:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", f"parity record: {len(rec)} comparisons")
+    worst = {}
+    for r in rec:
+        w = worst.get(r["what"])
+        if w is None or r["max_abs"] > w["max_abs"]:
+            worst[r["what"]] = r
+    for what, r in sorted(worst.items()):
+        tr.write_line(f"{what[:70]:70s} max_abs {r['max_abs']:.3e} (bound {r['bound']:.0e}) "
+                      f"min_cos {r['min_cos']:.9f} ulp_flips {r['ulp_flips']}/{r['elements']}")
+    path = os.environ.get("BM_PARITY_LOG")
+    if path:
+        with open(path, "w") as f:
+            json.dump(rec, f, indent=0)

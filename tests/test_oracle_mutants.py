@@ -252,3 +252,95 @@ def test_decode_equivalence_catches_prefill_mutant(monkeypatch, name, attr, muta
     monkeypatch.setattr(om, attr, mutant)
     with pytest.raises(AssertionError):
         tmod.test_prefill_equals_token_by_token_decode((cfg, w))
+
+
+# ---------------------------------------------------------------- decoder-layer composition
+
+def _layer_mutant(mistake):
+    """A copy of the oracle's decoder layer with one composition mistake."""
+    import oracle.model as om
+
+    def after_attention(cfg, lw, x, o, trace=None):
+        H, qh, d, g = cfg.hidden, cfg.q_heads, cfg.head_dim, cfg.group
+        B = x.shape[0]
+        Wo = om.dequant_w4(lw["wo"][0], lw["wo"][1], qh * d, g)
+        h = om._round(x + om.rowwise(Wo, o))
+        norm_w = None if mistake == "ffn norm weight dropped" else lw.get("ffn_norm")
+        hn = om.rmsnorm(h, norm_w, cfg.eps)
+        if mistake != "hn not rounded":
+            hn = om._round(hn)
+        ids, w = om.route_topk(h if mistake == "router reads h" else hn, lw["wr"], cfg.top_k, cfg.renorm_topk)
+        xin = h if mistake == "experts read h" else hn
+        y = np.empty_like(h)
+        outs = np.empty((B, cfg.top_k, H))
+        for b in range(B):
+            acc = np.zeros(H)
+            for r in range(cfg.top_k):
+                ew = lw["expert"](int(ids[b, r]))
+                Wg = om.dequant_w4(ew["wg"][0], ew["wg"][1], H, g)
+                Wu = om.dequant_w4(ew["wu"][0], ew["wu"][1], H, g)
+                Wd = om.dequant_w4(ew["wd"][0], ew["wd"][1], cfg.ffn, g)
+                a = om._round(om.silu(Wg @ xin[b]) * (Wu @ xin[b]))
+                outs[b, r] = Wd @ a
+                acc = acc + w[b, r] * outs[b, r]
+            y[b] = om._round((hn[b] if mistake == "combine residual from hn" else h[b]) + acc)
+        if trace is not None:
+            trace.update(dict(h=h, hn=hn, ids=ids, w=w, expert_out=outs, y=y))
+        return y
+
+    def decoder_layer(cfg, lw, x, slots, kv, layer, trace=None):
+        H, qh, kvh, d, g = cfg.hidden, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.group
+        x = np.asarray(x, dtype=np.float64)
+        B = x.shape[0]
+        xn = om._round(om.rmsnorm(x, lw.get("attn_norm"), cfg.eps))
+        qkv = om._round(om.rowwise(om.dequant_w4(lw["wqkv"][0], lw["wqkv"][1], H, g), xn))
+        q = qkv[:, : qh * d].reshape(B, qh, d)
+        k = qkv[:, qh * d: (qh + kvh) * d].reshape(B, kvh, d)
+        v = qkv[:, (qh + kvh) * d:].reshape(B, kvh, d)
+        if mistake == "v taken from the k rows":
+            v = k
+        o = np.empty((B, qh * d))
+        q_rot = np.empty_like(q)
+        for b in range(B):
+            pos = kv.map.length[slots[b]]
+            q_rot[b] = om._round(om.rope_rotate_half(q[b], pos, cfg.rope_base))
+            k_rot = om._round(om.rope_rotate_half(k[b], pos, cfg.rope_base))
+            if mistake == "attention before the append":
+                Kc, Vc = kv.view(layer, slots[b], pos)
+                kv.write_pending(layer, slots[b], k_rot, v[b])
+            else:
+                kv.write_pending(layer, slots[b], k_rot, v[b])
+                Kc, Vc = kv.view(layer, slots[b], pos + 1)
+            o[b] = om._round(om.slot_attention(q_rot[b], Kc, Vc)).reshape(-1)
+        y = after_attention(cfg, lw, xn if mistake == "attention residual from xn" else x, o, trace)
+        if trace is not None:
+            trace.update(dict(xn=xn, qkv=qkv, q_rot=q_rot, attn=o))
+        return y
+
+    return decoder_layer
+
+
+LAYER_MUTANTS = ["attention residual from xn", "combine residual from hn", "router reads h", "experts read h",
+                 "ffn norm weight dropped", "hn not rounded", "attention before the append",
+                 "v taken from the k rows"]
+
+
+def test_layer_golden_holds_on_the_oracle_and_its_copy():
+    import test_oracle_layer_golden as tl
+    tl.check_layer()
+    orig = None
+    import oracle.model as om
+    orig, om.decoder_layer = om.decoder_layer, _layer_mutant("none")
+    try:
+        tl.check_layer()   # the copy without a mistake passes: the mutants differ by their mistake only
+    finally:
+        om.decoder_layer = orig
+
+
+@pytest.mark.parametrize("mistake", LAYER_MUTANTS)
+def test_layer_golden_catches_composition_mutant(monkeypatch, mistake):
+    import oracle.model as om
+    import test_oracle_layer_golden as tl
+    monkeypatch.setattr(om, "decoder_layer", _layer_mutant(mistake))
+    with pytest.raises(AssertionError):
+        tl.check_layer()

@@ -103,6 +103,10 @@ def lib():
             "kv_slot_prefill": ([V, I, I, V, V, V, V], S),
             "bm_engine_profile_step": ([V, I, V, V, V, ctypes.POINTER(bm_kernel_profile), I, PI, V], S),
             "bm_w4_quantize": ([V, I, I, I, V, V, V], S),
+            "bm_engine_moe": ([V, I, V, V, V, V, I, V], S),
+            "bm_engine_attention": ([V, I, V, V, V, I, V], S),
+            "bm_engine_read_hidden": ([V, I, V, V], S),
+            "bm_engine_test_drop_expert_item": ([V, I], S),
             "bm_slot_map_create": ([I, I, ctypes.POINTER(V)], S),
             "bm_slot_map_destroy": ([V], None),
             "bm_slot_map_acquire": ([V, I, PI], S),
@@ -308,6 +312,27 @@ def bm_engine_profile_step(e, slots, tokens, next_tokens, stream=None):
                                         32, ctypes.byref(n), stream_handle(stream)))
     return [{"name": out[i].name.decode(), "launches": out[i].launches, "ms": out[i].ms,
              "bytes": out[i].bytes, "flops": out[i].flops} for i in range(n.value)]
+
+
+def bm_engine_moe(e, layer, h, y, topk_ids=None, topk_w=None, stream=None):
+    """The decode step's routing and expert kernels on one layer; h, y: bf16 [B][H]."""
+    _check(lib().bm_engine_moe(e, layer, ptr(h), ptr(y), ptr(topk_ids), ptr(topk_w), int(h.shape[0]),
+                               stream_handle(stream)))
+
+
+def bm_engine_attention(e, layer, slots, qkv, out, stream=None):
+    """The decode step's fused attention on one layer; qkv: bf16 rows, out: fp16 [B][qh][d]."""
+    arr = _i32_array(slots)
+    _check(lib().bm_engine_attention(e, layer, ctypes.addressof(arr), ptr(qkv), ptr(out), len(slots),
+                                     stream_handle(stream)))
+
+
+def bm_engine_read_hidden(e, B, out, stream=None):
+    _check(lib().bm_engine_read_hidden(e, int(B), ptr(out), stream_handle(stream)))
+
+
+def bm_engine_test_drop_expert_item(e, item):
+    _check(lib().bm_engine_test_drop_expert_item(e, int(item)))
 
 
 def bm_w4_quantize(W, N, K, g, packed, scales, stream=None):

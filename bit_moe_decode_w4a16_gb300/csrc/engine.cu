@@ -138,6 +138,7 @@ struct bm_engine {
   cudaStream_t cap_stream = nullptr;
   std::map<int, cudaGraphExec_t> graphs;   // decode graphs by B; prompt blocks under negative keys
   std::map<int, int> graph_kernels;         // kernels in each graph
+  int test_drop_item = -1;                  // failure-detection tests: an expert item whose copies are not issued
   bm_stats st{};
 
   bm_engine(const bm_config& c) : cfg(c), slots(c.max_streams, c.ctx_cap) {}
@@ -756,8 +757,12 @@ bm_status bm_engine_sync(bm_engine* e, void* stream) {
   BM_CUDA(cudaMemcpy(&flag, e->d_err, sizeof(int), cudaMemcpyDeviceToHost), "device check read");
   if (flag) {
     BM_CUDA(cudaMemset(e->d_err, 0, sizeof(int)), "device check reset");
-    return set_error(BM_ERR_DEVICE_CHECK, "a kernel skipped an out-of-range index (code " + std::to_string(flag) +
-                                              ": 1 slot id, 2 position, 3 token id)");
+    static const char* what[] = {"", "an out-of-range slot id was skipped", "an out-of-range position was skipped",
+                                 "an out-of-range token id was skipped",
+                                 "a tensor-core projection's pipeline wait timed out",
+                                 "an expert projection's pipeline wait timed out (the CTA stopped consuming)"};
+    return set_error(BM_ERR_DEVICE_CHECK, std::string("device check code ") + std::to_string(flag) + ": " +
+                                              (flag >= 1 && flag <= 5 ? what[flag] : "unknown"));
   }
   return bm::ok();
 }
@@ -1223,6 +1228,90 @@ bm_status moe_grouped_w4(const bm_moe_weights* w, const uint16_t* X, const uint1
   if (topk_w)
     BM_CUDA(cudaMemcpyAsync(topk_w, b.topk_w, sizeof(float) * B * w->top_k, cudaMemcpyDeviceToDevice, s),
             "topk weights copy");
+  return bm::ok();
+}
+
+bm_status bm_engine_moe(bm_engine* e, int layer, const uint16_t* h, uint16_t* y, int32_t* topk_ids, float* topk_w,
+                        int B, void* stream) {
+  if (!e || !h || !y) return set_error(BM_ERR_INVALID_ARG, "bm_engine_moe: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  if (layer < 0 || layer >= c.layers) return set_error(BM_ERR_INVALID_ARG, "bm_engine_moe: layer out of range");
+  if (B < 1 || B > c.max_streams) return set_error(BM_ERR_INVALID_ARG, "bm_engine_moe: B out of range");
+  if (!e->L[layer].set) return set_error(BM_ERR_NOT_READY, "bm_engine_moe: layer weights not set");
+  if (e->family != BM_POLICY_MMA)
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_moe: needs an engine on the warp-MMA kernel family");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const LayerW& w = e->L[layer];
+  const int H = c.hidden, F = c.ffn, g = c.group;
+  auto u32 = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
+  const bf16* hin = reinterpret_cast<const bf16*>(h);
+  MoeArgs ma{B, c.experts, c.top_k, H, F, g, c.renorm_topk,
+             w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
+             hin, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, hin, reinterpret_cast<bf16*>(y),
+             e->d_u_log + layer, 1};
+  const MoeBufs mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, F);
+  BM_CUDA(launch_moe_route_fused(ma, mb, e->route_cnt, e->route_cnt + c.max_streams, s, Marker(), false),
+          "bm_engine_moe routing");
+  MmaArgs m3{};
+  m3.W = w.wg; m3.S = u32(w.wg_s); m3.rows = 2 * F; m3.K = H; m3.g = g; m3.X = mb.xn; m3.ldx = H;
+  m3.pair_token = mb.pair_token; m3.n_jobs = mb.n_jobs; m3.jobs = mb.jobs;
+  m3.max_jobs = moe_max_jobs(B, c.experts, c.top_k);
+  m3.w_expert_stride = (size_t)2 * F * H / 2; m3.s_expert_stride = (size_t)F * (H / g);
+  m3.act16 = reinterpret_cast<__half*>(mb.act); m3.F = F; m3.err = e->d_err;
+  m3.drop_item1 = e->test_drop_item + 1;
+  BM_CUDA(launch_w4_mma_gateup(m3, s), "bm_engine_moe gate/up");
+  MmaArgs m4{};
+  m4.W = w.wd; m4.S = u32(w.wd_s); m4.rows = H; m4.K = F; m4.g = g; m4.X = mb.act; m4.ldx = F;
+  m4.pair_token = mb.pair_token; m4.n_jobs = mb.n_jobs; m4.jobs = mb.jobs; m4.max_jobs = m3.max_jobs;
+  m4.w_expert_stride = (size_t)H * F / 2; m4.s_expert_stride = (size_t)H * (F / g) / 2;
+  m4.out = mb.out; m4.H = H; m4.err = e->d_err;
+  BM_CUDA(launch_w4_mma_down(m4, s), "bm_engine_moe down");
+  BM_CUDA(launch_moe_combine_norm(ma, mb, nullptr, e->xn, 1, s, Marker(), false), "bm_engine_moe combine");
+  if (topk_ids)
+    BM_CUDA(cudaMemcpyAsync(topk_ids, mb.topk_ids, sizeof(int32_t) * B * c.top_k, cudaMemcpyDefault, s),
+            "bm_engine_moe ids copy");
+  if (topk_w)
+    BM_CUDA(cudaMemcpyAsync(topk_w, mb.topk_w, sizeof(float) * B * c.top_k, cudaMemcpyDefault, s),
+            "bm_engine_moe weights copy");
+  e->st.kernel_launches += 4;
+  return bm::ok();
+}
+
+bm_status bm_engine_attention(bm_engine* e, int layer, const int32_t* slots, const uint16_t* qkv, uint16_t* out,
+                              int B, void* stream) {
+  if (!e || !slots || !qkv || !out) return set_error(BM_ERR_INVALID_ARG, "bm_engine_attention: null argument");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  if (layer < 0 || layer >= c.layers) return set_error(BM_ERR_INVALID_ARG, "bm_engine_attention: layer out of range");
+  if (e->family != BM_POLICY_MMA || !attention_fused_supports(e->arena, c.q_heads))
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_attention: needs the warp-MMA kernel family and fused attention");
+  std::string err;
+  bm_status st = e->slots.check_batch(slots, B, &err);
+  if (st != BM_OK) return set_error(st, "bm_engine_attention: " + err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = stage_aux_slots(e, slots, B, s)) != BM_OK) return st;
+  AttnFusedArgs fa{e->arena, layer, e->d_slots_aux, reinterpret_cast<const bf16*>(qkv), e->qkv_rows, c.q_heads,
+                   e->d_rope, reinterpret_cast<__half*>(out), e->attn_part, (c.ctx_cap + kAttnChunk - 1) / kAttnChunk,
+                   e->attn_cnt, B, chk_of(e), 0};
+  BM_CUDA(launch_attention_fused(fa, s, false), "bm_engine_attention launch");
+  e->st.kernel_launches += 1;
+  return bm::ok();
+}
+
+bm_status bm_engine_read_hidden(bm_engine* e, int B, uint16_t* out, void* stream) {
+  if (!e || !out) return set_error(BM_ERR_INVALID_ARG, "bm_engine_read_hidden: null argument");
+  if (B < 1 || B > e->cfg.max_streams) return set_error(BM_ERR_INVALID_ARG, "bm_engine_read_hidden: B out of range");
+  BM_CUDA(cudaMemcpyAsync(out, e->x, sizeof(uint16_t) * B * (size_t)e->cfg.hidden, cudaMemcpyDefault,
+                          static_cast<cudaStream_t>(stream)),
+          "bm_engine_read_hidden copy");
+  return bm::ok();
+}
+
+bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "bm_engine_test_drop_expert_item: null engine");
+  std::lock_guard<std::mutex> lk(e->mu);
+  e->test_drop_item = item < 0 ? -1 : item;
   return bm::ok();
 }
 

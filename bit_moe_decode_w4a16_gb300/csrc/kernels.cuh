@@ -173,6 +173,8 @@ struct MmaArgs {
   int x_bf16;                // dense only: X holds bf16 values (converted on load) instead of fp16
   int pdl;                   // launch with programmatic dependent launch
   int ks;                    // set by the launchers
+  int drop_item1;            // failure-detection tests only: 1 + the index of a staged expert work item whose
+                             // copies the producer does not issue (its consumers' bounded wait runs out); 0 = none
 };
 // Shape support of the warp-MMA kernels: rows % 32 == 0, K % 128 == 0,
 // K <= 4096, g in {32, 64, 128}.

@@ -46,7 +46,7 @@ constexpr int kStageK = 64;                 // K per stage: 32 TMEM columns of A
 constexpr uint32_t kTmemCols = 256;
 constexpr int kMaxSlots = 6;
 constexpr int kLmSlots = 6;                 // output projection: A-only slots, one accumulator
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimit = 1u << 18;         // polls of ~3.7 us each: a wait gives up after about a second
 constexpr int kMaxSplit = 8;
 
 // One packed word (codes ordered k0 k2 k4 k6 k1 k3 k5 k7) -> the four TMEM

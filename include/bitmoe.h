@@ -52,7 +52,8 @@ typedef enum bm_status {
   BM_ERR_CUDA = 5,          /* a CUDA runtime call failed                       */
   BM_ERR_OOM = 6,           /* device or pinned host allocation failed         */
   BM_ERR_NOT_READY = 7,     /* decode_step before every layer's weights were set */
-  BM_ERR_DEVICE_CHECK = 8,  /* a kernel found an out-of-range index and skipped it */
+  BM_ERR_DEVICE_CHECK = 8,  /* a kernel skipped an out-of-range index, or a bounded
+                               pipeline wait inside a kernel gave up              */
   BM_ERR_UNSUPPORTED = 9    /* a shape or option this build does not handle    */
 } bm_status;
 
@@ -173,9 +174,13 @@ bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w
 bm_status bm_engine_set_embeddings(bm_engine* e, const uint16_t* embed, const uint16_t* lm_head,
                                    const uint16_t* final_norm, void* stream);
 
-/* Synchronise `stream` and report device-side index checks (BM_ERR_DEVICE_CHECK
- * if any kernel of this engine skipped an out-of-range slot, token or
- * expert id since the last call; the flag is then cleared). */
+/* Synchronise `stream` and report device-side checks since the last call
+ * (BM_ERR_DEVICE_CHECK; the flag is then cleared).  The message names the
+ * code: 1 an out-of-range slot id, 2 an out-of-range position, 3 an
+ * out-of-range token id (each skipped by the kernel that met it), 4 a
+ * tensor-core projection's pipeline wait that timed out, 5 an expert
+ * projection's pipeline wait that timed out (that CTA stopped after waiting
+ * for the copies it had issued).  No check traps: the context stays usable. */
 bm_status bm_engine_sync(bm_engine* e, void* stream);
 
 /* Counters and standing memory. */
@@ -382,6 +387,62 @@ bm_status kv_slot_prefill(bm_engine* e, int slot, int n_tokens, const int32_t* t
 bm_status bm_engine_profile_step(bm_engine* e, int B, const int32_t* slots, const int32_t* tokens,
                                  int32_t* next_tokens, bm_kernel_profile* out, int max_out, int* n_out,
                                  void* stream);
+
+/* ---------------------------------------------------------------- layer ops of the step
+ * The decode step's own kernels on one layer, with the engine's weights (in
+ * the layout the step reads) and its scratch, launched exactly as decode_step
+ * launches them (same grids, same per-output summation order), so that each
+ * block can be checked on its own at any batch size.  The engine must be on
+ * the warp-MMA kernel family (BM_ERR_UNSUPPORTED otherwise).  Like every call
+ * on an engine they are serialised by the engine and must not overlap with
+ * other work on it in flight. */
+
+/* The mixture-of-experts half of decoder layer `layer` for B rows
+ * ([Batched serving] §1: the experts selected by all B streams run as one
+ * grouped operation against the resident int4 bank): hn = RMSNorm(h) with
+ * the layer's ffn norm, fp32 router logits, softmax top-k (ties: lower
+ * expert id) with renormalised weights, the (row, rank) pairs grouped by
+ * expert, each active expert's gate/up (SiLU) and down projections over its
+ * rows, and y = h + sum_r w[r] * out[r] in rank order.  Four launches:
+ * routing (router, top-k and grouping in one kernel), gate/up, down, combine.
+ * h: DEVICE bf16 [B][H]; y: DEVICE bf16 [B][H] (may not alias h);
+ * topk_ids: int32 [B][k] and topk_w: fp32 [B][k], HOST or DEVICE, or NULL.
+ * Errors: BM_ERR_INVALID_ARG (NULL h or y, layer or B out of range),
+ * BM_ERR_NOT_READY, BM_ERR_UNSUPPORTED, BM_ERR_CUDA.  A pipeline wait that
+ * gives up inside the expert kernels is reported by bm_engine_sync
+ * (BM_ERR_DEVICE_CHECK, code 5). */
+bm_status bm_engine_moe(bm_engine* e, int layer, const uint16_t* h, uint16_t* y, int32_t* topk_ids, float* topk_w,
+                        int B, void* stream);
+
+/* The attention block of decoder layer `layer` for B streams in one launch
+ * ([KV-slot isolation] §1: each stream's K/V lives in its own slot of the
+ * fixed arena): rotate-half RoPE of the q heads and of the new k at position
+ * p = length(slots[i]), k and v written to the slot at p, then grouped-query
+ * attention of each q head over positions 0..p of that slot (split into
+ * 128-position chunks and merged in ascending order), output rounded to bf16.
+ * The length does not advance (kv_slot_advance commits the position).
+ * slots: HOST int32 [B], distinct active slots; qkv: DEVICE bf16 [B][(q_heads
+ * + 2 kv_heads) * head_dim], rows of the QKV projection (q heads, then k,
+ * then v, head-major, not rotated); out: DEVICE [B][q_heads][head_dim] fp16
+ * bit patterns, each holding a bf16-rounded value (the form the output
+ * projection of the step consumes).  Errors as kv_slot_append, plus
+ * BM_ERR_UNSUPPORTED. */
+bm_status bm_engine_attention(bm_engine* e, int layer, const int32_t* slots, const uint16_t* qkv, uint16_t* out,
+                              int B, void* stream);
+
+/* Copy the residual-stream rows left by the last decode_step (the last
+ * layer's output, before the final norm), bf16 [B][H], to `out` (HOST or
+ * DEVICE).  B <= max_streams.  For tests that check a deep step layer by
+ * layer. */
+bm_status bm_engine_read_hidden(bm_engine* e, int B, uint16_t* out, void* stream);
+
+/* Failure-detection tests only: make the next bm_engine_moe calls skip the
+ * copies of staged expert work item `item` of the gate/up kernel (-1 = none,
+ * the default), so that its consumers' bounded wait runs out, the affected
+ * CTA stops, and bm_engine_sync reports BM_ERR_DEVICE_CHECK with code 5.
+ * Nothing faults: every copy that was issued is waited for before the CTA
+ * exits.  decode_step ignores this setting. */
+bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item);
 
 /* Encode fp32 weights to the canonical int4 layout: per row and group of g,
  * s = fp16(absmax / 7) (fp32 division, round to nearest even), q =

@@ -31,12 +31,13 @@ from .numerics import (bf16_round, bf16_bits, from_bf16_bits, unpack_int4,
                        pack_int4, dequant_w4, quantize_w4)
 from .ops import (w4_gemm, rmsnorm, rope_rotate_half, slot_attention, causal_block_attention,
                   silu, route_topk, expert_ffn, moe_combine)
-from .model import (OracleConfig, OracleSlotMap, OracleKV, decoder_layer, model_step,
-                    prefill_layer, model_prefill)
+from .model import (OracleConfig, OracleSlotMap, OracleKV, decoder_layer, moe_block, lm_head_logits,
+                    model_step, prefill_layer, model_prefill)
 
 __all__ = [
     "bf16_round", "bf16_bits", "from_bf16_bits", "unpack_int4", "pack_int4",
     "dequant_w4", "quantize_w4", "w4_gemm", "rmsnorm", "rope_rotate_half",
     "slot_attention", "causal_block_attention", "silu", "route_topk", "expert_ffn", "moe_combine",
-    "OracleConfig", "OracleSlotMap", "OracleKV", "decoder_layer", "model_step", "prefill_layer", "model_prefill",
+    "OracleConfig", "OracleSlotMap", "OracleKV", "decoder_layer", "moe_block", "lm_head_logits", "model_step",
+    "prefill_layer", "model_prefill",
 ]

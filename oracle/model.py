@@ -199,9 +199,20 @@ def _after_attention(cfg, lw, x, o, trace=None):
     residual, RMSNorm, top-k routing, the selected experts, and the weighted
     combine with the residual (x, o: bf16 values [B][H], [B][qh*d])."""
     H, qh, d, g = cfg.hidden, cfg.q_heads, cfg.head_dim, cfg.group
-    B = x.shape[0]
     Wo = dequant_w4(lw["wo"][0], lw["wo"][1], qh * d, g)
     h = _round(x + rowwise(Wo, o))
+    return moe_block(cfg, lw, h, trace)
+
+
+def moe_block(cfg, lw, h, trace=None):
+    """The mixture-of-experts half of a decoder layer on the residual rows h
+    (bf16 values [B][H]): RMSNorm with the ffn norm, top-k routing, the
+    selected experts' FFNs, and the combine with the residual, row by row
+    ([Batched serving, §1 Contribution]: the experts the router selects for
+    each stream run against the resident int4 bank)."""
+    H, g = cfg.hidden, cfg.group
+    h = np.asarray(h, dtype=np.float64)
+    B = h.shape[0]
     hn = _round(rmsnorm(h, lw.get("ffn_norm"), cfg.eps))
     ids, w = route_topk(hn, lw["wr"], cfg.top_k, cfg.renorm_topk)
     F = cfg.ffn

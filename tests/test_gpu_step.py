@@ -191,11 +191,21 @@ def test_ragged_schedule_solo_batched_bytes_and_oracle(bm, policy):
 
 
 def logit_bound(layers):
-    """The 2e-2 bound holds per op and per layer output; through L layers
-    the bf16 rounding points of the two sides flip independently and the
-    logit differences add up, so an L-layer step is held to L x 2e-2
-    (the cosine bound is unchanged)."""
-    return 2e-2 * layers
+    """The specified 2e-2 max-abs bound (cosine >= 0.9999), at every depth the
+    tiny-layer tests run: their measured logit errors stay below 0.01 at two
+    layers."""
+    return 2e-2
+
+
+# End to end through two full-width layers the logits of the two sides drift
+# a little further (measured 0.0217): each layer's bf16 hand-offs round the
+# fp32 (GPU) and fp64 (oracle) values of the residual stream independently, a
+# value near a rounding boundary flips one ulp on one side, and the flips of
+# layer 1 reach layer 2 through attention, routing and the experts.  Layer by
+# layer, with the GPU's own layer-1 output as the oracle's input, every
+# output stays within 2e-2 (test_step_at_full_width), so the end-to-end
+# two-layer comparison alone is held to 2 x 2e-2.
+FULL_WIDTH_DEPTH_BOUND = {1: 2e-2, 2: 4e-2}
 
 
 @FAMILIES
@@ -222,11 +232,48 @@ def test_step_at_full_width(bm, policy, layers):
             k, v = synth.kv_prefix("full_width", cfg, i, L, layers=layers)
             oslots.append(kv.seed(k.double().numpy(), v.double().numpy()))
         ref, _ = oracle.model_step(ocfg, ow, kv, oslots, toks)
-        err, _ = assert_close_rows(logits, ref, max_abs=logit_bound(layers), what=f"full-width {layers}-layer step",
-                                   bf16_out=False)
+        err, _ = assert_close_rows(logits, ref, max_abs=FULL_WIDTH_DEPTH_BOUND[layers],
+                                   what=f"full-width {layers}-layer step", bf16_out=False)
         check_greedy(nxt, ref, err)
+        if layers == 2:
+            _full_width_layer_by_layer(bm, e, cfg, policy, lens, toks, logits, ow)
     finally:
         bm.bm_engine_destroy(e)
+
+
+def _full_width_layer_by_layer(bm, e2, cfg, policy, lens, toks, logits, ow):
+    """The two-layer step checked layer by layer: the GPU's layer-1 output
+    (a one-layer engine with the same weights, prefixes and tokens) feeds the
+    oracle's layer 2, whose output must match the two-layer engine's last
+    hidden state, and the oracle's output projection of that state must match
+    the GPU's logits, each within 2e-2."""
+    B, H = len(lens), cfg["hidden"]
+    y2 = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+    bm.bm_engine_read_hidden(e2, B, y2)
+    e1 = build_engine("full_width", cfg, 1, max_streams=4, ctx_cap=256, policy=policy, gen_device="cpu")
+    try:
+        slots = []
+        for i, L in enumerate(lens):
+            k, v = synth.kv_prefix("full_width", cfg, i, L, layers=2)
+            slots.append(bm.kv_slot_seed(e1, k[:1].contiguous().cuda(), v[:1].contiguous().cuda(), L))
+        _step(bm, e1, slots, toks, cfg["vocab"])
+        y1 = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+        bm.bm_engine_read_hidden(e1, B, y1)
+        bm.bm_engine_sync(e1)
+    finally:
+        bm.bm_engine_destroy(e1)
+    ocfg = oracle_config(cfg, layers=2, max_streams=4, ctx_cap=256)
+    kv = _oracle_kv(ocfg, 2)
+    oslots = []
+    for i, L in enumerate(lens):
+        k, v = synth.kv_prefix("full_width", cfg, i, L, layers=2)
+        oslots.append(kv.seed(k.double().numpy(), v.double().numpy()))
+    y2_ref = oracle.decoder_layer(ocfg, ow["layers"][1], y1.double().cpu().numpy(), oslots, kv, 1)
+    assert_close_rows(y2, y2_ref, what="full-width layer 2 on the GPU's layer-1 output")
+    xf = oracle.bf16_round(oracle.rmsnorm(y2.double().cpu().numpy(), None, 1e-6))
+    ref = oracle.lm_head_logits(xf, ow["lm_head_bits"])
+    assert_close_rows(logits, ref, what="full-width output projection of the GPU's last hidden state",
+                      bf16_out=False)
 
 
 @pytest.mark.parametrize("policy,cap", [(MMA, 4096), (TC, 4096), (MMA, 8192)], ids=["mma", "tc", "mma_cap8192"])

@@ -52,6 +52,22 @@ def parse():
                          "kv: seed synthetic K/V of the same lengths (faster start, for profiler runs)")
     ap.add_argument("--prefill-steps", type=int, default=5,
                     help="timed ingestions of one longest-workload prompt (0 to skip)")
+    ap.add_argument("--arrivals", type=int, default=64,
+                    help="streams of the seeded join/finish run (each ingests its prompt on arrival, decodes "
+                         "--gen-tokens greedy tokens and retires; at most max_streams live); 0 to skip")
+    ap.add_argument("--gen-tokens", type=int, default=256)
+    ap.add_argument("--prefill-path", default="tc", choices=["tc", "decode"],
+                    help="kv_slot_prefill on the tcgen05 prompt-length GEMMs (tc) or through the decode kernels "
+                         "in blocks of max_streams rows (decode)")
+    ap.add_argument("--gemm-sweep", default="16,32,64,128,256,512",
+                    help="M values of the prompt-length tcgen05 GEMM timing ('' to skip)")
+    ap.add_argument("--tc-probe", action="store_true",
+                    help="time the tcgen05 MMA alone (N, A source, operand layout) and the prompt-length GEMM "
+                         "against M, without building the model; print one JSON line")
+    ap.add_argument("--attention-long", type=int, default=1,
+                    help="time the fused attention at the slot-attention workload's lengths (0 to skip)")
+    ap.add_argument("--kernel-sweep", default="1,4,8,16,32",
+                    help="B values of the per-kernel GB/s table ('' to skip)")
     return ap.parse_args()
 
 
@@ -227,12 +243,12 @@ def peaks():
 
 # ---------------------------------------------------------------- our arm
 
-def build_model(bm, cfg, layers, max_streams, policy):
+def build_model(bm, cfg, layers, max_streams, policy, prefill_tc=0):
     import torch
     from gpu_side import build_engine
     t = time.time()
     e = build_engine(WORKLOAD, cfg, layers, max_streams=max_streams, ctx_cap=cfg["ctx_cap"], policy=policy,
-                     gen_device="cuda")
+                     gen_device="cuda", prefill_tc=prefill_tc)
     torch.cuda.synchronize()
     return e, time.time() - t
 
@@ -285,7 +301,8 @@ def run_ours(args, dist, world, rank, local):
     cfg = dict(synth.CONFIGS[WORKLOAD])
     B = args.batch
     cfg["max_streams"] = max(args.max_streams or cfg["max_streams"], B)
-    e, t_build = build_model(bm, cfg, args.layers, cfg["max_streams"], args.policy)
+    e, t_build = build_model(bm, cfg, args.layers, cfg["max_streams"], args.policy,
+                             prefill_tc=1 if args.prefill_path == "tc" else 0)
     slots, last, lens = prefill(bm, e, cfg, B, args.layers, args.prefill)
     stream = torch.cuda.current_stream()
     cur = last.clone()
@@ -368,6 +385,13 @@ def run_ours(args, dist, world, rank, local):
                              new_event=lambda: torch.cuda.Event(enable_timing=True), device="cuda",
                              label="sweep_timed")
             sweep[str(b)] = round(world * b * args.sweep_steps / d, 1)
+    # per-kernel GB/s at each B of the kernel sweep (eager steps with events)
+    ktab = None
+    if args.kernel_sweep:
+        try:
+            ktab = kernel_table(bm, e, slots, cur, stream, [int(x) for x in args.kernel_sweep.split(",") if x], peak)
+        except Exception as ex:   # a reporting extra: never lose the measured line over it
+            ktab = {"error": str(ex)}
     # prompt ingestion: one prompt of the workload's longest length into a
     # fresh slot per step (blocks of max_streams rows)
     pf = None
@@ -386,9 +410,29 @@ def run_ours(args, dist, world, rank, local):
         d = timed_region(pstep, torch.cuda.synchronize, dist, args.prefill_steps, 3,
                          new_event=lambda: torch.cuda.Event(enable_timing=True), device="cuda",
                          label="prefill_timed")
-        pf = {"prompt_tokens": P, "block_rows": cfg["max_streams"], "steps": args.prefill_steps,
+        pf = {"prompt_tokens": P, "path": "tcgen05 prompt-length GEMMs" if args.prefill_path == "tc" else
+              f"decode kernels in blocks of {cfg['max_streams']} rows", "steps": args.prefill_steps,
               "ms_per_prompt": round(1e3 * d / args.prefill_steps, 3),
               "tok_s": round(world * P * args.prefill_steps / d, 1)}
+    # the prompt-length GEMM on the tensor cores against M
+    pg = None
+    if args.gemm_sweep:
+        try:
+            pg = prompt_gemm_sweep(bm, [int(x) for x in args.gemm_sweep.split(",") if x], bf16_peak())
+        except Exception as ex:   # a reporting extra: never lose the measured line over it
+            pg = {"error": str(ex)}
+    att = None
+    if args.attention_long:
+        try:
+            att = attention_long(bm, peak)
+        except Exception as ex:   # a reporting extra: never lose the measured line over it
+            att = {"error": str(ex)}
+    # the configured continuous-batching run: streams join and retire, B varies
+    arr = None
+    if args.arrivals > 0:
+        for s in slots[1:] if args.prefill_steps > 0 else slots:
+            bm.kv_slot_release(e, s)
+        arr = run_arrivals(bm, e, cfg, args, stream, world)
     # each measured B against the weight-bytes roofline at the measured copy bandwidth
     sweep_roof = {}
     try:
@@ -416,12 +460,228 @@ def run_ours(args, dist, world, rank, local):
         "roofline": roof,
         "step_algorithmic_GB": round(step_bytes / 1e9, 3),
         "step_GB_per_s": round(step_bytes / (dt / args.steps) / 1e9, 1),
-        "kernels": kernels, "sweep_tok_s": sweep, "sweep_weight_roofline": sweep_roof, "prefill": pf,
+        "kernels": kernels, "sweep_tok_s": sweep, "sweep_weight_roofline": sweep_roof, "kernels_by_B": ktab,
+        "arrivals": arr, "prefill": pf, "prompt_gemm": pg, "attention_long": att,
         "weight_GB": round(stats["weight_bytes"] / 1e9, 3), "arena_GB": round(stats["arena_bytes"] / 1e9, 3),
         "setup_s": round(t_build, 1),
     }
     bm.bm_engine_destroy(e)
     return result
+
+
+def arrival_schedule(n_streams, max_live, gen_tokens, seed):
+    """Seeded arrivals of n_streams streams (one per step with probability
+    0.35, a burst of up to four with probability 0.05, never more than
+    max_live live at once, the first at step 0); each stream decodes
+    gen_tokens tokens and retires.  Returns the arrival step of every stream,
+    the order in which they may join."""
+    import random
+    rng = random.Random(seed)
+    arrive, live_until, step = [], [], 0
+    while len(arrive) < n_streams:
+        live_until = [t for t in live_until if t > step]
+        want = 1 if (not arrive or rng.random() < 0.35) else 0
+        if rng.random() < 0.05:
+            want += rng.randint(1, 3)
+        for _ in range(want):
+            if len(arrive) == n_streams or len(live_until) >= max_live:
+                break
+            arrive.append(step)
+            live_until.append(step + gen_tokens)
+        step += 1
+    return arrive
+
+
+def run_arrivals(bm, e, cfg, args, stream, world):
+    """The workload's continuous-batching run: streams join on a seeded
+    schedule (slot seeded empty, prompt of U[16,512] seeded ids ingested with
+    kv_slot_prefill), decode gen_tokens greedy tokens in one decode_step per
+    step over every live stream, and retire (slot released, no wipe), so B
+    changes as streams come and go.  Decode tok/s = decode tokens / summed
+    device time of the decode steps (CUDA events around each step on the
+    launching stream); prompt ingestion is timed apart.  Graphs for every B
+    are captured in a warm-up pass before the run."""
+    import torch
+    import synth
+    S, n = cfg["max_streams"], args.arrivals
+    arrive = arrival_schedule(n, S, args.gen_tokens, synth.seed_of(WORKLOAD, "arrivals"))
+    lens = synth.prompt_lengths(n, cfg["prompt"][0], cfg["prompt"][1], synth.seed_of(WORKLOAD, "arrival_lens"))
+    empty = torch.empty((args.layers, cfg["kv_heads"], 0, cfg["head_dim"]), dtype=torch.bfloat16, device="cuda")
+    # warm-up: one step at every B so that each graph is captured outside the run
+    warm = [bm.kv_slot_seed(e, empty, empty, 0) for _ in range(S)]
+    toks = torch.zeros(S, dtype=torch.int32, device="cuda")
+    outs = torch.empty(S, dtype=torch.int32, device="cuda")
+    for b in range(1, S + 1):
+        bm.decode_step(e, warm[:b], toks[:b], outs[:b], None, stream)
+    torch.cuda.synchronize()
+    for s in warm:
+        bm.kv_slot_release(e, s)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    live = []          # [slot, remaining tokens, row in cur]
+    cur = torch.zeros(n, dtype=torch.int32, device="cuda")   # next input token of each stream
+    nxt = torch.empty(S, dtype=torch.int32, device="cuda")
+    decode_ev, prefill_ev, bs = [], [], []
+    nxt_stream, step, tokens_out = 0, 0, 0
+    t_wall = time.perf_counter()
+    while nxt_stream < n or live:
+        while nxt_stream < n and arrive[nxt_stream] <= step and len(live) < S:
+            i = nxt_stream
+            prompt = synth.tokens(WORKLOAD, f"arrival_prompt{i}", lens[i], cfg["vocab"], device="cuda")
+            s = bm.kv_slot_seed(e, empty, empty, 0)
+            a, b = ev(), ev()
+            a.record(stream)
+            bm.kv_slot_prefill(e, s, prompt, cur[i:i + 1], None, stream)
+            b.record(stream)
+            prefill_ev.append((a, b, lens[i]))
+            live.append([s, args.gen_tokens, i])
+            nxt_stream += 1
+        if not live:
+            step += 1
+            continue
+        B = len(live)
+        idx = torch.tensor([r[2] for r in live], dtype=torch.int64, device="cuda")
+        inp = cur.index_select(0, idx).to(torch.int32)
+        a, b = ev(), ev()
+        a.record(stream)
+        bm.decode_step(e, [r[0] for r in live], inp, nxt[:B], None, stream)
+        b.record(stream)
+        decode_ev.append((a, b, B))
+        cur.index_copy_(0, idx, nxt[:B])
+        tokens_out += B
+        bs.append(B)
+        for r in live:
+            r[1] -= 1
+        for r in [r for r in live if r[1] == 0]:
+            bm.kv_slot_release(e, r[0])
+        live = [r for r in live if r[1] > 0]
+        step += 1
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    t_dec = sum(a.elapsed_time(b) for a, b, _ in decode_ev) / 1e3
+    t_pre = sum(a.elapsed_time(b) for a, b, _ in prefill_ev) / 1e3
+    hist = {}
+    for b in bs:
+        hist[b] = hist.get(b, 0) + 1
+    return {"streams": n, "gen_tokens": args.gen_tokens, "decode_steps": len(bs), "decode_tokens": tokens_out,
+            "decode_tok_s": round(world * tokens_out / t_dec, 1), "decode_s": round(t_dec, 3),
+            "B_mean": round(sum(bs) / len(bs), 2), "B_min": min(bs), "B_max": max(bs),
+            "prompt_tokens": sum(lens), "prefill_tok_s": round(world * sum(lens) / t_pre, 1),
+            "prefill_s": round(t_pre, 3), "wall_s": round(wall, 2),
+            "schedule": "seeded arrivals (p=0.35 per step, bursts), prompts U[16,512] ingested on arrival, "
+                        f"{args.gen_tokens} greedy tokens each, at most {S} live"}
+
+
+def kernel_table(bm, e, slots, cur, stream, Bs, peak, steps=2):
+    """Per-kernel CUDA-event times of eager steps at each B of Bs, with the
+    algorithmic GB/s and their fraction of the measured copy bandwidth."""
+    import torch
+    out = {}
+    for B in Bs:
+        if B > len(slots):
+            continue
+        c, n = cur[:B].clone(), torch.empty(B, dtype=torch.int32, device="cuda")
+        acc = {}
+        for _ in range(steps):
+            for k in bm.bm_engine_profile_step(e, slots[:B], c, n, stream):
+                p = acc.setdefault(k["name"], [0, 0.0, 0.0])
+                p[0] += k["launches"]
+                p[1] += k["ms"]
+                p[2] += k["bytes"]
+            c, n = n, c
+        rows = {}
+        for name, (launches, ms, byts) in sorted(acc.items(), key=lambda kv: -kv[1][1]):
+            gbs = byts / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+            rows[name] = {"us_per_launch": round(1e3 * ms / launches, 2), "GB_per_s": round(gbs, 1),
+                          "frac_hbm": round(gbs / peak, 3)}
+        out[str(B)] = rows
+    return out
+
+
+def prompt_gemm_sweep(bm, Ms, peak_tflops, reps=20):
+    """The prompt-length W4A16 GEMM (w4_gemm_prompt_tc) on the QKV shape
+    (N 5120, K 2048, g 64) for each M: CUDA-event time per launch (each launch
+    timed alone after warm-up, weights L2-resident after the first), the
+    achieved TFLOP/s (2 M N K per launch) and its fraction of the measured
+    dense bf16 peak (fp16 runs at the same nominal rate)."""
+    import torch
+    import synth
+    N, K, g = 5120, 2048, 64
+    raw = synth.normal((N, K), 0.02, synth.seed_of("bench", "prompt_gemm", N, K), "cuda")
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((N, K // g), dtype=torch.float16, device="cuda")
+    bm.bm_w4_quantize(raw, N, K, g, packed, scales)
+    wm = torch.empty_like(packed)
+    sm = torch.empty((N * (K // g) // 2,), dtype=torch.int32, device="cuda")
+    bm.bm_w4_repack_mma(packed, scales, N, K, g, wm, sm)
+    X = synth.normal((max(Ms), K), 1.0, synth.seed_of("bench", "prompt_gemm_x"), "cuda").half()
+    out = {}
+    for M in Ms:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            bm.w4_gemm_prompt_tc(wm, sm, X[:M], Y, None, M, N, K, g)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record()
+        for _ in range(reps):
+            bm.w4_gemm_prompt_tc(wm, sm, X[:M], Y, None, M, N, K, g)
+        t1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * t0.elapsed_time(t1) / reps
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        out[str(M)] = {"us": round(us, 2), "TFLOP_s": round(tf, 1), "frac_bf16_peak": round(tf / peak_tflops, 3)}
+    return {"shape": f"N {N} x K {K}, g {g}", "peak_tflops": peak_tflops, "by_M": out}
+
+
+def attention_long(bm, peak_gbs, reps=20):
+    """The step's fused attention kernel at the slot-attention workload's
+    lengths (16 slots of an 8192-position arena, 32 q / 4 kv heads of 128,
+    lengths U[1, 8192]) through bm_engine_attention: CUDA-event time per
+    launch (the launch rewrites each slot's position len with the same k, v,
+    so repeats are identical) and the K/V bytes attended per second against
+    the measured copy bandwidth.  The arena (1.07 GB) is far larger than L2,
+    but a launch reads only the attended positions (~270 MB)."""
+    import torch
+    import synth
+    S, cap, qh, kvh, d = 16, 8192, 32, 4, 128
+    cfg = {"hidden": 512, "q_heads": qh, "kv_heads": kvh, "head_dim": d, "experts": 8, "top_k": 2, "ffn": 256,
+           "group": 32, "vocab": 64, "layers": 1, "rope_base": 1e4, "rms_eps": 1e-6, "max_streams": S,
+           "ctx_cap": cap, "renorm_topk": 1, "kernel_policy": 3, "use_graph": 0}
+    e = bm.bm_engine_create(cfg)
+    try:
+        lens = synth.prompt_lengths(S, 1, cap - 1, synth.seed_of("slot_attention", "bench_lens"))
+        slots = []
+        for i, L in enumerate(lens):
+            k = synth.normal_bf16((1, kvh, L, d), 1.0, synth.seed_of("slot_attention", "bk", i, L), "cuda")
+            v = synth.normal_bf16((1, kvh, L, d), 1.0, synth.seed_of("slot_attention", "bv", i, L), "cuda")
+            slots.append(bm.kv_slot_seed(e, k, v, L))
+            del k, v
+        qkv = synth.normal_bf16((S, (qh + 2 * kvh) * d), 1.0, synth.seed_of("slot_attention", "bqkv"), "cuda")
+        out = torch.empty((S, qh, d), dtype=torch.float16, device="cuda")
+        for _ in range(3):
+            bm.bm_engine_attention(e, 0, slots, qkv, out)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record()
+        for _ in range(reps):
+            bm.bm_engine_attention(e, 0, slots, qkv, out)
+        t1.record()
+        torch.cuda.synchronize()
+        bm.bm_engine_sync(e)
+        us = 1e3 * t0.elapsed_time(t1) / reps
+        byts = sum((L + 1) * kvh * d * 2 * 2 for L in lens)
+        gbs = byts / (us * 1e-6) / 1e9
+        return {"streams": S, "kv_len_mean": round(sum(lens) / S, 1), "us": round(us, 2),
+                "kv_MB": round(byts / 1e6, 1), "GB_per_s": round(gbs, 1), "frac_hbm": round(gbs / peak_gbs, 3)}
+    finally:
+        bm.bm_engine_destroy(e)
+
+
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
 
 
 # ---------------------------------------------------------------- oracle arm
@@ -520,12 +780,50 @@ def run_reference(args, world, rank, budget_s=150.0):
             "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "wall_s": round(wall, 1), "sample_streams": b}
+            "wall_s": round(wall, 1), "sample_streams": b,
+            "projection": (f"value and ms_per_step are projected: each step times ONE decoder layer of {b} streams "
+                           f"and the output projection, and scales the layer time to {args.layers} layers; "
+                           f"the {args.steps} steps took {wall:.1f} s of wall time")}
+
+
+def tc_probe():
+    """SM cycles per tcgen05 MMA of M 128 x N x K 16 (kind::f16) issued back to
+    back by one thread into one accumulator, for N, the A source and the
+    shared-memory operand layout (bm_probe_tcgen05_mma)."""
+    import torch
+    import bit_moe_decode_w4a16_gb300 as bm
+    torch.cuda.init()
+    bm.build()
+    rows = []
+    for a_tmem in (1, 0):
+        for swz in (0, 1):
+            for n in (16, 32, 64, 128, 256):
+                bm.bm_probe_tcgen05_mma(n, a_tmem, swz, 64)   # warm
+                issue, done = bm.bm_probe_tcgen05_mma(n, a_tmem, swz, 1024)
+                macs = 128 * n * 16
+                rows.append({"N": n, "A": "tmem" if a_tmem else "smem", "layout": "sw128" if swz else "none",
+                             "issue_cycles": round(issue, 1), "complete_cycles": round(done, 1),
+                             "MAC_per_cycle": round(macs / done, 1)})
+    for n in (16, 128):
+        bm.bm_probe_tcgen05_mma(n, 1, 0, 64, 1)
+        issue, done = bm.bm_probe_tcgen05_mma(n, 1, 0, 256, 1)
+        rows.append({"N": n, "A": "tmem", "layout": "none", "roundtrip": True, "issue_cycles": round(issue, 1),
+                     "complete_cycles": round(done, 1), "stage_roundtrip_cycles": round(4 * done, 1)})
+    return {"probe": "tcgen05.mma.cta_group::1.kind::f16, M 128 x N x K 16, 1024 stages of 4 MMAs, one accumulator "
+                     "(roundtrip rows: 256 stages, each committed and waited for)",
+            "rows": rows}
 
 
 def main():
     args = parse()
     world, rank, local = dist_env()
+    if args.tc_probe:
+        if rank == 0:
+            import bit_moe_decode_w4a16_gb300 as bm
+            out = tc_probe()
+            out["prompt_gemm"] = prompt_gemm_sweep(bm, [int(x) for x in args.gemm_sweep.split(",") if x], bf16_peak())
+            print(json.dumps(out), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank)), flush=True)

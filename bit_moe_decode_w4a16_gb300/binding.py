@@ -35,7 +35,7 @@ class bm_config(ctypes.Structure):
                                             "ffn", "group", "vocab", "layers")] + \
                [("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float)] + \
                [(n, ctypes.c_int) for n in ("max_streams", "ctx_cap", "renorm_topk", "kernel_policy",
-                                            "use_graph")]
+                                            "use_graph", "prefill_tc")]
 
 
 _P = ctypes.c_void_p
@@ -96,6 +96,7 @@ def lib():
             "w4_gemm_batched_tc": ([V, V, V, V, V, I, I, I, I, V], S),
             "bm_w4_repack_mma": ([V, V, I, I, I, V, V, V], S),
             "w4_gemm_batched_mma": ([V, V, V, V, V, I, I, I, I, V], S),
+            "w4_gemm_prompt_tc": ([V, V, V, V, V, I, I, I, I, V], S),
             "moe_grouped_w4": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V, SZ, V], S),
             "moe_grouped_w4_noalloc": ([ctypes.POINTER(bm_moe_weights), V, V, V, V, V, I, V], S),
             "bm_moe_noalloc_max_bytes": ([], SZ),
@@ -104,6 +105,7 @@ def lib():
             "bm_engine_profile_step": ([V, I, V, V, V, ctypes.POINTER(bm_kernel_profile), I, PI, V], S),
             "bm_w4_quantize": ([V, I, I, I, V, V, V], S),
             "bm_engine_moe": ([V, I, V, V, V, V, I, V], S),
+            "bm_probe_tcgen05_mma": ([I, I, I, I, I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], S),
             "bm_engine_attention": ([V, I, V, V, V, I, V], S),
             "bm_engine_read_hidden": ([V, I, V, V], S),
             "bm_engine_test_drop_expert_item": ([V, I], S),
@@ -264,6 +266,10 @@ def w4_gemm_batched_mma(Wm, Sm, X, Y, R, M, N, K, g, stream=None):
     _check(lib().w4_gemm_batched_mma(ptr(Wm), ptr(Sm), ptr(X), ptr(Y), ptr(R), M, N, K, g, stream_handle(stream)))
 
 
+def w4_gemm_prompt_tc(Wm, Sm, X16, Y, R, M, N, K, g, stream=None):
+    _check(lib().w4_gemm_prompt_tc(ptr(Wm), ptr(Sm), ptr(X16), ptr(Y), ptr(R), M, N, K, g, stream_handle(stream)))
+
+
 def bm_moe_workspace_bytes(B, experts, top_k, hidden, ffn):
     return lib().bm_moe_workspace_bytes(B, experts, top_k, hidden, ffn)
 
@@ -333,6 +339,14 @@ def bm_engine_read_hidden(e, B, out, stream=None):
 
 def bm_engine_test_drop_expert_item(e, item):
     _check(lib().bm_engine_test_drop_expert_item(e, int(item)))
+
+
+def bm_probe_tcgen05_mma(n, a_in_tmem, swizzle128, iters, roundtrip=0):
+    """SM cycles per tcgen05 MMA (M 128 x N n x K 16): (to issue, to complete)."""
+    a, b = ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().bm_probe_tcgen05_mma(int(n), int(a_in_tmem), int(swizzle128), int(iters), int(roundtrip),
+                                      ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def bm_w4_quantize(W, N, K, g, packed, scales, stream=None):

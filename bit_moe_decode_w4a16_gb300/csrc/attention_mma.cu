@@ -83,7 +83,7 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, 
 
 // Position of row b: the slot's length, plus b for the rows of a prompt.
 __device__ __forceinline__ int row_position(const AttnFusedArgs& a, int b, int slot) {
-  return a.ar.len[slot] + (a.prefill ? b : 0);
+  return a.ar.len[slot] + (a.prefill ? a.row0 + b : 0);
 }
 
 template <int D>
@@ -417,7 +417,7 @@ cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool
 }
 
 cudaError_t launch_append_rows(const AttnFusedArgs& a, cudaStream_t st, bool pdl) {
-  if (!attention_fused_supports(a.ar, a.qh) || a.B < 1 || a.B > kMaxBatch) return cudaErrorInvalidValue;
+  if (!attention_fused_supports(a.ar, a.qh) || a.B < 1 || a.B > 65535) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)a.B, (unsigned)a.ar.kvh);
   if (a.ar.d == 128) return launch_k(pdl, k_append_rows<128>, grid, dim3(64), 0, st, a);
   return launch_k(pdl, k_append_rows<64>, grid, dim3(64), 0, st, a);

@@ -55,6 +55,7 @@ bm_status ensure_attributes() {
   BM_CUDA(init_misc_attributes(), "kernel attributes (lm_head)");
   BM_CUDA(init_tc_attributes(), "kernel attributes (tensor-core projections)");
   BM_CUDA(init_mma_attributes(), "kernel attributes (warp-MMA projections)");
+  BM_CUDA(init_prefill_attributes(), "kernel attributes (prompt-length tensor-core GEMMs)");
   g_attr_devices.insert(dev);
   return BM_OK;
 }
@@ -134,11 +135,21 @@ struct bm_engine {
   int32_t* d_u_log = nullptr;   // [layers] active experts of the last step, per layer
   float* tc_part = nullptr;     // split-K partial sums of the tensor-core projections
   int* tc_counters = nullptr;   // split-K arrival counters (zero between launches)
+  size_t tc_counter_count = 0;
   std::vector<cudaEvent_t> prof_events;
   cudaStream_t cap_stream = nullptr;
   std::map<int, cudaGraphExec_t> graphs;   // decode graphs by B; prompt blocks under negative keys
   std::map<int, int> graph_kernels;         // kernels in each graph
   int test_drop_item = -1;                  // failure-detection tests: an expert item whose copies are not issued
+  // prompt ingestion on the tensor cores (prefill_tc): rows per block and its scratch
+  int pf_rows = 0;
+  void* pf_mem = nullptr;
+  bf16 *pf_x = nullptr, *pf_xn = nullptr, *pf_qkv = nullptr, *pf_h = nullptr;
+  __half* pf_attn = nullptr;
+  void* pf_moe = nullptr;
+  float* pf_part = nullptr;
+  unsigned int* pf_acnt = nullptr;
+  int32_t *pf_slots = nullptr, *pf_tokens = nullptr;
   bm_stats st{};
 
   bm_engine(const bm_config& c) : cfg(c), slots(c.max_streams, c.ctx_cap) {}
@@ -288,6 +299,86 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
   }
   if ((err = launch_lm_mma(la, s)) != cudaSuccess) return err;
   mark(KT_LM_HEAD);
+  ++n;
+  if (launches) *launches = n;
+  return cudaSuccess;
+}
+
+// Prompt rows on the tensor cores: P rows of one slot (e->pf_slots holds P
+// copies of it, e->pf_tokens the tokens) at positions len .. len + P - 1,
+// each layer's dense projections and experts as prompt-length tcgen05 GEMMs,
+// the rows' k and v appended first, attention in launches of up to 128 rows
+// (row j attends to positions 0 .. len + j), the combine with the next
+// RMSNorm; then the slot's length moves by P, through the output projection
+// of the last row when `last`.
+cudaError_t enqueue_prefill_tc(bm_engine* e, int P, bool last, cudaStream_t s, int* launches) {
+  const bm_config& c = e->cfg;
+  const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
+  cudaError_t err;
+  int n = 0;
+  auto attn_nw = [&](int l) -> const bf16* { return e->L[l].has_attn_norm ? e->L[l].attn_norm_buf : nullptr; };
+  auto u32 = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
+  __half* xn16 = reinterpret_cast<__half*>(e->pf_xn);
+  if ((err = launch_embed_norm(e->embed, c.vocab, H, e->pf_tokens, e->pf_x, attn_nw(0), c.rms_eps, xn16, P, chk_of(e),
+                               s, false)) != cudaSuccess)
+    return err;
+  ++n;
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerW& w = e->L[l];
+    PrefillGemmArgs q{};
+    q.W = w.wqkv; q.S = u32(w.wqkv_s); q.rows = e->qkv_rows; q.K = H; q.g = g;
+    q.X = xn16; q.ldx = H; q.ntok = P; q.Y = e->pf_qkv; q.ldy = e->qkv_rows; q.err = e->d_err;
+    if ((err = launch_prefill_dense(q, s)) != cudaSuccess) return err;
+    AttnFusedArgs fa{e->arena, l, e->pf_slots, e->pf_qkv, e->qkv_rows, c.q_heads, e->d_rope, e->pf_attn, e->pf_part,
+                     (c.ctx_cap + kAttnChunk - 1) / kAttnChunk, e->pf_acnt, P, chk_of(e), 1, 0};
+    if ((err = launch_append_rows(fa, s, false)) != cudaSuccess) return err;
+    n += 2;
+    for (int r0 = 0; r0 < P; r0 += 128) {
+      AttnFusedArgs fb = fa;
+      fb.row0 = r0;
+      fb.B = P - r0 < 128 ? P - r0 : 128;
+      fb.slots = e->pf_slots + r0;
+      fb.qkv = e->pf_qkv + (size_t)r0 * e->qkv_rows;
+      fb.out = e->pf_attn + (size_t)r0 * qd;
+      if ((err = launch_attention_fused(fb, s, false)) != cudaSuccess) return err;
+      ++n;
+    }
+    PrefillGemmArgs o{};
+    o.W = w.wo; o.S = u32(w.wo_s); o.rows = H; o.K = qd; o.g = g;
+    o.X = e->pf_attn; o.ldx = qd; o.ntok = P; o.Res = e->pf_x; o.ldr = H; o.Y = e->pf_h; o.ldy = H; o.err = e->d_err;
+    if ((err = launch_prefill_dense(o, s)) != cudaSuccess) return err;
+    MoeArgs ma{P, c.experts, c.top_k, H, F, g, c.renorm_topk,
+               w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
+               e->pf_h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->pf_h, e->pf_x, nullptr, 1};
+    const MoeBufs mb = moe_carve(e->pf_moe, P, c.experts, c.top_k, H, F);
+    if ((err = launch_moe_route_wide(ma, mb, s)) != cudaSuccess) return err;
+    PrefillGemmArgs gu{};
+    gu.W = w.wg; gu.S = u32(w.wg_s); gu.rows = 2 * F; gu.K = H; gu.g = g; gu.X = mb.xn; gu.ldx = H;
+    gu.n_active = mb.n_active; gu.active_e = mb.active_e; gu.active_off = mb.active_off; gu.row_map = mb.pair_token;
+    gu.experts = c.experts; gu.w_expert_stride = (size_t)2 * F * H / 2; gu.s_expert_stride = (size_t)F * (H / g);
+    gu.act16 = reinterpret_cast<__half*>(mb.act); gu.F = F; gu.err = e->d_err;
+    if ((err = launch_prefill_gateup(gu, P, s)) != cudaSuccess) return err;
+    PrefillGemmArgs dn{};
+    dn.W = w.wd; dn.S = u32(w.wd_s); dn.rows = H; dn.K = F; dn.g = g; dn.X = mb.act; dn.ldx = F;
+    dn.n_active = mb.n_active; dn.active_e = mb.active_e; dn.active_off = mb.active_off;
+    dn.experts = c.experts; dn.w_expert_stride = (size_t)H * F / 2; dn.s_expert_stride = (size_t)H * (F / g) / 2;
+    dn.out = mb.out; dn.H = H; dn.err = e->d_err;
+    if ((err = launch_prefill_down(dn, P, s)) != cudaSuccess) return err;
+    const bool lastl = l + 1 == c.layers;
+    const bf16* next_nw = !lastl ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
+    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->pf_xn, lastl ? 0 : 1, s, Marker(), false)) != cudaSuccess)
+      return err;
+    n += 8;   // o_proj, routing (3), gate/up, down, combine
+  }
+  if (!last) {
+    if ((err = launch_advance(e->arena.len, e->pf_slots, 1, s, P)) != cudaSuccess) return err;
+  } else {
+    LmArgs la{};
+    la.W = e->lm_head; la.V = c.vocab; la.K = H; la.X = e->pf_xn + (size_t)(P - 1) * H; la.B = 1;
+    la.logits = e->logits; la.next = e->d_next; la.len = e->arena.len; la.slots = e->pf_slots; la.advance = P;
+    la.keys = e->lm_keys; la.counter = e->lm_counter;
+    if ((err = launch_lm_mma(la, s)) != cudaSuccess) return err;
+  }
   ++n;
   if (launches) *launches = n;
   return cudaSuccess;
@@ -469,6 +560,15 @@ bm_status check_config(const bm_config& c) {
   if (c.kernel_policy == BM_POLICY_MMA && !mma_shapes_ok(c))
     return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: shapes outside the warp-MMA family (rows multiples "
                                          "of 32, reduction lengths multiples of 128 up to 4096, vocab % 16 == 0)");
+  if (c.prefill_tc) {
+    const int qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim, qd = c.q_heads * c.head_dim;
+    const bool mma_ok = c.kernel_policy == BM_POLICY_MMA || (c.kernel_policy == BM_POLICY_AUTO && mma_shapes_ok(c));
+    if (!mma_ok || !prefill_gemm_supports(qkv_rows, c.hidden, c.group) || !prefill_gemm_supports(c.hidden, qd, c.group) ||
+        !prefill_gemm_supports(2 * c.ffn, c.hidden, c.group) || !prefill_gemm_supports(c.hidden, c.ffn, c.group) ||
+        c.top_k > 16 || c.experts > 256)
+      return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: prefill_tc needs the warp-MMA family and rows that are "
+                                           "multiples of 128 with reduction lengths multiples of 128");
+  }
   if (c.kernel_policy == BM_POLICY_TC && !tc_shapes_ok(c))
     return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: shapes outside the tensor-core family (rows must be "
                                          "multiples of 128, reduction lengths multiples of 64 up to 4096)");
@@ -487,6 +587,7 @@ void free_engine(bm_engine* e) {
   if (e->wslab) cudaFree(e->wslab);
   if (e->arena_mem) cudaFree(e->arena_mem);
   if (e->scratch) cudaFree(e->scratch);
+  if (e->pf_mem) cudaFree(e->pf_mem);
   delete e;
 }
 
@@ -635,10 +736,38 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
   e->lm_counter = reinterpret_cast<unsigned int*>(sb + s_cnt.off);
   e->route_cnt = reinterpret_cast<unsigned int*>(sb + s_rcnt.off);
   e->attn_cnt = reinterpret_cast<unsigned int*>(sb + s_acnt.off);
+
   e->tc_part = tc_floats ? reinterpret_cast<float*>(sb + s_tcp.off) : nullptr;
   e->tc_counters = tc_jobs ? reinterpret_cast<int*>(sb + s_tcc.off) : nullptr;
+  e->tc_counter_count = tc_jobs;
   BM_CUDA(cudaMemset(e->scratch, 0, e->scratch_bytes), "scratch reset");
 
+  if (c.prefill_tc) {
+    // blocks of up to 512 prompt rows (4096 routed pairs)
+    const int P = 4096 / c.top_k < 512 ? 4096 / c.top_k : 512;
+    e->pf_rows = P;
+    size_t o2 = 0;
+    auto take2 = [&](size_t bytes) { size_t r = o2; o2 += al(bytes); return r; };
+    const size_t p_x = take2((size_t)P * H * 2), p_xn = take2((size_t)P * H * 2),
+                 p_qkv = take2((size_t)P * e->qkv_rows * 2), p_attn = take2((size_t)P * qd * 2),
+                 p_h = take2((size_t)P * H * 2), p_moe = take2(moe_scratch_bytes(P, E, c.top_k, H, F)),
+                 p_part = take2(attn_partial_floats(128, c.q_heads, c.ctx_cap, c.head_dim) * 4),
+                 p_acnt = take2((size_t)128 * c.kv_heads * 4), p_sl = take2((size_t)P * 4), p_tk = take2((size_t)P * 4);
+    BM_CUDA(cudaMalloc(&e->pf_mem, o2), "prompt scratch allocation");
+    char* pb = static_cast<char*>(e->pf_mem);
+    e->pf_x = reinterpret_cast<bf16*>(pb + p_x);
+    e->pf_xn = reinterpret_cast<bf16*>(pb + p_xn);
+    e->pf_qkv = reinterpret_cast<bf16*>(pb + p_qkv);
+    e->pf_attn = reinterpret_cast<__half*>(pb + p_attn);
+    e->pf_h = reinterpret_cast<bf16*>(pb + p_h);
+    e->pf_moe = pb + p_moe;
+    e->pf_part = reinterpret_cast<float*>(pb + p_part);
+    e->pf_acnt = reinterpret_cast<unsigned int*>(pb + p_acnt);
+    e->pf_slots = reinterpret_cast<int32_t*>(pb + p_sl);
+    e->pf_tokens = reinterpret_cast<int32_t*>(pb + p_tk);
+    BM_CUDA(cudaMemset(e->pf_mem, 0, o2), "prompt scratch reset");
+    e->scratch_bytes += o2;
+  }
   BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * (2 * bm_engine::kStageRing + 1) * S),
           "pinned staging allocation");
   e->h_aux = e->h_stage + 2 * bm_engine::kStageRing * S;
@@ -757,6 +886,14 @@ bm_status bm_engine_sync(bm_engine* e, void* stream) {
   BM_CUDA(cudaMemcpy(&flag, e->d_err, sizeof(int), cudaMemcpyDeviceToHost), "device check read");
   if (flag) {
     BM_CUDA(cudaMemset(e->d_err, 0, sizeof(int)), "device check reset");
+    // a kernel that stopped early may have left its arrival counters short:
+    // every counter goes back to zero so the next launches start clean
+    const size_t S = e->cfg.max_streams;
+    BM_CUDA(cudaMemset(e->route_cnt, 0, (S + 1) * 4), "counter reset");
+    BM_CUDA(cudaMemset(e->attn_cnt, 0, S * e->cfg.kv_heads * 4), "counter reset");
+    BM_CUDA(cudaMemset(e->lm_counter, 0, 4), "counter reset");
+    BM_CUDA(cudaMemset(e->lm_keys, 0, S * 8), "counter reset");
+    if (e->tc_counters) BM_CUDA(cudaMemset(e->tc_counters, 0, e->tc_counter_count * 4), "counter reset");
     static const char* what[] = {"", "an out-of-range slot id was skipped", "an out-of-range position was skipped",
                                  "an out-of-range token id was skipped",
                                  "a tensor-core projection's pipeline wait timed out",
@@ -1036,6 +1173,24 @@ bm_status kv_slot_prefill(bm_engine* e, int slot, int n_tokens, const int32_t* t
     return set_error(BM_ERR_UNSUPPORTED, "kv_slot_prefill: needs the warp-MMA kernel family and fused attention");
   if ((long)e->slots.length(slot) + n_tokens > c.ctx_cap)
     return set_error(BM_ERR_CTX_CAP, "kv_slot_prefill: the prompt does not fit the context cap");
+  if (c.prefill_tc) {
+    const int T = e->pf_rows;
+    for (int i = 0; i < n_tokens; i += T) {
+      const int b = n_tokens - i < T ? n_tokens - i : T;
+      BM_CUDA(cudaMemcpyAsync(e->pf_tokens, tokens + i, sizeof(int32_t) * b, cudaMemcpyDefault, s), "prompt tokens");
+      BM_CUDA(launch_fill_i32(e->pf_slots, slot, b, s), "prompt slots");
+      int n = 0;
+      const cudaError_t ce = enqueue_prefill_tc(e, b, i + b == n_tokens, s, &n);
+      if (ce != cudaSuccess) return set_error(BM_ERR_CUDA, std::string("kv_slot_prefill launch: ") + cudaGetErrorString(ce));
+      e->st.kernel_launches += n + 1;
+    }
+    BM_CUDA(cudaMemcpyAsync(next_token, e->d_next, sizeof(int32_t), cudaMemcpyDefault, s), "next token copy");
+    if (logits)
+      BM_CUDA(cudaMemcpyAsync(logits, e->logits, sizeof(float) * (size_t)c.vocab, cudaMemcpyDefault, s), "logits copy");
+    e->slots.advance_by(slot, n_tokens);
+    e->st.tokens += n_tokens;
+    return bm::ok();
+  }
   const int T = c.max_streams;
   std::vector<int32_t> rows(T, slot);
   for (int i = 0; i < n_tokens; i += T) {
@@ -1170,6 +1325,22 @@ bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint1
   a.X = X; a.ldx = K; a.ntok = M; a.x_bf16 = 1;
   a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
   BM_CUDA(launch_w4_mma_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_batched_mma launch");
+  return bm::ok();
+}
+
+bm_status w4_gemm_prompt_tc(const uint8_t* Wm, const uint32_t* Sm, const uint16_t* X16, uint16_t* Y,
+                            const uint16_t* R, int M, int N, int K, int g, void* stream) {
+  if (!Wm || !Sm || !X16 || !Y) return set_error(BM_ERR_INVALID_ARG, "w4_gemm_prompt_tc: null pointer");
+  if (M < 1 || !mma_supports(N, K, g) || !prefill_gemm_supports(N, K, g))
+    return set_error(BM_ERR_INVALID_ARG, "w4_gemm_prompt_tc: need M >= 1, N % 128 == 0, K % 128 == 0, K <= 4096, "
+                                         "g in {32, 64, 128}, K % g == 0");
+  bm_status st = ensure_attributes();
+  if (st != BM_OK) return st;
+  PrefillGemmArgs a{};
+  a.W = Wm; a.S = Sm; a.rows = N; a.K = K; a.g = g;
+  a.X = X16; a.ldx = K; a.ntok = M;
+  a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
+  BM_CUDA(launch_prefill_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_prompt_tc launch");
   return bm::ok();
 }
 

@@ -93,6 +93,11 @@ cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t 
 // tok_cnt [B] and all_cnt [1] are zero before the launch and left zero.
 cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned int* tok_cnt, unsigned int* all_cnt,
                                   cudaStream_t st, const Marker& mark, bool pdl = false);
+// Routing of a prompt block of up to 4096 (row, rank) pairs: router logits
+// with the RMSNorm (bufs.xn written, fp16 with xn_f16), top-k per row, and the
+// stable grouping by expert (pair_token, pos_of, n_active, active_e,
+// active_off; no job list).  Three launches.
+cudaError_t launch_moe_route_wide(const MoeArgs& a, const MoeBufs& b, cudaStream_t st);
 // The combine with the next RMSNorm fused: also xn[b] = RMSNorm(y[b]) * nw
 // (nw null = ones; a.eps), rounded to bf16 and stored as fp16 (xn_f16) or
 // bf16.  H <= 8192.
@@ -209,6 +214,44 @@ cudaError_t launch_lm_mma(const LmArgs& a, cudaStream_t st);
 bool lm_mma_supports(int V, int K, int B);
 cudaError_t init_mma_attributes();
 
+// ---------------------------------------------------------------- prompt-length tcgen05 GEMMs
+// W4A16 GEMMs over the rows of a prompt block on the tcgen05 tensor cores,
+// reading the weights in the warp-MMA layout; fp16 activations; the group
+// scale is folded into fp16 weights (one rounding of q x s).  See
+// prefill_tc.cu.
+struct PrefillGemmArgs {
+  const uint8_t* W;          // mma layout (whole bank for the experts)
+  const uint32_t* S;         // mma-layout scales
+  int rows, K, g;            // rows of one matrix (one expert for the banks); rows % 128 == 0
+  const void* X;             // fp16 activation rows [.][ldx]
+  int ldx;
+  int ntok;                  // dense: rows of X
+  const bf16* Res;           // dense: residual [ntok][ldr] or null
+  int ldr;
+  bf16* Y;                   // dense: output [ntok][ldy]
+  int ldy;
+  const int32_t* n_active;   // experts: the grouping of the routing kernels
+  const int32_t* active_e;
+  const int32_t* active_off;
+  const int32_t* row_map;    // gate/up: activation row of each sorted pair
+  int experts;               // grid bound of the expert launches
+  size_t w_expert_stride;    // bytes of one expert's matrix
+  size_t s_expert_stride;    // 32-bit scale words of one expert's matrix
+  __half* act16;             // gate/up output [pairs][F], bf16-rounded values in fp16
+  int F;
+  float* out;                // down output [pairs][H]
+  int H;
+  int* err;                  // device error flag or null
+};
+bool prefill_gemm_supports(int rows, int K, int g);
+cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, cudaStream_t st);
+// max_rows_per_expert bounds the grid (an expert has at most one row per token)
+cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st);
+cudaError_t launch_prefill_down(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st);
+cudaError_t init_prefill_attributes();
+// p[0..n) = value
+cudaError_t launch_fill_i32(int32_t* p, int32_t value, int n, cudaStream_t st);
+
 // ---------------------------------------------------------------- attention
 struct AttnArena {
   bf16* K;        // [layers][S][kvh][cap][d]
@@ -255,7 +298,8 @@ struct AttnFusedArgs {
   unsigned int* counters;
   int B;
   DevCheck chk;
-  int prefill;          // rows of one slot at positions len + b; k/v appended beforehand
+  int prefill;          // rows of one slot at positions len + row0 + b; k/v appended beforehand
+  int row0;             // prefill: position offset of this launch's first row
 };
 bool attention_fused_supports(const AttnArena& ar, int qh);
 cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool pdl = false);

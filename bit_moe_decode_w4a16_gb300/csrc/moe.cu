@@ -65,12 +65,16 @@ __device__ __forceinline__ float router_fma(const float* xs, int H, int k0, cons
 // The router logits of one token and kRouterExperts experts (one CTA); the
 // dependency wait of a programmatic launch is taken inside, after the
 // weight prefetch.
+// EPC = experts per CTA: 16 (two per warp) or 8 (one per warp, for small
+// batches: twice the CTAs and no second router row on the dependency chain).
+// A logit's arithmetic does not depend on EPC.
+template <int EPC = kRouterExperts>
 __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, float* xs) {
   __shared__ float red[kRouterWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tkn = blockIdx.y, H = a.H;
   float4 w4[kRouterStrips];
-  const int e_first = blockIdx.x * kRouterExperts + warp;
+  const int e_first = blockIdx.x * EPC + warp;
   if (e_first < a.E) router_load(a.wr + (size_t)e_first * H, H, lane * 4, w4);
   pdl_wait();
   const bf16* x = a.x + (size_t)tkn * H;
@@ -105,8 +109,8 @@ __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, f
     }
   }
   __syncthreads();
-  for (int ei = warp; ei < kRouterExperts; ei += kRouterWarps) {
-    const int e = blockIdx.x * kRouterExperts + ei;
+  for (int ei = warp; ei < EPC; ei += kRouterWarps) {
+    const int e = blockIdx.x * EPC + ei;
     if (e >= a.E) break;
     const float* wr = a.wr + (size_t)e * H;
     float acc = 0.f;
@@ -285,6 +289,7 @@ __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
 // are made visible with __threadfence before each arrival, and the late
 // readers load through L2.  The counters are zero before the launch and are
 // left zero.  The result is the same as k_router + k_topk_sort.
+template <int EPC>
 __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsigned int* tok_cnt,
                                                      unsigned int* all_cnt) {
   extern __shared__ __align__(16) float xs[];   // [H] normalised row
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsig
   __shared__ int off_s[257];
   __shared__ int flag_s;
   const int tkn = blockIdx.y, warp = threadIdx.x >> 5;
-  router_cta(a, b, xs);   // takes the dependency wait after its weight prefetch
+  router_cta<EPC>(a, b, xs);   // takes the dependency wait after its weight prefetch
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) flag_s = atomicAdd(&tok_cnt[tkn], 1u) == gridDim.x - 1;
@@ -314,6 +319,81 @@ __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsig
   __syncthreads();
   group_pairs(a, b, ids_s, cnt_s, off_s, rank_s);
   if (threadIdx.x == 0) *all_cnt = 0u;
+}
+
+// ---- routing of a prompt block (hundreds of rows, up to kMaxPairsWide
+// pairs): k_router, then one warp per row for its top-k, then one CTA groups
+// the pairs by expert.  The same top-k as the decode step; the grouping
+// computes the same offsets, ranks and active list with plain scans (no job
+// list: the prompt-length expert GEMMs take an expert's rows directly).
+constexpr int kMaxPairsWide = 4096;
+
+__global__ void __launch_bounds__(256) k_topk_rows(MoeArgs a, MoeBufs b) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < a.B) topk_warp(a, b, t, false, nullptr);
+}
+
+__global__ void __launch_bounds__(1024) k_group_wide(MoeArgs a, MoeBufs b) {
+  __shared__ int ids_s[kMaxPairsWide];
+  __shared__ int rank_s[kMaxPairsWide];
+  __shared__ int cnt_s[256];
+  __shared__ int off_s[257];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, k = a.k, P = a.B * a.k;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) ids_s[p] = b.topk_ids[p];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  __syncthreads();
+  if (warp == 0) {
+    // stable ranks, 32 pairs at a time in pair order (as group_pairs)
+    const unsigned lt = (1u << lane) - 1u;
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + lane;
+      const int e = p < P ? ids_s[p] : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int before = p < P ? cnt_s[e] : 0;
+      __syncwarp();
+      if (p < P) {
+        rank_s[p] = before + __popc(same & lt);
+        if ((same & lt) == 0u) cnt_s[e] = before + __popc(same);
+      }
+      __syncwarp();
+    }
+    // exclusive scans of the counts and the active flags, 32 experts at a time
+    int run_off = 0, run_u = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? cnt_s[e] : 0, act = c > 0;
+      int ic = c, ia = act;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int c2 = __shfl_up_sync(0xffffffffu, ic, o), a2 = __shfl_up_sync(0xffffffffu, ia, o);
+        if (lane >= o) { ic += c2; ia += a2; }
+      }
+      if (e < E) {
+        const int off = run_off + ic - c, u = run_u + ia - act;
+        off_s[e] = off;
+        if (act) {
+          b.active_e[u] = e;
+          b.active_off[u] = off;
+        }
+      }
+      run_off += __shfl_sync(0xffffffffu, ic, 31);
+      run_u += __shfl_sync(0xffffffffu, ia, 31);
+    }
+    if (lane == 0) {
+      off_s[E] = run_off;
+      b.active_off[run_u] = run_off;
+      *b.n_active = run_u;
+      *b.n_jobs = 0;
+      if (a.u_log) *a.u_log = run_u;
+    }
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int pos = off_s[ids_s[p]] + rank_s[p];
+    b.pair_token[pos] = p / k;
+    b.pos_of[p] = pos;
+  }
 }
 
 // Gate/up: a lane group computes rows f of W_g[e] and W_u[e] together.
@@ -595,10 +675,32 @@ cudaError_t launch_moe_route(const MoeArgs& a, const MoeBufs& b, cudaStream_t st
 cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned int* tok_cnt, unsigned int* all_cnt,
                                   cudaStream_t st, const Marker& mark, bool pdl) {
   if (a.B * a.k > kMaxPairs || a.E > 256 || a.k > 16 || !tok_cnt || !all_cnt) return cudaErrorInvalidValue;
-  const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
-  cudaError_t err = launch_k(pdl, k_route_fused, rgrid, dim3(256), sizeof(float) * a.H, st, a, b, tok_cnt, all_cnt);
+  // up to 16 rows: one expert per warp, so that the grid covers more SMs and
+  // each warp has a single router row to fetch
+  cudaError_t err;
+  if (a.B <= 16) {
+    const dim3 rgrid((a.E + kRouterWarps - 1) / kRouterWarps, a.B);
+    err = launch_k(pdl, k_route_fused<kRouterWarps>, rgrid, dim3(256), sizeof(float) * a.H, st, a, b, tok_cnt,
+                   all_cnt);
+  } else {
+    const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
+    err = launch_k(pdl, k_route_fused<kRouterExperts>, rgrid, dim3(256), sizeof(float) * a.H, st, a, b, tok_cnt,
+                   all_cnt);
+  }
   if (err == cudaSuccess) mark(KT_ROUTER);
   return err;
+}
+
+cudaError_t launch_moe_route_wide(const MoeArgs& a, const MoeBufs& b, cudaStream_t st) {
+  if (a.B * a.k > kMaxPairsWide || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
+  const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
+  k_router<<<rgrid, 256, sizeof(float) * a.H, st>>>(a, b);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  k_topk_rows<<<(a.B + 7) / 8, 256, 0, st>>>(a, b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  k_group_wide<<<1, 1024, 0, st>>>(a, b);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_moe_combine(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, const Marker& mark) {

@@ -1,0 +1,351 @@
+// Prompt-length W4A16 GEMMs on the 5th-generation tensor cores (tcgen05) for
+// prompt ingestion: the dense QKV and output projections over all P rows of
+// a prompt, and the grouped expert gate/up (SiLU fused) and down projections
+// over each active expert's rows.  At P = hundreds of rows each weight tile
+// meets enough rows for the contraction to be compute-dense, which the decode
+// kernels (at most a few dozen rows) never see.
+//
+// A CTA owns a tile of 128 weight rows (MMA M, TMEM lanes) and up to 128 rows
+// of activations (MMA N) over the whole K, in stages of 64:
+//   - sixteen producer warps in four groups; group g makes stages g, g + 4,
+//     ..., one weight row per lane of its four warps: the thread reads the
+//     row's int4 codes of the stage straight from the warp-MMA layout the
+//     engine keeps (64 contiguous bytes: the four lane slots of the row's
+//     8-row group), turns them into the fp16 products q x s with the row's
+//     group scale (one rounding: the scale is folded into the weights here,
+//     unlike the decode kernels, which scale exact fp32 group sums), and
+//     writes them into the stage's TMEM slot as the MMA's A operand; the
+//     group also copies the stage's 64-wide slice of the activation rows into
+//     shared memory (cp.async, a round ahead, gathered through a row map for
+//     the experts) as the B operand, in the no-swizzle K-major core-matrix
+//     layout;
+//   - one elected lane of a seventeenth warp issues each stage's four MMAs
+//     (M 128 x N x K 16, fp16 in, fp32 accumulated in tensor memory) and
+//     commits them to the slot's `done` barrier.
+// Twelve slots rotate; a group refills a slot once the MMAs of the stage that
+// used it have completed.  One stage takes a group longer than the MMAs take
+// to run it, so the four groups work on four stages at once.  Every mbarrier
+// wait is bounded; a wait that gives up sets the error flag and the kernel
+// runs on to its end (every later wait is bounded too), so nothing can hang.
+// After the last stage the producers read the accumulators back with
+// tcgen05.ld and write the epilogue: bf16 output (+ residual), SiLU(gate) x
+// up as bf16-rounded fp16, or fp32 expert outputs for the combine.
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace bm {
+
+namespace {
+
+constexpr int kPfM = 128;              // weight rows per CTA
+constexpr int kPfN = 128;              // activation rows per CTA
+constexpr int kPfSlots = 12;           // stages in flight: TMEM A slots and shared-memory B tiles
+constexpr int kPfGroups = 4;           // producer groups; group g makes stages g, g + 4, ...
+constexpr int kPfProducers = kPfM * kPfGroups;   // a group: 4 warps, one weight row per lane
+constexpr int kPfThreads = kPfProducers + 32;   // producers + the MMA warp
+constexpr uint32_t kPfTmemCols = 512;  // accumulator [0, 128) + 12 A slots of 32 columns
+constexpr uint32_t kPfWaitLimit = 1u << 18;   // polls of ~3.7 us: a wait gives up after about a second
+constexpr int kPfBTile = kPfN * 128;   // bytes of one stage's B tile (N rows x 64 fp16)
+// dynamic shared memory per CTA: the B tiles of every slot (192 KB: one CTA per
+// SM, which also holds all 512 TMEM columns)
+constexpr int kPfSmem = kPfSlots * kPfBTile;
+static_assert(kPfN + kPfSlots * 32 <= (int)kPfTmemCols, "TMEM holds the accumulator and the A slots");
+
+enum PfMode { PF_DENSE = 0, PF_GATEUP = 1, PF_DOWN = 2 };
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+template <int MODE, int G>
+__global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];   // kPfSlots B tiles
+  __shared__ __align__(8) uint64_t full_bar[kPfSlots];
+  __shared__ __align__(8) uint64_t done_bar[kPfSlots];
+  __shared__ __align__(8) uint64_t final_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ const void* row_src[kPfN];   // activation row of each B row (null: zero)
+  static_assert(G == 32 || G == 64 || G == 128, "group size");
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int K = a.K, NC = K / 64, NG = K / G;
+  const uint8_t* W = a.W;
+  const uint32_t* S = a.S;
+  int n0, ntok;   // first activation row (dense: token; experts: sorted pair) and count
+  if (MODE == PF_DENSE) {
+    n0 = blockIdx.y * kPfN;
+    ntok = min(kPfN, a.ntok - n0);
+  } else {
+    const int u = blockIdx.z;
+    if (u >= *a.n_active) return;
+    const int e = a.active_e[u], off = a.active_off[u], cnt = a.active_off[u + 1] - off;
+    n0 = off + blockIdx.y * kPfN;
+    ntok = min(kPfN, cnt - (int)blockIdx.y * kPfN);
+    W += (size_t)e * a.w_expert_stride;
+    S += (size_t)e * a.s_expert_stride;
+  }
+  if (ntok <= 0) return;   // uniform over the CTA, before any barrier or TMEM use
+  const int nmma = (ntok + 15) & ~15;   // MMA N: a multiple of 16
+
+  if (t < kPfN) {
+    const void* src = nullptr;
+    if (t < ntok) {
+      const int row = MODE == PF_GATEUP ? a.row_map[n0 + t] : n0 + t;
+      src = static_cast<const __half*>(a.X) + (size_t)row * a.ldx;
+    }
+    row_src[t] = src;
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tc::smem_u32(&tmem_slot), kPfTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (t == 0) {
+    for (int i = 0; i < kPfSlots; ++i) {
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfProducers / 32 / kPfGroups);   // one per warp of the stage's group
+      tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&final_bar), 1);
+    tc::fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t b_base = tc::smem_u32(smem);
+  bool ok = true;
+
+  if (warp == kPfProducers / 32) {
+    // ---------------- MMA warp: one lane issues
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_f16_f32(kPfM, nmma);
+      for (int i = 0; i < NC; ++i) {
+        const int s = i % kPfSlots;
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), (uint32_t)((i / kPfSlots) & 1), kPfWaitLimit)) ok = false;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // B: core matrices of 8 rows x 16 bytes, 128 bytes apart along K and
+          // 1024 bytes apart along N; this MMA's 16 values of K start 2 core
+          // matrices (256 bytes) after the previous one's; A: the slot's 8
+          // TMEM columns (16 fp16 values of K) per MMA
+          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)s * kPfBTile + (uint32_t)q * 256u, 128u,
+                                                       1024u);
+          tc::mma_f16_tmem_a(tmem, tmem + kPfN + s * 32 + q * 8, bd, idesc, (uint32_t)(i > 0 || q > 0));
+        }
+        tc::mma_commit(tc::smem_u32(&done_bar[s]));
+      }
+      tc::mma_commit(tc::smem_u32(&final_bar));
+    }
+    __syncwarp();
+  } else {
+    // ---------------- producers: group g = w / 4 makes stages g, g + 4, ...;
+    // its warp w % 4 takes TMEM lane quarter w % 4 (weight rows 32 (w % 4) +
+    // lane) and all 64 values of K of each of its stages: the 64 bytes of the
+    // row's 8-row group's four lane slots in the mma layout.  Four groups keep
+    // four stages in the making while the MMA warp works through the earlier
+    // ones.
+    const int quarter = warp & 3, group = warp >> 2, lane_row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int T16 = ((int)blockIdx.x * kPfM + lane_row) >> 4, gq = lane_row & 7, half = (lane_row >> 3) & 1;
+    const uint8_t* wrow = W + ((size_t)T16 * NC * 32 + gq * 4) * 16;   // + chunk * 512
+    const uint32_t* srow = S + (size_t)T16 * NG * 8 + gq;              // + group * 8
+    const uint32_t m_lo = half ? 0x00F000F0u : 0x000F000Fu;
+    const uint32_t magic = half ? 0x54005400u : 0x64006400u;
+    const __half2 bias = bits_h2(half ? 0x54805480u : 0x64086408u);   // (72, 72) or (1032, 1032)
+    const int gtid = t - group * kPfM;   // 0 .. 127 within the group
+
+    // B copies of stage i: chunk L = ((row / 8) * 8 + k8) * 8 + row % 8 of the
+    // slot's tile, 16 bytes each; the group's thread j takes chunks j, j + 128, ...
+    auto issue_b = [&](int i) {
+      const uint32_t dst0 = b_base + (uint32_t)(i % kPfSlots) * kPfBTile;
+#pragma unroll
+      for (int jj = 0; jj < kPfN * 8 / kPfM; ++jj) {
+        const int L = gtid + jj * kPfM;
+        const int row = (L >> 6) * 8 + (L & 7), k8 = (L >> 3) & 7;
+        const void* src = row_src[row];
+        const uint32_t n = src ? 16u : 0u;
+        const void* g = src ? static_cast<const void*>(static_cast<const __half*>(src) + i * 64 + k8 * 8) : a.X;
+        cp_async16_zfill(dst0 + (uint32_t)L * 16u, g, n);
+      }
+    };
+    uint4 wreg[4];
+    uint32_t sreg[2];
+    auto load_a = [&](int i) {
+      const uint8_t* p = wrow + (size_t)i * 512;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) wreg[v] = ldg_nc_v4(p + v * 16);
+      const int k0 = i * 64;
+      sreg[0] = __ldg(srow + (size_t)(k0 / G) * 8);
+      sreg[1] = G == 32 ? __ldg(srow + (size_t)(k0 / G + 1) * 8) : sreg[0];
+    };
+    if (group < NC) {
+      issue_b(group);
+      load_a(group);
+    }
+    cp_async_commit();
+
+    for (int i = group; i < NC; i += kPfGroups) {
+      const int s = i % kPfSlots, nxt = i + kPfGroups;
+      // the MMAs of stage j = nxt - kPfSlots have finished: its slot takes
+      // stage nxt's B, and (MMAs complete in order) stage i - kPfSlots's slot
+      // takes stage i's A
+      const int j = nxt - kPfSlots;
+      if (j >= 0) {
+        if (!tc::mbar_wait(tc::smem_u32(&done_bar[j % kPfSlots]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
+          ok = false;
+        tc::fence_after_sync();
+      }
+      if (nxt < NC) issue_b(nxt);
+      cp_async_commit();
+      // A of stage i: fp16 (q x s) pairs in K order, 32 columns; word
+      // (t, ss) of the row's 64 bytes covers K 32 (ss / 2) + 8 t + 4 (ss % 2)
+      // .. + 3: columns 16 (ss / 2) + 4 t + 2 (ss % 2) and the next
+      uint32_t v[32];
+      {
+        const __half2 sc0 = bits_h2(half ? (sreg[0] >> 16) * 0x10001u : (sreg[0] & 0xFFFFu) * 0x10001u);
+        const __half2 sc1 = bits_h2(half ? (sreg[1] >> 16) * 0x10001u : (sreg[1] & 0xFFFFu) * 0x10001u);
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const uint32_t wv[4] = {wreg[tt].x, wreg[tt].y, wreg[tt].z, wreg[tt].w};
+#pragma unroll
+          for (int ss = 0; ss < 4; ++ss) {
+            const uint32_t w = wv[ss], w8 = w >> 8;
+            const __half2 sc = (ss >> 1) ? sc1 : sc0;   // g = 32: the second half of the stage's K
+            const __half2 lo = __hsub2(bits_h2((w & m_lo) | magic), bias);
+            const __half2 hi = __hsub2(bits_h2((w8 & m_lo) | magic), bias);
+            const int col = 16 * (ss >> 1) + 4 * tt + 2 * (ss & 1);
+            v[col] = h2_bits(__hmul2(lo, sc));
+            v[col + 1] = h2_bits(__hmul2(hi, sc));
+          }
+        }
+      }
+      if (nxt < NC) load_a(nxt);
+      tc::tmem_st32(tmem + lane_base + kPfN + s * 32, v);
+      tc::tmem_wait_st();
+      cp_async_wait<1>();   // this thread's B copies of stage i (issued a round earlier) have landed
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[s]));
+    }
+    cp_async_wait<0>();
+    if (!tc::mbar_wait(tc::smem_u32(&final_bar), 0u, kPfWaitLimit)) ok = false;
+    tc::fence_after_sync();
+
+    // ---------------- epilogue: row lane_row's accumulators, this group's
+    // chunks of 32 rows of the activations (columns 32 group, + 128, ...)
+    const int grow = (int)blockIdx.x * kPfM + lane_row;   // weight row within the matrix
+    for (int c0 = 32 * group; c0 < nmma; c0 += 32 * kPfGroups) {
+      uint32_t d[32];
+      tc::tmem_ld32(tmem + lane_base + c0, d);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int n = c0 + jj;
+        float acc = __uint_as_float(d[jj]);
+        if (MODE == PF_GATEUP) {
+          // rows 8 apart hold the gate and up rows of one feature
+          const float up = __shfl_down_sync(0xffffffffu, acc, 8);
+          if (half == 0 && n < ntok) {
+            const int f = T16 * 8 + gq;
+            const float sg = acc / (1.f + expf(-acc));
+            a.act16[(size_t)(n0 + n) * a.F + f] = __float2half_rn(round_bf16(sg * up));
+          }
+        } else if (n < ntok) {
+          const size_t m = (size_t)(n0 + n);
+          if (MODE == PF_DENSE) {
+            if (a.Res) acc += bf2f(a.Res[m * a.ldr + grow]);
+            a.Y[m * a.ldy + grow] = f2bf(acc);
+          } else {
+            a.out[m * a.H + grow] = acc;
+          }
+        }
+      }
+    }
+  }
+  if (!ok && a.err) atomicExch(a.err, 4);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kPfTmemCols);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const PrefillGemmArgs& a, int grid_y, int grid_z, cudaStream_t st) {
+  const size_t smem = kPfSmem;
+  const dim3 grid(a.rows / kPfM, grid_y, grid_z);
+  if (a.g == 32) {
+    k_w4_tc_prefill<MODE, 32><<<grid, kPfThreads, smem, st>>>(a);
+  } else if (a.g == 64) {
+    k_w4_tc_prefill<MODE, 64><<<grid, kPfThreads, smem, st>>>(a);
+  } else {
+    k_w4_tc_prefill<MODE, 128><<<grid, kPfThreads, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t set_attr() {
+  const int smem = kPfSmem;
+  cudaError_t e = cudaFuncSetAttribute(k_w4_tc_prefill<MODE, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_w4_tc_prefill<MODE, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_w4_tc_prefill<MODE, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
+}
+
+}  // namespace
+
+bool prefill_gemm_supports(int rows, int K, int g) {
+  return rows > 0 && rows % kPfM == 0 && K >= 128 && K % 128 == 0 && (g == 32 || g == 64 || g == 128) &&
+         K % g == 0;
+}
+
+cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, cudaStream_t st) {
+  if (!prefill_gemm_supports(a.rows, a.K, a.g) || a.ntok < 1) return cudaErrorInvalidValue;
+  return launch_mode<PF_DENSE>(a, (a.ntok + kPfN - 1) / kPfN, 1, st);
+}
+
+cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st) {
+  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.row_map || !a.n_active) return cudaErrorInvalidValue;
+  return launch_mode<PF_GATEUP>(a, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
+}
+
+cudaError_t launch_prefill_down(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st) {
+  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active) return cudaErrorInvalidValue;
+  return launch_mode<PF_DOWN>(a, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
+}
+
+cudaError_t init_prefill_attributes() {
+  cudaError_t e = set_attr<PF_DENSE>();
+  if (e == cudaSuccess) e = set_attr<PF_GATEUP>();
+  if (e == cudaSuccess) e = set_attr<PF_DOWN>();
+  return e;
+}
+
+}  // namespace bm
+
+namespace bm {
+
+namespace {
+__global__ void k_fill_i32(int32_t* p, int32_t value, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = value;
+}
+}  // namespace
+
+cudaError_t launch_fill_i32(int32_t* p, int32_t value, int n, cudaStream_t st) {
+  if (n < 1) return cudaSuccess;
+  k_fill_i32<<<(n + 255) / 256, 256, 0, st>>>(p, value, n);
+  return cudaGetLastError();
+}
+
+}  // namespace bm

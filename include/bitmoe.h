@@ -92,6 +92,10 @@ typedef struct bm_config {
   int renorm_topk;   /* 1: top-k weights renormalised to sum to one           */
   int kernel_policy; /* bm_kernel_policy                                      */
   int use_graph;     /* 1: decode_step replays one captured CUDA graph per B  */
+  int prefill_tc;    /* kv_slot_prefill: 0 = through the decode kernels in blocks
+                        of max_streams rows (the bytes of as many decode steps);
+                        1 = prompt-length GEMMs on the tcgen05 tensor cores in
+                        blocks of up to 512 rows (needs the warp-MMA family)   */
 } bm_config;
 
 /* One decoder layer's weights, canonical layout, DEVICE pointers.  Borrowed
@@ -298,6 +302,22 @@ bm_status bm_w4_repack_mma(const uint8_t* W, const uint16_t* S, int N, int K, in
 bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint16_t* X, uint16_t* Y,
                               const uint16_t* R, int M, int N, int K, int g, void* stream);
 
+/* The batched W4A16 GEMM at prompt length on the tcgen05 tensor cores (the
+ * kernel kv_slot_prefill runs with prefill_tc): Y[m][n] = sum_k X[m][k] *
+ * W[n][k] (+ R[m][n]) for M rows at once, weights in the layout of
+ * bm_w4_repack_mma.  A CTA takes 128 weight rows and up to 128 rows of X over
+ * the whole K; each weight enters the MMA as the fp16 product q * s (one
+ * rounding; the decode kernels instead scale exact fp32 group sums), X as
+ * fp16, and the sums are fp32 in tensor memory.  A row's result does not
+ * depend on M or on the other rows.  ([Batched serving] §1: a dense
+ * projection is one batched GEMM over all rows.)
+ * Wm, Sm: DEVICE (bm_w4_repack_mma); X16: DEVICE fp16 [M][K]; R: DEVICE bf16
+ * [M][N] or NULL; Y: DEVICE bf16 [M][N].  Errors: BM_ERR_INVALID_ARG unless
+ * M >= 1, N % 128 == 0, K % 128 == 0, K <= 4096, g in {32, 64, 128},
+ * K % g == 0, or on a NULL pointer. */
+bm_status w4_gemm_prompt_tc(const uint8_t* Wm, const uint32_t* Sm, const uint16_t* X16, uint16_t* Y,
+                            const uint16_t* R, int M, int N, int K, int g, void* stream);
+
 /* Bytes of DEVICE workspace moe_grouped_w4 needs for B tokens. */
 size_t bm_moe_workspace_bytes(int B, int experts, int top_k, int hidden, int ffn);
 
@@ -443,6 +463,21 @@ bm_status bm_engine_read_hidden(bm_engine* e, int B, uint16_t* out, void* stream
  * Nothing faults: every copy that was issued is waited for before the CTA
  * exits.  decode_step ignores this setting. */
 bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item);
+
+/* Measurement only: time the tcgen05 MMA on the current GPU.  One CTA issues
+ * `iters` stages of four kind::f16 MMAs of M 128 x N n x K 16 (zero operands)
+ * into one tensor-memory accumulator, A from tensor memory (a_in_tmem = 1) or
+ * shared memory, the shared-memory operands in the no-swizzle core-matrix
+ * layout (swizzle128 = 0) or the 128-byte-swizzled K-major layout (1); with
+ * roundtrip = 1 each stage is committed and waited for before the next.
+ * Writes the SM cycles per MMA to issue the run and to see it complete.  The
+ * pages have no counterpart: it measures the instruction the prompt-length
+ * GEMMs are built on.  Allocates 24 bytes of device memory and synchronises
+ * the device.  Errors: BM_ERR_INVALID_ARG (n not a multiple of 16 in
+ * [16, 256], iters outside [1, 4096], NULL outputs), BM_ERR_CUDA,
+ * BM_ERR_DEVICE_CHECK (the completion wait gave up). */
+bm_status bm_probe_tcgen05_mma(int n, int a_in_tmem, int swizzle128, int iters, int roundtrip,
+                               double* issue_cycles, double* complete_cycles);
 
 /* Encode fp32 weights to the canonical int4 layout: per row and group of g,
  * s = fp16(absmax / 7) (fp32 division, round to nearest even), q =

@@ -54,7 +54,8 @@ def assert_close_rows(gpu, ref, max_abs=MAX_ABS, min_cos=MIN_COS, what="", bf16_
                    "min_cos": float(cos.min()) if cos.size else 1.0, "bound": float(max_abs),
                    "ulp_flips": int(over.sum()) if bf16_out else 0})
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond max({max_abs:g}, 1 bf16 ulp); worst "
-                           f"|diff| {diff[bad].max():.3g} at |y| {np.abs(r2[bad]).max():.3g}")
+                           f"|diff| {diff[bad].max():.3g} at |y| {np.abs(r2[bad]).max():.3g}; rows "
+                           f"{np.nonzero(bad.any(axis=1))[0][:8].tolist()}")
     assert np.all(cos >= min_cos), f"{what}: cosine {cos.min():.8f} < {min_cos}"
     return float(err.max()), float(cos.min())
 

@@ -150,6 +150,8 @@ struct bm_engine {
   float* pf_part = nullptr;
   unsigned int* pf_acnt = nullptr;
   int32_t *pf_slots = nullptr, *pf_tokens = nullptr;
+  __half* pf_xg = nullptr;                 // the experts' input rows in sorted-pair order
+  TmapBytes tm_xn{}, tm_attn{}, tm_xg{}, tm_act{};   // B operands of the prompt GEMMs
   bm_stats st{};
 
   bm_engine(const bm_config& c) : cfg(c), slots(c.max_streams, c.ctx_cap) {}
@@ -328,7 +330,7 @@ cudaError_t enqueue_prefill_tc(bm_engine* e, int P, bool last, cudaStream_t s, i
     PrefillGemmArgs q{};
     q.W = w.wqkv; q.S = u32(w.wqkv_s); q.rows = e->qkv_rows; q.K = H; q.g = g;
     q.X = xn16; q.ldx = H; q.ntok = P; q.Y = e->pf_qkv; q.ldy = e->qkv_rows; q.err = e->d_err;
-    if ((err = launch_prefill_dense(q, s)) != cudaSuccess) return err;
+    if ((err = launch_prefill_dense(q, e->tm_xn, s)) != cudaSuccess) return err;
     AttnFusedArgs fa{e->arena, l, e->pf_slots, e->pf_qkv, e->qkv_rows, c.q_heads, e->d_rope, e->pf_attn, e->pf_part,
                      (c.ctx_cap + kAttnChunk - 1) / kAttnChunk, e->pf_acnt, P, chk_of(e), 1, 0};
     if ((err = launch_append_rows(fa, s, false)) != cudaSuccess) return err;
@@ -346,29 +348,34 @@ cudaError_t enqueue_prefill_tc(bm_engine* e, int P, bool last, cudaStream_t s, i
     PrefillGemmArgs o{};
     o.W = w.wo; o.S = u32(w.wo_s); o.rows = H; o.K = qd; o.g = g;
     o.X = e->pf_attn; o.ldx = qd; o.ntok = P; o.Res = e->pf_x; o.ldr = H; o.Y = e->pf_h; o.ldy = H; o.err = e->d_err;
-    if ((err = launch_prefill_dense(o, s)) != cudaSuccess) return err;
+    if ((err = launch_prefill_dense(o, e->tm_attn, s)) != cudaSuccess) return err;
     MoeArgs ma{P, c.experts, c.top_k, H, F, g, c.renorm_topk,
                w.wr, w.wg, w.wg_s, w.wu, w.wu_s, w.wd, w.wd_s,
                e->pf_h, 1, w.has_ffn_norm ? w.ffn_norm_buf : nullptr, c.rms_eps, e->pf_h, e->pf_x, nullptr, 1};
-    const MoeBufs mb = moe_carve(e->pf_moe, P, c.experts, c.top_k, H, F);
-    if ((err = launch_moe_route_wide(ma, mb, s)) != cudaSuccess) return err;
+    // the carve of the largest block: the tensor maps describe its buffers
+    const MoeBufs mb = moe_carve(e->pf_moe, e->pf_rows, c.experts, c.top_k, H, F);
+    MoeArgs mw = ma;
+    if ((err = launch_moe_route_wide(mw, mb, s)) != cudaSuccess) return err;
+    if ((err = launch_gather_rows(reinterpret_cast<const __half*>(mb.xn), mb.pair_token, P * c.top_k, H, e->pf_xg, s)) !=
+        cudaSuccess)
+      return err;
     PrefillGemmArgs gu{};
-    gu.W = w.wg; gu.S = u32(w.wg_s); gu.rows = 2 * F; gu.K = H; gu.g = g; gu.X = mb.xn; gu.ldx = H;
+    gu.W = w.wg; gu.S = u32(w.wg_s); gu.rows = 2 * F; gu.K = H; gu.g = g; gu.X = e->pf_xg; gu.ldx = H;
     gu.n_active = mb.n_active; gu.active_e = mb.active_e; gu.active_off = mb.active_off; gu.row_map = mb.pair_token;
     gu.experts = c.experts; gu.w_expert_stride = (size_t)2 * F * H / 2; gu.s_expert_stride = (size_t)F * (H / g);
     gu.act16 = reinterpret_cast<__half*>(mb.act); gu.F = F; gu.err = e->d_err;
-    if ((err = launch_prefill_gateup(gu, P, s)) != cudaSuccess) return err;
+    if ((err = launch_prefill_gateup(gu, e->tm_xg, P, s)) != cudaSuccess) return err;
     PrefillGemmArgs dn{};
     dn.W = w.wd; dn.S = u32(w.wd_s); dn.rows = H; dn.K = F; dn.g = g; dn.X = mb.act; dn.ldx = F;
     dn.n_active = mb.n_active; dn.active_e = mb.active_e; dn.active_off = mb.active_off;
     dn.experts = c.experts; dn.w_expert_stride = (size_t)H * F / 2; dn.s_expert_stride = (size_t)H * (F / g) / 2;
     dn.out = mb.out; dn.H = H; dn.err = e->d_err;
-    if ((err = launch_prefill_down(dn, P, s)) != cudaSuccess) return err;
+    if ((err = launch_prefill_down(dn, e->tm_act, P, s)) != cudaSuccess) return err;
     const bool lastl = l + 1 == c.layers;
     const bf16* next_nw = !lastl ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
     if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->pf_xn, lastl ? 0 : 1, s, Marker(), false)) != cudaSuccess)
       return err;
-    n += 8;   // o_proj, routing (3), gate/up, down, combine
+    n += 9;   // o_proj, routing (3), gather, gate/up, down, combine
   }
   if (!last) {
     if ((err = launch_advance(e->arena.len, e->pf_slots, 1, s, P)) != cudaSuccess) return err;
@@ -752,7 +759,8 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
                  p_qkv = take2((size_t)P * e->qkv_rows * 2), p_attn = take2((size_t)P * qd * 2),
                  p_h = take2((size_t)P * H * 2), p_moe = take2(moe_scratch_bytes(P, E, c.top_k, H, F)),
                  p_part = take2(attn_partial_floats(128, c.q_heads, c.ctx_cap, c.head_dim) * 4),
-                 p_acnt = take2((size_t)128 * c.kv_heads * 4), p_sl = take2((size_t)P * 4), p_tk = take2((size_t)P * 4);
+                 p_acnt = take2((size_t)128 * c.kv_heads * 4), p_sl = take2((size_t)P * 4), p_tk = take2((size_t)P * 4),
+                 p_xg = take2((size_t)P * c.top_k * H * 2);
     BM_CUDA(cudaMalloc(&e->pf_mem, o2), "prompt scratch allocation");
     char* pb = static_cast<char*>(e->pf_mem);
     e->pf_x = reinterpret_cast<bf16*>(pb + p_x);
@@ -765,7 +773,13 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
     e->pf_acnt = reinterpret_cast<unsigned int*>(pb + p_acnt);
     e->pf_slots = reinterpret_cast<int32_t*>(pb + p_sl);
     e->pf_tokens = reinterpret_cast<int32_t*>(pb + p_tk);
+    e->pf_xg = reinterpret_cast<__half*>(pb + p_xg);
     BM_CUDA(cudaMemset(e->pf_mem, 0, o2), "prompt scratch reset");
+    const MoeBufs pmb = moe_carve(e->pf_moe, P, E, c.top_k, H, F);
+    BM_CUDA(encode_rows_tmap(&e->tm_xn, e->pf_xn, P, H, H), "prompt tensor map (normed rows)");
+    BM_CUDA(encode_rows_tmap(&e->tm_attn, e->pf_attn, P, qd, qd), "prompt tensor map (attention rows)");
+    BM_CUDA(encode_rows_tmap(&e->tm_xg, e->pf_xg, P * c.top_k, H, H), "prompt tensor map (expert input rows)");
+    BM_CUDA(encode_rows_tmap(&e->tm_act, pmb.act, P * c.top_k, F, F), "prompt tensor map (expert activations)");
     e->scratch_bytes += o2;
   }
   BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * (2 * bm_engine::kStageRing + 1) * S),
@@ -1340,7 +1354,9 @@ bm_status w4_gemm_prompt_tc(const uint8_t* Wm, const uint32_t* Sm, const uint16_
   a.W = Wm; a.S = Sm; a.rows = N; a.K = K; a.g = g;
   a.X = X16; a.ldx = K; a.ntok = M;
   a.Res = reinterpret_cast<const bf16*>(R); a.ldr = N; a.Y = reinterpret_cast<bf16*>(Y); a.ldy = N;
-  BM_CUDA(launch_prefill_dense(a, static_cast<cudaStream_t>(stream)), "w4_gemm_prompt_tc launch");
+  TmapBytes tm{};
+  BM_CUDA(encode_rows_tmap(&tm, X16, M, K, K), "w4_gemm_prompt_tc tensor map");
+  BM_CUDA(launch_prefill_dense(a, tm, static_cast<cudaStream_t>(stream)), "w4_gemm_prompt_tc launch");
   return bm::ok();
 }
 

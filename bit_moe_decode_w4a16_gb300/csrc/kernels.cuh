@@ -243,11 +243,26 @@ struct PrefillGemmArgs {
   int H;
   int* err;                  // device error flag or null
 };
+// The bytes of a TMA tensor map (CUtensorMap), passed to kernels by value.
+struct alignas(64) TmapBytes {
+  unsigned char b[128];
+};
+// A 2-D tensor map over fp16 rows [rows][ld] (K used of each row) with boxes
+// of 64 values x 128 rows, 128-byte swizzle, zero fill outside: the B operand
+// tiles of the prompt-length GEMMs.  Returns cudaSuccess or the encode error.
+cudaError_t encode_rows_tmap(TmapBytes* out, const void* base, int rows, int K, int ld);
 bool prefill_gemm_supports(int rows, int K, int g);
-cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, cudaStream_t st);
+// X of the args is the matrix `tm` describes: rows of the B operand in order
+// (dense: the M rows; experts: the sorted pairs' rows, gathered beforehand for
+// the gate/up projection).
+cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, const TmapBytes& tm, cudaStream_t st);
 // max_rows_per_expert bounds the grid (an expert has at most one row per token)
-cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st);
-cudaError_t launch_prefill_down(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st);
+cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, const TmapBytes& tm, int max_rows_per_expert,
+                                  cudaStream_t st);
+cudaError_t launch_prefill_down(const PrefillGemmArgs& a, const TmapBytes& tm, int max_rows_per_expert,
+                                cudaStream_t st);
+// dst[r] = src[map[r]] for r < n, rows of `cols` fp16 values (cols % 8 == 0)
+cudaError_t launch_gather_rows(const __half* src, const int32_t* map, int n, int cols, __half* dst, cudaStream_t st);
 cudaError_t init_prefill_attributes();
 // p[0..n) = value
 cudaError_t launch_fill_i32(int32_t* p, int32_t value, int n, cudaStream_t st);

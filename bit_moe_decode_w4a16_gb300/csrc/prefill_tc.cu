@@ -42,37 +42,49 @@ constexpr int kPfN = 128;              // activation rows per CTA
 constexpr int kPfSlots = 12;           // stages in flight: TMEM A slots and shared-memory B tiles
 constexpr int kPfGroups = 4;           // producer groups; group g makes stages g, g + 4, ...
 constexpr int kPfProducers = kPfM * kPfGroups;   // a group: 4 warps, one weight row per lane
-constexpr int kPfThreads = kPfProducers + 32;   // producers + the MMA warp
+constexpr int kPfThreads = kPfProducers + 64;   // producers + the MMA warp + the B loader warp
 constexpr uint32_t kPfTmemCols = 512;  // accumulator [0, 128) + 12 A slots of 32 columns
 constexpr uint32_t kPfWaitLimit = 1u << 18;   // polls of ~3.7 us: a wait gives up after about a second
 constexpr int kPfBTile = kPfN * 128;   // bytes of one stage's B tile (N rows x 64 fp16)
-// dynamic shared memory per CTA: the B tiles of every slot (192 KB: one CTA per
-// SM, which also holds all 512 TMEM columns)
-constexpr int kPfSmem = kPfSlots * kPfBTile;
+// dynamic shared memory per CTA: the B tiles of every slot, 1024-byte aligned
+// for the 128-byte swizzle (193 KB: one CTA per SM, which also holds all 512
+// TMEM columns)
+constexpr int kPfSmem = kPfSlots * kPfBTile + 1024;
 static_assert(kPfN + kPfSlots * 32 <= (int)kPfTmemCols, "TMEM holds the accumulator and the A slots");
 
 enum PfMode { PF_DENSE = 0, PF_GATEUP = 1, PF_DOWN = 2 };
 
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+
+// One 2-D TMA tile load (box of the tensor map at column x, row y) into shared
+// memory, completion counted in bytes on `mbar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// K-major operand with the 128-byte swizzle: rows of 128 bytes (64 fp16), 8-row
+// atoms of 1024 bytes (SBO), LBO unused (encoded 1), layout type 2; the start
+// address moves by 32 bytes per 16 values of K.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 template <int MODE, int G>
-__global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs a) {
-  extern __shared__ __align__(1024) unsigned char smem[];   // kPfSlots B tiles
+__global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs a, const __grid_constant__ TmapBytes tm) {
+  extern __shared__ unsigned char smem_raw[];   // kPfSlots B tiles, 1024-byte aligned below
   __shared__ __align__(8) uint64_t full_bar[kPfSlots];
   __shared__ __align__(8) uint64_t done_bar[kPfSlots];
+  __shared__ __align__(8) uint64_t bfull_bar[kPfSlots];
   __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
-  __shared__ const void* row_src[kPfN];   // activation row of each B row (null: zero)
   static_assert(G == 32 || G == 64 || G == 128, "group size");
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -95,14 +107,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
   if (ntok <= 0) return;   // uniform over the CTA, before any barrier or TMEM use
   const int nmma = (ntok + 15) & ~15;   // MMA N: a multiple of 16
 
-  if (t < kPfN) {
-    const void* src = nullptr;
-    if (t < ntok) {
-      const int row = MODE == PF_GATEUP ? a.row_map[n0 + t] : n0 + t;
-      src = static_cast<const __half*>(a.X) + (size_t)row * a.ldx;
-    }
-    row_src[t] = src;
-  }
   if (warp == 0) {
     tc::tmem_alloc(tc::smem_u32(&tmem_slot), kPfTmemCols);
     tc::tmem_relinquish();
@@ -111,6 +115,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
     for (int i = 0; i < kPfSlots; ++i) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfProducers / 32 / kPfGroups);   // one per warp of the stage's group
       tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
+      tc::mbar_init(tc::smem_u32(&bfull_bar[i]), 1);
     }
     tc::mbar_init(tc::smem_u32(&final_bar), 1);
     tc::fence_mbar_init();
@@ -119,25 +124,45 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const uint32_t b_base = tc::smem_u32(smem);
+  const uint32_t raw_base = tc::smem_u32(smem_raw);
+  const uint32_t b_base = raw_base + ((1024u - (raw_base & 1023u)) & 1023u);
   bool ok = true;
 
-  if (warp == kPfProducers / 32) {
+  if (warp == kPfProducers / 32 + 1) {
+    // ---------------- B loader: one lane, one TMA tile load per stage into the
+    // slot's 128-row B tile, once the MMAs of the stage that used it are done
+    if (lane == 0) {
+      for (int i = 0; i < NC; ++i) {
+        const int s = i % kPfSlots, j = i - kPfSlots;
+        if (j >= 0 &&
+            !tc::mbar_wait(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
+          ok = false;
+        const uint32_t bar = tc::smem_u32(&bfull_bar[s]);
+        mbar_expect_tx(bar, (uint32_t)kPfBTile);
+        tma_load_2d(b_base + (uint32_t)s * kPfBTile, &tm, i * 64, n0, bar);
+      }
+      // every tile load issued has landed before the CTA may exit
+      for (int i = NC - kPfSlots > 0 ? NC - kPfSlots : 0; i < NC; ++i)
+        if (!tc::mbar_wait(tc::smem_u32(&bfull_bar[i % kPfSlots]), (uint32_t)((i / kPfSlots) & 1), kPfWaitLimit))
+          ok = false;
+    }
+    __syncwarp();
+  } else if (warp == kPfProducers / 32) {
     // ---------------- MMA warp: one lane issues
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16_f32(kPfM, nmma);
       for (int i = 0; i < NC; ++i) {
         const int s = i % kPfSlots;
-        if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), (uint32_t)((i / kPfSlots) & 1), kPfWaitLimit)) ok = false;
+        const uint32_t ph = (uint32_t)((i / kPfSlots) & 1);
+        if (!tc::mbar_wait(tc::smem_u32(&bfull_bar[s]), ph, kPfWaitLimit)) ok = false;
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, kPfWaitLimit)) ok = false;
         tc::fence_after_sync();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          // B: core matrices of 8 rows x 16 bytes, 128 bytes apart along K and
-          // 1024 bytes apart along N; this MMA's 16 values of K start 2 core
-          // matrices (256 bytes) after the previous one's; A: the slot's 8
-          // TMEM columns (16 fp16 values of K) per MMA
-          const uint64_t bd = tc::smem_desc_noswizzle(b_base + (uint32_t)s * kPfBTile + (uint32_t)q * 256u, 128u,
-                                                       1024u);
+          // B: the slot's swizzled tile, this MMA's 16 values of K 32 bytes into
+          // each 128-byte row; A: the slot's 8 TMEM columns (16 fp16 values of
+          // K) per MMA
+          const uint64_t bd = smem_desc_sw128(b_base + (uint32_t)s * kPfBTile + (uint32_t)q * 32u);
           tc::mma_f16_tmem_a(tmem, tmem + kPfN + s * 32 + q * 8, bd, idesc, (uint32_t)(i > 0 || q > 0));
         }
         tc::mma_commit(tc::smem_u32(&done_bar[s]));
@@ -146,7 +171,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
     }
     __syncwarp();
   } else {
-    // ---------------- producers: group g = w / 4 makes stages g, g + 4, ...;
+    // ---------------- producers (warps 0-15): group g = w / 4 makes stages g, g + 4, ...;
     // its warp w % 4 takes TMEM lane quarter w % 4 (weight rows 32 (w % 4) +
     // lane) and all 64 values of K of each of its stages: the 64 bytes of the
     // row's 8-row group's four lane slots in the mma layout.  Four groups keep
@@ -162,20 +187,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
     const __half2 bias = bits_h2(half ? 0x54805480u : 0x64086408u);   // (72, 72) or (1032, 1032)
     const int gtid = t - group * kPfM;   // 0 .. 127 within the group
 
-    // B copies of stage i: chunk L = ((row / 8) * 8 + k8) * 8 + row % 8 of the
-    // slot's tile, 16 bytes each; the group's thread j takes chunks j, j + 128, ...
-    auto issue_b = [&](int i) {
-      const uint32_t dst0 = b_base + (uint32_t)(i % kPfSlots) * kPfBTile;
-#pragma unroll
-      for (int jj = 0; jj < kPfN * 8 / kPfM; ++jj) {
-        const int L = gtid + jj * kPfM;
-        const int row = (L >> 6) * 8 + (L & 7), k8 = (L >> 3) & 7;
-        const void* src = row_src[row];
-        const uint32_t n = src ? 16u : 0u;
-        const void* g = src ? static_cast<const void*>(static_cast<const __half*>(src) + i * 64 + k8 * 8) : a.X;
-        cp_async16_zfill(dst0 + (uint32_t)L * 16u, g, n);
-      }
-    };
     uint4 wreg[4];
     uint32_t sreg[2];
     auto load_a = [&](int i) {
@@ -186,25 +197,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       sreg[0] = __ldg(srow + (size_t)(k0 / G) * 8);
       sreg[1] = G == 32 ? __ldg(srow + (size_t)(k0 / G + 1) * 8) : sreg[0];
     };
-    if (group < NC) {
-      issue_b(group);
-      load_a(group);
-    }
-    cp_async_commit();
+    if (group < NC) load_a(group);
 
     for (int i = group; i < NC; i += kPfGroups) {
       const int s = i % kPfSlots, nxt = i + kPfGroups;
-      // the MMAs of stage j = nxt - kPfSlots have finished: its slot takes
-      // stage nxt's B, and (MMAs complete in order) stage i - kPfSlots's slot
-      // takes stage i's A
-      const int j = nxt - kPfSlots;
+      // the MMAs of stage j = i - kPfSlots, the last to use this slot, have finished
+      const int j = i - kPfSlots;
       if (j >= 0) {
-        if (!tc::mbar_wait(tc::smem_u32(&done_bar[j % kPfSlots]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
-          ok = false;
+        if (!tc::mbar_wait(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit)) ok = false;
         tc::fence_after_sync();
       }
-      if (nxt < NC) issue_b(nxt);
-      cp_async_commit();
       // A of stage i: fp16 (q x s) pairs in K order, 32 columns; word
       // (t, ss) of the row's 64 bytes covers K 32 (ss / 2) + 8 t + 4 (ss % 2)
       // .. + 3: columns 16 (ss / 2) + 4 t + 2 (ss % 2) and the next
@@ -230,13 +232,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       if (nxt < NC) load_a(nxt);
       tc::tmem_st32(tmem + lane_base + kPfN + s * 32, v);
       tc::tmem_wait_st();
-      cp_async_wait<1>();   // this thread's B copies of stage i (issued a round earlier) have landed
-      tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[s]));
     }
-    cp_async_wait<0>();
     if (!tc::mbar_wait(tc::smem_u32(&final_bar), 0u, kPfWaitLimit)) ok = false;
     tc::fence_after_sync();
 
@@ -278,15 +277,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
 }
 
 template <int MODE>
-cudaError_t launch_mode(const PrefillGemmArgs& a, int grid_y, int grid_z, cudaStream_t st) {
+cudaError_t launch_mode(const PrefillGemmArgs& a, const TmapBytes& tm, int grid_y, int grid_z, cudaStream_t st) {
   const size_t smem = kPfSmem;
   const dim3 grid(a.rows / kPfM, grid_y, grid_z);
   if (a.g == 32) {
-    k_w4_tc_prefill<MODE, 32><<<grid, kPfThreads, smem, st>>>(a);
+    k_w4_tc_prefill<MODE, 32><<<grid, kPfThreads, smem, st>>>(a, tm);
   } else if (a.g == 64) {
-    k_w4_tc_prefill<MODE, 64><<<grid, kPfThreads, smem, st>>>(a);
+    k_w4_tc_prefill<MODE, 64><<<grid, kPfThreads, smem, st>>>(a, tm);
   } else {
-    k_w4_tc_prefill<MODE, 128><<<grid, kPfThreads, smem, st>>>(a);
+    k_w4_tc_prefill<MODE, 128><<<grid, kPfThreads, smem, st>>>(a, tm);
   }
   return cudaGetLastError();
 }
@@ -309,19 +308,21 @@ bool prefill_gemm_supports(int rows, int K, int g) {
          K % g == 0;
 }
 
-cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, cudaStream_t st) {
+cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, const TmapBytes& tm, cudaStream_t st) {
   if (!prefill_gemm_supports(a.rows, a.K, a.g) || a.ntok < 1) return cudaErrorInvalidValue;
-  return launch_mode<PF_DENSE>(a, (a.ntok + kPfN - 1) / kPfN, 1, st);
+  return launch_mode<PF_DENSE>(a, tm, (a.ntok + kPfN - 1) / kPfN, 1, st);
 }
 
-cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st) {
-  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.row_map || !a.n_active) return cudaErrorInvalidValue;
-  return launch_mode<PF_GATEUP>(a, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
-}
-
-cudaError_t launch_prefill_down(const PrefillGemmArgs& a, int max_rows_per_expert, cudaStream_t st) {
+cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, const TmapBytes& tm, int max_rows_per_expert,
+                                  cudaStream_t st) {
   if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active) return cudaErrorInvalidValue;
-  return launch_mode<PF_DOWN>(a, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
+  return launch_mode<PF_GATEUP>(a, tm, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
+}
+
+cudaError_t launch_prefill_down(const PrefillGemmArgs& a, const TmapBytes& tm, int max_rows_per_expert,
+                                cudaStream_t st) {
+  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active) return cudaErrorInvalidValue;
+  return launch_mode<PF_DOWN>(a, tm, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
 }
 
 cudaError_t init_prefill_attributes() {
@@ -345,6 +346,65 @@ __global__ void k_fill_i32(int32_t* p, int32_t value, int n) {
 cudaError_t launch_fill_i32(int32_t* p, int32_t value, int n, cudaStream_t st) {
   if (n < 1) return cudaSuccess;
   k_fill_i32<<<(n + 255) / 256, 256, 0, st>>>(p, value, n);
+  return cudaGetLastError();
+}
+
+}  // namespace bm
+
+#include <cuda.h>   // the tensor-map types; the encoder itself is fetched from the driver at run time
+
+namespace bm {
+
+namespace {
+
+__global__ void k_gather_rows(const __half* __restrict__ src, const int32_t* __restrict__ map, int cols,
+                              __half* __restrict__ dst) {
+  const int r = blockIdx.x;
+  const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)map[r] * cols);
+  uint4* d = reinterpret_cast<uint4*>(dst + (size_t)r * cols);
+  for (int i = threadIdx.x; i < cols / 8; i += blockDim.x) d[i] = s[i];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t encode_rows_tmap(TmapBytes* out, const void* base, int rows, int K, int ld) {
+  static_assert(sizeof(CUtensorMap) == sizeof(TmapBytes), "tensor map size");
+  EncodeTiledFn fn = encoder();
+  if (!fn) return cudaErrorNotSupported;
+  if (rows < 1 || K < 64 || K % 64 || ld < K || (ld * 2) % 16 || (reinterpret_cast<uintptr_t>(base) & 15))
+    return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kPfN};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gather_rows(const __half* src, const int32_t* map, int n, int cols, __half* dst, cudaStream_t st) {
+  if (n < 1) return cudaSuccess;
+  if (cols % 8) return cudaErrorInvalidValue;
+  k_gather_rows<<<n, 256, 0, st>>>(src, map, cols, dst);
   return cudaGetLastError();
 }
 

@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
   extern __shared__ unsigned char smem_raw[];   // kPfSlots B tiles, 1024-byte aligned below
   __shared__ __align__(8) uint64_t full_bar[kPfSlots];
   __shared__ __align__(8) uint64_t done_bar[kPfSlots];
-  __shared__ __align__(8) uint64_t bfull_bar[kPfSlots];
   __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
   static_assert(G == 32 || G == 64 || G == 128, "group size");
@@ -113,9 +112,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
   }
   if (t == 0) {
     for (int i = 0; i < kPfSlots; ++i) {
-      tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfProducers / 32 / kPfGroups);   // one per warp of the stage's group
+      // one arrival per warp of the stage's group, one from the B loader (with its bytes)
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfProducers / 32 / kPfGroups + 1);
       tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
-      tc::mbar_init(tc::smem_u32(&bfull_bar[i]), 1);
     }
     tc::mbar_init(tc::smem_u32(&final_bar), 1);
     tc::fence_mbar_init();
@@ -135,15 +134,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       for (int i = 0; i < NC; ++i) {
         const int s = i % kPfSlots, j = i - kPfSlots;
         if (j >= 0 &&
-            !tc::mbar_wait(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
+            !tc::mbar_wait_spin(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
           ok = false;
-        const uint32_t bar = tc::smem_u32(&bfull_bar[s]);
+        const uint32_t bar = tc::smem_u32(&full_bar[s]);
         mbar_expect_tx(bar, (uint32_t)kPfBTile);
         tma_load_2d(b_base + (uint32_t)s * kPfBTile, &tm, i * 64, n0, bar);
       }
-      // every tile load issued has landed before the CTA may exit
+      // every tile load issued has landed before the CTA may exit (the last
+      // slots' stages complete their full barriers)
       for (int i = NC - kPfSlots > 0 ? NC - kPfSlots : 0; i < NC; ++i)
-        if (!tc::mbar_wait(tc::smem_u32(&bfull_bar[i % kPfSlots]), (uint32_t)((i / kPfSlots) & 1), kPfWaitLimit))
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[i % kPfSlots]), (uint32_t)((i / kPfSlots) & 1), kPfWaitLimit))
           ok = false;
     }
     __syncwarp();
@@ -154,8 +154,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       for (int i = 0; i < NC; ++i) {
         const int s = i % kPfSlots;
         const uint32_t ph = (uint32_t)((i / kPfSlots) & 1);
-        if (!tc::mbar_wait(tc::smem_u32(&bfull_bar[s]), ph, kPfWaitLimit)) ok = false;
-        if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, kPfWaitLimit)) ok = false;
+        if (!tc::mbar_wait_spin(tc::smem_u32(&full_bar[s]), ph, kPfWaitLimit)) ok = false;
         tc::fence_after_sync();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       // the MMAs of stage j = i - kPfSlots, the last to use this slot, have finished
       const int j = i - kPfSlots;
       if (j >= 0) {
-        if (!tc::mbar_wait(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit)) ok = false;
+        if (!tc::mbar_wait_spin(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit)) ok = false;
         tc::fence_after_sync();
       }
       // A of stage i: fp16 (q x s) pairs in K order, 32 columns; word

@@ -176,5 +176,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar_smem, uint32_t parity, u
   return false;
 }
 
+// As mbar_wait, but first polls with the non-blocking test_wait (up to 1024
+// times) so that a phase that completes within a few hundred cycles is seen
+// without the suspend-and-wake of try_wait; then falls back to mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t mbar_smem, uint32_t parity, uint32_t limit) {
+  for (int i = 0; i < 1024; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(mbar_smem), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return mbar_wait(mbar_smem, parity, limit);
+}
+
 }  // namespace tc
 }  // namespace bm

@@ -35,7 +35,7 @@ class bm_config(ctypes.Structure):
                                             "ffn", "group", "vocab", "layers")] + \
                [("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float)] + \
                [(n, ctypes.c_int) for n in ("max_streams", "ctx_cap", "renorm_topk", "kernel_policy",
-                                            "use_graph", "prefill_tc")]
+                                            "use_graph", "prefill_tc", "persistent_step")]
 
 
 _P = ctypes.c_void_p
@@ -109,6 +109,7 @@ def lib():
             "bm_engine_attention": ([V, I, V, V, V, I, V], S),
             "bm_engine_read_hidden": ([V, I, V, V], S),
             "bm_engine_test_drop_expert_item": ([V, I], S),
+            "bm_engine_test_drop_persist_unit": ([V, I], S),
             "bm_slot_map_create": ([I, I, ctypes.POINTER(V)], S),
             "bm_slot_map_destroy": ([V], None),
             "bm_slot_map_acquire": ([V, I, PI], S),
@@ -339,6 +340,10 @@ def bm_engine_read_hidden(e, B, out, stream=None):
 
 def bm_engine_test_drop_expert_item(e, item):
     _check(lib().bm_engine_test_drop_expert_item(e, int(item)))
+
+
+def bm_engine_test_drop_persist_unit(e, unit):
+    _check(lib().bm_engine_test_drop_persist_unit(e, int(unit)))
 
 
 def bm_probe_tcgen05_mma(n, a_in_tmem, swizzle128, iters, roundtrip=0):

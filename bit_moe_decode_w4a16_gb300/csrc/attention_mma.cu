@@ -42,330 +42,21 @@
 // (a row reads positions that other rows of the launch produce), and the
 // kernel then skips its own append; a row's arithmetic is that of a decode
 // step at the same position, so both paths leave the same bytes.
-#include <float.h>
-
-#include "kernels.cuh"
-#include "w4_mma.cuh"
+#include "attn_fused.cuh"
 
 namespace bm {
 
 namespace {
 
-constexpr int kWarpsA = 8;   // a warp takes 16 of a chunk's 128 positions
-constexpr int kMaxBatch = 128;
-
-__device__ __forceinline__ size_t rec_index(int b, int h, int c, int qh, int max_chunks, int d) {
-  return (((size_t)b * qh + h) * max_chunks + c) * (size_t)(d + 2);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-// Rotate-half RoPE of one pair (x0 = x[i], x1 = x[i + d/2]) with explicit
-// roundings, so every kernel that rotates k produces the same bits.
-__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, bf16& y0, bf16& y1) {
-  y0 = f2bf(__fmaf_rn(x0, c, -__fmul_rn(x1, s)));
-  y1 = f2bf(__fmaf_rn(x1, c, __fmul_rn(x0, s)));
-}
-
-// Position of row b: the slot's length, plus b for the rows of a prompt.
-__device__ __forceinline__ int row_position(const AttnFusedArgs& a, int b, int slot) {
-  return a.ar.len[slot] + (a.prefill ? a.row0 + b : 0);
-}
-
-template <int D>
-struct AttnSmem {
-  static constexpr int kVS = D + 8;   // padded V row: conflict-free ldmatrix
-  union {
-    bf16 vs[kAttnChunk][kVS];          // V rows of the chunk
-    float ored[kWarpsA][8][D];         // per-warp partial O (after the V reads)
-  } u;
-  bf16 qs[8][D];                       // rotated q of the kv group
-  bf16 knew[D];                        // rotated k of a decode row's new position
-  float red_m[kWarpsA][8], red_l[kWarpsA][8];
-  float stat_m[8], stat_l[8];
-  float mm[8][kMaxMergeChunks], ll[8][kMaxMergeChunks], ww[8][kMaxMergeChunks];   // merge: m, l, weights
-  float mden[8];
-  int slot[kMaxBatch], nc[kMaxBatch], pos[kMaxBatch], pre[kMaxBatch + 1];
-  int last;
-};
+using namespace attnf;
 
 template <int D>
 __global__ void __launch_bounds__(kWarpsA * 32, 3) k_attn_fused(AttnFusedArgs a) {
   __shared__ __align__(16) AttnSmem<D> sm;
-  constexpr int kVS = AttnSmem<D>::kVS;
-  constexpr int kBlk = D / 32;
-  constexpr int kV8 = D / 8;
-  constexpr int kNT = D / 8;
   pdl_wait();
   pdl_trigger();   // the grid is at most one wave: the output projection may start its weight loads
-  const AttnArena& ar = a.ar;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int kvh = ar.kvh, G = a.qh / kvh, B = a.B, half = D / 2;
-  const float scale = 1.0f / sqrtf((float)D);
-
-  // ---- slots, positions, chunk counts and the item prefix (chunk-major within a stream)
-  for (int b = tid; b < B; b += blockDim.x) {
-    const int slot = a.slots[b];
-    int nc = 0, pos = 0;
-    if (slot < 0 || slot >= ar.S) {
-      if (blockIdx.x == 0) a.chk.fail(1);
-    } else {
-      pos = row_position(a, b, slot);
-      if (pos < 0 || pos + 1 > ar.cap) {
-        if (blockIdx.x == 0) a.chk.fail(2);
-      } else {
-        nc = (pos + kAttnChunk) / kAttnChunk;
-      }
-    }
-    sm.slot[b] = slot;
-    sm.nc[b] = nc;
-    sm.pos[b] = pos;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    sm.pre[0] = 0;
-    for (int b = 0; b < B; ++b) sm.pre[b + 1] = sm.pre[b] + sm.nc[b] * kvh;
-  }
-  __syncthreads();
-  const int total = sm.pre[B];
-
-  for (int it = blockIdx.x; it < total; it += gridDim.x) {
-    int b = 0;
-    while (sm.pre[b + 1] <= it) ++b;
-    const int r = it - sm.pre[b], kh = r % kvh, c = r / kvh;
-    const int slot = sm.slot[b], nc = sm.nc[b], pos = sm.pos[b], L = pos + 1;
-    const int j0 = c * kAttnChunk, n = min(kAttnChunk, L - j0);
-    const bool last_chunk = c == nc - 1;
-    // on the chunk that holds a decode row's new position, k and v of that
-    // position come from this row's qkv (rotated here), not from the arena
-    const bool own_new = last_chunk && !a.prefill;
-    const int p_new = own_new ? pos - j0 : -1;
-    const bf16* row = a.qkv + (size_t)b * a.ld_qkv;
-    const bf16* ksrc = row + (size_t)(a.qh + kh) * D;
-    const bf16* vsrc = row + (size_t)(a.qh + kvh + kh) * D;
-    const size_t base = (size_t)a.layer * ar.layer_stride() + (size_t)slot * ar.slot_stride() + (size_t)kh * ar.cap * D;
-    bf16* Kb = ar.K + base;
-    bf16* Vb = ar.V + base;
-
-    // ---- every load of the item at once: V rows (async, to shared memory),
-    // the lane's K rows, the rotation table, q and the new k / v
-    for (int i = tid; i < kAttnChunk * kV8; i += blockDim.x) {
-      const int rr = i / kV8, v8 = i - rr * kV8;
-      if (rr == p_new) cp_async16(&sm.u.vs[rr][v8 * 8], vsrc + v8 * 8);
-      else if (rr < n) cp_async16(&sm.u.vs[rr][v8 * 8], Vb + (size_t)(j0 + rr) * D + v8 * 8);
-      else *reinterpret_cast<uint4*>(&sm.u.vs[rr][v8 * 8]) = make_uint4(0, 0, 0, 0);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    uint4 kb[2][kBlk];   // this lane's B column of n-tile nt: position 16w + 8nt + g
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int p = 16 * warp + 8 * nt + g;
-#pragma unroll
-      for (int blk = 0; blk < kBlk; ++blk)
-        kb[nt][blk] = p < n && p != p_new
-                          ? __ldcg(reinterpret_cast<const uint4*>(Kb + (size_t)(j0 + p) * D + 32 * blk + 8 * t))
-                          : make_uint4(0, 0, 0, 0);
-    }
-
-    // ---- RoPE of the kv group's q heads (and of the new k, with its append)
-    const float2* cs = a.rope + (size_t)pos * half;
-    for (int idx = tid; idx < 8 * half; idx += blockDim.x) {
-      const int h = idx / half, i = idx - h * half;
-      bf16 y0 = f2bf(0.f), y1 = f2bf(0.f);
-      if (h < G) {
-        const bf16* src = row + (size_t)(kh * G + h) * D;
-        const float2 v = cs[i];
-        rope_pair(bf2f(src[i]), bf2f(src[i + half]), v.x, v.y, y0, y1);
-      }
-      sm.qs[h][i] = y0;
-      sm.qs[h][i + half] = y1;
-    }
-    if (own_new) {
-      for (int i = tid; i < half; i += blockDim.x) {
-        const float2 v = cs[i];
-        bf16 y0, y1;
-        rope_pair(bf2f(ksrc[i]), bf2f(ksrc[i + half]), v.x, v.y, y0, y1);
-        sm.knew[i] = y0;
-        sm.knew[i + half] = y1;
-        Kb[(size_t)pos * D + i] = y0;
-        Kb[(size_t)pos * D + i + half] = y1;
-      }
-      for (int i = tid; i < D; i += blockDim.x) Vb[(size_t)pos * D + i] = vsrc[i];
-    }
-    __syncthreads();
-    if (own_new) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-        if (16 * warp + 8 * nt + g == p_new) {
-#pragma unroll
-          for (int blk = 0; blk < kBlk; ++blk) kb[nt][blk] = *reinterpret_cast<const uint4*>(&sm.knew[32 * blk + 8 * t]);
-        }
-    }
-
-    // ---- scores: warp w takes positions [16w, 16w + 16): 2 n-tiles of 8
-    uint32_t qa[kBlk][4];
-#pragma unroll
-    for (int blk = 0; blk < kBlk; ++blk) {
-      const uint4 q4 = *reinterpret_cast<const uint4*>(&sm.qs[g][32 * blk + 8 * t]);
-      qa[blk][0] = q4.x; qa[blk][1] = q4.y; qa[blk][2] = q4.z; qa[blk][3] = q4.w;
-    }
-    float s[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) s[nt][q] = 0.f;
-#pragma unroll
-      for (int blk = 0; blk < kBlk; ++blk) {
-        const uint32_t a0[4] = {qa[blk][0], 0u, qa[blk][1], 0u};
-        const uint32_t a1[4] = {qa[blk][2], 0u, qa[blk][3], 0u};
-        mma::mma_bf16(s[nt], a0, kb[nt][blk].x, kb[nt][blk].y);
-        mma::mma_bf16(s[nt], a1, kb[nt][blk].z, kb[nt][blk].w);
-      }
-    }
-    // s[nt][0..1] = S[head g][position 16w + 8nt + 2t (+1)]; rows g + 8 (c2, c3) are padding
-    float mx = -FLT_MAX;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int p = 16 * warp + 8 * nt + 2 * t + j;
-        s[nt][j] = p < n ? s[nt][j] * scale : -FLT_MAX;
-        mx = fmaxf(mx, s[nt][j]);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (t == 0) sm.red_m[warp][g] = mx;
-    __syncthreads();
-    if (tid < 8) {
-      float m = sm.red_m[0][tid];
-      for (int w = 1; w < kWarpsA; ++w) m = fmaxf(m, sm.red_m[w][tid]);
-      sm.stat_m[tid] = m;
-    }
-    __syncthreads();
-    const float mrow = sm.stat_m[g];
-    float ls = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int p = 16 * warp + 8 * nt + 2 * t + j;
-        s[nt][j] = p < n ? expf(s[nt][j] - mrow) : 0.f;
-        ls += s[nt][j];
-      }
-    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-    if (t == 0) sm.red_l[warp][g] = ls;
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (tid < 8) {
-      float l = 0.f;
-      for (int w = 0; w < kWarpsA; ++w) l += sm.red_l[w][tid];
-      sm.stat_l[tid] = l;
-    }
-
-    // ---- O = P V over the warp's 16 positions (one k-step)
-    float o[kNT][4];
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) o[nt][q] = 0.f;
-    {
-      const uint32_t pa[4] = {pack_f16(s[0][0], s[0][1]), 0u, pack_f16(s[1][0], s[1][1]), 0u};
-      const int vrow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-      for (int dt = 0; dt < kNT / 2; ++dt) {
-        uint32_t vb[4];
-        ldsm_x4_trans(vb, static_cast<uint32_t>(__cvta_generic_to_shared(&sm.u.vs[vrow][16 * dt + (lane >> 4) * 8])));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) vb[q] = mma::bf2_to_h2(vb[q]);   // exact: V is bf16 inside fp16's range
-        mma::mma_f16(o[2 * dt], pa, vb[0], vb[1]);
-        mma::mma_f16(o[2 * dt + 1], pa, vb[2], vb[3]);
-      }
-    }
-    __syncthreads();   // all V reads are done: the union now holds the partial O
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      sm.u.ored[warp][g][8 * nt + 2 * t] = o[nt][0];
-      sm.u.ored[warp][g][8 * nt + 2 * t + 1] = o[nt][1];
-    }
-    __syncthreads();
-
-    if (nc == 1) {
-      // ---- one chunk: its record is the result (the merge of one chunk has
-      // weight exp(0) = 1, so o / l is the merge's value bit for bit)
-      for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx - h * D;
-        float v = 0.f;
-        for (int w = 0; w < kWarpsA; ++w) v += sm.u.ored[w][h][d];
-        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(v / sm.stat_l[h]));
-      }
-      __syncthreads();
-      continue;
-    }
-
-    // ---- the chunk's record: o (warps added in order), m, l
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
-      const int h = idx / D, d = idx - h * D;
-      float v = 0.f;
-      for (int w = 0; w < kWarpsA; ++w) v += sm.u.ored[w][h][d];
-      a.part[rec_index(b, kh * G + h, c, a.qh, a.max_chunks, D) + d] = v;
-    }
-    if (tid < G) {
-      float* rec = a.part + rec_index(b, kh * G + tid, c, a.qh, a.max_chunks, D);
-      rec[D] = sm.stat_m[tid];
-      rec[D + 1] = sm.stat_l[tid];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) sm.last = atomicAdd(&a.counters[b * kvh + kh], 1u) == (unsigned)(nc - 1);
-    __syncthreads();
-    if (sm.last) {
-      // ---- merge the stream's chunks for this kv group, ascending chunk order
-      __threadfence();
-      for (int idx = tid; idx < G * nc; idx += blockDim.x) {
-        const int h = idx / nc, cc = idx - h * nc;
-        const float* rec = a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D);
-        sm.mm[h][cc] = __ldcg(rec + D);
-        sm.ll[h][cc] = __ldcg(rec + D + 1);
-      }
-      __syncthreads();
-      if (tid < G) {
-        float M = -FLT_MAX;
-        for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, sm.mm[tid][cc]);
-        float den = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-          const float w = expf(sm.mm[tid][cc] - M);
-          sm.ww[tid][cc] = w;
-          den = fmaf(sm.ll[tid][cc], w, den);
-        }
-        sm.mden[tid] = den;
-      }
-      __syncthreads();
-      for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx - h * D;
-        float acc = 0.f;
-        for (int cc = 0; cc < nc; ++cc)
-          acc = fmaf(__ldcg(a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D) + d), sm.ww[h][cc], acc);
-        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(acc / sm.mden[h]));
-      }
-      if (tid == 0) a.counters[b * kvh + kh] = 0u;
-    }
-    __syncthreads();   // shared memory is reused by the next item
-  }
+  const int total = attn_prologue<D>(a, sm, blockIdx.x == 0, CtaSync{});
+  for (int it = blockIdx.x; it < total; it += gridDim.x) attn_item<D>(a, sm, it, CtaSync{});
 }
 
 // Rotated k and v of every row to the arena at the row's position: one CTA

@@ -21,6 +21,7 @@
 
 #include "errors.h"
 #include "kernels.cuh"
+#include "persist.h"
 #include "slot_map.h"
 
 namespace bm {
@@ -141,6 +142,7 @@ struct bm_engine {
   std::map<int, cudaGraphExec_t> graphs;   // decode graphs by B; prompt blocks under negative keys
   std::map<int, int> graph_kernels;         // kernels in each graph
   int test_drop_item = -1;                  // failure-detection tests: an expert item whose copies are not issued
+  int test_drop_unit = -1;                  // failure-detection tests: a persistent-step weight unit not issued
   // prompt ingestion on the tensor cores (prefill_tc): rows per block and its scratch
   int pf_rows = 0;
   void* pf_mem = nullptr;
@@ -152,6 +154,14 @@ struct bm_engine {
   int32_t *pf_slots = nullptr, *pf_tokens = nullptr;
   __half* pf_xg = nullptr;                 // the experts' input rows in sorted-pair order
   TmapBytes tm_xn{}, tm_attn{}, tm_xg{}, tm_act{};   // B operands of the prompt GEMMs
+  // persistent small-batch decode step (persistent_step)
+  int persist_rows = 0;                    // decode steps of B <= persist_rows rows run persistent; 0 = off
+  PersistGeo pgeo{};
+  void* pmem = nullptr;
+  PersistLayer* d_players = nullptr;       // [layers]
+  unsigned int* pst_bar = nullptr;         // grid barrier counter
+  std::vector<PersistLayer> h_players;
+  bool players_dirty = true;
   bm_stats st{};
 
   bm_engine(const bm_config& c) : cfg(c), slots(c.max_streams, c.ctx_cap) {}
@@ -201,8 +211,13 @@ void tc_workspace(const bm_config& c, int qkv_rows, size_t* max_jobs, size_t* ma
 // reaches the output projection.
 enum PromptBlock { kDecode = 0, kPromptBlock = 1, kPromptLast = 2 };
 
+cudaError_t enqueue_step_persist(bm_engine* e, int B, cudaStream_t s, int* launches);
+
 cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches, const Marker& mark,
                              int prompt = kDecode) {
+  // small decode batches: one persistent launch for all layers (the same
+  // bits); the per-kernel profiler keeps the multi-kernel step
+  if (prompt == kDecode && B <= e->persist_rows && !mark.fn) return enqueue_step_persist(e, B, s, launches);
   const bm_config& c = e->cfg;
   const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
   cudaError_t err;
@@ -303,6 +318,53 @@ cudaError_t enqueue_step_mma(bm_engine* e, int B, cudaStream_t s, int* launches,
   mark(KT_LM_HEAD);
   ++n;
   if (launches) *launches = n;
+  return cudaSuccess;
+}
+
+// The decode step of B <= persist_rows rows: the embedding and its RMSNorm,
+// one cooperative launch for every layer (persist.cu), then the output
+// projection with the fused argmax, as in the multi-kernel step.
+cudaError_t enqueue_step_persist(bm_engine* e, int B, cudaStream_t s, int* launches) {
+  const bm_config& c = e->cfg;
+  const int H = c.hidden, qd = c.q_heads * c.head_dim, F = c.ffn, g = c.group;
+  cudaError_t err;
+  __half* xn16 = reinterpret_cast<__half*>(e->xn);
+  const bf16* nw0 = e->L[0].has_attn_norm ? e->L[0].attn_norm_buf : nullptr;
+  if ((err = launch_embed_norm(e->embed, c.vocab, H, e->d_tokens, e->x, nw0, c.rms_eps, xn16, B, chk_of(e), s,
+                               false)) != cudaSuccess)
+    return err;
+  if ((err = cudaMemsetAsync(e->pst_bar, 0, sizeof(unsigned int), s)) != cudaSuccess) return err;
+  PersistArgs a{};
+  a.L = e->d_players;
+  a.layers = c.layers;
+  a.B = B;
+  a.H = H; a.qd = qd; a.qkv_rows = e->qkv_rows; a.F = F; a.E = c.experts; a.k = c.top_k;
+  a.eps = c.rms_eps;
+  a.final_nw = e->has_final_norm ? e->final_norm_buf : nullptr;
+  a.x = e->x; a.xn16 = xn16; a.xn_out = e->xn; a.qkv = e->qkv;
+  a.attn = reinterpret_cast<__half*>(e->attn);
+  a.h = e->h;
+  a.moe = MoeArgs{B, c.experts, c.top_k, H, F, g, c.renorm_topk, nullptr, nullptr, nullptr, nullptr, nullptr,
+                  nullptr, nullptr, e->h, 1, nullptr, c.rms_eps, e->h, e->x, nullptr, 1};
+  a.mb = moe_carve(e->moe_ws, B, c.experts, c.top_k, H, F);
+  a.mb_act16 = reinterpret_cast<__half*>(a.mb.act);
+  a.at = AttnFusedArgs{e->arena, 0, e->d_slots, e->qkv, e->qkv_rows, c.q_heads, e->d_rope,
+                       reinterpret_cast<__half*>(e->attn), e->attn_part, (c.ctx_cap + kAttnChunk - 1) / kAttnChunk,
+                       e->attn_cnt, B, chk_of(e), 0, 0};
+  a.wg_stride = (size_t)2 * F * H / 2; a.sg_stride = (size_t)F * (H / g);
+  a.wd_stride = (size_t)H * F / 2;     a.sd_stride = (size_t)H * (F / g) / 2;
+  a.u_log = e->d_u_log;
+  a.bar = e->pst_bar;
+  a.err = e->d_err;
+  a.drop_unit1 = e->test_drop_unit >= 0 ? e->test_drop_unit + 1 : 0;
+  a.geo = e->pgeo;
+  if ((err = launch_persist_step(a, c.head_dim, g, s)) != cudaSuccess) return err;
+  LmArgs la{};
+  la.W = e->lm_head; la.V = c.vocab; la.K = H; la.X = e->xn; la.B = B; la.logits = e->logits;
+  la.next = e->d_next; la.len = e->arena.len; la.slots = e->d_slots; la.advance = 1;
+  la.keys = e->lm_keys; la.counter = e->lm_counter; la.pdl = 0;
+  if ((err = launch_lm_mma(la, s)) != cudaSuccess) return err;
+  if (launches) *launches = 3;
   return cudaSuccess;
 }
 
@@ -576,6 +638,20 @@ bm_status check_config(const bm_config& c) {
       return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: prefill_tc needs the warp-MMA family and rows that are "
                                            "multiples of 128 with reduction lengths multiples of 128");
   }
+  if (c.persistent_step) {
+    const bool mma_ok = c.kernel_policy == BM_POLICY_MMA || (c.kernel_policy == BM_POLICY_AUTO && mma_shapes_ok(c));
+    PersistGeo geo{};
+    const char* why = "";
+    const int rows = std::min(c.max_streams, kPMaxRows);
+    if (!mma_ok)
+      return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: persistent_step needs the warp-MMA kernel family");
+    if (!attention_fused_supports(AttnArena{nullptr, nullptr, nullptr, c.layers, c.max_streams, c.kv_heads, c.ctx_cap,
+                                            c.head_dim},
+                                  c.q_heads) ||
+        !persist_plan(c.hidden, c.q_heads * c.head_dim, (c.q_heads + 2 * c.kv_heads) * c.head_dim, c.ffn, c.experts,
+                      c.top_k, c.group, c.head_dim, c.ctx_cap, std::min(rows, 64 / c.top_k), &geo, &why))
+      return set_error(BM_ERR_UNSUPPORTED, std::string("bm_engine_create: persistent_step: ") + why);
+  }
   if (c.kernel_policy == BM_POLICY_TC && !tc_shapes_ok(c))
     return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: shapes outside the tensor-core family (rows must be "
                                          "multiples of 128, reduction lengths multiples of 64 up to 4096)");
@@ -595,6 +671,7 @@ void free_engine(bm_engine* e) {
   if (e->arena_mem) cudaFree(e->arena_mem);
   if (e->scratch) cudaFree(e->scratch);
   if (e->pf_mem) cudaFree(e->pf_mem);
+  if (e->pmem) cudaFree(e->pmem);
   delete e;
 }
 
@@ -782,6 +859,19 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
     BM_CUDA(encode_rows_tmap(&e->tm_act, pmb.act, P * c.top_k, F, F), "prompt tensor map (expert activations)");
     e->scratch_bytes += o2;
   }
+  if (c.persistent_step) {
+    e->persist_rows = std::min(std::min(c.max_streams, kPMaxRows), 64 / c.top_k);
+    const char* why = "";
+    if (!persist_plan(H, qd, e->qkv_rows, F, E, c.top_k, g, c.head_dim, c.ctx_cap, e->persist_rows, &e->pgeo, &why))
+      return set_error(BM_ERR_UNSUPPORTED, std::string("bm_engine_create: persistent_step: ") + why);
+    BM_CUDA(persist_init(e->pgeo, c.head_dim, g, &e->pgeo.grid), "persistent step attributes");
+    const size_t lb = al(sizeof(PersistLayer) * c.layers);
+    BM_CUDA(cudaMalloc(&e->pmem, lb + 256), "persistent step allocation");
+    BM_CUDA(cudaMemset(e->pmem, 0, lb + 256), "persistent step reset");
+    e->d_players = static_cast<PersistLayer*>(e->pmem);
+    e->pst_bar = reinterpret_cast<unsigned int*>(static_cast<char*>(e->pmem) + lb);
+    e->h_players.assign(c.layers, PersistLayer{});
+  }
   BM_CUDA(cudaMallocHost(&e->h_stage, sizeof(int32_t) * (2 * bm_engine::kStageRing + 1) * S),
           "pinned staging allocation");
   e->h_aux = e->h_stage + 2 * bm_engine::kStageRing * S;
@@ -872,6 +962,13 @@ bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w
   d.has_ffn_norm = w->ffn_norm != nullptr;
   if (w->attn_norm) BM_CUDA(cp(d.attn_norm_buf, w->attn_norm, (size_t)H * 2), "set_layer attn norm");
   if (w->ffn_norm) BM_CUDA(cp(d.ffn_norm_buf, w->ffn_norm, (size_t)H * 2), "set_layer ffn norm");
+  if (e->persist_rows) {
+    auto u32c = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
+    e->h_players[layer] = PersistLayer{d.wqkv, u32c(d.wqkv_s), d.wo, u32c(d.wo_s), d.wr, d.wg, u32c(d.wg_s), d.wd,
+                                       u32c(d.wd_s), d.has_attn_norm ? d.attn_norm_buf : nullptr,
+                                       d.has_ffn_norm ? d.ffn_norm_buf : nullptr};
+    e->players_dirty = true;
+  }
   d.set = true;
   return bm::ok();
 }
@@ -911,9 +1008,10 @@ bm_status bm_engine_sync(bm_engine* e, void* stream) {
     static const char* what[] = {"", "an out-of-range slot id was skipped", "an out-of-range position was skipped",
                                  "an out-of-range token id was skipped",
                                  "a tensor-core projection's pipeline wait timed out",
-                                 "an expert projection's pipeline wait timed out (the CTA stopped consuming)"};
+                                 "an expert projection's pipeline wait timed out (the CTA stopped consuming)",
+                                 "a wait of the persistent decode step timed out (every CTA left the step)"};
     return set_error(BM_ERR_DEVICE_CHECK, std::string("device check code ") + std::to_string(flag) + ": " +
-                                              (flag >= 1 && flag <= 5 ? what[flag] : "unknown"));
+                                              (flag >= 1 && flag <= 6 ? what[flag] : "unknown"));
   }
   return bm::ok();
 }
@@ -1090,6 +1188,13 @@ bm_status stage_inputs(bm_engine* e, int B, const int32_t* slots, const int32_t*
 // eagerly.  *n_out = the kernels it launches.
 bm_status run_step(bm_engine* e, int B, int prompt, cudaStream_t s, int* n_out, const char* who) {
   int n = 0;
+  if (e->persist_rows && e->players_dirty) {
+    BM_CUDA(cudaMemcpyAsync(e->d_players, e->h_players.data(), sizeof(PersistLayer) * e->h_players.size(),
+                            cudaMemcpyHostToDevice, s),
+            "persistent step layer table");
+    BM_CUDA(cudaStreamSynchronize(s), "persistent step layer table");
+    e->players_dirty = false;
+  }
   if (e->cfg.use_graph) {
     const int key = prompt == kDecode ? B : -(4 * B + prompt);   // prompt graphs under negative keys
     auto it = e->graphs.find(key);
@@ -1499,6 +1604,23 @@ bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item) {
   if (!e) return set_error(BM_ERR_INVALID_ARG, "bm_engine_test_drop_expert_item: null engine");
   std::lock_guard<std::mutex> lk(e->mu);
   e->test_drop_item = item < 0 ? -1 : item;
+  return bm::ok();
+}
+
+bm_status bm_engine_test_drop_persist_unit(bm_engine* e, int unit) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "bm_engine_test_drop_persist_unit: null engine");
+  std::lock_guard<std::mutex> lk(e->mu);
+  e->test_drop_unit = unit < 0 ? -1 : unit;
+  // the captured decode graphs hold the old setting: capture again
+  for (auto it = e->graphs.begin(); it != e->graphs.end();) {
+    if (it->first > 0) {
+      cudaGraphExecDestroy(it->second);
+      e->graph_kernels.erase(it->first);
+      it = e->graphs.erase(it);
+    } else {
+      ++it;
+    }
+  }
   return bm::ok();
 }
 

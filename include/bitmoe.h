@@ -96,6 +96,15 @@ typedef struct bm_config {
                         of max_streams rows (the bytes of as many decode steps);
                         1 = prompt-length GEMMs on the tcgen05 tensor cores in
                         blocks of up to 512 rows (needs the warp-MMA family)   */
+  int persistent_step; /* 1: decode steps of B <= min(8, max_streams, 64 / top_k)
+                        rows run every layer in one persistent cooperative
+                        kernel (one CTA per SM, grid barriers between the
+                        phases), the solo / small-batch path of [KV-slot
+                        isolation] (follow-up update).  It computes every
+                        value with the multi-kernel step's arithmetic, so the
+                        bytes are the same whichever path ran a step.  Needs
+                        the warp-MMA family; larger steps use the
+                        multi-kernel step.                                     */
 } bm_config;
 
 /* One decoder layer's weights, canonical layout, DEVICE pointers.  Borrowed
@@ -184,7 +193,10 @@ bm_status bm_engine_set_embeddings(bm_engine* e, const uint16_t* embed, const ui
  * out-of-range token id (each skipped by the kernel that met it), 4 a
  * tensor-core projection's pipeline wait that timed out, 5 an expert
  * projection's pipeline wait that timed out (that CTA stopped after waiting
- * for the copies it had issued).  No check traps: the context stays usable. */
+ * for the copies it had issued), 6 a wait of the persistent decode step
+ * (persistent_step) that timed out (every CTA left the step at its next grid
+ * barrier; the step's outputs are not valid).  No check traps: the context
+ * stays usable. */
 bm_status bm_engine_sync(bm_engine* e, void* stream);
 
 /* Counters and standing memory. */
@@ -463,6 +475,16 @@ bm_status bm_engine_read_hidden(bm_engine* e, int B, uint16_t* out, void* stream
  * Nothing faults: every copy that was issued is waited for before the CTA
  * exits.  decode_step ignores this setting. */
 bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item);
+
+/* Failure-detection tests only: make the persistent decode step (engines
+ * created with persistent_step) skip the copy of weight unit `unit` of its
+ * CTAs' producers (the unit-th 16-row x 256-column block each producer would
+ * stream; -1 = none, the default).  The consumer's bounded wait runs out
+ * after about a second, every CTA leaves the step at its next grid barrier,
+ * and bm_engine_sync reports BM_ERR_DEVICE_CHECK with code 6.  Nothing
+ * faults: every copy that was issued lands before its CTA exits.  Captured
+ * decode graphs are dropped so that the next steps use the setting. */
+bm_status bm_engine_test_drop_persist_unit(bm_engine* e, int unit);
 
 /* Measurement only: time the tcgen05 MMA on the current GPU.  One CTA issues
  * `iters` stages of four kind::f16 MMAs of M 128 x N n x K 16 (zero operands)

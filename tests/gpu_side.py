@@ -49,18 +49,21 @@ def layer_weights(cfg_name, cfg, layer, gen_device="cuda"):
             "attn_norm": None, "ffn_norm": None}
 
 
-def engine_config(cfg, layers, max_streams, ctx_cap, policy=bm.POLICY_AUTO, use_graph=1, prefill_tc=0):
+def engine_config(cfg, layers, max_streams, ctx_cap, policy=bm.POLICY_AUTO, use_graph=1, prefill_tc=0,
+                  persistent_step=0):
     return {"hidden": cfg["hidden"], "q_heads": cfg["q_heads"], "kv_heads": cfg["kv_heads"],
             "head_dim": cfg["head_dim"], "experts": cfg["experts"], "top_k": cfg["top_k"], "ffn": cfg["ffn"],
             "group": cfg["group"], "vocab": cfg["vocab"], "layers": layers, "rope_base": cfg["rope_base"],
             "rms_eps": 1e-6, "max_streams": max_streams, "ctx_cap": ctx_cap, "renorm_topk": 1,
-            "kernel_policy": policy, "use_graph": use_graph, "prefill_tc": prefill_tc}
+            "kernel_policy": policy, "use_graph": use_graph, "prefill_tc": prefill_tc,
+            "persistent_step": persistent_step}
 
 
 def build_engine(cfg_name, cfg, layers, max_streams, ctx_cap, policy=bm.POLICY_AUTO, use_graph=1,
-                 gen_device="cuda", prefill_tc=0):
+                 gen_device="cuda", prefill_tc=0, persistent_step=0):
     """An engine with every layer's weights and the embeddings loaded."""
-    e = bm.bm_engine_create(engine_config(cfg, layers, max_streams, ctx_cap, policy, use_graph, prefill_tc))
+    e = bm.bm_engine_create(engine_config(cfg, layers, max_streams, ctx_cap, policy, use_graph, prefill_tc,
+                                          persistent_step))
     for l in range(layers):
         w = layer_weights(cfg_name, cfg, l, gen_device)
         bm.bm_engine_set_layer(e, l, w)

@@ -68,6 +68,10 @@ def parse():
                     help="time the fused attention at the slot-attention workload's lengths (0 to skip)")
     ap.add_argument("--kernel-sweep", default="1,4,8,16,32",
                     help="B values of the per-kernel GB/s table ('' to skip)")
+    ap.add_argument("--persistent", type=int, default=0,
+                    help="1: decode steps of B <= 8 run as the one-launch persistent step (same bytes as the "
+                         "multi-kernel step); 0: the multi-kernel step.  Either way the sweep times those B on "
+                         "both paths (the solo / batched toggle)")
     return ap.parse_args()
 
 
@@ -243,12 +247,12 @@ def peaks():
 
 # ---------------------------------------------------------------- our arm
 
-def build_model(bm, cfg, layers, max_streams, policy, prefill_tc=0):
+def build_model(bm, cfg, layers, max_streams, policy, prefill_tc=0, persistent_step=0):
     import torch
     from gpu_side import build_engine
     t = time.time()
     e = build_engine(WORKLOAD, cfg, layers, max_streams=max_streams, ctx_cap=cfg["ctx_cap"], policy=policy,
-                     gen_device="cuda", prefill_tc=prefill_tc)
+                     gen_device="cuda", prefill_tc=prefill_tc, persistent_step=persistent_step)
     torch.cuda.synchronize()
     return e, time.time() - t
 
@@ -302,7 +306,8 @@ def run_ours(args, dist, world, rank, local):
     B = args.batch
     cfg["max_streams"] = max(args.max_streams or cfg["max_streams"], B)
     e, t_build = build_model(bm, cfg, args.layers, cfg["max_streams"], args.policy,
-                             prefill_tc=1 if args.prefill_path == "tc" else 0)
+                             prefill_tc=1 if args.prefill_path == "tc" else 0, persistent_step=1)
+    bm.bm_engine_set_persistent_step(e, args.persistent)
     slots, last, lens = prefill(bm, e, cfg, B, args.layers, args.prefill)
     stream = torch.cuda.current_stream()
     cur = last.clone()
@@ -367,12 +372,11 @@ def run_ours(args, dist, world, rank, local):
                 "peak_source": f"{peak_kind} hbm_gbs (copy)"}
     step_bytes = sum(p["bytes"] for p in prof.values()) / max(1, args.profile_steps)
 
-    # B sweep (subsets of the joined streams)
-    sweep = {}
+    # B sweep (subsets of the joined streams); with the persistent step on,
+    # its B also run with it switched off (the multi-kernel step, same bytes)
+    sweep, sweep_mk = {}, {}
     if args.sweep:
-        for b in [int(x) for x in args.sweep.split(",") if x]:
-            if b > B:
-                continue
+        def time_b(b):
             sub = slots[:b]
             c1, n1 = cur[:b].clone(), torch.empty(b, dtype=torch.int32, device="cuda")
 
@@ -384,7 +388,16 @@ def run_ours(args, dist, world, rank, local):
             d = timed_region(sstep, torch.cuda.synchronize, dist, args.sweep_steps, 3,
                              new_event=lambda: torch.cuda.Event(enable_timing=True), device="cuda",
                              label="sweep_timed")
-            sweep[str(b)] = round(world * b * args.sweep_steps / d, 1)
+            return round(world * b * args.sweep_steps / d, 1)
+
+        for b in [int(x) for x in args.sweep.split(",") if x]:
+            if b > B:
+                continue
+            sweep[str(b)] = time_b(b)
+            if b <= min(8, 64 // cfg["top_k"]):
+                bm.bm_engine_set_persistent_step(e, 1 - args.persistent)
+                sweep_mk[str(b)] = time_b(b)   # the other path
+                bm.bm_engine_set_persistent_step(e, args.persistent)
     # per-kernel GB/s at each B of the kernel sweep (eager steps with events)
     ktab = None
     if args.kernel_sweep:
@@ -460,7 +473,17 @@ def run_ours(args, dist, world, rank, local):
         "roofline": roof,
         "step_algorithmic_GB": round(step_bytes / 1e9, 3),
         "step_GB_per_s": round(step_bytes / (dt / args.steps) / 1e9, 1),
-        "kernels": kernels, "sweep_tok_s": sweep, "sweep_weight_roofline": sweep_roof, "kernels_by_B": ktab,
+        "kernels": kernels, "sweep_tok_s": sweep, "sweep_weight_roofline": sweep_roof,
+        "small_batch_path": {
+            "default": "persistent kernel" if args.persistent else "multi-kernel step",
+            "rows": min(8, 64 // cfg["top_k"]),
+            "persistent_tok_s": sweep_mk if not args.persistent else {b: sweep[b] for b in sweep_mk},
+            "multikernel_tok_s": {b: sweep[b] for b in sweep_mk} if not args.persistent else sweep_mk,
+            "persistent_over_multikernel": {
+                b: round((sweep_mk[b] / sweep[b]) if not args.persistent else (sweep[b] / sweep_mk[b]), 3)
+                for b in sweep_mk if sweep_mk[b] and sweep[b]},
+            "bytes": "identical on both paths (tests/test_gpu_persist.py)"},
+        "kernels_by_B": ktab,
         "arrivals": arr, "prefill": pf, "prompt_gemm": pg, "attention_long": att,
         "weight_GB": round(stats["weight_bytes"] / 1e9, 3), "arena_GB": round(stats["arena_bytes"] / 1e9, 3),
         "setup_s": round(t_build, 1),

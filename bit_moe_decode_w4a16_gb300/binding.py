@@ -110,6 +110,7 @@ def lib():
             "bm_engine_read_hidden": ([V, I, V, V], S),
             "bm_engine_test_drop_expert_item": ([V, I], S),
             "bm_engine_test_drop_persist_unit": ([V, I], S),
+            "bm_engine_set_persistent_step": ([V, I], S),
             "bm_slot_map_create": ([I, I, ctypes.POINTER(V)], S),
             "bm_slot_map_destroy": ([V], None),
             "bm_slot_map_acquire": ([V, I, PI], S),
@@ -340,6 +341,10 @@ def bm_engine_read_hidden(e, B, out, stream=None):
 
 def bm_engine_test_drop_expert_item(e, item):
     _check(lib().bm_engine_test_drop_expert_item(e, int(item)))
+
+
+def bm_engine_set_persistent_step(e, enable):
+    _check(lib().bm_engine_set_persistent_step(e, int(enable)))
 
 
 def bm_engine_test_drop_persist_unit(e, unit):

@@ -962,7 +962,7 @@ bm_status bm_engine_set_layer(bm_engine* e, int layer, const bm_layer_weights* w
   d.has_ffn_norm = w->ffn_norm != nullptr;
   if (w->attn_norm) BM_CUDA(cp(d.attn_norm_buf, w->attn_norm, (size_t)H * 2), "set_layer attn norm");
   if (w->ffn_norm) BM_CUDA(cp(d.ffn_norm_buf, w->ffn_norm, (size_t)H * 2), "set_layer ffn norm");
-  if (e->persist_rows) {
+  if (e->cfg.persistent_step) {
     auto u32c = [](const __half* p) { return reinterpret_cast<const uint32_t*>(p); };
     e->h_players[layer] = PersistLayer{d.wqkv, u32c(d.wqkv_s), d.wo, u32c(d.wo_s), d.wr, d.wg, u32c(d.wg_s), d.wd,
                                        u32c(d.wd_s), d.has_attn_norm ? d.attn_norm_buf : nullptr,
@@ -1188,7 +1188,7 @@ bm_status stage_inputs(bm_engine* e, int B, const int32_t* slots, const int32_t*
 // eagerly.  *n_out = the kernels it launches.
 bm_status run_step(bm_engine* e, int B, int prompt, cudaStream_t s, int* n_out, const char* who) {
   int n = 0;
-  if (e->persist_rows && e->players_dirty) {
+  if (e->cfg.persistent_step && e->players_dirty) {
     BM_CUDA(cudaMemcpyAsync(e->d_players, e->h_players.data(), sizeof(PersistLayer) * e->h_players.size(),
                             cudaMemcpyHostToDevice, s),
             "persistent step layer table");
@@ -1604,6 +1604,28 @@ bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item) {
   if (!e) return set_error(BM_ERR_INVALID_ARG, "bm_engine_test_drop_expert_item: null engine");
   std::lock_guard<std::mutex> lk(e->mu);
   e->test_drop_item = item < 0 ? -1 : item;
+  return bm::ok();
+}
+
+bm_status bm_engine_set_persistent_step(bm_engine* e, int enable) {
+  if (!e) return set_error(BM_ERR_INVALID_ARG, "bm_engine_set_persistent_step: null engine");
+  std::lock_guard<std::mutex> lk(e->mu);
+  const bm_config& c = e->cfg;
+  if (!c.persistent_step)
+    return set_error(BM_ERR_UNSUPPORTED, "bm_engine_set_persistent_step: the engine was created without persistent_step");
+  const int rows = enable ? std::min(std::min(c.max_streams, kPMaxRows), 64 / c.top_k) : 0;
+  if (rows != e->persist_rows) {
+    e->persist_rows = rows;
+    for (auto it = e->graphs.begin(); it != e->graphs.end();) {   // decode graphs of the other path
+      if (it->first > 0) {
+        cudaGraphExecDestroy(it->second);
+        e->graph_kernels.erase(it->first);
+        it = e->graphs.erase(it);
+      } else {
+        ++it;
+      }
+    }
+  }
   return bm::ok();
 }
 

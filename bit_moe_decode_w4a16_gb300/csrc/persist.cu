@@ -20,11 +20,14 @@
 // So a stream's bytes do not depend on which path ran its step.
 //
 // Warp roles.  Warps 0-15 compute; warp 16 is the weight producer: one lane
-// streams, in the order the compute warps consume them, "units" of 16 weight
-// rows x 256 of K (2 KB of int4 in the mma layout, plus their scales) into a
-// ring of shared-memory slots with cp.async.bulk, each slot's completion
-// counted in bytes on its `full` mbarrier; a compute warp copies a unit to
-// registers and releases the slot (`empty` mbarrier).  The dense weights do
+// streams, in the order the compute warps consume them, weight "items" into a
+// byte ring in shared memory with cp.async.bulk.  An item is one tile job, a
+// 16-row tile of a matrix over its whole K (contiguous in the mma layout:
+// 16 KB of int4 for K = 2048, and its scales), copied with one bulk copy per
+// 16 KB and counted in bytes on the item's `full` mbarrier; it is consumed in
+// "units" of 256 of K (2 KB) by the compute warps, which copy a unit to
+// registers and count it off; the last one releases the item (`empty`
+// mbarrier).  Few large copies keep many bytes in flight per SM.  The dense weights do
 // not depend on the data, so the producer runs ahead across phases and layers
 // (the next layer's QKV and output projection arrive while the experts of
 // this one compute); the expert units wait for this CTA's routing (the
@@ -66,15 +69,21 @@ constexpr int kPCThreads = kPCompute * 32;
 constexpr int kUnitChunks = 4;                // CPW: chunks of 64 along K per unit
 constexpr int kUnitW = kUnitChunks * 512;     // weight bytes of a unit
 constexpr int kRoundUnits = 32;               // units per reduction round
-constexpr int kMaxSlots = 64;
+constexpr int kMaxItems = 64;                 // weight items in flight per CTA
 constexpr int kPMaxPairs = 64;
 constexpr int kPMaxE = 256;
 constexpr int kBarCompute = 1, kBarGroup = 2;
 constexpr unsigned long long kPWaitNs = 1000000000ull;   // a bounded wait gives up after about a second
 constexpr int kPErr = 6;
+constexpr int kGUTiles = 1;                   // gate/up tiles per weight item (one expert's consecutive tiles)
+constexpr int kMaxGUJobs = 64;                // gate/up tile jobs of one CTA
+constexpr uint32_t kCopyMax = 65536;          // bytes per bulk copy: the per-copy cost is paid per copy, not per byte
 
 struct PSmem {
-  uint64_t full[kMaxSlots], empty[kMaxSlots], route;
+  uint64_t full[kMaxItems], empty[kMaxItems], route;   // per weight item (descriptor d = item % kMaxItems)
+  unsigned long long it_v[kMaxItems];   // producer: virtual ring offset of the item
+  uint32_t it_off[kMaxItems];           // ring offset of the item's bytes
+  int it_cnt[kMaxItems];                // units of the item consumed so far
   int ids[kPMaxPairs], rank[kPMaxPairs], pos_of[kPMaxPairs], pair_token[kPMaxPairs];
   float w[kPMaxPairs];
   int cnt[kPMaxE], off[kPMaxE + 1];
@@ -83,6 +92,9 @@ struct PSmem {
   float out[kPMaxPairs][16];      // down outputs of this CTA's tile, [sorted pair][row]
   float rnorm[kPMaxRows][32];     // RMSNorm partial sums of the 32 warps of the replayed reduction
   float router_red[routedev::kRouterWarps];
+  float hres[kPMaxRows][16];      // the residual rows of this CTA's down tile, for the combine
+  short gu_item[kMaxGUJobs], gu_tt[kMaxGUJobs], gu_n[kMaxGUJobs];   // gate/up job -> item, tile in item, tiles
+  int gu_items;
   int abort;   // set by any thread of the CTA that gives up
   int stop;    // thread 0's copy of abort at the last grid barrier
 };
@@ -166,23 +178,9 @@ __device__ __forceinline__ bool grid_barrier(const PersistArgs& a, PSmem& ps, un
 }
 
 // ---------------------------------------------------------------- units
-// Unit (tile T, ks) of a matrix in the mma layout: chunks [4 ks, 4 ks + 4)
-// of 16-row tile T (2 KB, contiguous) and the scale words of their groups
-// (contiguous too).
-struct Mat {
-  const uint8_t* W;
-  const uint32_t* S;
-  int NC, NG;   // chunks of 64 and scale groups along K
-};
-
-template <int G>
-__device__ __forceinline__ const uint8_t* unit_w(const Mat& m, int T, int ks) {
-  return m.W + ((size_t)T * m.NC + ks * kUnitChunks) * 512;
-}
-template <int G>
-__device__ __forceinline__ const uint32_t* unit_s(const Mat& m, int T, int ks) {
-  return m.S + ((size_t)T * m.NG + (ks * kUnitChunks * 64) / G) * 8;
-}
+// A unit is 256 of K of a 16-row tile: 4 chunks of 64 (2 KB of int4 in the
+// mma layout) and the scale words of their groups; a tile's units are
+// contiguous, and so are its scale words.
 template <int G>
 __host__ __device__ constexpr uint32_t unit_s_bytes() {
   return (uint32_t)(kUnitChunks * 64 / G) * 32u;
@@ -194,15 +192,15 @@ __host__ __device__ constexpr uint32_t unit_s_bytes() {
 // The arithmetic is the consumer step of the staged expert kernel
 // (w4_mma_staged.cuh), which is that of k_w4_mma.
 template <int G>
-__device__ __forceinline__ void unit_mma(const unsigned char* slot, uint32_t empty_bar, const __half* xrow, int c0,
-                                         float (&acc)[4]) {
+__device__ __forceinline__ void unit_mma(const unsigned char* wp, const unsigned char* sp, PSmem& ps, int d, int KS,
+                                         const __half* xrow, int c0, float (&acc)[4]) {
   constexpr int kSpg = G / 16;
   constexpr int kSpc = G >= kChunkK ? 1 : kChunkK / G;
   const int lane = threadIdx.x & 31;
   uint4 wreg[kUnitChunks], xreg[kUnitChunks][2];
   uint32_t sreg[kUnitChunks][kSpc];
-  const uint4* ws = reinterpret_cast<const uint4*>(slot);
-  const uint32_t* ss = reinterpret_cast<const uint32_t*>(slot + kUnitW);
+  const uint4* ws = reinterpret_cast<const uint4*>(wp);
+  const uint32_t* ss = reinterpret_cast<const uint32_t*>(sp);
 #pragma unroll
   for (int j = 0; j < kUnitChunks; ++j) {
     wreg[j] = ws[j * 32 + lane];
@@ -220,7 +218,10 @@ __device__ __forceinline__ void unit_mma(const unsigned char* slot, uint32_t emp
     }
   }
   __syncwarp();
-  if (lane == 0) tc::mbar_arrive(empty_bar);
+  if (lane == 0 && atomicAdd(&ps.it_cnt[d], 1) == KS - 1) {   // the item's last unit: release it
+    ps.it_cnt[d] = 0;
+    tc::mbar_arrive(tc::smem_u32(&ps.empty[d]));
+  }
   float tmp[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) acc[c] = 0.f;
@@ -261,8 +262,8 @@ struct PPtrs {
 };
 
 // Stage `rows` activation rows of K fp16 values (row stride ld in global,
-// xs in shared) with 16-byte loads; rows past `rows` up to kPMaxRows are not
-// touched (their columns are never stored).
+// xs in shared) with 16-byte loads; rows past `rows` are not touched (their
+// columns are never stored).
 __device__ __forceinline__ void stage_rows(__half* dst, int xs, const __half* src, int ld, int rows, int K) {
   const int per = K / 8;
   for (int i = threadIdx.x; i < rows * per; i += kPCThreads) {
@@ -276,12 +277,16 @@ __device__ __forceinline__ void stage_rows(__half* dst, int xs, const __half* sr
 // it: 1024 threads, thread t summing y[h]^2 for h = t, t + 1024, ... with
 // fmaf, each warp's butterfly, then the 32 warp sums in order; then
 // round_bf16(y * rinv * nw).  Compute thread c plays threads c and c + 512.
-// f16: write fp16 rows to shared memory (stride xs); else bf16 rows to global.
-__device__ __forceinline__ void norm_rows(const PersistArgs& a, PSmem& ps, const bf16* nw, __half* xs_dst, int xs,
-                                          bf16* g_dst) {
+// The rows are first staged in shared memory (ys, B x H bf16) with all
+// loads in flight at once.  xs_dst: fp16 rows to shared memory (stride xs);
+// else bf16 rows to global g_dst.
+__device__ __forceinline__ void norm_rows(const PersistArgs& a, PSmem& ps, const bf16* nw, bf16* ys,
+                                          __half* xs_dst, int xs, bf16* g_dst) {
   const int H = a.H, B = a.B, ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
+  stage_rows(reinterpret_cast<__half*>(ys), H, reinterpret_cast<const __half*>(a.x), H, B, H);
+  NamedSync{kBarCompute, kPCThreads}();
   for (int b = 0; b < B; ++b) {
-    const bf16* y = a.x + (size_t)b * H;
+    const bf16* y = ys + (size_t)b * H;
 #pragma unroll
     for (int hv = 0; hv < 2; ++hv) {
       const int vt = ct + hv * kPCThreads;   // the replayed thread
@@ -299,7 +304,7 @@ __device__ __forceinline__ void norm_rows(const PersistArgs& a, PSmem& ps, const
     float tot = 0.f;
     for (int w = 0; w < 32; ++w) tot += ps.rnorm[b][w];
     const float r = 1.0f / sqrtf(tot / (float)H + a.eps);
-    const bf16* y = a.x + (size_t)b * H;
+    const bf16* y = ys + (size_t)b * H;
     for (int h = ct; h < H; h += kPCThreads) {
       const float v = round_bf16(bf2f(y[h]) * r * (nw ? bf2f(nw[h]) : 1.f));
       if (xs_dst) xs_dst[(size_t)b * xs + h] = __float2half_rn(v);
@@ -320,18 +325,18 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
   const int cta = blockIdx.x, grid = gridDim.x;
   const PersistGeo& geo = a.geo;
   PPtrs p{dsm + geo.ring_off, reinterpret_cast<float*>(dsm + geo.red_off), dsm + geo.uni_off};
-  const int ns = geo.ns;
   constexpr uint32_t kSBytes = unit_s_bytes<G>();
-  const uint32_t slot_bytes = geo.slot_bytes;
+  const uint32_t R = geo.ring_bytes;
   const int H = a.H, B = a.B, F = a.F, E = a.E, K = a.k;
   const int KSq = (H / 64) / kUnitChunks, KSo = (a.qd / 64) / kUnitChunks, KSd = (F / 64) / kUnitChunks;
   const int NTq = a.qkv_rows / 16, NTo = H / 16, NTg = 2 * F / 16, NTd = H / 16;
   const int nEB = E / 8;   // router items per token: 8 experts each
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < ns; ++i) {
+    for (int i = 0; i < kMaxItems; ++i) {
       tc::mbar_init(tc::smem_u32(&ps.full[i]), 1);
       tc::mbar_init(tc::smem_u32(&ps.empty[i]), 1);
+      ps.it_cnt[i] = 0;
     }
     tc::mbar_init(tc::smem_u32(&ps.route), 1);
     tc::fence_mbar_init();
@@ -343,35 +348,45 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
   if (warp == kPCompute) {
     // ================================================================ producer
     if (lane != 0) return;
-    unsigned n = 0;   // units issued
+    unsigned nit = 0, oldest = 0;   // items issued; items seen released
+    unsigned long long vhead = 0;    // virtual ring offset: physical = v % R
     bool ok = true;
-    auto issue = [&](const uint8_t* wsrc, const uint32_t* ssrc) {
-      if (n + 1 == (unsigned)a.drop_unit1) {   // failure-detection tests: this unit never arrives
-        ++n;
-        return;
-      }
-      const int s = (int)(n % (unsigned)ns);
-      if (n >= (unsigned)ns) {
-        if (!pwait(tc::smem_u32(&ps.empty[s]), ((n / ns) - 1) & 1, &ps.abort)) {
+    // One item: [wb bytes of int4 | sb bytes of scales] at a ring offset
+    // where it does not wrap, once the items that held those bytes (and the
+    // item's descriptor) are released.
+    auto issue = [&](const uint8_t* wsrc, uint32_t wb, const uint32_t* ssrc, uint32_t sb) {
+      const uint32_t S = wb + sb;
+      unsigned long long v = vhead;
+      if (v % R + S > R) v = (v / R + 1) * R;
+      while (oldest < nit && (v + S - ps.it_v[oldest % kMaxItems] > R || nit - oldest >= (unsigned)kMaxItems)) {
+        if (!pwait(tc::smem_u32(&ps.empty[oldest % kMaxItems]), (oldest / kMaxItems) & 1, &ps.abort)) {
           ok = false;
           return;
         }
-        tc::fence_proxy_async_smem();
+        ++oldest;
       }
-      const uint32_t dst = tc::smem_u32(p.ring + (size_t)s * slot_bytes);
-      const uint32_t bar = tc::smem_u32(&ps.full[s]);
-      arrive_expect_tx(bar, (uint32_t)kUnitW + kSBytes);
-      bulk_g2s(dst, wsrc, (uint32_t)kUnitW, bar);
-      bulk_g2s(dst + kUnitW, ssrc, kSBytes, bar);
-      ++n;
+      tc::fence_proxy_async_smem();
+      const int d = (int)(nit % kMaxItems);
+      ps.it_v[d] = v;
+      vhead = v + S;
+      const uint32_t off = (uint32_t)(v % R);
+      ps.it_off[d] = off;
+      if (++nit == (unsigned)a.drop_unit1) return;   // failure-detection tests: this item never arrives
+      const uint32_t dst = tc::smem_u32(p.ring + off);
+      const uint32_t bar = tc::smem_u32(&ps.full[d]);
+      arrive_expect_tx(bar, S);
+      for (uint32_t o = 0; o < wb; o += kCopyMax) bulk_g2s(dst + o, wsrc + o, min(kCopyMax, wb - o), bar);
+      bulk_g2s(dst + wb, ssrc, sb, bar);
     };
+    const uint32_t wbH = (uint32_t)(H / 64) * 512u, sbH = (uint32_t)(H / G) * 32u;
+    const uint32_t wbO = (uint32_t)(a.qd / 64) * 512u, sbO = (uint32_t)(a.qd / G) * 32u;
+    const uint32_t wbF = (uint32_t)(F / 64) * 512u, sbF = (uint32_t)(F / G) * 32u;
     for (int l = 0; l < a.layers && ok; ++l) {
       const PersistLayer& Lw = a.L[l];
-      const Mat mq{Lw.wqkv, Lw.sqkv, H / 64, H / G}, mo{Lw.wo, Lw.so, a.qd / 64, a.qd / G};
       for (int T = cta; T < NTq && ok; T += grid)
-        for (int ks = 0; ks < KSq && ok; ++ks) issue(unit_w<G>(mq, T, ks), unit_s<G>(mq, T, ks));
+        issue(Lw.wqkv + (size_t)T * wbH, wbH, Lw.sqkv + (size_t)T * (sbH / 4), sbH);
       for (int T = cta; T < NTo && ok; T += grid)
-        for (int ks = 0; ks < KSo && ok; ++ks) issue(unit_w<G>(mo, T, ks), unit_s<G>(mo, T, ks));
+        issue(Lw.wo + (size_t)T * wbO, wbO, Lw.so + (size_t)T * (sbO / 4), sbO);
       // this CTA's router rows to L2 ahead of the routing phase
       for (int i = cta; i < nEB * B; i += grid) {
         const float* wr = Lw.wr + (size_t)(i % nEB) * 8 * H;
@@ -381,49 +396,60 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
       if (!ok) break;
       if (!pwait(tc::smem_u32(&ps.route), (uint32_t)(l & 1), &ps.abort)) { ok = false; break; }
       const int U = ps.n_active;
-      for (int j = cta; j < U * NTg && ok; j += grid) {
-        const int e = ps.active_e[j / NTg], T = j % NTg;
-        const Mat mg{Lw.wg + (size_t)e * a.wg_stride, Lw.sg + (size_t)e * a.sg_stride, H / 64, H / G};
-        for (int ks = 0; ks < KSq && ok; ++ks) issue(unit_w<G>(mg, T, ks), unit_s<G>(mg, T, ks));
+      // gate/up: this CTA's contiguous range of (expert, tile) jobs, expert
+      // major, in items of up to kGUTiles consecutive tiles of one expert
+      const int J = U * NTg;
+      const int jb = (int)((long long)J * cta / grid), je = (int)((long long)J * (cta + 1) / grid);
+      for (int j = jb; j < je && ok;) {
+        const int u = j / NTg, T = j - u * NTg, nt = min(min(kGUTiles, je - j), NTg - T);
+        const int e = ps.active_e[u];
+        issue(Lw.wg + (size_t)e * a.wg_stride + (size_t)T * wbH, (uint32_t)nt * wbH,
+              Lw.sg + (size_t)e * a.sg_stride + (size_t)T * (sbH / 4), (uint32_t)nt * sbH);
+        j += nt;
       }
       for (int T = cta; T < NTd && ok; T += grid)
         for (int u = 0; u < U && ok; ++u) {
           const int e = ps.active_e[u];
-          const Mat md{Lw.wd + (size_t)e * a.wd_stride, Lw.sd + (size_t)e * a.sd_stride, F / 64, F / G};
-          for (int ks = 0; ks < KSd && ok; ++ks) issue(unit_w<G>(md, T, ks), unit_s<G>(md, T, ks));
+          issue(Lw.wd + (size_t)e * a.wd_stride + (size_t)T * wbF, wbF,
+                Lw.sd + (size_t)e * a.sd_stride + (size_t)T * (sbF / 4), sbF);
         }
     }
     if (!ok) fail(a, ps);
     // the copies still in flight land before this thread (and so the CTA) exits
-    for (unsigned m = n > (unsigned)ns ? n - ns : 0u; m < n; ++m)
-      tc::mbar_wait(tc::smem_u32(&ps.full[m % ns]), (m / ns) & 1, 1u << 16);
+    for (unsigned m = nit > (unsigned)kMaxItems ? nit - kMaxItems : 0u; m < nit; ++m)
+      tc::mbar_wait(tc::smem_u32(&ps.full[m % kMaxItems]), (m / kMaxItems) & 1, 1u << 16);
     return;
   }
 
   // ================================================================ compute warps
-  unsigned n = 0;      // units consumed (the producer's order)
+  unsigned nit = 0;    // items consumed (the producer's order)
   unsigned nbar = 0;   // grid barriers passed
   __half* xs16 = reinterpret_cast<__half*>(p.uni);
 
-  // One phase of tile jobs: job j (0 <= j < nj) has KS units; rounds of
-  // whole jobs (at most kRoundUnits units); col(j, g) = the staged row of
-  // token column g of job j (or -1); epi(j, l, jj, v0, v1) stores a result.
-  auto run_jobs = [&](int nj, int KS, int xstride, auto col, auto epi) {
+  // One phase of tile jobs: job j (0 <= j < nj) has KS units and sits in
+  // weight item place(j) = (item, tile in item, tiles of the item) of the
+  // phase's n_items items; rounds of whole jobs (at most kRoundUnits units);
+  // col(j, g) = the staged row of token column g of job j (or -1);
+  // epi(j, l, jj, v0, v1) stores a result.
+  auto run_jobs = [&](int nj, int KS, int n_items, int xstride, auto place, auto col, auto epi) {
     const int per_round = kRoundUnits / KS;
     for (int j0 = 0; j0 < nj; j0 += per_round) {
       const int rj = min(per_round, nj - j0), nu = rj * KS;
       for (int i = warp; i < nu; i += kPCompute) {
         const int jl = i / KS, ks = i - jl * KS;
-        const unsigned un = n + (unsigned)(j0 * KS + i);
-        const int s = (int)(un % (unsigned)ns);
+        const int3 pl = place(j0 + jl);
+        const unsigned it = nit + (unsigned)pl.x;
+        const int d = (int)(it % kMaxItems);
         float acc[4];
-        if (!pwait(tc::smem_u32(&ps.full[s]), (un / ns) & 1, &ps.abort)) {
+        if (!pwait(tc::smem_u32(&ps.full[d]), (it / kMaxItems) & 1, &ps.abort)) {
           if (lane == 0) fail(a, ps);
           for (int c = 0; c < 4; ++c) acc[c] = 0.f;
         } else {
           const int r = col(j0 + jl, lane >> 2);
-          unit_mma<G>(p.ring + (size_t)s * slot_bytes, tc::smem_u32(&ps.empty[s]), r >= 0 ? xs16 + (size_t)r * xstride : nullptr,
-                      ks * kUnitChunks, acc);
+          const unsigned char* item = p.ring + ps.it_off[d];
+          const int un = pl.y * KS + ks;   // unit within the item
+          unit_mma<G>(item + (size_t)un * kUnitW, item + (size_t)pl.z * KS * kUnitW + (size_t)un * kSBytes, ps, d,
+                      pl.z * KS, r >= 0 ? xs16 + (size_t)r * xstride : nullptr, ks * kUnitChunks, acc);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) p.red[(i * 4 + c) * 32 + lane] = acc[c];
@@ -441,8 +467,9 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
       }
       NamedSync{kBarCompute, kPCThreads}();
     }
-    n += (unsigned)(nj * KS);
+    nit += (unsigned)n_items;
   };
+  auto one = [](int j) { return make_int3(j, 0, 1); };   // one tile per item
 
   for (int l = 0; l < a.layers; ++l) {
     const PersistLayer& Lw = a.L[l];
@@ -453,11 +480,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
       stage_rows(xs16, xq, a.xn16, H, B, H);
       NamedSync{kBarCompute, kPCThreads}();
     } else {
-      norm_rows(a, ps, Lw.attn_nw, xs16, xq, nullptr);
+      norm_rows(a, ps, Lw.attn_nw, reinterpret_cast<bf16*>(xs16 + (size_t)B * xq), xs16, xq, nullptr);
     }
     {
       const int njq = cta < NTq ? (NTq - 1 - cta) / grid + 1 : 0;
-      run_jobs(njq, KSq, xq, [&](int, int g) { return g < B ? g : -1; },
+      run_jobs(njq, KSq, njq, xq, one, [&](int, int g) { return g < B ? g : -1; },
                [&](int j, int ll, int jj, float v0, float v1) {
                  const int T = cta + j * grid, m = 2 * (ll & 3) + jj;
                  if (m >= B) return;
@@ -485,7 +512,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
     NamedSync{kBarCompute, kPCThreads}();
     {
       const int njo = cta < NTo ? (NTo - 1 - cta) / grid + 1 : 0;
-      run_jobs(njo, KSo, xo, [&](int, int g) { return g < B ? g : -1; },
+      run_jobs(njo, KSo, njo, xo, one, [&](int, int g) { return g < B ? g : -1; },
                [&](int j, int ll, int jj, float v0, float v1) {
                  const int T = cta + j * grid, m = 2 * (ll & 3) + jj;
                  if (m >= B) return;
@@ -586,20 +613,39 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
         if (a.u_log) a.u_log[l] = U;
       }
     }
+    // this CTA's contiguous range of gate/up jobs and their items (the
+    // producer's grouping); the residual rows of its down tile
+    const int J = U * NTg;
+    const int jb = (int)((long long)J * cta / grid), je = (int)((long long)J * (cta + 1) / grid);
+    if (threadIdx.x == 0) {
+      int ni = 0;
+      for (int j = jb; j < je; ++ni) {
+        const int u = j / NTg, T = j - u * NTg, nt = min(min(kGUTiles, je - j), NTg - T);
+        for (int tt = 0; tt < nt; ++tt) {
+          ps.gu_item[j - jb + tt] = (short)ni;
+          ps.gu_tt[j - jb + tt] = (short)tt;
+          ps.gu_n[j - jb + tt] = (short)nt;
+        }
+        j += nt;
+      }
+      ps.gu_items = ni;
+    }
+    if (cta < NTd)
+      for (int idx = threadIdx.x; idx < B * 16; idx += kPCThreads)
+        ps.hres[idx >> 4][idx & 15] = bf2f(__ldcg(a.h + (size_t)(idx >> 4) * H + cta * 16 + (idx & 15)));
     const int xg = H + 32;
     stage_rows(xs16, xg, reinterpret_cast<const __half*>(a.mb.xn), H, B, H);
     NamedSync{kBarCompute, kPCThreads}();
     {
-      const int ng = U * NTg;
-      const int njg = cta < ng ? (ng - 1 - cta) / grid + 1 : 0;
-      run_jobs(njg, KSq, xg,
+      run_jobs(je - jb, KSq, ps.gu_items, xg,
+               [&](int j) { return make_int3(ps.gu_item[j], ps.gu_tt[j], ps.gu_n[j]); },
                [&](int j, int g) {
-                 const int jj = cta + j * grid, u = jj / NTg;
+                 const int u = (jb + j) / NTg;
                  const int off = ps.active_off[u], cnt = ps.active_off[u + 1] - off;
                  return g < cnt ? ps.pair_token[off + g] : -1;
                },
                [&](int j, int ll, int jq, float v0, float v1) {
-                 const int jj = cta + j * grid, u = jj / NTg, T = jj - u * NTg;
+                 const int jj = jb + j, u = jj / NTg, T = jj - u * NTg;
                  const int off = ps.active_off[u], cnt = ps.active_off[u + 1] - off, tk = 2 * (ll & 3) + jq;
                  if (tk >= cnt) return;
                  const int f = T * 8 + (ll >> 2);
@@ -614,7 +660,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
     stage_rows(xs16, xd, a.mb_act16, F, P, F);
     NamedSync{kBarCompute, kPCThreads}();
     for (int T = cta; T < NTd; T += grid) {
-      run_jobs(U, KSd, xd,
+      run_jobs(U, KSd, U, xd, one,
                [&](int u, int g) {
                  const int off = ps.active_off[u], cnt = ps.active_off[u + 1] - off;
                  return g < cnt ? off + g : -1;
@@ -631,14 +677,15 @@ __global__ void __launch_bounds__(kPThreads, 1) k_persist_step(PersistArgs a) {
         const size_t o = (size_t)b * H + T * 16 + rr;
         float acc = 0.f;
         for (int r = 0; r < K; ++r) acc = fmaf(ps.w[b * K + r], ps.out[ps.pos_of[b * K + r]][rr], acc);
-        a.x[o] = f2bf(bf2f(a.h[o]) + acc);
+        const float res = T == cta ? ps.hres[b][rr] : bf2f(__ldcg(a.h + o));
+        a.x[o] = f2bf(res + acc);
       }
       NamedSync{kBarCompute, kPCThreads}();
     }
     if (!grid_barrier(a, ps, nbar)) break;
   }
   // the final RMSNorm for the output projection (bf16 rows)
-  if (cta == 0 && !ps.stop) norm_rows(a, ps, a.final_nw, nullptr, 0, a.xn_out);
+  if (cta == 0 && !ps.stop) norm_rows(a, ps, a.final_nw, reinterpret_cast<bf16*>(xs16), nullptr, 0, a.xn_out);
 }
 
 namespace {
@@ -683,22 +730,31 @@ bool persist_plan(int H, int qd, int qkv_rows, int F, int E, int k, int g, int d
   if (E % 8 || E > kPMaxE) return no("experts must be a multiple of 8, at most 256");
   if (max_rows < 1 || max_rows > kPMaxRows || max_rows * k > kPMaxPairs) return no("rows x top_k above 64");
   if ((cap + kAttnChunk - 1) / kAttnChunk > kMaxMergeChunks) return no("ctx_cap too large for the chunk merge");
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+    const long J = (long)std::min(E, max_rows * k) * (2 * F / 16);
+    if ((J + sms - 1) / sms > kMaxGUJobs) return no("too many gate/up tiles per SM");
+  }
   PersistGeo r{};
-  r.slot_bytes = kUnitW + (int)(kUnitChunks * 64 / g) * 32;
   const size_t attn = d == 128 ? sizeof(attnf::AttnSmem<128>) : sizeof(attnf::AttnSmem<64>);
   size_t uni = attn;
-  uni = std::max(uni, (size_t)H * 4);                                     // router row
-  uni = std::max(uni, (size_t)max_rows * (H + 32) * 2);                   // QKV / gate-up rows
-  uni = std::max(uni, (size_t)max_rows * (qd + 32) * 2);                  // output projection rows
-  uni = std::max(uni, (size_t)max_rows * k * (F + 32) * 2);               // down rows (pairs)
+  uni = std::max(uni, (size_t)H * 4);                                             // router row
+  uni = std::max(uni, (size_t)max_rows * (H + 32) * 2 + (size_t)max_rows * H * 2); // QKV rows + staged residual rows
+  uni = std::max(uni, (size_t)max_rows * (qd + 32) * 2);                          // output projection rows
+  uni = std::max(uni, (size_t)max_rows * k * (F + 32) * 2);                       // down rows (pairs)
   r.uni_bytes = (uint32_t)((uni + 127) & ~(size_t)127);
   const size_t red = (size_t)kRoundUnits * 4 * 32 * sizeof(float);
   const size_t limit = 227 * 1024 - sizeof(PSmem) - 256;
-  if (red + r.uni_bytes + (size_t)kRoundUnits * r.slot_bytes > limit) return no("shared memory");
-  int ns = (int)((limit - red - r.uni_bytes) / r.slot_bytes);
-  r.ns = ns > kMaxSlots ? kMaxSlots : ns;
+  // the largest item: one 16-row tile over the longest K, with its scales
+  const size_t tileH = (size_t)(H / 64) * 512 + (size_t)(H / g) * 32;
+  const size_t item = std::max(std::max((size_t)kGUTiles * tileH, (size_t)(qd / 64) * 512 + (size_t)(qd / g) * 32),
+                               (size_t)(F / 64) * 512 + (size_t)(F / g) * 32);
+  if (red + r.uni_bytes + 2 * item > limit) return no("shared memory");
+  r.ring_bytes = (uint32_t)((limit - red - r.uni_bytes) & ~(size_t)127);
   r.ring_off = 0;
-  r.red_off = (uint32_t)(((size_t)r.ns * r.slot_bytes + 127) & ~(size_t)127);
+  r.red_off = r.ring_bytes;
   r.uni_off = r.red_off + (uint32_t)red;
   *geo = r;
   return true;

@@ -20,8 +20,7 @@ struct PersistLayer {
 
 // Shared-memory plan of the kernel (bytes) and its grid.
 struct PersistGeo {
-  int ns;               // weight ring slots
-  int slot_bytes;       // one unit: 2 KB of int4 + its scales
+  uint32_t ring_bytes;  // the weight ring
   uint32_t ring_off, red_off, uni_off, uni_bytes;
   int grid;             // CTAs: one per SM
 };
@@ -47,8 +46,8 @@ struct PersistArgs {
   int32_t* u_log;          // [layers] active experts, or null
   unsigned int* bar;       // grid barrier counter, zero at launch
   int* err;                // device error flag (code 6: a bounded wait gave up)
-  int drop_unit1;          // failure-detection tests only: 1 + the index of a weight unit the producer does
-                           // not issue (its consumer's bounded wait runs out); 0 = none
+  int drop_unit1;          // failure-detection tests only: 1 + the index of a weight item (tile job) the
+                           // producer does not issue (its consumers' bounded wait runs out); 0 = none
   PersistGeo geo;
 };
 

@@ -476,10 +476,18 @@ bm_status bm_engine_read_hidden(bm_engine* e, int B, uint16_t* out, void* stream
  * exits.  decode_step ignores this setting. */
 bm_status bm_engine_test_drop_expert_item(bm_engine* e, int item);
 
+/* Switch the persistent small-batch step of an engine created with
+ * persistent_step on (enable = 1) or off (0: every decode step runs the
+ * multi-kernel step): the solo / batched toggle of [KV-slot isolation]
+ * (follow-up update), for measuring both paths on one engine.  Both paths
+ * leave the same bytes.  Captured decode graphs are dropped.  Errors:
+ * BM_ERR_INVALID_ARG, BM_ERR_UNSUPPORTED (created without persistent_step). */
+bm_status bm_engine_set_persistent_step(bm_engine* e, int enable);
+
 /* Failure-detection tests only: make the persistent decode step (engines
- * created with persistent_step) skip the copy of weight unit `unit` of its
- * CTAs' producers (the unit-th 16-row x 256-column block each producer would
- * stream; -1 = none, the default).  The consumer's bounded wait runs out
+ * created with persistent_step) skip the copy of weight item `unit` of its
+ * CTAs' producers (the unit-th 16-row tile each producer would stream in a
+ * step; -1 = none, the default).  The consumer's bounded wait runs out
  * after about a second, every CTA leaves the step at its next grid barrier,
  * and bm_engine_sync reports BM_ERR_DEVICE_CHECK with code 6.  Nothing
  * faults: every copy that was issued lands before its CTA exits.  Captured

@@ -80,7 +80,10 @@ def _schedule(name, cfg, layers, lens, batches, bm, ref, per, gen_device):
     for i in range(len(lens)):
         a, b = _slot_bytes(bm, ref, layers, sr[i], cfg), _slot_bytes(bm, per, layers, sp[i], cfg)
         assert all(torch.equal(x, y) for x, y in zip(a, b)), f"K/V bytes of stream {i} differ"
-    return sr, sp
+    for s in sr:
+        bm.kv_slot_release(ref, s)
+    for s in sp:
+        bm.kv_slot_release(per, s)
 
 
 TINY = "tiny_layer"
@@ -99,6 +102,16 @@ def test_tiny_persistent_step_same_bytes_as_multikernel(bm, use_graph):
         _schedule(TINY, TCFG, layers, lens, batches, bm, ref, per, "cpu")
         st = bm.bm_engine_stats(per)
         assert st["kernels_per_step"] == 3, st   # embedding, the persistent step, the output projection
+        # the toggle: switched off, the same engine runs the multi-kernel step, switched on again the
+        # persistent one, and the streams stay byte-equal throughout
+        bm.bm_engine_set_persistent_step(per, 0)
+        _schedule(TINY, TCFG, layers, [5, 90], [[0, 1], [1]], bm, ref, per, "cpu")
+        assert bm.bm_engine_stats(per)["kernels_per_step"] > 3
+        bm.bm_engine_set_persistent_step(per, 1)
+        _schedule(TINY, TCFG, layers, [33, 2], [[1, 0], [0]], bm, ref, per, "cpu")
+        assert bm.bm_engine_stats(per)["kernels_per_step"] == 3
+        with pytest.raises(bm.BitMoeError):
+            bm.bm_engine_set_persistent_step(ref, 1)   # created without it
     finally:
         bm.bm_engine_destroy(ref)
         bm.bm_engine_destroy(per)

@@ -397,16 +397,8 @@ cudaError_t enqueue_prefill_tc(bm_engine* e, int P, bool last, cudaStream_t s, i
                      (c.ctx_cap + kAttnChunk - 1) / kAttnChunk, e->pf_acnt, P, chk_of(e), 1, 0};
     if ((err = launch_append_rows(fa, s, false)) != cudaSuccess) return err;
     n += 2;
-    for (int r0 = 0; r0 < P; r0 += 128) {
-      AttnFusedArgs fb = fa;
-      fb.row0 = r0;
-      fb.B = P - r0 < 128 ? P - r0 : 128;
-      fb.slots = e->pf_slots + r0;
-      fb.qkv = e->pf_qkv + (size_t)r0 * e->qkv_rows;
-      fb.out = e->pf_attn + (size_t)r0 * qd;
-      if ((err = launch_attention_fused(fb, s, false)) != cudaSuccess) return err;
-      ++n;
-    }
+    if ((err = launch_attention_prefill(fa, s)) != cudaSuccess) return err;
+    ++n;
     PrefillGemmArgs o{};
     o.W = w.wo; o.S = u32(w.wo_s); o.rows = H; o.K = qd; o.g = g;
     o.X = e->pf_attn; o.ldx = qd; o.ntok = P; o.Res = e->pf_x; o.ldr = H; o.Y = e->pf_h; o.ldy = H; o.err = e->d_err;
@@ -424,13 +416,16 @@ cudaError_t enqueue_prefill_tc(bm_engine* e, int P, bool last, cudaStream_t s, i
     PrefillGemmArgs gu{};
     gu.W = w.wg; gu.S = u32(w.wg_s); gu.rows = 2 * F; gu.K = H; gu.g = g; gu.X = e->pf_xg; gu.ldx = H;
     gu.n_active = mb.n_active; gu.active_e = mb.active_e; gu.active_off = mb.active_off; gu.row_map = mb.pair_token;
-    gu.experts = c.experts; gu.w_expert_stride = (size_t)2 * F * H / 2; gu.s_expert_stride = (size_t)F * (H / g);
+    gu.n_jobs = mb.n_jobs; gu.jobs = mb.jobs;
+    gu.max_jobs = std::min(c.experts, P * c.top_k) + (P * c.top_k + kPromptTileRows - 1) / kPromptTileRows;
+    gu.w_expert_stride = (size_t)2 * F * H / 2; gu.s_expert_stride = (size_t)F * (H / g);
     gu.act16 = reinterpret_cast<__half*>(mb.act); gu.F = F; gu.err = e->d_err;
     if ((err = launch_prefill_gateup(gu, e->tm_xg, P, s)) != cudaSuccess) return err;
     PrefillGemmArgs dn{};
     dn.W = w.wd; dn.S = u32(w.wd_s); dn.rows = H; dn.K = F; dn.g = g; dn.X = mb.act; dn.ldx = F;
     dn.n_active = mb.n_active; dn.active_e = mb.active_e; dn.active_off = mb.active_off;
-    dn.experts = c.experts; dn.w_expert_stride = (size_t)H * F / 2; dn.s_expert_stride = (size_t)H * (F / g) / 2;
+    dn.n_jobs = mb.n_jobs; dn.jobs = mb.jobs; dn.max_jobs = gu.max_jobs;
+    dn.w_expert_stride = (size_t)H * F / 2; dn.s_expert_stride = (size_t)H * (F / g) / 2;
     dn.out = mb.out; dn.H = H; dn.err = e->d_err;
     if ((err = launch_prefill_down(dn, e->tm_act, P, s)) != cudaSuccess) return err;
     const bool lastl = l + 1 == c.layers;
@@ -632,7 +627,9 @@ bm_status check_config(const bm_config& c) {
   if (c.prefill_tc) {
     const int qkv_rows = (c.q_heads + 2 * c.kv_heads) * c.head_dim, qd = c.q_heads * c.head_dim;
     const bool mma_ok = c.kernel_policy == BM_POLICY_MMA || (c.kernel_policy == BM_POLICY_AUTO && mma_shapes_ok(c));
-    if (!mma_ok || !prefill_gemm_supports(qkv_rows, c.hidden, c.group) || !prefill_gemm_supports(c.hidden, qd, c.group) ||
+    const AttnArena ar0{nullptr, nullptr, nullptr, c.layers, c.max_streams, c.kv_heads, c.ctx_cap, c.head_dim};
+    if (!mma_ok || !attention_prefill_supports(ar0, c.q_heads) || !prefill_gemm_supports(qkv_rows, c.hidden, c.group) ||
+        !prefill_gemm_supports(c.hidden, qd, c.group) ||
         !prefill_gemm_supports(2 * c.ffn, c.hidden, c.group) || !prefill_gemm_supports(c.hidden, c.ffn, c.group) ||
         c.top_k > 16 || c.experts > 256)
       return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: prefill_tc needs the warp-MMA family and rows that are "

@@ -96,8 +96,12 @@ cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned 
 // Routing of a prompt block of up to 4096 (row, rank) pairs: router logits
 // with the RMSNorm (bufs.xn written, fp16 with xn_f16), top-k per row, and the
 // stable grouping by expert (pair_token, pos_of, n_active, active_e,
-// active_off; no job list).  Three launches.
+// active_off; and the prompt GEMM jobs, see kPromptTileRows).  Three launches.
 cudaError_t launch_moe_route_wide(const MoeArgs& a, const MoeBufs& b, cudaStream_t st);
+// Rows per expert tile of the prompt-length expert GEMMs: the wide grouping
+// lists jobs (active expert u, tile t of kPromptTileRows of its rows) as
+// u | t << 16 in bufs.jobs, their number in bufs.n_jobs.
+constexpr int kPromptTileRows = 128;
 // The combine with the next RMSNorm fused: also xn[b] = RMSNorm(y[b]) * nw
 // (nw null = ones; a.eps), rounded to bf16 and stored as fp16 (xn_f16) or
 // bf16.  H <= 8192.
@@ -234,7 +238,9 @@ struct PrefillGemmArgs {
   const int32_t* active_e;
   const int32_t* active_off;
   const int32_t* row_map;    // gate/up: activation row of each sorted pair
-  int experts;               // grid bound of the expert launches
+  const int32_t* n_jobs;     // experts: (active expert, 128-row tile) jobs, u | tile << 16
+  const int32_t* jobs;
+  int max_jobs;              // grid bound of the expert launches
   size_t w_expert_stride;    // bytes of one expert's matrix
   size_t s_expert_stride;    // 32-bit scale words of one expert's matrix
   __half* act16;             // gate/up output [pairs][F], bf16-rounded values in fp16
@@ -317,6 +323,11 @@ struct AttnFusedArgs {
   int row0;             // prefill: position offset of this launch's first row
 };
 bool attention_fused_supports(const AttnArena& ar, int qh);
+// Causal attention of a prompt block (attention_prefill.cu): a.B rows of the
+// slot a.slots[0] at positions len + b, their k and v already in the slot;
+// out as the fused kernel's.  One launch for the block.
+bool attention_prefill_supports(const AttnArena& ar, int qh);
+cudaError_t launch_attention_prefill(const AttnFusedArgs& a, cudaStream_t st);
 cudaError_t launch_attention_fused(const AttnFusedArgs& a, cudaStream_t st, bool pdl = false);
 // Rotated k and v of each row b to the arena at the row's position (len of
 // its slot, plus b when a.prefill): the prompt path's append.

@@ -181,66 +181,186 @@ __global__ void __launch_bounds__(256) k_topk_rows(MoeArgs a, MoeBufs b) {
   if (t < a.B) topk_warp(a, b, t, false, nullptr);
 }
 
+// The grouping of up to kMaxPairsWide pairs by 32 warps: warp w ranks the
+// pairs of its block [w * per, (w + 1) * per) within their experts (32 at a
+// time, as group_pairs), the blocks' counts are scanned per expert in warp
+// order, then the experts' offsets in ascending id; the ranks are the stable
+// ones of the serial grouping (pair order within an expert).
 __global__ void __launch_bounds__(1024) k_group_wide(MoeArgs a, MoeBufs b) {
-  __shared__ int ids_s[kMaxPairsWide];
-  __shared__ int rank_s[kMaxPairsWide];
-  __shared__ int cnt_s[256];
+  __shared__ short rank_s[kMaxPairsWide];
+  __shared__ unsigned char ids_s[kMaxPairsWide];
+  __shared__ short cnt_w[32][256];   // per warp block and expert: pairs, then the exclusive base
   __shared__ int off_s[257];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, P = a.B * a.k;
-  for (int p = threadIdx.x; p < P; p += blockDim.x) ids_s[p] = b.topk_ids[p];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  const int per = ((P + 31) / 32 + 31) & ~31;   // pairs per warp block, a multiple of 32
+  for (int p = threadIdx.x; p < P; p += blockDim.x) ids_s[p] = (unsigned char)b.topk_ids[p];
+  for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) (&cnt_w[0][0])[i] = 0;
   __syncthreads();
-  if (warp == 0) {
-    // stable ranks, 32 pairs at a time in pair order (as group_pairs)
+  {
     const unsigned lt = (1u << lane) - 1u;
-    for (int p0 = 0; p0 < P; p0 += 32) {
+    const int p_end = min(P, (warp + 1) * per);
+    for (int p0 = warp * per; p0 < p_end; p0 += 32) {
       const int p = p0 + lane;
-      const int e = p < P ? ids_s[p] : -1 - lane;
+      const int e = p < p_end ? (int)ids_s[p] : -1 - lane;
       const unsigned same = __match_any_sync(0xffffffffu, e);
-      const int before = p < P ? cnt_s[e] : 0;
+      const int before = p < p_end ? cnt_w[warp][e] : 0;
       __syncwarp();
-      if (p < P) {
-        rank_s[p] = before + __popc(same & lt);
-        if ((same & lt) == 0u) cnt_s[e] = before + __popc(same);
+      if (p < p_end) {
+        rank_s[p] = (short)(before + __popc(same & lt));
+        if ((same & lt) == 0u) cnt_w[warp][e] = (short)(before + __popc(same));
       }
       __syncwarp();
     }
-    // exclusive scans of the counts and the active flags, 32 experts at a time
-    int run_off = 0, run_u = 0;
+  }
+  __syncthreads();
+  // per expert: the blocks' counts -> exclusive bases in warp order, and the total
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt_w[w][e];
+      cnt_w[w][e] = (short)run;
+      run += c;
+    }
+    off_s[e] = run;   // the count, scanned below
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scans over the experts of the counts, the active flags and
+    // the prompt GEMM jobs (tiles of kPromptTileRows rows); each active
+    // expert writes its jobs u | t << 16
+    int run_off = 0, run_u = 0, run_j = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
-      const int c = e < E ? cnt_s[e] : 0, act = c > 0;
-      int ic = c, ia = act;
+      const int c = e < E ? off_s[e] : 0, act = c > 0, nj = (c + kPromptTileRows - 1) / kPromptTileRows;
+      int ic = c, ia = act, ij = nj;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int c2 = __shfl_up_sync(0xffffffffu, ic, o), a2 = __shfl_up_sync(0xffffffffu, ia, o);
-        if (lane >= o) { ic += c2; ia += a2; }
+        const int j2 = __shfl_up_sync(0xffffffffu, ij, o);
+        if (lane >= o) { ic += c2; ia += a2; ij += j2; }
       }
+      __syncwarp();
       if (e < E) {
-        const int off = run_off + ic - c, u = run_u + ia - act;
+        const int off = run_off + ic - c, u = run_u + ia - act, j0 = run_j + ij - nj;
         off_s[e] = off;
         if (act) {
           b.active_e[u] = e;
           b.active_off[u] = off;
+          for (int t = 0; t < nj; ++t) b.jobs[j0 + t] = u | (t << 16);
         }
       }
       run_off += __shfl_sync(0xffffffffu, ic, 31);
       run_u += __shfl_sync(0xffffffffu, ia, 31);
+      run_j += __shfl_sync(0xffffffffu, ij, 31);
     }
     if (lane == 0) {
       off_s[E] = run_off;
       b.active_off[run_u] = run_off;
       *b.n_active = run_u;
-      *b.n_jobs = 0;
+      *b.n_jobs = run_j;
       if (a.u_log) *a.u_log = run_u;
     }
   }
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int pos = off_s[ids_s[p]] + rank_s[p];
+    const int e = ids_s[p];
+    const int pos = off_s[e] + cnt_w[p / per][e] + rank_s[p];
     b.pair_token[pos] = p / k;
     b.pos_of[p] = pos;
+  }
+}
+
+// Router logits of prompt rows: a CTA takes kRowsR rows and 8 experts (one
+// per warp).  The rows' RMSNorm is that of router_cta, row by row (thread t
+// sums the squares of elements 8t .. 8t + 7, each warp's butterfly, then the
+// 8 warps in order), and each logit is router_cta's dot product (the warp's
+// 128-float strips, lane l holding 4l .. 4l + 3, then the butterfly), so a
+// prompt row's logits and normed row are the bits a decode step gives it.
+// The normed rows are kept as bf16 values in shared memory; the CTAs of
+// expert block 0 also write them out (fp16 for the expert GEMMs).
+constexpr int kRowsR = 16;
+
+__global__ void __launch_bounds__(256) k_router_rows(MoeArgs a, MoeBufs b) {
+  extern __shared__ __align__(16) bf16 xr[];   // [kRowsR][H]
+  __shared__ float red[kRowsR][kRouterWarps];
+  __shared__ float rinv[kRowsR];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, H = a.H;
+  const int eb = blockIdx.x, r0 = blockIdx.y * kRowsR, rows = min(kRowsR, a.B - r0);
+  const int e = eb * 8 + warp;
+  float4 w4[kRouterStrips];
+  if (e < a.E) router_load(a.wr + (size_t)e * H, H, lane * 4, w4);
+  // the rows: thread t holds elements 8t .. 8t + 7 of each (H <= 2048), eight
+  // rows' loads in flight before any use
+  const int kk = threadIdx.x * 8;
+  const bool has = kk < H;
+  for (int rb = 0; rb < rows; rb += 8) {
+    uint4 pv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      pv[j] = has && rb + j < rows ? *reinterpret_cast<const uint4*>(a.x + (size_t)(r0 + rb + j) * H + kk)
+                                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (rb + j >= rows) break;   // uniform over the CTA
+      if (has) *reinterpret_cast<uint4*>(xr + (size_t)(rb + j) * H + kk) = pv[j];
+      const uint32_t w[4] = {pv[j].x, pv[j].y, pv[j].z, pv[j].w};
+      float ss = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float v0 = bf_lo(w[q]), v1 = bf_hi(w[q]);
+        ss = fmaf(v0, v0, ss);
+        ss = fmaf(v1, v1, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) red[rb + j][warp] = ss;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < rows) {
+    float tot = 0.f;
+    for (int w = 0; w < kRouterWarps; ++w) tot += red[threadIdx.x][w];
+    rinv[threadIdx.x] = 1.0f / sqrtf(tot / (float)H + a.eps);
+  }
+  __syncthreads();
+  // the normed rows, 8 values per thread and pass
+  for (int i8 = threadIdx.x; i8 < rows * (H / 8); i8 += 256) {
+    const int r = i8 / (H / 8), k8 = (i8 - r * (H / 8)) * 8;
+    const float ri = rinv[r];
+    bf16* xp = xr + (size_t)r * H + k8;
+    uint4 pv = *reinterpret_cast<const uint4*>(xp);
+    bf16* v = reinterpret_cast<bf16*>(&pv);
+    __half hv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float w = a.norm_w ? bf2f(a.norm_w[k8 + q]) : 1.f;
+      v[q] = f2bf(bf2f(v[q]) * ri * w);
+      hv[q] = __float2half_rn(bf2f(v[q]));
+    }
+    *reinterpret_cast<uint4*>(xp) = pv;
+    if (eb == 0) {
+      if (a.xn_f16) *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(b.xn) + (size_t)(r0 + r) * H + k8) =
+          *reinterpret_cast<const uint4*>(hv);
+      else *reinterpret_cast<uint4*>(b.xn + (size_t)(r0 + r) * H + k8) = pv;
+    }
+  }
+  __syncthreads();
+  if (e >= a.E) return;
+  for (int r = 0; r < rows; ++r) {
+    const bf16* xrow = xr + (size_t)r * H;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRouterStrips; ++i) {
+      const int kk = lane * 4 + 128 * i;
+      if (kk < H) {
+        const uint2 p = *reinterpret_cast<const uint2*>(xrow + kk);
+        acc = fmaf(bf_lo(p.x), w4[i].x, acc); acc = fmaf(bf_hi(p.x), w4[i].y, acc);
+        acc = fmaf(bf_lo(p.y), w4[i].z, acc); acc = fmaf(bf_hi(p.y), w4[i].w, acc);
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) b.logits[(size_t)(r0 + r) * a.E + e] = acc;
   }
 }
 
@@ -540,9 +660,18 @@ cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned 
 }
 
 cudaError_t launch_moe_route_wide(const MoeArgs& a, const MoeBufs& b, cudaStream_t st) {
-  if (a.B * a.k > kMaxPairsWide || a.E > 256 || a.k > 16) return cudaErrorInvalidValue;
-  const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
-  k_router<<<rgrid, 256, sizeof(float) * a.H, st>>>(a, b);
+  if (a.B * a.k > kMaxPairsWide || a.E > 256 || a.k > 16 || a.H > 2048 * kRouterStrips / 16 || a.H % 8)
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  const size_t smem = (size_t)kRowsR * a.H * sizeof(bf16);
+  if (!attr) {
+    cudaError_t e0 = cudaFuncSetAttribute(k_router_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024 - 2048);
+    if (e0 != cudaSuccess) return e0;
+    attr = true;
+  }
+  if (smem > 227 * 1024 - 2048) return cudaErrorInvalidValue;
+  const dim3 rgrid((a.E + 7) / 8, (a.B + kRowsR - 1) / kRowsR);
+  k_router_rows<<<rgrid, 256, smem, st>>>(a, b);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   k_topk_rows<<<(a.B + 7) / 8, 256, 0, st>>>(a, b);

@@ -53,6 +53,7 @@ constexpr int kPfSmem = kPfSlots * kPfBTile + 1024;
 static_assert(kPfN + kPfSlots * 32 <= (int)kPfTmemCols, "TMEM holds the accumulator and the A slots");
 
 enum PfMode { PF_DENSE = 0, PF_GATEUP = 1, PF_DOWN = 2 };
+static_assert(kPfN == kPromptTileRows, "the grouping's job tiles are the GEMM's activation tiles");
 
 
 // One 2-D TMA tile load (box of the tensor map at column x, row y) into shared
@@ -95,11 +96,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
     n0 = blockIdx.y * kPfN;
     ntok = min(kPfN, a.ntok - n0);
   } else {
-    const int u = blockIdx.z;
-    if (u >= *a.n_active) return;
+    // job y of the grouping's list: (active expert u, tile of kPfN of its rows)
+    if ((int)blockIdx.y >= *a.n_jobs) return;
+    const int job = a.jobs[blockIdx.y], u = job & 0xFFFF, tile = job >> 16;
     const int e = a.active_e[u], off = a.active_off[u], cnt = a.active_off[u + 1] - off;
-    n0 = off + blockIdx.y * kPfN;
-    ntok = min(kPfN, cnt - (int)blockIdx.y * kPfN);
+    n0 = off + tile * kPfN;
+    ntok = min(kPfN, cnt - tile * kPfN);
     W += (size_t)e * a.w_expert_stride;
     S += (size_t)e * a.s_expert_stride;
   }
@@ -314,14 +316,16 @@ cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, const TmapBytes& tm, 
 
 cudaError_t launch_prefill_gateup(const PrefillGemmArgs& a, const TmapBytes& tm, int max_rows_per_expert,
                                   cudaStream_t st) {
-  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active) return cudaErrorInvalidValue;
-  return launch_mode<PF_GATEUP>(a, tm, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
+  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active || !a.n_jobs || a.max_jobs < 1 || max_rows_per_expert < 1)
+    return cudaErrorInvalidValue;
+  return launch_mode<PF_GATEUP>(a, tm, a.max_jobs, 1, st);
 }
 
 cudaError_t launch_prefill_down(const PrefillGemmArgs& a, const TmapBytes& tm, int max_rows_per_expert,
                                 cudaStream_t st) {
-  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active) return cudaErrorInvalidValue;
-  return launch_mode<PF_DOWN>(a, tm, (max_rows_per_expert + kPfN - 1) / kPfN, a.experts, st);
+  if (!prefill_gemm_supports(a.rows, a.K, a.g) || !a.n_active || !a.n_jobs || a.max_jobs < 1 || max_rows_per_expert < 1)
+    return cudaErrorInvalidValue;
+  return launch_mode<PF_DOWN>(a, tm, a.max_jobs, 1, st);
 }
 
 cudaError_t init_prefill_attributes() {

@@ -326,12 +326,37 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
       sm.mden[tid] = den;
     }
     sync();
-    for (int idx = tid; idx < G * D; idx += kAttnThreads) {
-      const int h = idx / D, d = idx - h * D;
-      float acc = 0.f;
-      for (int cc = 0; cc < nc; ++cc)
-        acc = fmaf(__ldcg(a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D) + d), sm.ww[h][cc], acc);
-      a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(acc / sm.mden[h]));
+    // a thread's outputs (at most 8 D / kAttnThreads of the G x D), the
+    // chunk records read eight chunks at a time with every load in flight
+    // before the sums, which run in ascending chunk order
+    constexpr int kOut = 8 * D / kAttnThreads;
+    float acc[kOut];
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) acc[o] = 0.f;
+    for (int c0 = 0; c0 < nc; c0 += 8) {
+      float pv[kOut][8];
+#pragma unroll
+      for (int o = 0; o < kOut; ++o) {
+        const int idx = tid + o * kAttnThreads, h = idx / D, d = idx - h * D;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          pv[o][u] = idx < G * D && c0 + u < nc
+                         ? __ldcg(a.part + rec_index(b, kh * G + h, c0 + u, a.qh, a.max_chunks, D) + d)
+                         : 0.f;
+      }
+#pragma unroll
+      for (int o = 0; o < kOut; ++o) {
+        const int idx = tid + o * kAttnThreads, h = idx / D;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (idx < G * D && c0 + u < nc) acc[o] = fmaf(pv[o][u], sm.ww[h][c0 + u], acc[o]);
+      }
+    }
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) {
+      const int idx = tid + o * kAttnThreads, h = idx / D, d = idx - h * D;
+      if (idx < G * D)
+        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(acc[o] / sm.mden[h]));
     }
     if (tid == 0) a.counters[b * kvh + kh] = 0u;
   }

@@ -633,7 +633,7 @@ bm_status check_config(const bm_config& c) {
         !prefill_gemm_supports(2 * c.ffn, c.hidden, c.group) || !prefill_gemm_supports(c.hidden, c.ffn, c.group) ||
         c.top_k > 16 || c.experts > 256)
       return set_error(BM_ERR_UNSUPPORTED, "bm_engine_create: prefill_tc needs the warp-MMA family and rows that are "
-                                           "multiples of 128 with reduction lengths multiples of 128");
+                                           "multiples of 128 with reduction lengths multiples of 256");
   }
   if (c.persistent_step) {
     const bool mma_ok = c.kernel_policy == BM_POLICY_MMA || (c.kernel_policy == BM_POLICY_AUTO && mma_shapes_ok(c));
@@ -1448,7 +1448,7 @@ bm_status w4_gemm_prompt_tc(const uint8_t* Wm, const uint32_t* Sm, const uint16_
                             const uint16_t* R, int M, int N, int K, int g, void* stream) {
   if (!Wm || !Sm || !X16 || !Y) return set_error(BM_ERR_INVALID_ARG, "w4_gemm_prompt_tc: null pointer");
   if (M < 1 || !mma_supports(N, K, g) || !prefill_gemm_supports(N, K, g))
-    return set_error(BM_ERR_INVALID_ARG, "w4_gemm_prompt_tc: need M >= 1, N % 128 == 0, K % 128 == 0, K <= 4096, "
+    return set_error(BM_ERR_INVALID_ARG, "w4_gemm_prompt_tc: need M >= 1, N % 128 == 0, K % 256 == 0, K <= 4096, "
                                          "g in {32, 64, 128}, K % g == 0");
   bm_status st = ensure_attributes();
   if (st != BM_OK) return st;

@@ -46,6 +46,9 @@ constexpr int kPfThreads = kPfProducers + 64;   // producers + the MMA warp + th
 constexpr uint32_t kPfTmemCols = 512;  // accumulator [0, 128) + 12 A slots of 32 columns
 constexpr uint32_t kPfWaitLimit = 1u << 18;   // polls of ~3.7 us: a wait gives up after about a second
 constexpr int kPfBTile = kPfN * 128;   // bytes of one stage's B tile (N rows x 64 fp16)
+constexpr int kPfMmaGroup = 4;         // stages the MMA lane takes at a time (K % 256 == 0)
+constexpr int kPfQS = kPfSlots / kPfMmaGroup;   // groups of slots
+static_assert(kPfSlots % kPfMmaGroup == 0, "groups of stages tile the slots");
 // dynamic shared memory per CTA: the B tiles of every slot, 1024-byte aligned
 // for the 128-byte swizzle (193 KB: one CTA per SM, which also holds all 512
 // TMEM columns)
@@ -81,7 +84,7 @@ __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cas
 template <int MODE, int G>
 __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs a, const __grid_constant__ TmapBytes tm) {
   extern __shared__ unsigned char smem_raw[];   // kPfSlots B tiles, 1024-byte aligned below
-  __shared__ __align__(8) uint64_t full_bar[kPfSlots];
+  __shared__ __align__(8) uint64_t full_bar[kPfSlots / kPfMmaGroup];   // per group of kPfMmaGroup stages
   __shared__ __align__(8) uint64_t done_bar[kPfSlots];
   __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
@@ -113,11 +116,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
     tc::tmem_relinquish();
   }
   if (t == 0) {
-    for (int i = 0; i < kPfSlots; ++i) {
-      // one arrival per warp of the stage's group, one from the B loader (with its bytes)
-      tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfProducers / 32 / kPfGroups + 1);
-      tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
-    }
+    // a group of kPfMmaGroup stages completes with one arrival per producer
+    // warp of each of its stages and one per stage from the B loader (with
+    // the stage's bytes)
+    for (int i = 0; i < kPfSlots / kPfMmaGroup; ++i)
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfMmaGroup * (kPfProducers / 32 / kPfGroups + 1));
+    for (int i = 0; i < kPfSlots; ++i) tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
     tc::mbar_init(tc::smem_u32(&final_bar), 1);
     tc::fence_mbar_init();
   }
@@ -138,35 +142,43 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
         if (j >= 0 &&
             !tc::mbar_wait_spin(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
           ok = false;
-        const uint32_t bar = tc::smem_u32(&full_bar[s]);
+        const int qb = i / kPfMmaGroup;
+        const uint32_t bar = tc::smem_u32(&full_bar[qb % kPfQS]);
         mbar_expect_tx(bar, (uint32_t)kPfBTile);
         tma_load_2d(b_base + (uint32_t)s * kPfBTile, &tm, i * 64, n0, bar);
       }
       // every tile load issued has landed before the CTA may exit (the last
-      // slots' stages complete their full barriers)
-      for (int i = NC - kPfSlots > 0 ? NC - kPfSlots : 0; i < NC; ++i)
-        if (!tc::mbar_wait(tc::smem_u32(&full_bar[i % kPfSlots]), (uint32_t)((i / kPfSlots) & 1), kPfWaitLimit))
-          ok = false;
+      // groups' barriers complete)
+      const int NQ = NC / kPfMmaGroup;
+      for (int q = NQ - kPfQS > 0 ? NQ - kPfQS : 0; q < NQ; ++q)
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[q % kPfQS]), (uint32_t)((q / kPfQS) & 1), kPfWaitLimit)) ok = false;
     }
     __syncwarp();
   } else if (warp == kPfProducers / 32) {
     // ---------------- MMA warp: one lane issues
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16_f32(kPfM, nmma);
-      for (int i = 0; i < NC; ++i) {
-        const int s = i % kPfSlots;
-        const uint32_t ph = (uint32_t)((i / kPfSlots) & 1);
-        if (!tc::mbar_wait_spin(tc::smem_u32(&full_bar[s]), ph, kPfWaitLimit)) ok = false;
+      // stages in groups of kPfMmaGroup: one wait for the group (the
+      // producers run well ahead, so it has mostly completed already), its
+      // MMAs back to back, then one commit per stage (the slots are released
+      // one by one); a wait per stage puts its latency before every four MMAs
+      for (int i0 = 0; i0 < NC; i0 += kPfMmaGroup) {
+        const int ng = kPfMmaGroup, qb = i0 / kPfMmaGroup;
+        if (!tc::mbar_wait_spin(tc::smem_u32(&full_bar[qb % kPfQS]), (uint32_t)((qb / kPfQS) & 1), kPfWaitLimit))
+          ok = false;
         tc::fence_after_sync();
+        for (int u = 0; u < ng; ++u) {
+          const int i = i0 + u, s = i % kPfSlots;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // B: the slot's swizzled tile, this MMA's 16 values of K 32 bytes into
-          // each 128-byte row; A: the slot's 8 TMEM columns (16 fp16 values of
-          // K) per MMA
-          const uint64_t bd = smem_desc_sw128(b_base + (uint32_t)s * kPfBTile + (uint32_t)q * 32u);
-          tc::mma_f16_tmem_a(tmem, tmem + kPfN + s * 32 + q * 8, bd, idesc, (uint32_t)(i > 0 || q > 0));
+          for (int q = 0; q < 4; ++q) {
+            // B: the slot's swizzled tile, this MMA's 16 values of K 32 bytes
+            // into each 128-byte row; A: the slot's 8 TMEM columns (16 fp16
+            // values of K) per MMA
+            const uint64_t bd = smem_desc_sw128(b_base + (uint32_t)s * kPfBTile + (uint32_t)q * 32u);
+            tc::mma_f16_tmem_a(tmem, tmem + kPfN + s * 32 + q * 8, bd, idesc, (uint32_t)(i > 0 || q > 0));
+          }
         }
-        tc::mma_commit(tc::smem_u32(&done_bar[s]));
+        for (int u = 0; u < ng; ++u) tc::mma_commit(tc::smem_u32(&done_bar[(i0 + u) % kPfSlots]));
       }
       tc::mma_commit(tc::smem_u32(&final_bar));
     }
@@ -235,7 +247,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[s]));
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[(i / kPfMmaGroup) % kPfQS]));
     }
     if (!tc::mbar_wait(tc::smem_u32(&final_bar), 0u, kPfWaitLimit)) ok = false;
     tc::fence_after_sync();
@@ -305,8 +317,8 @@ cudaError_t set_attr() {
 }  // namespace
 
 bool prefill_gemm_supports(int rows, int K, int g) {
-  return rows > 0 && rows % kPfM == 0 && K >= 128 && K % 128 == 0 && (g == 32 || g == 64 || g == 128) &&
-         K % g == 0;
+  return rows > 0 && rows % kPfM == 0 && K >= 64 * kPfMmaGroup && K % (64 * kPfMmaGroup) == 0 &&
+         (g == 32 || g == 64 || g == 128) && K % g == 0;
 }
 
 cudaError_t launch_prefill_dense(const PrefillGemmArgs& a, const TmapBytes& tm, cudaStream_t st) {

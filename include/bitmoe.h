@@ -325,7 +325,7 @@ bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint1
  * projection is one batched GEMM over all rows.)
  * Wm, Sm: DEVICE (bm_w4_repack_mma); X16: DEVICE fp16 [M][K]; R: DEVICE bf16
  * [M][N] or NULL; Y: DEVICE bf16 [M][N].  Errors: BM_ERR_INVALID_ARG unless
- * M >= 1, N % 128 == 0, K % 128 == 0, K <= 4096, g in {32, 64, 128},
+ * M >= 1, N % 128 == 0, K % 256 == 0, K <= 4096, g in {32, 64, 128},
  * K % g == 0, or on a NULL pointer. */
 bm_status w4_gemm_prompt_tc(const uint8_t* Wm, const uint32_t* Sm, const uint16_t* X16, uint16_t* Y,
                             const uint16_t* R, int M, int N, int K, int g, void* stream);

@@ -76,3 +76,6 @@ def test_prompt_gemm_residual_and_rejections(bm):
     with pytest.raises(bm.BitMoeError) as ei:
         bm.w4_gemm_prompt_tc(wm, sm, X.cuda().half(), Y, None, 200, 96, K, g)   # N not a multiple of 128
     assert ei.value.status == 1
+    with pytest.raises(bm.BitMoeError) as ei:
+        bm.w4_gemm_prompt_tc(wm, sm, X.cuda().half(), Y, None, 200, N, 384, g)   # K not a multiple of 256
+    assert ei.value.status == 1

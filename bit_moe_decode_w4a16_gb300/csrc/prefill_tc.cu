@@ -85,7 +85,7 @@ template <int MODE, int G>
 __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs a, const __grid_constant__ TmapBytes tm) {
   extern __shared__ unsigned char smem_raw[];   // kPfSlots B tiles, 1024-byte aligned below
   __shared__ __align__(8) uint64_t full_bar[kPfSlots / kPfMmaGroup];   // per group of kPfMmaGroup stages
-  __shared__ __align__(8) uint64_t done_bar[kPfSlots];
+  __shared__ __align__(8) uint64_t done_bar[kPfSlots / kPfMmaGroup];   // a group's MMAs are done
   __shared__ __align__(8) uint64_t final_bar;
   __shared__ uint32_t tmem_slot;
   static_assert(G == 32 || G == 64 || G == 128, "group size");
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
     // the stage's bytes)
     for (int i = 0; i < kPfSlots / kPfMmaGroup; ++i)
       tc::mbar_init(tc::smem_u32(&full_bar[i]), kPfMmaGroup * (kPfProducers / 32 / kPfGroups + 1));
-    for (int i = 0; i < kPfSlots; ++i) tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
+    for (int i = 0; i < kPfQS; ++i) tc::mbar_init(tc::smem_u32(&done_bar[i]), 1);
     tc::mbar_init(tc::smem_u32(&final_bar), 1);
     tc::fence_mbar_init();
   }
@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       for (int i = 0; i < NC; ++i) {
         const int s = i % kPfSlots, j = i - kPfSlots;
         if (j >= 0 &&
-            !tc::mbar_wait_spin(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit))
+            !tc::mbar_wait_spin(tc::smem_u32(&done_bar[(j / kPfMmaGroup) % kPfQS]), (uint32_t)((j / kPfSlots) & 1),
+                                kPfWaitLimit))
           ok = false;
         const int qb = i / kPfMmaGroup;
         const uint32_t bar = tc::smem_u32(&full_bar[qb % kPfQS]);
@@ -160,8 +161,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       const uint32_t idesc = tc::idesc_f16_f32(kPfM, nmma);
       // stages in groups of kPfMmaGroup: one wait for the group (the
       // producers run well ahead, so it has mostly completed already), its
-      // MMAs back to back, then one commit per stage (the slots are released
-      // one by one); a wait per stage puts its latency before every four MMAs
+      // MMAs back to back, then one commit that releases the group's slots;
+      // a wait per stage puts its latency before every four MMAs
       for (int i0 = 0; i0 < NC; i0 += kPfMmaGroup) {
         const int ng = kPfMmaGroup, qb = i0 / kPfMmaGroup;
         if (!tc::mbar_wait_spin(tc::smem_u32(&full_bar[qb % kPfQS]), (uint32_t)((qb / kPfQS) & 1), kPfWaitLimit))
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
             tc::mma_f16_tmem_a(tmem, tmem + kPfN + s * 32 + q * 8, bd, idesc, (uint32_t)(i > 0 || q > 0));
           }
         }
-        for (int u = 0; u < ng; ++u) tc::mma_commit(tc::smem_u32(&done_bar[(i0 + u) % kPfSlots]));
+        tc::mma_commit(tc::smem_u32(&done_bar[qb % kPfQS]));
       }
       tc::mma_commit(tc::smem_u32(&final_bar));
     }
@@ -217,7 +218,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_w4_tc_prefill(PrefillGemmArgs
       // the MMAs of stage j = i - kPfSlots, the last to use this slot, have finished
       const int j = i - kPfSlots;
       if (j >= 0) {
-        if (!tc::mbar_wait_spin(tc::smem_u32(&done_bar[s]), (uint32_t)((j / kPfSlots) & 1), kPfWaitLimit)) ok = false;
+        if (!tc::mbar_wait_spin(tc::smem_u32(&done_bar[(j / kPfMmaGroup) % kPfQS]), (uint32_t)((j / kPfSlots) & 1),
+                                kPfWaitLimit))
+          ok = false;
         tc::fence_after_sync();
       }
       // A of stage i: fp16 (q x s) pairs in K order, 32 columns; word

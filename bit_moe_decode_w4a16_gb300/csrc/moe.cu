@@ -347,20 +347,27 @@ __global__ void __launch_bounds__(256) k_router_rows(MoeArgs a, MoeBufs b) {
   }
   __syncthreads();
   if (e >= a.E) return;
-  for (int r = 0; r < rows; ++r) {
-    const bf16* xrow = xr + (size_t)r * H;
-    float acc = 0.f;
+  // four rows at a time: four independent fmaf chains (each logit's own
+  // order is router_cta's)
+  for (int rb = 0; rb < rows; rb += 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < kRouterStrips; ++i) {
       const int kk = lane * 4 + 128 * i;
       if (kk < H) {
-        const uint2 p = *reinterpret_cast<const uint2*>(xrow + kk);
-        acc = fmaf(bf_lo(p.x), w4[i].x, acc); acc = fmaf(bf_hi(p.x), w4[i].y, acc);
-        acc = fmaf(bf_lo(p.y), w4[i].z, acc); acc = fmaf(bf_hi(p.y), w4[i].w, acc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 p = *reinterpret_cast<const uint2*>(xr + (size_t)min(rb + j, rows - 1) * H + kk);
+          acc[j] = fmaf(bf_lo(p.x), w4[i].x, acc[j]); acc[j] = fmaf(bf_hi(p.x), w4[i].y, acc[j]);
+          acc[j] = fmaf(bf_lo(p.y), w4[i].z, acc[j]); acc[j] = fmaf(bf_hi(p.y), w4[i].w, acc[j]);
+        }
       }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) b.logits[(size_t)(r0 + r) * a.E + e] = acc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = warp_sum(acc[j]);
+      if (lane == 0 && rb + j < rows) b.logits[(size_t)(r0 + rb + j) * a.E + e] = v;
+    }
   }
 }
 

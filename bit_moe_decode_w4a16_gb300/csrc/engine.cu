@@ -430,8 +430,7 @@ cudaError_t enqueue_prefill_tc(bm_engine* e, int P, bool last, cudaStream_t s, i
     if ((err = launch_prefill_down(dn, e->tm_act, P, s)) != cudaSuccess) return err;
     const bool lastl = l + 1 == c.layers;
     const bf16* next_nw = !lastl ? attn_nw(l + 1) : (e->has_final_norm ? e->final_norm_buf : nullptr);
-    if ((err = launch_moe_combine_norm(ma, mb, next_nw, e->pf_xn, lastl ? 0 : 1, s, Marker(), false)) != cudaSuccess)
-      return err;
+    if ((err = launch_moe_combine_norm_rows(ma, mb, next_nw, e->pf_xn, lastl ? 0 : 1, s)) != cudaSuccess) return err;
     n += 9;   // o_proj, routing (3), gather, gate/up, down, combine
   }
   if (!last) {

@@ -107,6 +107,12 @@ constexpr int kPromptTileRows = 128;
 // bf16.  H <= 8192.
 cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
                                     cudaStream_t st, const Marker& mark, bool pdl = false);
+// The same for the rows of a prompt (a.B rows), a CTA per row with 8
+// elements per thread: each element's combine is the same; the squares of
+// the norm meet in another order.  Falls back to launch_moe_combine_norm
+// where k > 8 or H is not a multiple of 8 or above 4096.
+cudaError_t launch_moe_combine_norm_rows(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
+                                         cudaStream_t st);
 
 // ---------------------------------------------------------------- tensor-core W4A16
 struct TcArgs {

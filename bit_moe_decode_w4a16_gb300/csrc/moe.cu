@@ -518,6 +518,83 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
   }
 }
 
+// The same for the rows of a prompt, many at once: one CTA of kRowThreads
+// per row and 8 consecutive elements per thread, every expert output of its
+// elements loaded at once (16-byte loads).  Each element is the same fmaf
+// chain over the row's experts as in k_combine_norm; only the order in which
+// the squares meet for the norm differs (a row's result still depends on
+// nothing but the row).  k <= 8, H % 8 == 0, H <= 8 x kRowThreads x 2.
+constexpr int kRowThreads = 256, kRowMaxK = 8, kRowVecs = 2;
+
+__global__ void __launch_bounds__(kRowThreads) k_combine_norm_rows(MoeArgs a, MoeBufs b, const bf16* __restrict__ nw,
+                                                                   void* __restrict__ xn, int xn_f16) {
+  __shared__ float red[kRowThreads / 32];
+  __shared__ float w_s[kRowMaxK];
+  __shared__ int pos_s[kRowMaxK];
+  const int t = blockIdx.x, H = a.H, kk = a.k;
+  if (threadIdx.x < kk) {
+    w_s[threadIdx.x] = b.topk_w[t * kk + threadIdx.x];
+    pos_s[threadIdx.x] = b.pos_of[t * kk + threadIdx.x];
+  }
+  __syncthreads();
+  float ss = 0.f;
+  for (int vi = 0; vi < kRowVecs; ++vi) {
+    const int h0 = (vi * kRowThreads + (int)threadIdx.x) * 8;
+    if (h0 >= H) break;
+    float4 ov[kRowMaxK][2];
+#pragma unroll
+    for (int r = 0; r < kRowMaxK; ++r) {
+      if (r < kk) {
+        const float4* src = reinterpret_cast<const float4*>(b.out + (size_t)pos_s[r] * H + h0);
+        ov[r][0] = __ldg(src);
+        ov[r][1] = __ldg(src + 1);
+      }
+    }
+    uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+    if (a.res) rv = *reinterpret_cast<const uint4*>(a.res + (size_t)t * H + h0);
+    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+    uint32_t yw[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < kRowMaxK; ++r) {
+        if (r < kk) {
+          const float4 q = ov[r][i >> 2];
+          const float o = (i & 3) == 0 ? q.x : (i & 3) == 1 ? q.y : (i & 3) == 2 ? q.z : q.w;
+          acc = fmaf(w_s[r], o, acc);
+        }
+      }
+      const float res = a.res ? ((i & 1) ? bf_hi(rw[i >> 1]) : bf_lo(rw[i >> 1])) : 0.f;
+      const bf16 y = f2bf(res + acc);
+      const uint32_t yb = (uint32_t)__bfloat16_as_ushort(y);
+      yw[i >> 1] = (i & 1) ? (yw[i >> 1] | (yb << 16)) : yb;
+      const float yf = bf2f(y);
+      ss = fmaf(yf, yf, ss);
+    }
+    *reinterpret_cast<uint4*>(a.y + (size_t)t * H + h0) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+  }
+  const float rinv = block_rms_inv(ss, H, a.eps, red);
+  for (int vi = 0; vi < kRowVecs; ++vi) {
+    const int h0 = (vi * kRowThreads + (int)threadIdx.x) * 8;
+    if (h0 >= H) break;
+    // this thread's own y values, just written
+    const uint4 yv = *reinterpret_cast<const uint4*>(a.y + (size_t)t * H + h0);
+    const uint32_t yr[4] = {yv.x, yv.y, yv.z, yv.w};
+    uint32_t ow[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float yf = (i & 1) ? bf_hi(yr[i >> 1]) : bf_lo(yr[i >> 1]);
+      const float v = round_bf16(yf * rinv * (nw ? bf2f(nw[h0 + i]) : 1.f));
+      const uint32_t bits =
+          xn_f16 ? (uint32_t)__half_as_ushort(__float2half_rn(v)) : (uint32_t)__bfloat16_as_ushort(f2bf(v));
+      ow[i >> 1] = (i & 1) ? (ow[i >> 1] | (bits << 16)) : bits;
+    }
+    uint16_t* dst = static_cast<uint16_t*>(xn) + (size_t)t * H + h0;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  }
+}
+
 template <int LPR, int CPL>
 cudaError_t run_gateup(const MoeArgs& a, const MoeBufs& b, const bf16* xin, int max_u, cudaStream_t st) {
   constexpr int kGroups = kWarp / LPR;
@@ -607,6 +684,13 @@ cudaError_t launch_moe_combine_norm(const MoeArgs& a, const MoeBufs& b, const bf
   cudaError_t err = launch_k(pdl, k_combine_norm, dim3(a.B), dim3(kCombineThreads), 0, st, a, b, nw, xn, xn_f16);
   if (err == cudaSuccess) mark(KT_COMBINE);
   return err;
+}
+
+cudaError_t launch_moe_combine_norm_rows(const MoeArgs& a, const MoeBufs& b, const bf16* nw, void* xn, int xn_f16,
+                                         cudaStream_t st) {
+  if (a.k > kRowMaxK || a.H % 8 || a.H > 8 * kRowThreads * kRowVecs) return launch_moe_combine_norm(a, b, nw, xn, xn_f16, st, Marker(), false);
+  k_combine_norm_rows<<<a.B, kRowThreads, 0, st>>>(a, b, nw, xn, xn_f16);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_moe(const MoeArgs& a, const MoeBufs& b, cudaStream_t st, int* launches, const Marker& mark) {

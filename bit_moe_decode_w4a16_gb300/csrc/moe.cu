@@ -20,6 +20,8 @@
 // which other tokens share the launch.
 #include <float.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "route_dev.cuh"
 #include "w4_simt.cuh"
@@ -272,103 +274,130 @@ __global__ void __launch_bounds__(1024) k_group_wide(MoeArgs a, MoeBufs b) {
   }
 }
 
-// Router logits of prompt rows: a CTA takes kRowsR rows and 8 experts (one
-// per warp).  The rows' RMSNorm is that of router_cta, row by row (thread t
-// sums the squares of elements 8t .. 8t + 7, each warp's butterfly, then the
-// 8 warps in order), and each logit is router_cta's dot product (the warp's
-// 128-float strips, lane l holding 4l .. 4l + 3, then the butterfly), so a
-// prompt row's logits and normed row are the bits a decode step gives it.
-// The normed rows are kept as bf16 values in shared memory; the CTAs of
-// expert block 0 also write them out (fp16 for the expert GEMMs).
-constexpr int kRowsR = 16;
-
-__global__ void __launch_bounds__(256) k_router_rows(MoeArgs a, MoeBufs b) {
-  extern __shared__ __align__(16) bf16 xr[];   // [kRowsR][H]
-  __shared__ float red[kRowsR][kRouterWarps];
-  __shared__ float rinv[kRowsR];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, H = a.H;
-  const int eb = blockIdx.x, r0 = blockIdx.y * kRowsR, rows = min(kRowsR, a.B - r0);
-  const int e = eb * 8 + warp;
-  float4 w4[kRouterStrips];
-  if (e < a.E) router_load(a.wr + (size_t)e * H, H, lane * 4, w4);
-  // the rows: thread t holds elements 8t .. 8t + 7 of each (H <= 2048), eight
-  // rows' loads in flight before any use
+// RMSNorm of prompt rows for the router and the experts, a CTA per row:
+// router_cta's arithmetic (thread t sums the squares of elements 8t .. 8t + 7,
+// each warp's butterfly, then the 8 warps in order; each element bf16(x rinv
+// w)), so a prompt row's normed row is the bits a decode step gives it.
+// Written to xn as fp16 (xn_f16) or bf16; either holds the bf16 values
+// exactly.  H <= 2048, H % 8 == 0.
+__global__ void __launch_bounds__(256) k_norm_rows(MoeArgs a, MoeBufs b) {
+  __shared__ float red[kRouterWarps];
+  const int t = blockIdx.x, H = a.H, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kk = threadIdx.x * 8;
   const bool has = kk < H;
-  for (int rb = 0; rb < rows; rb += 8) {
-    uint4 pv[8];
+  const uint4 pv = has ? *reinterpret_cast<const uint4*>(a.x + (size_t)t * H + kk) : make_uint4(0, 0, 0, 0);
+  const uint32_t w[4] = {pv.x, pv.y, pv.z, pv.w};
+  float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      pv[j] = has && rb + j < rows ? *reinterpret_cast<const uint4*>(a.x + (size_t)(r0 + rb + j) * H + kk)
-                                   : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (rb + j >= rows) break;   // uniform over the CTA
-      if (has) *reinterpret_cast<uint4*>(xr + (size_t)(rb + j) * H + kk) = pv[j];
-      const uint32_t w[4] = {pv[j].x, pv[j].y, pv[j].z, pv[j].w};
-      float ss = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float v0 = bf_lo(w[q]), v1 = bf_hi(w[q]);
-        ss = fmaf(v0, v0, ss);
-        ss = fmaf(v1, v1, ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) red[rb + j][warp] = ss;
-    }
+  for (int q = 0; q < 4; ++q) {
+    const float v0 = bf_lo(w[q]), v1 = bf_hi(w[q]);
+    ss = fmaf(v0, v0, ss);
+    ss = fmaf(v1, v1, ss);
   }
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
   __syncthreads();
-  if (threadIdx.x < rows) {
-    float tot = 0.f;
-    for (int w = 0; w < kRouterWarps; ++w) tot += red[threadIdx.x][w];
-    rinv[threadIdx.x] = 1.0f / sqrtf(tot / (float)H + a.eps);
+  float tot = 0.f;
+  for (int i = 0; i < kRouterWarps; ++i) tot += red[i];
+  const float ri = 1.0f / sqrtf(tot / (float)H + a.eps);
+  if (!has) return;
+  uint4 nwv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);   // bf16 ones
+  if (a.norm_w) nwv = *reinterpret_cast<const uint4*>(a.norm_w + kk);
+  const uint32_t nw[4] = {nwv.x, nwv.y, nwv.z, nwv.w};
+  uint32_t hw[4], bw[4];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float x = (q & 1) ? bf_hi(w[q >> 1]) : bf_lo(w[q >> 1]);
+    const float g = (q & 1) ? bf_hi(nw[q >> 1]) : bf_lo(nw[q >> 1]);
+    const bf16 v = f2bf(x * ri * g);
+    const uint32_t hb = (uint32_t)__half_as_ushort(__float2half_rn(bf2f(v)));
+    const uint32_t bb = (uint32_t)__bfloat16_as_ushort(v);
+    hw[q >> 1] = (q & 1) ? (hw[q >> 1] | (hb << 16)) : hb;
+    bw[q >> 1] = (q & 1) ? (bw[q >> 1] | (bb << 16)) : bb;
   }
-  __syncthreads();
-  // the normed rows, 8 values per thread and pass
-  for (int i8 = threadIdx.x; i8 < rows * (H / 8); i8 += 256) {
-    const int r = i8 / (H / 8), k8 = (i8 - r * (H / 8)) * 8;
-    const float ri = rinv[r];
-    bf16* xp = xr + (size_t)r * H + k8;
-    uint4 pv = *reinterpret_cast<const uint4*>(xp);
-    bf16* v = reinterpret_cast<bf16*>(&pv);
-    __half hv[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float w = a.norm_w ? bf2f(a.norm_w[k8 + q]) : 1.f;
-      v[q] = f2bf(bf2f(v[q]) * ri * w);
-      hv[q] = __float2half_rn(bf2f(v[q]));
-    }
-    *reinterpret_cast<uint4*>(xp) = pv;
-    if (eb == 0) {
-      if (a.xn_f16) *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(b.xn) + (size_t)(r0 + r) * H + k8) =
-          *reinterpret_cast<const uint4*>(hv);
-      else *reinterpret_cast<uint4*>(b.xn + (size_t)(r0 + r) * H + k8) = pv;
-    }
+  const uint4 out = a.xn_f16 ? make_uint4(hw[0], hw[1], hw[2], hw[3]) : make_uint4(bw[0], bw[1], bw[2], bw[3]);
+  *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(b.xn) + (size_t)t * H + kk) = out;
+}
+
+// Router logits of prompt rows: a CTA takes kRowsR normed rows (k_norm_rows)
+// and 8 experts (one per warp); each logit is router_cta's dot product (the
+// warp's 128-float strips, lane l holding 4l .. 4l + 3, then the butterfly),
+// so a prompt row's logits are the bits a decode step gives it.  The rows
+// stay 16-bit in shared memory (xn's bf16 values, as fp16 or bf16; both
+// convert to fp32 exactly), so a strip of a row is one 8-byte load.
+constexpr int kRowsR = 8;
+
+template <bool F16>
+__device__ __forceinline__ float4 x4_of(uint2 p) {
+  if (F16) {
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&p.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&p.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
   }
-  __syncthreads();
-  if (e >= a.E) return;
-  // four rows at a time: four independent fmaf chains (each logit's own
-  // order is router_cta's)
-  for (int rb = 0; rb < rows; rb += 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  return make_float4(bf_lo(p.x), bf_hi(p.x), bf_lo(p.y), bf_hi(p.y));
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(256) k_router_rows(MoeArgs a, MoeBufs b) {
+  extern __shared__ __align__(16) uint16_t xs16[];   // [2][kRowsR][H]: two row blocks
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, H = a.H;
+  const int eb = blockIdx.x, e = eb * 8 + warp;
+  const int nrb = (a.B + kRowsR - 1) / kRowsR;
+  // the warp's router row stays in registers while the CTA walks row blocks
+  // blockIdx.y, + gridDim.y, ..., each block's copies in flight during the
+  // previous block's logits
+  float4 w4[kRouterStrips];
+  if (e < a.E) router_load(a.wr + (size_t)e * H, H, lane * 4, w4);
+  const int kk = threadIdx.x * 8;
+  auto issue = [&](int rbk, int buf) {
+    if (kk >= H) return;
+    for (int j = 0; j < kRowsR; ++j) {
+      const int r = rbk * kRowsR + j;
+      if (r >= a.B) break;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(xs16 + ((size_t)buf * kRowsR + j) * H + kk);
+      const void* src = reinterpret_cast<const uint16_t*>(b.xn) + (size_t)r * H + kk;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    }
+  };
+  int buf = 0;
+  if ((int)blockIdx.y < nrb) issue(blockIdx.y, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int rbk = blockIdx.y; rbk < nrb; rbk += gridDim.y, buf ^= 1) {
+    const int nxt = rbk + (int)gridDim.y;
+    if (nxt < nrb) issue(nxt, buf ^ 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");   // this block's rows have landed
+    __syncthreads();
+    const int r0 = rbk * kRowsR, rows = min(kRowsR, a.B - r0);
+    const uint16_t* xb = xs16 + (size_t)buf * kRowsR * H;
+    if (e < a.E) {
+      // all of the block's rows at once: independent fmaf chains (each logit's
+      // own order is router_cta's); rows past the last read a valid row and
+      // are not stored
+      float acc[kRowsR];
 #pragma unroll
-    for (int i = 0; i < kRouterStrips; ++i) {
-      const int kk = lane * 4 + 128 * i;
-      if (kk < H) {
+      for (int j = 0; j < kRowsR; ++j) acc[j] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint2 p = *reinterpret_cast<const uint2*>(xr + (size_t)min(rb + j, rows - 1) * H + kk);
-          acc[j] = fmaf(bf_lo(p.x), w4[i].x, acc[j]); acc[j] = fmaf(bf_hi(p.x), w4[i].y, acc[j]);
-          acc[j] = fmaf(bf_lo(p.y), w4[i].z, acc[j]); acc[j] = fmaf(bf_hi(p.y), w4[i].w, acc[j]);
+      for (int i = 0; i < kRouterStrips; ++i) {
+        const int k = lane * 4 + 128 * i;
+        if (k < H) {
+#pragma unroll
+          for (int j = 0; j < kRowsR; ++j) {
+            const float4 x = x4_of<F16>(*reinterpret_cast<const uint2*>(xb + (size_t)(j < rows ? j : 0) * H + k));
+            acc[j] = fmaf(x.x, w4[i].x, acc[j]); acc[j] = fmaf(x.y, w4[i].y, acc[j]);
+            acc[j] = fmaf(x.z, w4[i].z, acc[j]); acc[j] = fmaf(x.w, w4[i].w, acc[j]);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float v = warp_sum(acc[j]);
-      if (lane == 0 && rb + j < rows) b.logits[(size_t)(r0 + rb + j) * a.E + e] = v;
+      for (int j = 0; j < kRowsR; ++j) {
+        const float v = warp_sum(acc[j]);
+        if (lane == 0 && j < rows) b.logits[(size_t)(r0 + j) * a.E + e] = v;
+      }
     }
+    __syncthreads();   // every warp is done with this buffer before it is refilled
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // Gate/up: a lane group computes rows f of W_g[e] and W_u[e] together.
@@ -753,17 +782,32 @@ cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned 
 cudaError_t launch_moe_route_wide(const MoeArgs& a, const MoeBufs& b, cudaStream_t st) {
   if (a.B * a.k > kMaxPairsWide || a.E > 256 || a.k > 16 || a.H > 2048 * kRouterStrips / 16 || a.H % 8)
     return cudaErrorInvalidValue;
+  const size_t smem = 2 * (size_t)kRowsR * a.H * sizeof(uint16_t);
   static bool attr = false;
-  const size_t smem = (size_t)kRowsR * a.H * sizeof(bf16);
   if (!attr) {
-    cudaError_t e0 = cudaFuncSetAttribute(k_router_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024 - 2048);
+    cudaError_t e0 = cudaFuncSetAttribute(k_router_rows<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    if (e0 == cudaSuccess)
+      e0 = cudaFuncSetAttribute(k_router_rows<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e0 != cudaSuccess) return e0;
     attr = true;
   }
-  if (smem > 227 * 1024 - 2048) return cudaErrorInvalidValue;
-  const dim3 rgrid((a.E + 7) / 8, (a.B + kRowsR - 1) / kRowsR);
-  k_router_rows<<<rgrid, 256, smem, st>>>(a, b);
+  if (smem > 96 * 1024) return cudaErrorInvalidValue;
+  k_norm_rows<<<a.B, 256, 0, st>>>(a, b);
   cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  // about two CTAs per SM, each walking its share of the row blocks
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 132;
+  }
+  const int eblocks = (a.E + 7) / 8, nrb = (a.B + kRowsR - 1) / kRowsR;
+  const int gy = std::max(1, std::min(nrb, (2 * sms + eblocks - 1) / eblocks));
+  const dim3 rgrid(eblocks, gy);
+  if (a.xn_f16) k_router_rows<true><<<rgrid, 256, smem, st>>>(a, b);
+  else k_router_rows<false><<<rgrid, 256, smem, st>>>(a, b);
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   k_topk_rows<<<(a.B + 7) / 8, 256, 0, st>>>(a, b);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -16,12 +16,12 @@
 // per step against at most a few dozen tokens, so it is bound by HBM, and the
 // per-instruction cost of the multiply decides whether the weight stream can
 // be kept at the memory rate.  Measured on this GPU, one tcgen05.mma of
-// M=128 x N=16 x K=16 takes about 200 SM cycles to issue, whatever its operand
-// sources, so a CTA can retire at most ~1 KB of int4 weights per 200 cycles
-// through it (~1.4 TB/s over the whole GPU).  mma.sync.m16n8k16 retires at 2
-// cycles per SM with four or more warps issuing, i.e. 128 bytes of int4
-// weights per instruction per SM every 2 cycles: the tensor pipe stops being
-// the limit and the kernel can run at the HBM rate.
+// M=128 x N x K=16 costs about 97 SM cycles for every N up to 128, whatever
+// its operand sources, so at a decode batch's N a CTA retires ~1 KB of int4
+// weights per 97 cycles through it (~3.3 TB/s over the whole GPU before any
+// other cost).  mma.sync.m16n8k16 retires at 2 cycles per SM with four or
+// more warps issuing, i.e. 128 bytes of int4 weights per instruction per SM
+// every 2 cycles: the tensor pipe stops being the limit.
 //
 // Work split.  A warp owns two 16-row tiles (32 weight rows) and a fixed
 // range of K (CPW chunks of 64); the KS warps that share the rows cover the

@@ -525,19 +525,34 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
   const float* __restrict__ outp = b.out;
   const int kk = a.k;
   float ss = 0.f;
-  for (int h = threadIdx.x; h < H; h += kCombineThreads) {
-    float ov[16];
+  // two elements per thread at a time (H <= 2048 in one pass), every expert
+  // output of both loaded before either sum; the sums and the squares run in
+  // the same order as one element at a time
+  for (int h = threadIdx.x; h < H; h += 2 * kCombineThreads) {
+    const int h2 = h + kCombineThreads;
+    const bool two = h2 < H;
+    float ov[2][8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) ov[r] = r < kk ? __ldg(outp + (size_t)pos_s[r] * H + h) : 0.f;
-    const float res = a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
-    float acc = 0.f;
+    for (int r = 0; r < 8; ++r) {
+      ov[0][r] = r < kk ? __ldg(outp + (size_t)pos_s[r] * H + h) : 0.f;
+      ov[1][r] = r < kk && two ? __ldg(outp + (size_t)pos_s[r] * H + h2) : 0.f;
+    }
+    const float res0 = a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
+    const float res1 = a.res && two ? bf2f(a.res[(size_t)t * H + h2]) : 0.f;
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < kk) acc = fmaf(w_s[r], ov[r], acc);
-    const bf16 y = f2bf(res + acc);
-    a.y[(size_t)t * H + h] = y;
-    ys[h] = bf2f(y);
-    ss = fmaf(ys[h], ys[h], ss);
+    for (int e2 = 0; e2 < 2; ++e2) {
+      const int he = e2 ? h2 : h;
+      if (e2 && !two) break;
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < kk) acc = fmaf(w_s[r], ov[e2][r], acc);
+      for (int r = 8; r < kk; ++r) acc = fmaf(w_s[r], __ldg(outp + (size_t)pos_s[r] * H + he), acc);
+      const bf16 y = f2bf((e2 ? res1 : res0) + acc);
+      a.y[(size_t)t * H + he] = y;
+      ys[he] = bf2f(y);
+      ss = fmaf(ys[he], ys[he], ss);
+    }
   }
   const float r = block_rms_inv(ss, H, a.eps, red);
   for (int h = threadIdx.x; h < H; h += kCombineThreads) {

@@ -84,13 +84,26 @@ __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, f
     float tot = 0.f;
     for (int w = 0; w < kRouterWarps; ++w) tot += red[w];
     const float r = 1.0f / sqrtf(tot / (float)H + a.eps);
-    for (int k = threadIdx.x; k < H; k += 256) {
-      const float w = a.norm_w ? bf2f(a.norm_w[k]) : 1.f;
-      const bf16 v = f2bf(xs[k] * r * w);
-      xs[k] = bf2f(v);
+    // the thread's own 8 elements: one 16-byte load of the norm weights and
+    // one 16-byte store of the normed values
+    for (int k = threadIdx.x * 8; k < H; k += 256 * 8) {
+      uint4 nwv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);   // bf16 ones
+      if (a.norm_w) nwv = *reinterpret_cast<const uint4*>(a.norm_w + k);
+      const uint32_t nw[4] = {nwv.x, nwv.y, nwv.z, nwv.w};
+      uint32_t hw[4], bw[4];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float w = (q & 1) ? bf_hi(nw[q >> 1]) : bf_lo(nw[q >> 1]);
+        const bf16 v = f2bf(xs[k + q] * r * w);
+        xs[k + q] = bf2f(v);
+        const uint32_t hb = (uint32_t)__half_as_ushort(__float2half_rn(bf2f(v)));
+        const uint32_t bb = (uint32_t)__bfloat16_as_ushort(v);
+        hw[q >> 1] = (q & 1) ? (hw[q >> 1] | (hb << 16)) : hb;
+        bw[q >> 1] = (q & 1) ? (bw[q >> 1] | (bb << 16)) : bb;
+      }
       if (eb == 0) {
-        if (a.xn_f16) reinterpret_cast<__half*>(b.xn)[(size_t)tkn * H + k] = __float2half_rn(bf2f(v));
-        else b.xn[(size_t)tkn * H + k] = v;
+        const uint4 out = a.xn_f16 ? make_uint4(hw[0], hw[1], hw[2], hw[3]) : make_uint4(bw[0], bw[1], bw[2], bw[3]);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(b.xn) + (size_t)tkn * H + k) = out;
       }
     }
   }

@@ -19,6 +19,7 @@ namespace attnf {
 
 constexpr int kWarpsA = 8;   // a warp takes 16 of a chunk's 128 positions
 constexpr int kAttnThreads = kWarpsA * 32;
+static_assert(kAttnThreads >= 256, "a thread holds at most one element of a head (D <= 256)");
 constexpr int kMaxBatch = 128;
 
 __device__ __forceinline__ size_t rec_index(int b, int h, int c, int qh, int max_chunks, int d) {
@@ -152,31 +153,55 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
                         : make_uint4(0, 0, 0, 0);
   }
 
-  // ---- RoPE of the kv group's q heads (and of the new k, with its append)
+  // ---- RoPE of the kv group's q heads (and of the new k, with its append):
+  // every load first (the q pairs, the new k pair and v, the rotation
+  // table), then the rotations, so the phase waits on one round trip
   const float2* cs = a.rope + (size_t)pos * half;
-  for (int idx = tid; idx < 8 * half; idx += kAttnThreads) {
-    const int h = idx / half, i = idx - h * half;
-    bf16 y0 = f2bf(0.f), y1 = f2bf(0.f);
-    if (h < G) {
+  constexpr int kQ = (4 * D + kAttnThreads - 1) / kAttnThreads;   // q pairs per thread (8 heads x D / 2)
+  float qx0[kQ], qx1[kQ];
+  float2 qcs[kQ];
+#pragma unroll
+  for (int u = 0; u < kQ; ++u) {
+    const int idx = tid + u * kAttnThreads, h = idx / half, i = idx - h * half;
+    qx0[u] = qx1[u] = 0.f;
+    qcs[u] = make_float2(0.f, 0.f);
+    if (idx < 8 * half && h < G) {
       const bf16* src = row + (size_t)(kh * G + h) * D;
-      const float2 v = cs[i];
-      rope_pair(bf2f(src[i]), bf2f(src[i + half]), v.x, v.y, y0, y1);
+      qx0[u] = bf2f(src[i]);
+      qx1[u] = bf2f(src[i + half]);
+      qcs[u] = cs[i];
     }
-    sm.qs[h][i] = y0;
-    sm.qs[h][i + half] = y1;
   }
-  if (own_new) {
-    for (int i = tid; i < half; i += kAttnThreads) {
-      const float2 v = cs[i];
-      bf16 y0, y1;
-      rope_pair(bf2f(ksrc[i]), bf2f(ksrc[i + half]), v.x, v.y, y0, y1);
-      sm.knew[i] = y0;
-      sm.knew[i + half] = y1;
-      Kb[(size_t)pos * D + i] = y0;
-      Kb[(size_t)pos * D + i + half] = y1;
+  // the new position's k pair and v element of this thread (half <= D <= kAttnThreads)
+  const bool kt = own_new && tid < half, vt = own_new && tid < D;
+  float kx0 = 0.f, kx1 = 0.f;
+  float2 kcs = make_float2(0.f, 0.f);
+  bf16 vnew = f2bf(0.f);
+  if (kt) {
+    kx0 = bf2f(ksrc[tid]);
+    kx1 = bf2f(ksrc[tid + half]);
+    kcs = cs[tid];
+  }
+  if (vt) vnew = vsrc[tid];
+#pragma unroll
+  for (int u = 0; u < kQ; ++u) {
+    const int idx = tid + u * kAttnThreads, h = idx / half, i = idx - h * half;
+    if (idx < 8 * half) {
+      bf16 y0 = f2bf(0.f), y1 = f2bf(0.f);
+      if (h < G) rope_pair(qx0[u], qx1[u], qcs[u].x, qcs[u].y, y0, y1);
+      sm.qs[h][i] = y0;
+      sm.qs[h][i + half] = y1;
     }
-    for (int i = tid; i < D; i += kAttnThreads) Vb[(size_t)pos * D + i] = vsrc[i];
   }
+  if (kt) {
+    bf16 y0, y1;
+    rope_pair(kx0, kx1, kcs.x, kcs.y, y0, y1);
+    sm.knew[tid] = y0;
+    sm.knew[tid + half] = y1;
+    Kb[(size_t)pos * D + tid] = y0;
+    Kb[(size_t)pos * D + tid + half] = y1;
+  }
+  if (vt) Vb[(size_t)pos * D + tid] = vnew;
   sync();
   if (own_new) {
 #pragma unroll

@@ -317,8 +317,9 @@ bm_status w4_gemm_batched_mma(const uint8_t* Wm, const uint32_t* Sm, const uint1
 /* The batched W4A16 GEMM at prompt length on the tcgen05 tensor cores (the
  * kernel kv_slot_prefill runs with prefill_tc): Y[m][n] = sum_k X[m][k] *
  * W[n][k] (+ R[m][n]) for M rows at once, weights in the layout of
- * bm_w4_repack_mma.  A CTA takes 128 weight rows and up to 128 rows of X over
- * the whole K; each weight enters the MMA as the fp16 product q * s (one
+ * bm_w4_repack_mma.  Work items of 128 weight rows and up to 128 rows of X
+ * over the whole K, looped over by one CTA per SM; each weight enters the MMA
+ * as the fp16 product q * s (one
  * rounding; the decode kernels instead scale exact fp32 group sums), X as
  * fp16, and the sums are fp32 in tensor memory.  A row's result does not
  * depend on M or on the other rows.  ([Batched serving] §1: a dense
@@ -392,12 +393,18 @@ bm_status decode_step(bm_engine* e, int B, const int32_t* slots, const int32_t* 
  * K/V is written once when it joins, then grows one position per decode
  * step): the n_tokens prompt tokens go to positions len .. len + n_tokens - 1
  * of `slot`, each layer's rotated k and v are written there, and the slot's
- * length advances by n_tokens.  The prompt runs in blocks of up to
- * max_streams rows through the decode kernels (one CUDA graph per block
- * shape with use_graph); row j of a block attends causally to positions
- * 0..len + j.  Every row is computed exactly as a decode step at its
- * position, so the arena bytes, logits and next token equal those of
- * n_tokens single-stream decode_step calls fed the same tokens.
+ * length advances by n_tokens; row j attends causally to positions
+ * 0..len + j.  With bm_config.prefill_tc = 0 the prompt runs in blocks of up
+ * to max_streams rows through the decode kernels (one CUDA graph per block
+ * shape with use_graph), and every row is computed exactly as a decode step
+ * at its position, so the arena bytes, logits and next token equal those of
+ * n_tokens single-stream decode_step calls fed the same tokens.  With
+ * prefill_tc = 1 it runs in blocks of up to 512 rows as prompt-length
+ * kernels (the tcgen05 GEMMs of w4_gemm_prompt_tc for the projections and
+ * the grouped experts, a causal block attention, the rows' routing with the
+ * decode router's per-logit arithmetic); the results are within the
+ * tolerance of decoding the prompt, deterministic, and independent of how a
+ * prompt is split over calls.
  * tokens: int32 [n_tokens], HOST or DEVICE; next_token: int32 [1], HOST or
  * DEVICE, the greedy argmax after the last prompt token; logits: DEVICE fp32
  * [V] of that position, or NULL.

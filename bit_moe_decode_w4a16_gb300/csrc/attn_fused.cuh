@@ -327,63 +327,95 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
   }
   __threadfence();
   sync();
-  if (tid == 0) sm.last = atomicAdd(&a.counters[b * kvh + kh], 1u) == (unsigned)(nc - 1);
-  sync();
-  if (sm.last) {
-    // ---- merge the stream's chunks for this kv group, ascending chunk order
+  // ---- merges, ascending order throughout.  A stream of at most
+  // kAttnMergeBlock chunks: the last arriving chunk merges them all.  A longer
+  // one merges in two levels: the last chunk of each block of kAttnMergeBlock
+  // merges the block into a block record (over the block's first chunk
+  // record: o unnormalised, its m and l), and the last block merges the
+  // block records, so no merge reads more than kAttnMergeBlock records.
+  // `merge` runs over `count` records c_first, c_first + c_step, ...; `fin`:
+  // write the normalised output, else the block record.
+  auto merge = [&](int c_first, int c_step, int count, bool fin) {
     __threadfence();
-    for (int idx = tid; idx < G * nc; idx += kAttnThreads) {
-      const int h = idx / nc, cc = idx - h * nc;
-      const float* rec = a.part + rec_index(b, kh * G + h, cc, a.qh, a.max_chunks, D);
+    // a thread's outputs (at most 8 D / kAttnThreads of the G x D); every
+    // record load in flight before the sums
+    constexpr int kOut = 8 * D / kAttnThreads;
+    float pv[kOut][kAttnMergeBlock];
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) {
+      const int idx = tid + o * kAttnThreads, h = idx / D, d = idx - h * D;
+#pragma unroll
+      for (int u = 0; u < kAttnMergeBlock; ++u)
+        pv[o][u] = idx < G * D && u < count
+                       ? __ldcg(a.part + rec_index(b, kh * G + h, c_first + u * c_step, a.qh, a.max_chunks, D) + d)
+                       : 0.f;
+    }
+    for (int idx = tid; idx < G * count; idx += kAttnThreads) {
+      const int h = idx / count, cc = idx - h * count;
+      const float* rec = a.part + rec_index(b, kh * G + h, c_first + cc * c_step, a.qh, a.max_chunks, D);
       sm.mm[h][cc] = __ldcg(rec + D);
       sm.ll[h][cc] = __ldcg(rec + D + 1);
     }
     sync();
     if (tid < G) {
       float M = -FLT_MAX;
-      for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, sm.mm[tid][cc]);
+      for (int cc = 0; cc < count; ++cc) M = fmaxf(M, sm.mm[tid][cc]);
       float den = 0.f;
-      for (int cc = 0; cc < nc; ++cc) {
+      for (int cc = 0; cc < count; ++cc) {
         const float w = expf(sm.mm[tid][cc] - M);
         sm.ww[tid][cc] = w;
         den = fmaf(sm.ll[tid][cc], w, den);
       }
       sm.mden[tid] = den;
+      sm.stat_m[tid] = M;
     }
     sync();
-    // a thread's outputs (at most 8 D / kAttnThreads of the G x D), the
-    // chunk records read eight chunks at a time with every load in flight
-    // before the sums, which run in ascending chunk order
-    constexpr int kOut = 8 * D / kAttnThreads;
-    float acc[kOut];
-#pragma unroll
-    for (int o = 0; o < kOut; ++o) acc[o] = 0.f;
-    for (int c0 = 0; c0 < nc; c0 += 8) {
-      float pv[kOut][8];
-#pragma unroll
-      for (int o = 0; o < kOut; ++o) {
-        const int idx = tid + o * kAttnThreads, h = idx / D, d = idx - h * D;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          pv[o][u] = idx < G * D && c0 + u < nc
-                         ? __ldcg(a.part + rec_index(b, kh * G + h, c0 + u, a.qh, a.max_chunks, D) + d)
-                         : 0.f;
-      }
-#pragma unroll
-      for (int o = 0; o < kOut; ++o) {
-        const int idx = tid + o * kAttnThreads, h = idx / D;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (idx < G * D && c0 + u < nc) acc[o] = fmaf(pv[o][u], sm.ww[h][c0 + u], acc[o]);
-      }
-    }
 #pragma unroll
     for (int o = 0; o < kOut; ++o) {
       const int idx = tid + o * kAttnThreads, h = idx / D, d = idx - h * D;
-      if (idx < G * D)
-        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(acc[o] / sm.mden[h]));
+      if (idx >= G * D) continue;
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < kAttnMergeBlock; ++u)
+        if (u < count) acc = fmaf(pv[o][u], sm.ww[h][u], acc);
+      if (fin) {
+        a.out[((size_t)b * a.qh + kh * G + h) * D + d] = __float2half_rn(round_bf16(acc / sm.mden[h]));
+      } else {
+        a.part[rec_index(b, kh * G + h, c_first, a.qh, a.max_chunks, D) + d] = acc;
+      }
     }
-    if (tid == 0) a.counters[b * kvh + kh] = 0u;
+    if (!fin && tid < G) {
+      float* rec = a.part + rec_index(b, kh * G + tid, c_first, a.qh, a.max_chunks, D);
+      rec[D] = sm.stat_m[tid];
+      rec[D + 1] = sm.mden[tid];
+    }
+  };
+  unsigned int* scnt = &a.counters[b * kvh + kh];
+  if (nc <= kAttnMergeBlock) {
+    if (tid == 0) sm.last = atomicAdd(scnt, 1u) == (unsigned)(nc - 1);
+    sync();
+    if (sm.last) {
+      merge(0, 1, nc, true);
+      if (tid == 0) *scnt = 0u;
+    }
+  } else {
+    const int blk = c / kAttnMergeBlock, c0b = blk * kAttnMergeBlock, nbk = min(kAttnMergeBlock, nc - c0b);
+    const int nblk = (nc + kAttnMergeBlock - 1) / kAttnMergeBlock;
+    unsigned int* bcnt = a.counters + (size_t)a.B * kvh + (size_t)(b * kvh + kh) * kAttnMergeBlocks + blk;
+    if (tid == 0) sm.last = atomicAdd(bcnt, 1u) == (unsigned)(nbk - 1);
+    sync();
+    if (sm.last) {
+      merge(c0b, 1, nbk, false);
+      if (tid == 0) *bcnt = 0u;
+      __threadfence();
+      sync();
+      if (tid == 0) sm.last = atomicAdd(scnt, 1u) == (unsigned)(nblk - 1);
+      sync();
+      if (sm.last) {
+        merge(0, kAttnMergeBlock, nblk, true);
+        if (tid == 0) *scnt = 0u;
+      }
+    }
   }
   sync();   // shared memory is reused by the next item
 }

@@ -118,7 +118,7 @@ struct bm_engine {
   unsigned long long* lm_keys = nullptr;   // fused argmax keys [max_streams], zero between launches
   unsigned int* lm_counter = nullptr;
   unsigned int* route_cnt = nullptr;       // fused routing arrival counters [max_streams + 1], zero between launches
-  unsigned int* attn_cnt = nullptr;        // fused attention arrival counters [max_streams * kv_heads], zero between launches
+  unsigned int* attn_cnt = nullptr;        // fused attention arrival counters [attn_counter_count(max_streams, kv_heads)], zero between launches
   float* attn_part = nullptr;
   void* moe_ws = nullptr;
   float* logits = nullptr;
@@ -790,7 +790,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
              s_moe = take(moe_scratch_bytes(c.max_streams, E, c.top_k, H, F)),
              s_log = take(S * (size_t)c.vocab * 4), s_sl = take(S * 4), s_tk = take(S * 4), s_nx = take(S * 4),
              s_sa = take(S * 4), s_err = take(4), s_ulog = take((size_t)c.layers * 4), s_xn = take(S * H * 2),
-             s_keys = take(S * 8), s_cnt = take(4), s_rcnt = take((S + 1) * 4), s_acnt = take(S * c.kv_heads * 4);
+             s_keys = take(S * 8), s_cnt = take(4), s_rcnt = take((S + 1) * 4), s_acnt = take(attn_counter_count(S, c.kv_heads) * 4);
   size_t tc_jobs = 0, tc_floats = 0;
   if (e->family == BM_POLICY_TC) tc_workspace(c, e->qkv_rows, &tc_jobs, &tc_floats);
   const Part s_tcp = take(tc_floats * 4), s_tcc = take(tc_jobs * 4);
@@ -832,7 +832,7 @@ bm_status bm_engine_create(const bm_config* cfg, bm_engine** out) {
                  p_qkv = take2((size_t)P * e->qkv_rows * 2), p_attn = take2((size_t)P * qd * 2),
                  p_h = take2((size_t)P * H * 2), p_moe = take2(moe_scratch_bytes(P, E, c.top_k, H, F)),
                  p_part = take2(attn_partial_floats(128, c.q_heads, c.ctx_cap, c.head_dim) * 4),
-                 p_acnt = take2((size_t)128 * c.kv_heads * 4), p_sl = take2((size_t)P * 4), p_tk = take2((size_t)P * 4),
+                 p_acnt = take2(attn_counter_count(128, c.kv_heads) * 4), p_sl = take2((size_t)P * 4), p_tk = take2((size_t)P * 4),
                  p_xg = take2((size_t)P * c.top_k * H * 2);
     BM_CUDA(cudaMalloc(&e->pf_mem, o2), "prompt scratch allocation");
     char* pb = static_cast<char*>(e->pf_mem);
@@ -997,7 +997,7 @@ bm_status bm_engine_sync(bm_engine* e, void* stream) {
     // every counter goes back to zero so the next launches start clean
     const size_t S = e->cfg.max_streams;
     BM_CUDA(cudaMemset(e->route_cnt, 0, (S + 1) * 4), "counter reset");
-    BM_CUDA(cudaMemset(e->attn_cnt, 0, S * e->cfg.kv_heads * 4), "counter reset");
+    BM_CUDA(cudaMemset(e->attn_cnt, 0, attn_counter_count(S, e->cfg.kv_heads) * 4), "counter reset");
     BM_CUDA(cudaMemset(e->lm_counter, 0, 4), "counter reset");
     BM_CUDA(cudaMemset(e->lm_keys, 0, S * 8), "counter reset");
     if (e->tc_counters) BM_CUDA(cudaMemset(e->tc_counters, 0, e->tc_counter_count * 4), "counter reset");

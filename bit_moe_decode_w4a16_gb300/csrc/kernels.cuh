@@ -308,10 +308,16 @@ cudaError_t launch_set_len(int32_t* len, int slot, int value, cudaStream_t st);
 
 // RoPE + append + attention + merge in one launch (warp-MMA family).  q, k
 // and v come straight from the QKV projection's rows; out is fp16 holding
-// bf16-rounded values [B][qh][d]; counters [B * kvh] are zero before the
-// launch and left zero.  Needs d in {64, 128}, qh / kvh <= 8 and at most
-// kMaxMergeChunks chunks per stream.
+// bf16-rounded values [B][qh][d]; counters [attn_counter_count(B, kvh)] are
+// zero before the launch and left zero.  Needs d in {64, 128}, qh / kvh <= 8
+// and at most kMaxMergeChunks chunks per stream.  A stream of more than
+// kAttnMergeBlock chunks merges in two levels (blocks of kAttnMergeBlock).
 constexpr int kMaxMergeChunks = 64;
+constexpr int kAttnMergeBlock = 8;
+constexpr int kAttnMergeBlocks = kMaxMergeChunks / kAttnMergeBlock;
+// Arrival counters of a fused attention launch of B rows: one per (row, kv
+// head), then one per (row, kv head, merge block).
+constexpr size_t attn_counter_count(int B, int kvh) { return (size_t)B * kvh * (1 + kAttnMergeBlocks); }
 struct AttnFusedArgs {
   AttnArena ar;
   int layer;

@@ -33,6 +33,11 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kStagedWaitLimit = 1u << 18;   // polls of ~3.7 us each: a wait gives up after about a second
 constexpr int kXPad = 32;   // 16-bit elements of padding per staged activation row (conflict-free LDS.128)
 
+// Bytes the phase will see, without an arrival (the phase cannot complete
+// before the arrival that follows).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
 }
@@ -75,10 +80,19 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NW = geo.nw, RTP = geo.rtp, KS = NW / RTP;
   const int NC = a.K / kChunkK, NG = a.K / G;
-  pdl_wait();
+  // gate/up: the job list comes from the previous kernel; its grid is one
+  // wave, so the down projection may launch as its CTAs finish.  down: the
+  // job list was written by the routing launch, which completed before the
+  // gate/up launch took its own wait, so it is read (through L2) before this
+  // launch's wait, and the first stages' weights and scales are on their way
+  // while gate/up runs its last items; only the rows it wrote wait.
+  if (MODE != DOWN) {
+    pdl_wait();
+    pdl_trigger();
+  }
   // this CTA's items: a contiguous, balanced share of (job, row block) in
   // job order, so consecutive items of a CTA read the same activation rows
-  const int n_items = *a.n_jobs * geo.nrb;
+  const int n_items = (MODE == DOWN ? __ldcg(a.n_jobs) : *a.n_jobs) * geo.nrb;
   const int per = n_items / (int)gridDim.x, extra = n_items % (int)gridDim.x;
   const int first = (int)blockIdx.x * per + min((int)blockIdx.x, extra);
   const int count = per + ((int)blockIdx.x < extra ? 1 : 0);
@@ -98,7 +112,53 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
     // ---------------- producer: one lane issues every copy
     if (lane == 0) {
       int cur_j = -1, cur_e = 0, cur_tok0 = 0, cur_ntok = 0, cur_row[kJobTokens];
-      for (int n = 0; n < count; ++n) {
+      const uint32_t x_bytes = (uint32_t)a.K * 2u;
+      int n0 = 0;
+      if (MODE == DOWN) {
+        // the first stages: weights and scales now, the activation rows (and
+        // the stage's one arrival) after the wait
+        const int pre = min(geo.ns, count);
+        for (int n = 0; n < pre; ++n) {
+          const int it = first + n, j = it / geo.nrb, rb = it - j * geo.nrb;
+          if (j != cur_j) {
+            cur_j = j;
+            const int job = __ldcg(a.jobs + j);
+            cur_e = job & 0x1FF;
+            cur_tok0 = (job >> 9) & 0xFFF;
+            cur_ntok = (job >> 21) & 0x1F;
+            for (int r = 0; r < kJobTokens; ++r) cur_row[r] = r < cur_ntok ? cur_tok0 + r : -1;
+          }
+          ItemInfo& inf = info_s[n];
+          inf.tok0 = cur_tok0;
+          inf.ntok = cur_ntok;
+          inf.rb = rb;
+          for (int r = 0; r < kJobTokens; ++r) inf.row[r] = cur_row[r];
+          if (it + 1 == a.drop_item1) continue;
+          const uint32_t base = tc::smem_u32(smem + (size_t)n * geo.stage);
+          const uint32_t bar = tc::smem_u32(&full_bar[n]);
+          mbar_expect_tx(bar, geo.w_bytes + geo.s_bytes);
+          const uint8_t* wsrc = a.W + (size_t)cur_e * a.w_expert_stride + (size_t)rb * geo.w_bytes;
+          for (uint32_t off = 0; off < geo.w_bytes; off += 16384u) {
+            const uint32_t len = min(16384u, geo.w_bytes - off);
+            bulk_g2s(base + off, wsrc + off, len, bar);
+          }
+          const uint32_t* ssrc = a.S + (size_t)cur_e * a.s_expert_stride + (size_t)rb * (geo.s_bytes / 4);
+          bulk_g2s(base + geo.w_bytes, ssrc, geo.s_bytes, bar);
+        }
+        pdl_wait();
+        for (int n = 0; n < pre; ++n) {
+          if (first + n + 1 == a.drop_item1) continue;
+          const ItemInfo& inf = info_s[n];
+          const uint32_t base = tc::smem_u32(smem + (size_t)n * geo.stage);
+          const uint32_t bar = tc::smem_u32(&full_bar[n]);
+          mbar_arrive_expect_tx(bar, (uint32_t)inf.ntok * x_bytes);
+          for (int r = 0; r < inf.ntok; ++r)
+            bulk_g2s(base + geo.w_bytes + geo.s_bytes + (uint32_t)r * geo.x_stride,
+                     static_cast<const uint8_t*>(a.X) + (size_t)inf.row[r] * a.ldx * 2, x_bytes, bar);
+        }
+        n0 = pre;
+      }
+      for (int n = n0; n < count; ++n) {
         const int it = first + n, s = n % geo.ns;
         if (n >= geo.ns) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ((n / geo.ns) - 1) & 1, kStagedWaitLimit)) {
@@ -128,7 +188,6 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
         if (it + 1 == a.drop_item1) continue;
         const uint32_t base = tc::smem_u32(smem + (size_t)s * geo.stage);
         const uint32_t bar = tc::smem_u32(&full_bar[s]);
-        const uint32_t x_bytes = (uint32_t)a.K * 2u;
         mbar_arrive_expect_tx(bar, geo.w_bytes + geo.s_bytes + (uint32_t)ntok * x_bytes);
         const uint8_t* wsrc = a.W + (size_t)e * a.w_expert_stride + (size_t)rb * geo.w_bytes;
         for (uint32_t off = 0; off < geo.w_bytes; off += 16384u) {
@@ -145,6 +204,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
     return;
   }
 
+  if (MODE == DOWN) pdl_wait();   // before any write of this launch (its rows arrive after it anyway)
   // ---------------- consumers: warp (rtp, ks) takes chunks [ks * CPW, +CPW)
   // of tiles 2 rtp and 2 rtp + 1 of the item
   const int ks = warp % KS, rtp = warp / KS;

@@ -294,3 +294,36 @@ def test_step_attention_kernel_schedule(bm):
         assert checked >= A["steps"]
     finally:
         bm.bm_engine_destroy(e)
+
+
+def test_step_attention_merge_levels(bm):
+    # chunk counts on both sides of the two-level merge (blocks of 8 chunks of
+    # 128 positions): 1, 8 (one level), 9 (a block and one chunk), 16, 17 and
+    # 64 (eight blocks, the cap) in one launch, each row against the oracle;
+    # a two-level stream alone gives its batched bytes
+    e = _attn_engine(bm)
+    try:
+        lens = [5, 1023, 1024, 2047, 2048, CAP - 1]
+        slots, pre = [], {}
+        for i, L in enumerate(lens):
+            k, v = _prefix(7000 + i, L)
+            slots.append(bm.kv_slot_seed(e, k, v, L))
+            pre[slots[-1]] = (k[0].double().cpu().numpy(), v[0].double().cpu().numpy())
+        B = len(slots)
+        qkv = synth.normal_bf16((B, QKV), 1.0, synth.seed_of("slot_attention", "qkv_levels", B), "cuda")
+        out = torch.empty((B, QH, D), dtype=torch.float16, device="cuda")
+        bm.bm_engine_attention(e, 0, slots, qkv, out)
+        bm.bm_engine_sync(e)
+        rows = qkv.double().cpu().numpy()
+        for i, s in enumerate(slots):
+            Ko, Vo = pre[s]
+            ref, _, _ = _oracle_attend(rows[i], lens[i], Ko, Vo)
+            assert_close_rows(out[i:i + 1].float(), ref[None], what=f"attention merge levels, len {lens[i] + 1}")
+        # the same rows again, the 17-chunk stream alone: identical bytes (its
+        # position's k and v are rewritten with the same values)
+        one = torch.empty((1, QH, D), dtype=torch.float16, device="cuda")
+        bm.bm_engine_attention(e, 0, [slots[4]], qkv[4:5].contiguous(), one)
+        bm.bm_engine_sync(e)
+        assert torch.equal(one.view(torch.int16), out[4:5].view(torch.int16))
+    finally:
+        bm.bm_engine_destroy(e)

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(1024) k_topk_sort(MoeArgs a, MoeBufs b) {
 // left zero.  The result is the same as k_router + k_topk_sort.
 template <int EPC>
 __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsigned int* tok_cnt,
-                                                     unsigned int* all_cnt) {
+                                                     unsigned int* all_cnt, int trigger) {
   extern __shared__ __align__(16) float xs[];   // [H] normalised row
   __shared__ int ids_s[kMaxPairs];
   __shared__ int rank_s[kMaxPairs];
@@ -149,7 +149,9 @@ __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsig
   __shared__ int flag_s;
   __shared__ float red[kRouterWarps];
   const int tkn = blockIdx.y, warp = threadIdx.x >> 5;
-  router_cta<EPC>(a, b, xs, red, blockIdx.x, tkn, CtaSync{});   // takes the dependency wait after its weight prefetch
+  // takes the dependency wait after its weight prefetch (and triggers the
+  // expert launch, whose CTAs then set up as this launch's SMs free up)
+  router_cta<EPC>(a, b, xs, red, blockIdx.x, tkn, CtaSync{}, trigger != 0);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) flag_s = atomicAdd(&tok_cnt[tkn], 1u) == gridDim.x - 1;
@@ -781,14 +783,25 @@ cudaError_t launch_moe_route_fused(const MoeArgs& a, const MoeBufs& b, unsigned 
   // up to 16 rows: one expert per warp, so that the grid covers more SMs and
   // each warp has a single router row to fetch
   cudaError_t err;
+  const size_t smem = sizeof(float) * a.H;
+  // one wave (every CTA resident at once): the launch may trigger its
+  // dependents without their CTAs taking slots it still needs
+  auto one_wave = [&](auto kern, const dim3& grid) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess)
+      return 0;
+    return (long)grid.x * grid.y <= (long)sms * per_sm ? 1 : 0;
+  };
   if (a.B <= 16) {
     const dim3 rgrid((a.E + kRouterWarps - 1) / kRouterWarps, a.B);
-    err = launch_k(pdl, k_route_fused<kRouterWarps>, rgrid, dim3(256), sizeof(float) * a.H, st, a, b, tok_cnt,
-                   all_cnt);
+    const int trig = pdl ? one_wave(k_route_fused<kRouterWarps>, rgrid) : 0;
+    err = launch_k(pdl, k_route_fused<kRouterWarps>, rgrid, dim3(256), smem, st, a, b, tok_cnt, all_cnt, trig);
   } else {
     const dim3 rgrid((a.E + kRouterExperts - 1) / kRouterExperts, a.B);
-    err = launch_k(pdl, k_route_fused<kRouterExperts>, rgrid, dim3(256), sizeof(float) * a.H, st, a, b, tok_cnt,
-                   all_cnt);
+    const int trig = pdl ? one_wave(k_route_fused<kRouterExperts>, rgrid) : 0;
+    err = launch_k(pdl, k_route_fused<kRouterExperts>, rgrid, dim3(256), smem, st, a, b, tok_cnt, all_cnt, trig);
   }
   if (err == cudaSuccess) mark(KT_ROUTER);
   return err;

@@ -54,15 +54,18 @@ __device__ __forceinline__ float router_fma(const float* xs, int H, int k0, cons
 // The logits of token `tkn` and experts [EPC eb, EPC (eb + 1)), by threads
 // 0..255 of the caller (synchronised by `sync`); `red` holds kRouterWarps
 // floats of shared memory.
+// `trigger`: the launch is one wave, so its dependents may launch once this
+// CTA has taken its dependency wait.
 template <int EPC, class Sync>
 __device__ __forceinline__ void router_cta(const MoeArgs& a, const MoeBufs& b, float* xs, float* red, int eb, int tkn,
-                                           Sync sync) {
+                                           Sync sync, bool trigger = false) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H;
   float4 w4[kRouterStrips];
   const int e_first = eb * EPC + warp;
   if (e_first < a.E) router_load(a.wr + (size_t)e_first * H, H, lane * 4, w4);
   pdl_wait();
+  if (trigger) pdl_trigger();
   const bf16* x = a.x + (size_t)tkn * H;
   float ss = 0.f;
   for (int k = threadIdx.x * 8; k < H; k += 256 * 8) {

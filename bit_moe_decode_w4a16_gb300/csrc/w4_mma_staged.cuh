@@ -81,15 +81,14 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
   const int NW = geo.nw, RTP = geo.rtp, KS = NW / RTP;
   const int NC = a.K / kChunkK, NG = a.K / G;
   // gate/up: the job list comes from the previous kernel; its grid is one
-  // wave, so the down projection may launch as its CTAs finish.  down: the
+  // wave, and each CTA's producer triggers the dependents when it issues the
+  // CTA's last item, so the down projection launches on each SM as that SM's
+  // CTA finishes (an earlier trigger measured slower per launch).  down: the
   // job list was written by the routing launch, which completed before the
   // gate/up launch took its own wait, so it is read (through L2) before this
   // launch's wait, and the first stages' weights and scales are on their way
   // while gate/up runs its last items; only the rows it wrote wait.
-  if (MODE != DOWN) {
-    pdl_wait();
-    pdl_trigger();
-  }
+  if (MODE != DOWN) pdl_wait();
   // this CTA's items: a contiguous, balanced share of (job, row block) in
   // job order, so consecutive items of a CTA read the same activation rows
   const int n_items = (MODE == DOWN ? __ldcg(a.n_jobs) : *a.n_jobs) * geo.nrb;
@@ -158,8 +157,10 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) k_w4_mma_staged(MmaAr
         }
         n0 = pre;
       }
+      if (MODE == GATEUP && count == 0) pdl_trigger();
       for (int n = n0; n < count; ++n) {
         const int it = first + n, s = n % geo.ns;
+        if (MODE == GATEUP && n == count - 1) pdl_trigger();   // the CTA's last item: its dependents may launch
         if (n >= geo.ns) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ((n / geo.ns) - 1) & 1, kStagedWaitLimit)) {
             if (a.err) atomicExch(a.err, 5);

@@ -662,7 +662,7 @@ def attention_long(bm, peak_gbs, reps=20):
     launch (the launch rewrites each slot's position len with the same k, v,
     so repeats are identical) and the K/V bytes attended per second against
     the measured copy bandwidth.  The arena (1.07 GB) is far larger than L2,
-    but a launch reads only the attended positions (~270 MB)."""
+    but a launch reads only the attended positions (~97 MB)."""
     import torch
     import synth
     S, cap, qh, kvh, d = 16, 8192, 32, 4, 128

@@ -4,9 +4,10 @@
 // stream's chunks, in one persistent launch.
 //
 // Work items are (stream, kv head, chunk); each CTA reads the slot lengths
-// once, enumerates only the chunks that exist and walks them with a stride of
-// the grid, so no CTA is spent on positions past a stream's length.  For one
-// item the CTA:
+// once and enumerates only the chunks that exist, so no CTA is spent on
+// positions past a stream's length.  CTA i runs item i; a launch with more
+// items than CTAs hands out the rest through a work queue, one item per claim
+// by a CTA that has finished its previous one.  For one item the CTA:
 //   - issues all of the item's loads before any arithmetic: the chunk's V rows
 //     to shared memory (cp.async), the lane's K rows to registers, the
 //     rotation table entries, q and the new k / v;
@@ -56,7 +57,31 @@ __global__ void __launch_bounds__(kWarpsA * 32, 3) k_attn_fused(AttnFusedArgs a)
   pdl_wait();
   pdl_trigger();   // the grid is at most one wave: the output projection may start its weight loads
   const int total = attn_prologue<D>(a, sm, blockIdx.x == 0, CtaSync{});
-  for (int it = blockIdx.x; it < total; it += gridDim.x) attn_item<D>(a, sm, it, CtaSync{});
+  const int grid = gridDim.x;
+  // More items than CTAs: after its first item a CTA claims the next one from
+  // the launch's queue once it has finished, merges included.  With a fixed
+  // stride a CTA that merged started its next item late, was then likely the
+  // last arrival of that item's stream again and inherited its merge too; a
+  // claim made when the CTA is free gives it the item that the other CTAs
+  // free at that moment are also starting.  Which CTA runs an item does not
+  // change what the item computes.
+  const bool queued = total > grid;
+  unsigned int* queue = a.counters + attn_queue_index(a.B, a.ar.kvh);   // [0] claims, [1] CTAs done
+  for (int it = blockIdx.x; it < total;) {
+    attn_item<D>(a, sm, it, CtaSync{});   // ends with a CTA barrier: every thread has read sm.next
+    if (!queued) break;
+    if (threadIdx.x == 0) sm.next = grid + (int)atomicAdd(queue, 1u);
+    __syncthreads();
+    it = sm.next;
+  }
+  if (queued && threadIdx.x == 0) {
+    __threadfence();   // this CTA's last claim is performed before its done count
+    if (atomicAdd(queue + 1, 1u) == (unsigned)grid - 1) {
+      __threadfence();
+      queue[0] = 0u;   // every CTA has made its last claim: leave the queue zero
+      queue[1] = 0u;
+    }
+  }
 }
 
 // Rotated k and v of every row to the arena at the row's position: one CTA

@@ -69,6 +69,7 @@ struct AttnSmem {
   float mden[8];
   int slot[kMaxBatch], nc[kMaxBatch], pos[kMaxBatch], pre[kMaxBatch + 1];
   int last;
+  int next;                            // the work queue's claim for this CTA
 };
 
 // Slots, positions, chunk counts and the item prefix (chunk-major within a

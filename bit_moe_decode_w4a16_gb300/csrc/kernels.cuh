@@ -316,8 +316,10 @@ constexpr int kMaxMergeChunks = 64;
 constexpr int kAttnMergeBlock = 8;
 constexpr int kAttnMergeBlocks = kMaxMergeChunks / kAttnMergeBlock;
 // Arrival counters of a fused attention launch of B rows: one per (row, kv
-// head), then one per (row, kv head, merge block).
-constexpr size_t attn_counter_count(int B, int kvh) { return (size_t)B * kvh * (1 + kAttnMergeBlocks); }
+// head), then one per (row, kv head, merge block), then the launch's work
+// queue (items claimed, CTAs done) when it has more items than CTAs.
+__host__ __device__ constexpr size_t attn_queue_index(int B, int kvh) { return (size_t)B * kvh * (1 + kAttnMergeBlocks); }
+__host__ __device__ constexpr size_t attn_counter_count(int B, int kvh) { return attn_queue_index(B, kvh) + 2; }
 struct AttnFusedArgs {
   AttnArena ar;
   int layer;

@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(kWarpsA * 32, 3) k_attn_fused(AttnFusedArgs a)
   __shared__ __align__(16) AttnSmem<D> sm;
   pdl_wait();
   pdl_trigger();   // the grid is at most one wave: the output projection may start its weight loads
-  const int total = attn_prologue<D>(a, sm, blockIdx.x == 0, CtaSync{});
   const int grid = gridDim.x;
+  const int total = attn_prologue<D>(a, sm, blockIdx.x == 0, CtaSync{}, grid);
   // More items than CTAs: after its first item a CTA claims the next one from
   // the launch's queue once it has finished, merges included.  With a fixed
   // stride a CTA that merged started its next item late, was then likely the

@@ -68,6 +68,7 @@ struct AttnSmem {
   float mm[8][kMaxMergeChunks], ll[8][kMaxMergeChunks], ww[8][kMaxMergeChunks];   // merge: m, l, weights
   float mden[8];
   int slot[kMaxBatch], nc[kMaxBatch], pos[kMaxBatch], pre[kMaxBatch + 1];
+  int ord[kMaxBatch];                  // the streams in item order
   int last;
   int next;                            // the work queue's claim for this CTA
 };
@@ -75,8 +76,13 @@ struct AttnSmem {
 // Slots, positions, chunk counts and the item prefix (chunk-major within a
 // stream) of the launch's rows, into sm; returns the number of items.
 // `report`: this caller records bad slots and positions in the check flag.
+// Streams are in row order unless the launch has more than `slots` items
+// (more than its CTAs can take at once): then longest first, ties in row
+// order, so the last items handed out belong to the shortest streams, whose
+// merges are the cheapest.  The order does not change what an item computes.
 template <int D, class Sync>
-__device__ __forceinline__ int attn_prologue(const AttnFusedArgs& a, AttnSmem<D>& sm, bool report, Sync sync) {
+__device__ __forceinline__ int attn_prologue(const AttnFusedArgs& a, AttnSmem<D>& sm, bool report, Sync sync,
+                                             int slots = 0x7fffffff) {
   const AttnArena& ar = a.ar;
   const int tid = threadIdx.x;
   const int kvh = ar.kvh, B = a.B;
@@ -97,13 +103,26 @@ __device__ __forceinline__ int attn_prologue(const AttnFusedArgs& a, AttnSmem<D>
     sm.slot[b] = slot;
     sm.nc[b] = nc;
     sm.pos[b] = pos;
+    sm.ord[b] = b;
   }
   sync();
   if (tid == 0) {
     sm.pre[0] = 0;
-    for (int b = 0; b < B; ++b) sm.pre[b + 1] = sm.pre[b] + sm.nc[b] * kvh;
+    for (int r = 0; r < B; ++r) sm.pre[r + 1] = sm.pre[r] + sm.nc[r] * kvh;
   }
   sync();
+  if (sm.pre[B] > slots) {
+    for (int b = tid; b < B; b += kAttnThreads) {
+      const int nb = sm.nc[b];
+      int r = 0;
+      for (int o = 0; o < B; ++o) r += sm.nc[o] > nb || (sm.nc[o] == nb && o < b);
+      sm.ord[r] = b;
+    }
+    sync();
+    if (tid == 0)
+      for (int r = 0; r < B; ++r) sm.pre[r + 1] = sm.pre[r] + sm.nc[sm.ord[r]] * kvh;
+    sync();
+  }
   return sm.pre[B];
 }
 
@@ -117,9 +136,10 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int kvh = ar.kvh, G = a.qh / kvh, half = D / 2;
   const float scale = 1.0f / sqrtf((float)D);
-  int b = 0;
-  while (sm.pre[b + 1] <= it) ++b;
-  const int r = it - sm.pre[b], kh = r % kvh, c = r / kvh;
+  int rank = 0;
+  while (sm.pre[rank + 1] <= it) ++rank;
+  const int b = sm.ord[rank];
+  const int r = it - sm.pre[rank], kh = r % kvh, c = r / kvh;
   const int slot = sm.slot[b], nc = sm.nc[b], pos = sm.pos[b], L = pos + 1;
   const int j0 = c * kAttnChunk, n = min(kAttnChunk, L - j0);
   const bool last_chunk = c == nc - 1;

@@ -66,6 +66,9 @@ def parse():
                          "against M, without building the model; print one JSON line")
     ap.add_argument("--attention-long", type=int, default=1,
                     help="time the fused attention at the slot-attention workload's lengths (0 to skip)")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="time only the fused attention at the slot-attention workload's lengths (--steps "
+                         "launches after 3 untimed ones), without building the model; print one JSON line")
     ap.add_argument("--kernel-sweep", default="1,4,8,16,32",
                     help="B values of the per-kernel GB/s table ('' to skip)")
     ap.add_argument("--persistent", type=int, default=0,
@@ -846,6 +849,11 @@ def main():
             out = tc_probe()
             out["prompt_gemm"] = prompt_gemm_sweep(bm, [int(x) for x in args.gemm_sweep.split(",") if x], bf16_peak())
             print(json.dumps(out), flush=True)
+        return
+    if args.attention_only:
+        if rank == 0:
+            import bit_moe_decode_w4a16_gb300 as bm
+            print(json.dumps(attention_long(bm, peaks()[0], reps=args.steps)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:

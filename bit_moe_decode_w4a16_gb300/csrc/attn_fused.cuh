@@ -59,7 +59,8 @@ struct AttnSmem {
   static constexpr int kVS = D + 8;   // padded V row: conflict-free ldmatrix
   union {
     bf16 vs[kAttnChunk][kVS];          // V rows of the chunk
-    float ored[kWarpsA][8][D];         // per-warp partial O (after the V reads)
+    float ored[kWarpsA][8][kVS];       // per-warp partial O (after the V reads); rows padded like
+                                       // vs, so a warp's 8 head rows start in 8 bank groups
   } u;
   bf16 qs[8][D];                       // rotated q of the kv group
   bf16 knew[D];                        // rotated k of a decode row's new position
@@ -316,8 +317,7 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
   sync();   // all V reads are done: the union now holds the partial O
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
-    sm.u.ored[warp][g][8 * nt + 2 * t] = o[nt][0];
-    sm.u.ored[warp][g][8 * nt + 2 * t + 1] = o[nt][1];
+    *reinterpret_cast<float2*>(&sm.u.ored[warp][g][8 * nt + 2 * t]) = make_float2(o[nt][0], o[nt][1]);
   }
   sync();
 
@@ -346,7 +346,6 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
     rec[D] = sm.stat_m[tid];
     rec[D + 1] = sm.stat_l[tid];
   }
-  __threadfence();
   sync();
   // ---- merges, ascending order throughout.  A stream of at most
   // kAttnMergeBlock chunks: the last arriving chunk merges them all.  A longer
@@ -357,7 +356,6 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
   // `merge` runs over `count` records c_first, c_first + c_step, ...; `fin`:
   // write the normalised output, else the block record.
   auto merge = [&](int c_first, int c_step, int count, bool fin) {
-    __threadfence();
     // a thread's outputs (at most 8 D / kAttnThreads of the G x D); every
     // record load in flight before the sums
     constexpr int kOut = 8 * D / kAttnThreads;
@@ -411,11 +409,23 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
       rec[D + 1] = sm.mden[tid];
     }
   };
+  // Arrival on a counter after a CTA barrier: thread 0 fences (every thread's
+  // record stores are ordered before it by the barrier) and counts; the last
+  // of n arrivals fences again, so the other CTAs' records are visible to the
+  // merge's loads after the next barrier.
+  auto arrive = [&](unsigned int* cnt, int n) {
+    if (tid == 0) {
+      __threadfence();
+      const bool last = atomicAdd(cnt, 1u) == (unsigned)(n - 1);
+      if (last) __threadfence();
+      sm.last = last;
+    }
+    sync();
+    return sm.last != 0;
+  };
   unsigned int* scnt = &a.counters[b * kvh + kh];
   if (nc <= kAttnMergeBlock) {
-    if (tid == 0) sm.last = atomicAdd(scnt, 1u) == (unsigned)(nc - 1);
-    sync();
-    if (sm.last) {
+    if (arrive(scnt, nc)) {
       merge(0, 1, nc, true);
       if (tid == 0) *scnt = 0u;
     }
@@ -423,16 +433,11 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
     const int blk = c / kAttnMergeBlock, c0b = blk * kAttnMergeBlock, nbk = min(kAttnMergeBlock, nc - c0b);
     const int nblk = (nc + kAttnMergeBlock - 1) / kAttnMergeBlock;
     unsigned int* bcnt = a.counters + (size_t)a.B * kvh + (size_t)(b * kvh + kh) * kAttnMergeBlocks + blk;
-    if (tid == 0) sm.last = atomicAdd(bcnt, 1u) == (unsigned)(nbk - 1);
-    sync();
-    if (sm.last) {
+    if (arrive(bcnt, nbk)) {
       merge(c0b, 1, nbk, false);
       if (tid == 0) *bcnt = 0u;
-      __threadfence();
-      sync();
-      if (tid == 0) sm.last = atomicAdd(scnt, 1u) == (unsigned)(nblk - 1);
-      sync();
-      if (sm.last) {
+      sync();   // the block record is written
+      if (arrive(scnt, nblk)) {
         merge(0, kAttnMergeBlock, nblk, true);
         if (tid == 0) *scnt = 0u;
       }

@@ -268,13 +268,16 @@ __device__ __forceinline__ void attn_item(const AttnFusedArgs& a, AttnSmem<D>& s
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   if (t == 0) sm.red_m[warp][g] = mx;
   sync();
+  // every lane takes its head's maximum over the warps itself (a maximum does
+  // not depend on the order), so no second barrier waits for one thread's;
+  // the record's copy is written by the first 8 threads
+  float mrow = sm.red_m[0][g];
+  for (int w = 1; w < kWarpsA; ++w) mrow = fmaxf(mrow, sm.red_m[w][g]);
   if (tid < 8) {
     float m = sm.red_m[0][tid];
     for (int w = 1; w < kWarpsA; ++w) m = fmaxf(m, sm.red_m[w][tid]);
     sm.stat_m[tid] = m;
   }
-  sync();
-  const float mrow = sm.stat_m[g];
   float ls = 0.f;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)

@@ -152,20 +152,29 @@ __global__ void __launch_bounds__(256) k_route_fused(MoeArgs a, MoeBufs b, unsig
   // takes the dependency wait after its weight prefetch (and triggers the
   // expert launch, whose CTAs then set up as this launch's SMs free up)
   router_cta<EPC>(a, b, xs, red, blockIdx.x, tkn, CtaSync{}, trigger != 0);
-  __threadfence();
+  // Arrivals are one thread's: after the CTA barrier that orders the other
+  // threads' stores, thread 0 fences and counts, and the last arrival fences
+  // again before the barrier that releases the reads of the others' results.
   __syncthreads();
-  if (threadIdx.x == 0) flag_s = atomicAdd(&tok_cnt[tkn], 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const bool last = atomicAdd(&tok_cnt[tkn], 1u) == gridDim.x - 1;
+    if (last) __threadfence();
+    flag_s = last;
+  }
   __syncthreads();
   if (!flag_s) return;
-  __threadfence();
-  if (warp == 0) topk_warp(a, b, tkn, true, nullptr);
-  if (threadIdx.x == 0) tok_cnt[tkn] = 0u;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) flag_s = atomicAdd(all_cnt, 1u) == gridDim.y - 1;
+  if (warp == 0) topk_warp(a, b, tkn, true, nullptr);   // its results are thread 0's stores
+  __syncthreads();   // every thread has read flag_s
+  if (threadIdx.x == 0) {
+    tok_cnt[tkn] = 0u;
+    __threadfence();
+    const bool last = atomicAdd(all_cnt, 1u) == gridDim.y - 1;
+    if (last) __threadfence();
+    flag_s = last;
+  }
   __syncthreads();
   if (!flag_s) return;
-  __threadfence();
   const int P = a.B * a.k;
   for (int p = threadIdx.x; p < P; p += blockDim.x) ids_s[p] = __ldcg(b.topk_ids + p);
   __syncthreads();

@@ -221,15 +221,18 @@ __global__ void __launch_bounds__(kLmWarps * 32, NT * RT >= 2 ? 2 : 1) k_lm_mma(
     for (int w = 0; w < kLmWarps; ++w) best = best_s[w][threadIdx.x] > best ? best_s[w][threadIdx.x] : best;
     atomicMax(a.keys + tok0 + threadIdx.x, best);
   }
-  __threadfence();
+  // one thread fences and counts after the barrier that orders the CTA's
+  // atomics; the last arrival fences again before releasing the key reads
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned int total = gridDim.x * gridDim.y;
-    last_s = atomicAdd(a.counter, 1u) == total - 1;
+    __threadfence();
+    const bool last = atomicAdd(a.counter, 1u) == total - 1;
+    if (last) __threadfence();
+    last_s = last;
   }
   __syncthreads();
   if (!last_s) return;
-  __threadfence();
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     const unsigned long long key = atomicExch(a.keys + b, 0ull);
     a.next[b] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));

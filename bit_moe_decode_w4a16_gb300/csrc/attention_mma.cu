@@ -54,10 +54,14 @@ using namespace attnf;
 template <int D>
 __global__ void __launch_bounds__(kWarpsA * 32, 3) k_attn_fused(AttnFusedArgs a) {
   __shared__ __align__(16) AttnSmem<D> sm;
-  pdl_wait();
-  pdl_trigger();   // the grid is at most one wave: the output projection may start its weight loads
+  // The prologue reads only the slot ids (uploaded before the step) and the
+  // slot lengths (advanced by the previous step's last launch, which had
+  // completed before this launch's predecessor took its own dependency
+  // wait), so it runs before this launch's wait; q, k and v come after it.
   const int grid = gridDim.x;
   const int total = attn_prologue<D>(a, sm, blockIdx.x == 0, CtaSync{}, grid);
+  pdl_wait();
+  pdl_trigger();   // the grid is at most one wave: the output projection may start its weight loads
   // More items than CTAs: after its first item a CTA claims the next one from
   // the launch's queue once it has finished, merges included.  With a fixed
   // stride a CTA that merged started its next item late, was then likely the

@@ -525,13 +525,29 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
   __shared__ float w_s[16];
   __shared__ int pos_s[16];
   __shared__ float ys[kCombineMaxH];
-  pdl_wait();
-  pdl_trigger();   // one wave (a CTA per token): the next projection may start its weight loads
   const int t = blockIdx.x, H = a.H;
+  // Everything but the expert outputs is loaded before the dependency wait:
+  // the routing weights and positions and the residual row were written
+  // before the down projection took its own wait (this launch starts only
+  // once the down projection has triggered or completed, and it never
+  // triggers before that wait), and the norm weights are constant.  These
+  // are the first pass's elements h and h + kCombineThreads (all of them
+  // while H <= 2 kCombineThreads).
   if (threadIdx.x < a.k) {
     w_s[threadIdx.x] = b.topk_w[t * a.k + threadIdx.x];
     pos_s[threadIdx.x] = b.pos_of[t * a.k + threadIdx.x];
   }
+  float res_pre[2] = {0.f, 0.f}, nw_pre[2] = {1.f, 1.f};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int h = threadIdx.x + j * kCombineThreads;
+    if (h < H) {
+      if (a.res) res_pre[j] = bf2f(a.res[(size_t)t * H + h]);
+      if (nw) nw_pre[j] = bf2f(nw[h]);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();   // one wave (a CTA per token): the next projection may start its weight loads
   __syncthreads();
   const float* __restrict__ outp = b.out;
   const int kk = a.k;
@@ -541,15 +557,15 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
   // the same order as one element at a time
   for (int h = threadIdx.x; h < H; h += 2 * kCombineThreads) {
     const int h2 = h + kCombineThreads;
-    const bool two = h2 < H;
+    const bool two = h2 < H, first = h == (int)threadIdx.x;
     float ov[2][8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       ov[0][r] = r < kk ? __ldg(outp + (size_t)pos_s[r] * H + h) : 0.f;
       ov[1][r] = r < kk && two ? __ldg(outp + (size_t)pos_s[r] * H + h2) : 0.f;
     }
-    const float res0 = a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
-    const float res1 = a.res && two ? bf2f(a.res[(size_t)t * H + h2]) : 0.f;
+    const float res0 = first ? res_pre[0] : a.res ? bf2f(a.res[(size_t)t * H + h]) : 0.f;
+    const float res1 = first ? res_pre[1] : a.res && two ? bf2f(a.res[(size_t)t * H + h2]) : 0.f;
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       const int he = e2 ? h2 : h;
@@ -566,8 +582,8 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine_norm(MoeArgs a, Moe
     }
   }
   const float r = block_rms_inv(ss, H, a.eps, red);
-  for (int h = threadIdx.x; h < H; h += kCombineThreads) {
-    const float v = round_bf16(ys[h] * r * (nw ? bf2f(nw[h]) : 1.f));
+  for (int h = threadIdx.x, j = 0; h < H; h += kCombineThreads, ++j) {
+    const float v = round_bf16(ys[h] * r * (j < 2 ? nw_pre[j] : nw ? bf2f(nw[h]) : 1.f));
     if (xn_f16) static_cast<__half*>(xn)[(size_t)t * H + h] = __float2half_rn(v);
     else static_cast<bf16*>(xn)[(size_t)t * H + h] = f2bf(v);
   }

@@ -185,6 +185,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
     if (gridDim.y == 1) pdl_trigger();
   }
 
+  // dense with a residual: the residual of this thread's first epilogue
+  // units, loaded now so its round trip overlaps the MMA loop (a unit's
+  // rows and token follow from its index alone)
+  constexpr int kResPre = 2;   // the epilogue below selects these two by hand
+  float res_pre[kResPre][2];
+  if (MODE == DENSE && a.Res) {
+#pragma unroll
+    for (int u = 0; u < kResPre; ++u) {
+      const int uix = (int)threadIdx.x + u * (int)blockDim.x;
+      const int l = uix & 31, j = (uix >> 5) & 1, nt = (uix >> 6) % NT, rt = (uix / (64 * NT)) & 1,
+                rp = uix / (128 * NT);
+      const int token = nt * 8 + 2 * (l & 3) + j;
+      res_pre[u][0] = res_pre[u][1] = 0.f;
+      if (uix < RTP * NT * 128 && token < ntok) {
+        const int tile = ((int)blockIdx.x * RTP + rp) * 2 + rt;
+        const int r0 = tile * 16 + (l >> 2);
+        const size_t m = (size_t)tok0 + token;
+        res_pre[u][0] = bf2f(a.Res[m * a.ldr + r0]);
+        res_pre[u][1] = bf2f(a.Res[m * a.ldr + r0 + 8]);
+      }
+    }
+  }
+
   // ---- activation rows of the lane's B-fragment column (token g of each n-tile)
   const bf16* xr[NT];
 #pragma unroll
@@ -265,7 +288,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
   // ---- epilogue: unit (rtp, rt, nt, j, lane) = rows (g, g + 8) of the tile,
   // token nt * 8 + 2t + j; partials added in ks order
   const int units = RTP * NT * 128;
-  for (int uix = threadIdx.x; uix < units; uix += blockDim.x) {
+  for (int uix = threadIdx.x, u = 0; uix < units; uix += blockDim.x, ++u) {
     const int l = uix & 31, j = (uix >> 5) & 1, nt = (uix >> 6) % NT, rt = (uix / (64 * NT)) & 1,
               rp = uix / (128 * NT);
     const int token = nt * 8 + 2 * (l & 3) + j;
@@ -282,8 +305,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) k_w4_mma(MmaArgs a) {
     if (MODE == DENSE) {
       float y0 = v0, y1 = v1;
       if (a.Res) {
-        y0 += bf2f(a.Res[m * a.ldr + r0]);
-        y1 += bf2f(a.Res[m * a.ldr + r1]);
+        // (selects, not an index: the array stays in registers)
+        y0 += u == 0 ? res_pre[0][0] : u == 1 ? res_pre[1][0] : bf2f(a.Res[m * a.ldr + r0]);
+        y1 += u == 0 ? res_pre[0][1] : u == 1 ? res_pre[1][1] : bf2f(a.Res[m * a.ldr + r1]);
       }
       a.Y[m * a.ldy + r0] = f2bf(y0);
       a.Y[m * a.ldy + r1] = f2bf(y1);
